@@ -1,0 +1,358 @@
+"""CPU oracle of the fused MoE layer forward.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module. The CUDA library
+never calls it. It shares no code with the CUDA path.
+
+Plain, slow and meant to be read against the source pages. Every function
+names the passage it follows. Arithmetic is fp64 except where a page fixes the
+precision: the routing softmax is fp32, as in
+``F.softmax(router_logits, dim=1, dtype=torch.float)`` (SGLang issue "Expert
+parallelism support", MixtralMoE.forward). Router logits are one fp64 dot
+product per (token, expert), rounded once to fp32.
+
+Pins (checked by ``tests/test_oracle_pins.py``):
+  * routing, top-k, renormalise: pinned by the full-softmax closed form
+    (top_k = E), brute-force top-k on tiny inputs, and scipy's softmax;
+  * grouped top-k: pinned by its reductions to plain top-k and by brute force
+    over all group subsets;
+  * expert MLP: pinned by the SiLU closed form and the gate/up role test;
+  * forward: pinned by the page's dense per-expert masked loop, the EP
+    shard-sum identity, shared-expert merging and rsf linearity;
+  * align/permute: pinned by a brute-force stable sort and counting.
+  The output values themselves have no numeric worked example on the pages,
+  so they are pinned only by these identities.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# expert partition (expert parallelism)
+# ---------------------------------------------------------------------------
+def expert_map(num_experts: int, ep_size: int, ep_rank: int) -> np.ndarray:
+    """Global-to-local expert id map of one EP rank, -1 for non-local experts.
+
+    Rank r owns the contiguous range [r*E/ep, (r+1)*E/ep), and local id =
+    global id - r*E/ep (ep_fused_moe_patch.py, ``_ep_init``: start_expert_id =
+    ep_rank * num_experts_per_rank, with num_experts % ep_size asserted;
+    ``_ep_weight_loader``: local_expert_id = expert_id - start; vllm-omni
+    "Expert Parallel", Step 4 filters the same range).
+    """
+    if num_experts % ep_size != 0:
+        raise ValueError("num_experts must be divisible by ep_size")
+    if not 0 <= ep_rank < ep_size:
+        raise ValueError("ep_rank out of range")
+    n_local = num_experts // ep_size
+    start = ep_rank * n_local
+    m = np.full(num_experts, -1, dtype=np.int32)
+    m[start:start + n_local] = np.arange(n_local, dtype=np.int32)
+    return m
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+def router_logits(x, router_w, router_b=None) -> np.ndarray:
+    """logits[t, e] = sum_h x[t, h] * Wg[e, h] (+ b[e]), as fp32.
+
+    The gate is a bias-free replicated linear over all global experts
+    (MixtralMoE ``self.gate = ReplicatedLinear(hidden, num_experts,
+    bias=False)``; vllm-omni "Expert Parallel", Step 2). The optional per-expert
+    bias ``b`` is this library's logit-skew input, added before the softmax.
+    """
+    lg = np.asarray(x, np.float64) @ np.asarray(router_w, np.float64).T
+    if router_b is not None:
+        lg = lg + np.asarray(router_b, np.float64)[None, :]
+    return lg.astype(np.float32)
+
+
+def softmax_fp32(logits32: np.ndarray) -> np.ndarray:
+    """Softmax over experts in fp32 (MixtralMoE.forward, ``dtype=torch.float``)."""
+    l = np.asarray(logits32, np.float32)
+    m = l.max(axis=1, keepdims=True)
+    e = np.exp(l - m)
+    return (e / e.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
+
+
+def topk_plain(p: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest p per row, by descending p, ties to the lower id.
+
+    ``torch.topk(routing_weights, top_k, dim=-1)`` (MixtralMoE.forward). A
+    stable sort of -p puts equal values in ascending id order.
+    """
+    order = np.argsort(-p, axis=1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def topk_grouped(p: np.ndarray, k: int, n_group: int, topk_group: int) -> np.ndarray:
+    """Group-limited top-k (``use_grouped_topk``, ``num_expert_group``, ``topk_group``).
+
+    The pages only name the arguments (vLLM ``MoEMixin.recursive_replace``
+    reads ``n_group`` / ``topk_group``; ``ep_fused_moe_patch.py`` passes them to
+    ``select_experts``). Reading taken: the E experts form n_group contiguous
+    groups of E/n_group. A group scores the max p of its members. The
+    topk_group best groups are kept, ties going to the lower group id. Top-k
+    then runs over the members of the kept groups only.
+    """
+    T, E = p.shape
+    gs = E // n_group
+    gscore = p.reshape(T, n_group, gs).max(axis=2)
+    keep_g = np.argsort(-gscore, axis=1, kind="stable")[:, :topk_group]
+    keep = np.zeros((T, n_group), dtype=bool)
+    keep[np.arange(T)[:, None], keep_g] = True
+    masked = np.where(np.repeat(keep, gs, axis=1), p, -np.inf).astype(np.float32)
+    return topk_plain(masked, k)
+
+
+def route(x, router_w, router_b=None, *, top_k, renormalize,
+          n_group=0, topk_group=0):
+    """(topk_ids [T,K] int32 global ids, topk_w [T,K] fp32, p [T,E] fp32).
+
+    MixtralMoE.forward: softmax in fp32, topk, then ``routing_weights /=
+    routing_weights.sum(dim=-1, keepdim=True)`` when renormalising
+    (``renormalize = norm_topk_prob`` in ``MoEMixin.recursive_replace``).
+    The weights are the unmasked softmax values of the chosen experts.
+    Routing is global: every rank selects among all experts
+    (ep_fused_moe_patch.py, ``_ep_forward`` step 1).
+    """
+    p = softmax_fp32(router_logits(x, router_w, router_b))
+    if n_group > 0:
+        ids = topk_grouped(p, top_k, n_group, topk_group)
+    else:
+        ids = topk_plain(p, top_k)
+    w = np.take_along_axis(p, ids, axis=1).astype(np.float32)
+    if renormalize:
+        w = (w / w.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
+    return ids, w, p
+
+
+def routing_min_gap(p: np.ndarray, top_k: int, n_group: int = 0,
+                    topk_group: int = 0) -> np.ndarray:
+    """Smallest decision gap per token (for generating tie-free inputs).
+
+    It covers every gap that orders the chosen ids: adjacent ranks among the
+    top-k and the k-th vs (k+1)-th. For the grouped variant it also covers the
+    group scores up to topk_group and the k-th vs (k+1)-th among kept experts.
+    """
+    T, E = p.shape
+    gaps = []
+    if n_group > 0:
+        gs = E // n_group
+        gscore = np.sort(p.reshape(T, n_group, gs).max(axis=2), axis=1)[:, ::-1]
+        upto = min(topk_group, n_group - 1)
+        if upto > 0:
+            gaps.append(gscore[:, :upto] - gscore[:, 1:upto + 1])
+        keep_g = np.argsort(-p.reshape(T, n_group, gs).max(axis=2), axis=1,
+                            kind="stable")[:, :topk_group]
+        keep = np.zeros((T, n_group), dtype=bool)
+        keep[np.arange(T)[:, None], keep_g] = True
+        vals = np.where(np.repeat(keep, gs, axis=1), p, -np.inf)
+    else:
+        vals = p
+    s = np.sort(vals, axis=1)[:, ::-1]
+    upto = min(top_k, int(np.isfinite(s).sum(axis=1).min()) - 1)
+    if upto > 0:
+        gaps.append(s[:, :upto] - s[:, 1:upto + 1])
+    if not gaps:
+        return np.full(T, np.inf)
+    return np.concatenate(gaps, axis=1).min(axis=1)
+
+
+# ---------------------------------------------------------------------------
+# expert MLP
+# ---------------------------------------------------------------------------
+def silu(z):
+    """silu(z) = z * sigmoid(z) = z / (1 + exp(-z)) (``activation = "silu"``)."""
+    z = np.asarray(z, np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def expert_mlp(x_rows, w13_e, w2_e) -> np.ndarray:
+    """SiLU-gated expert MLP on rows of x, in fp64.
+
+    f(x) = W2 (silu(W_gate x) * (W_up x)). The stacked ``gate_up_proj`` has
+    shape (E, 2*I, H) (vLLM ``MoEMixin.recursive_replace``, packed experts).
+    Gate takes rows [0, I) and up takes rows [I, 2I). ``down_proj`` is stored
+    [H, I], i.e. [out, in] like gate_up_proj.
+    """
+    xr = np.asarray(x_rows, np.float64)
+    I = w2_e.shape[1]
+    g = xr @ np.asarray(w13_e[:I], np.float64).T
+    u = xr @ np.asarray(w13_e[I:], np.float64).T
+    h = silu(g) * u
+    return h @ np.asarray(w2_e, np.float64).T
+
+
+# ---------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------
+def moe_forward(x, router_w, w13, w2, *, top_k, renormalize=True, n_group=0,
+                topk_group=0, rsf=1.0, router_b=None, shared_w13=None,
+                shared_w2=None, emap=None, tokens=None, routing=None):
+    """Output rows of the MoE layer for ``tokens`` (default: all), fp64.
+
+    out[t] = rsf * sum_{k : emap[id_tk] >= 0} w_tk * f_{emap[id_tk]}(x_t)
+             + sum_s shared_s(x_t)
+
+    This is MixtralMoE.forward's per-expert accumulation written as a sum over
+    each token's k slots. ``w13``/``w2`` hold the local experts only, and
+    ``emap`` maps global ids to them (ep_fused_moe_patch.py: route globally,
+    compute local experts only). ``rsf`` scales the routed sum
+    (``routed_scaling_factor``, ``MoEMixin.recursive_replace``). Shared experts
+    add unweighted (vllm-omni "Expert Parallel", Step 5).
+    """
+    x = np.asarray(x)
+    T = x.shape[0]
+    tok = np.arange(T) if tokens is None else np.asarray(tokens)
+    if routing is None:
+        ids, w, _ = route(x[tok], router_w, router_b, top_k=top_k,
+                          renormalize=renormalize, n_group=n_group,
+                          topk_group=topk_group)
+    else:
+        ids, w = routing[0][tok], routing[1][tok]
+    E_l = w13.shape[0]
+    if emap is None:
+        emap = np.arange(E_l, dtype=np.int32)
+    loc = emap[ids]                                   # [n, K], -1 = not local
+    f = np.zeros(ids.shape + (x.shape[1],), dtype=np.float64)
+    for e in range(E_l):
+        rows, slots = np.nonzero(loc == e)
+        if rows.size:
+            f[rows, slots] = expert_mlp(x[tok[rows]], w13[e], w2[e])
+    routed = np.zeros((tok.size, x.shape[1]), dtype=np.float64)
+    for k in range(top_k):
+        keep = (loc[:, k] >= 0)[:, None]
+        routed += np.where(keep, w[:, k:k + 1].astype(np.float64) * f[:, k], 0.0)
+    out = np.float64(rsf) * routed
+    if shared_w13 is not None:
+        for s in range(shared_w13.shape[0]):
+            out += expert_mlp(x[tok], shared_w13[s], shared_w2[s])
+    return out
+
+
+def moe_forward_masked_loop(x, router_w, w13, w2, *, top_k, renormalize=True,
+                            n_group=0, topk_group=0, rsf=1.0, router_b=None,
+                            shared_w13=None, shared_w2=None, emap=None):
+    """The page's dense form: every local expert runs on all tokens.
+
+    MixtralMoE.forward loops over its expert indices. For each expert it forms
+    the mask selected_experts == idx and the weight (routing_weights *
+    mask).sum(-1). It runs the expert on all hidden states, scales by that
+    weight and accumulates. Used only to pin ``moe_forward`` on small inputs.
+    """
+    ids, w, _ = route(x, router_w, router_b, top_k=top_k,
+                      renormalize=renormalize, n_group=n_group,
+                      topk_group=topk_group)
+    E_l = w13.shape[0]
+    if emap is None:
+        emap = np.arange(E_l, dtype=np.int32)
+    final = np.zeros((x.shape[0], x.shape[1]), dtype=np.float64)
+    for g_id in np.nonzero(emap >= 0)[0]:
+        e = emap[g_id]
+        mask = ids == g_id
+        ew = (w.astype(np.float64) * mask).sum(axis=-1, keepdims=True)
+        final += expert_mlp(x, w13[e], w2[e]) * ew
+    final *= np.float64(rsf)
+    if shared_w13 is not None:
+        for s in range(shared_w13.shape[0]):
+            final += expert_mlp(x, shared_w13[s], shared_w2[s])
+    return final
+
+
+# ---------------------------------------------------------------------------
+# token permutation by expert
+# ---------------------------------------------------------------------------
+def align_cap(T: int, top_k: int, n_local: int, block: int) -> int:
+    """Rows needed for the padded permutation: T*K + E_local*(block-1)."""
+    return T * top_k + n_local * (block - 1)
+
+
+def align_permute(topk_ids, emap, n_local: int, block: int, cap=None):
+    """Per-local-expert segments of work items, padded to ``block`` rows.
+
+    Work item i = t*K + k stands for the pair (token t, slot k). This is the
+    flattening in ep_fused_moe_patch.py, ``_ep_forward`` step 2, where
+    ``flat_token_idx = arange(T)`` is expanded over K. Items whose expert is
+    not local (emap = -1) are dropped (step 3 keeps only local ids). Reading
+    taken where the page uses an unstable argsort: within a segment, items
+    appear in ascending item order.
+
+    Returns counts[E_l], offsets[E_l+1] (exclusive, padded), sorted_ids[cap]
+    (sentinel T*K on padding) and inv_pos[T*K] (row of each item, -1 dropped).
+    """
+    ids = np.asarray(topk_ids)
+    T, K = ids.shape
+    n_items = T * K
+    if cap is None:
+        cap = align_cap(T, K, n_local, block)
+    flat = ids.reshape(-1)
+    loc = np.asarray(emap)[flat]
+    counts = np.zeros(n_local, dtype=np.int32)
+    offsets = np.zeros(n_local + 1, dtype=np.int32)
+    sorted_ids = np.full(cap, n_items, dtype=np.int32)
+    inv_pos = np.full(n_items, -1, dtype=np.int32)
+    for e in range(n_local):
+        items = np.nonzero(loc == e)[0]              # ascending item order
+        counts[e] = items.size
+        padded = -(-items.size // block) * block
+        offsets[e + 1] = offsets[e] + padded
+        sorted_ids[offsets[e]:offsets[e] + items.size] = items
+        inv_pos[items] = offsets[e] + np.arange(items.size, dtype=np.int32)
+    return counts, offsets, sorted_ids, inv_pos
+
+
+def grouped_mlp(x, sorted_ids, offsets, w13, w2, top_k: int, rows=None):
+    """y_perm[r] = f_e(x[sorted_ids[r] // K]) for each non-padding row r of
+    segment e (fp64). Returns {row: vector} for ``rows`` (default: all)."""
+    x = np.asarray(x)
+    n_items = x.shape[0] * top_k
+    E_l = w13.shape[0]
+    seg = np.searchsorted(np.asarray(offsets), np.arange(len(sorted_ids)),
+                          side="right") - 1
+    want = np.arange(len(sorted_ids)) if rows is None else np.asarray(rows)
+    out = {}
+    for e in range(E_l):
+        rs = [r for r in want if seg[r] == e and sorted_ids[r] < n_items]
+        if rs:
+            toks = np.asarray(sorted_ids)[rs] // top_k
+            y = expert_mlp(x[toks], w13[e], w2[e])
+            for j, r in enumerate(rs):
+                out[int(r)] = y[j]
+    return out
+
+
+def combine(y_perm_rows, inv_pos, topk_w, rsf=1.0, shared_out=None):
+    """out[t] = rsf * sum_k w[t,k] * y_perm[inv_pos[t,k]] + shared_out[t].
+
+    This is the weighted gather back to token order. It is the same sum as the
+    ``scatter_add_`` by token index in ep_fused_moe_patch.py ``_ep_forward``
+    step 4, written per token. ``y_perm_rows`` is an array [cap, H]; rows with
+    inv_pos = -1 are skipped.
+    """
+    w = np.asarray(topk_w, np.float64)
+    T, K = w.shape
+    y = np.asarray(y_perm_rows, np.float64)
+    out = np.zeros((T, y.shape[1]), dtype=np.float64)
+    inv = np.asarray(inv_pos).reshape(T, K)
+    for t in range(T):
+        for k in range(K):
+            r = inv[t, k]
+            if r >= 0:
+                out[t] += w[t, k] * y[r]
+    out *= np.float64(rsf)
+    if shared_out is not None:
+        out += np.asarray(shared_out, np.float64)
+    return out
+
+
+def weight_bytes_per_card(n_experts, intermediate, hidden, n_layers, elem_bytes):
+    """MoE weight bytes held by one card: experts * (2*I*H + H*I) * bytes * layers.
+
+    The sizing formula of the ep_fused_moe_patch.py docstring ("Memory layout
+    comparison").
+    """
+    per_expert = 2 * intermediate * hidden + hidden * intermediate
+    return n_experts * per_expert * elem_bytes * n_layers
