@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Throughput of the fused MoE layer forward (libmoe, sm_103a) on GB300.
+
+One step = one moe_forward of a whole layer (routing, align/permute, grouped
+SiLU-gated MLP of the local and shared experts, combine) over one batch of
+synthetic tokens. The default workload is the Mixtral-8x7B-shape prefill layer
+(T=4096, H=4096, I=14336, E=8, top_k=2). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+With N > 1 (torchrun, one rank per GPU) every rank runs its own batch through
+its own copy of the layer (replicas: weak scaling, no collective on the data
+path). Rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s and TFLOP/s (bf16) on 1 GB300, % of tensor/HBM roofline"
+DATA = ("synthetic: seeded counter-based normals (SplitMix64 + Box-Muller), "
+        "random-init weights std 1/sqrt(fan_in)")
+L2_FLUSH_BYTES = 256 << 20
+
+WORKLOADS = {w.name: w for w in (synth.TINY, synth.MIXTRAL, synth.DEEPSEEK, synth.EP_SHARD)}
+for _t in synth.DECODE_TOKENS:
+    WORKLOADS[f"qwen3_decode_T{_t}"] = synth.QWEN_DECODE.with_(name=f"qwen3_decode_T{_t}", T=_t)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+# --------------------------------------------------------------------------- inputs
+def _pinned_bits(seed, tid, row0, nrows, ncols, std):
+    t = torch.empty(nrows * ncols, dtype=torch.int16, pin_memory=True)
+    synth.draw_bf16_bits(seed, tid, row0, nrows, ncols, std, out_ptr=t.data_ptr())
+    return t
+
+
+def device_layer(wl, device, seed=0):
+    """Device tensors of a layer, drawn from synth (no tie-gap redraws: the
+    bench measures speed; parity is the tests' job)."""
+    bf = wl.act == "bf16"
+    e0 = wl.ep_rank * wl.E_local
+
+    def dev(seedrows, shape, f32=False):
+        tid, row0, nrows, ncols, std = seedrows
+        if bf and not f32:
+            t = _pinned_bits(seed, tid, row0, nrows, ncols, std)
+            return t.to(device).view(torch.bfloat16).view(*shape)
+        a = synth.draw(seed, tid, row0, nrows, ncols, std, False)
+        return torch.from_numpy(a).to(device).view(*shape)
+
+    d = {}
+    d["x"] = dev((synth.X, 0, wl.T, wl.H, wl.std(synth.X)), (wl.T, wl.H))
+    if wl.router == "bf16":
+        d["router_w"] = dev((synth.ROUTER_W, 0, wl.E, wl.H, wl.std(synth.ROUTER_W)), (wl.E, wl.H))
+    else:
+        d["router_w"] = dev((synth.ROUTER_W, 0, wl.E, wl.H, wl.std(synth.ROUTER_W)),
+                            (wl.E, wl.H), f32=True)
+    d["router_b"] = None
+    if wl.router_bias:
+        d["router_b"] = torch.from_numpy(synth.draw_tensor(wl, synth.ROUTER_B, seed)).to(device)
+    d["w13"] = dev((synth.W13, e0 * 2 * wl.I, wl.E_local * 2 * wl.I, wl.H, wl.std(synth.W13)),
+                   (wl.E_local, 2 * wl.I, wl.H))
+    d["w2"] = dev((synth.W2, e0 * wl.H, wl.E_local * wl.H, wl.I, wl.std(synth.W2)),
+                  (wl.E_local, wl.H, wl.I))
+    d["shared_w13"] = d["shared_w2"] = None
+    if wl.n_shared:
+        d["shared_w13"] = dev((synth.SHARED_W13, 0, wl.n_shared * 2 * wl.I_shared, wl.H,
+                               wl.std(synth.SHARED_W13)), (wl.n_shared, 2 * wl.I_shared, wl.H))
+        d["shared_w2"] = dev((synth.SHARED_W2, 0, wl.n_shared * wl.H, wl.I_shared,
+                              wl.std(synth.SHARED_W2)), (wl.n_shared, wl.H, wl.I_shared))
+    return d
+
+
+def cfg_of(wl):
+    from expert_moe_layer_gb300 import binding as B
+    return B.make_config(wl.E, wl.K, wl.H, wl.I, wl.renormalize, wl.n_group, wl.topk_group,
+                         wl.rsf, wl.n_shared, wl.I_shared, wl.ep_size, wl.ep_rank, wl.act,
+                         wl.router)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, interval_ms=50):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [c.strip() for c in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, wl, rank, world, device):
+    from expert_moe_layer_gb300 import binding as B
+    B.lib()
+    torch.cuda.set_device(device)
+    peaks = load_peaks()
+    d = device_layer(wl, device)
+    cfg = cfg_of(wl)
+    T, H = wl.T, wl.H
+    ws = torch.empty(B.workspace_size(cfg, T), dtype=torch.uint8, device=device)
+    out = torch.empty(T, H, dtype=d["x"].dtype, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def fwd(events=None):
+        if events is None:
+            B.moe_forward(cfg, T, d["x"], d["router_w"], d["router_b"], d["w13"], d["w2"],
+                          d["shared_w13"], d["shared_w2"], None, out, ws, stream)
+            return 0
+        return B.moe_forward_timed(cfg, T, d["x"], d["router_w"], d["router_b"], d["w13"],
+                                   d["w2"], d["shared_w13"], d["shared_w2"], None, out, ws,
+                                   events, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize(device)
+    rc, flags = B.moe_get_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} after warm-up")
+
+    # routing statistics of this batch (for the algorithmic work counts)
+    lay = B.workspace_layout(cfg, T)
+    El = wl.E_local
+    counts = ws[lay.counts:lay.counts + 4 * El].view(torch.int32).cpu().numpy()
+    A = int(counts.sum())
+    touched = int((counts > 0).sum())
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for evs in events:          # create the CUDA events (torch creates them lazily)
+        for ev in evs:
+            ev.record(stream)
+    torch.cuda.synchronize(device)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    launches = 0
+    for i in range(args.steps):
+        flush.zero_()
+        launches += fwd(events[i])
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    rc, flags = B.moe_get_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} flags {flags:#x} in the timed region")
+
+    def span(a, b):
+        return [events[i][a].elapsed_time(events[i][b]) for i in range(args.steps)]
+
+    step_ms = span(0, 7)
+    total_ms = sum(step_ms)
+    stage_names = ["route", "align", "tiles_gather", "gemm1_silu", "gemm2", "shared", "combine"]
+    stages = {n: statistics.mean(span(i, i + 1)) for i, n in enumerate(stage_names)}
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_s = world * T * args.steps / (total_ms / 1e3)
+
+    # algorithmic work per step
+    rb = 2 if wl.router == "bf16" else 4
+    eb = 2 if wl.act == "bf16" else 4
+    flops = wl.flops(A)
+    alg_bytes = (touched * 3 * wl.H * wl.I * eb + wl.E * wl.H * rb
+                 + wl.n_shared * 3 * wl.H * wl.I_shared * eb + 2 * T * wl.H * eb)
+
+    # dominant kernel: GEMM1 (gate/up, SiLU epilogue)
+    g1_ms = stages["gemm1_silu"]
+    g1_flops = 4 * A * wl.H * wl.I
+    g1_bytes = touched * 2 * wl.I * wl.H * eb + A * wl.H * eb + A * wl.I * eb
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = g1_flops / max(g1_bytes, 1) >= ridge
+    if tensor_bound:
+        ach = g1_flops / (g1_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_basis": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
+                "frac_of_burst": round(ach / peaks["bf16_tflops"], 4)}
+    else:
+        ach = g1_bytes / (g1_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_basis": f"{peaks['source']} HBM copy",
+                "frac_of_nominal_8TBs": round(ach / 8000.0, 4)}
+    roof.update({"kernel": "moe_gemm_tc<SiLU-up> (GEMM1)", "ms_per_launch": round(g1_ms, 4),
+                 "algorithmic_flops": g1_flops, "algorithmic_bytes": g1_bytes,
+                 "traffic": traffic_from_profile(wl.name)})
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world)
+
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.act == "bf16" else "f32",
+        "data": DATA,
+        "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
+                   "E_local": El, "shared_experts": wl.n_shared, "ep": [wl.ep_size, wl.ep_rank],
+                   "assignments": A, "experts_touched": touched,
+                   "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MiB write) before every step, "
+                         "outside the timed events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
+        "gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
+        "alg_flops_per_step": flops, "alg_bytes_per_step": alg_bytes,
+        "stages_ms": {k: round(v, 4) for k, v in stages.items()},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    return res
+
+
+def run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world):
+    from expert_moe_layer_gb300 import binding as B
+    T, H = wl.T, wl.H
+    x_host = torch.empty(T, H, dtype=d["x"].dtype, pin_memory=True)
+    x_host.copy_(d["x"].cpu())
+    out_host = torch.empty(T, H, dtype=out.dtype, pin_memory=True)
+    x_dev = torch.empty_like(d["x"])
+    n = max(3, min(args.steps, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(n + 2):
+        flush.zero_()
+        if i >= 2:
+            ev[i - 2][0].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        B.moe_forward(cfg, T, x_dev, d["router_w"], d["router_b"], d["w13"], d["w2"],
+                      d["shared_w13"], d["shared_w2"], None, out, ws, stream)
+        out_host.copy_(out, non_blocking=True)
+        if i >= 2:
+            ev[i - 2][1].record(stream)
+    torch.cuda.synchronize(device)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    nbytes = T * H * x_host.element_size()
+    return {"value": round(world * T / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
+            "ms_per_step": round(ms, 4), "steps": n}
+
+
+def traffic_from_profile(workload):
+    """DRAM bytes per GEMM1 launch from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    v = d.get(workload)
+    return None if v is None else v.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- oracle arms
+def oracle_sample(wl, n_tokens, seed=0):
+    """Host inputs for the oracle on the first n_tokens of the workload."""
+    bf = wl.act == "bf16"
+    e0 = wl.ep_rank * wl.E_local
+    x = synth.draw(seed, synth.X, 0, n_tokens, wl.H, wl.std(synth.X), bf)
+    rw = synth.draw_tensor(wl, synth.ROUTER_W, seed)
+    rb = synth.draw_tensor(wl, synth.ROUTER_B, seed) if wl.router_bias else None
+    if bf:
+        w13 = synth.BF16Experts(synth.draw_bf16_bits(
+            seed, synth.W13, e0 * 2 * wl.I, wl.E_local * 2 * wl.I, wl.H,
+            wl.std(synth.W13)).reshape(wl.E_local, 2 * wl.I, wl.H))
+        w2 = synth.BF16Experts(synth.draw_bf16_bits(
+            seed, synth.W2, e0 * wl.H, wl.E_local * wl.H, wl.I,
+            wl.std(synth.W2)).reshape(wl.E_local, wl.H, wl.I))
+    else:
+        w13 = synth.draw_tensor(wl, synth.W13, seed)
+        w2 = synth.draw_tensor(wl, synth.W2, seed)
+    s13 = synth.draw_tensor(wl, synth.SHARED_W13, seed) if wl.n_shared else None
+    s2 = synth.draw_tensor(wl, synth.SHARED_W2, seed) if wl.n_shared else None
+    return x, rw, rb, w13, w2, s13, s2
+
+
+def oracle_step(wl, inputs):
+    from oracle import moe_oracle as O
+    x, rw, rb, w13, w2, s13, s2 = inputs
+    return O.moe_forward(x, rw, w13, w2, top_k=wl.K, renormalize=wl.renormalize,
+                         n_group=wl.n_group, topk_group=wl.topk_group, rsf=wl.rsf, router_b=rb,
+                         shared_w13=s13, shared_w2=s2,
+                         emap=O.expert_map(wl.E, wl.ep_size, wl.ep_rank))
+
+
+def oracle_tokens(wl):
+    # bounded sample: roughly 5-20 s of host work per call on the prefill layers
+    return min(wl.T, {"mixtral_prefill": 64, "deepseek_v2_prefill": 32,
+                      "ep_shard": 128}.get(wl.name, wl.T))
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(wl):
+    n = oracle_tokens(wl)
+    inputs = oracle_sample(wl, n)
+    t0 = time.perf_counter()
+    oracle_step(wl, inputs)
+    dt = time.perf_counter() - t0
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": cores_used(),
+            "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of {wl.name}, one oracle forward "
+                      f"(numpy fp64 MLP, fp32 softmax), {dt:.1f} s"}
+
+
+def run_reference(args, wl):
+    n = oracle_tokens(wl)
+    inputs = oracle_sample(wl, n)
+    for _ in range(args.warmup):
+        oracle_step(wl, inputs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(wl, inputs)
+    dt = time.perf_counter() - t0
+    v = n * args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "K": wl.K, "tokens_per_step": n},
+            "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": cores_used(),
+                             "kind": "oracle",
+                             "sample": f"first {n} of {wl.T} tokens per step"},
+            "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    res = run_ours(args, wl, rank, world, device)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""ctypes binding of libmoe.so (the C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (used as plain device memory). The
+functions take the same names and arguments as the C entry points and raise
+``MoeError`` on a non-zero status. There is no fallback: if the library cannot
+be loaded, every call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import _build
+
+MOE_F32, MOE_BF16 = 0, 1
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_STATUS",
+                6: "MOE_ERR_TIMEOUT"}
+DEV_BAD_EXPERT_ID, DEV_CAP_OVERFLOW, DEV_TIMEOUT, DEV_BAD_SEGMENT = 0x1, 0x2, 0x4, 0x8
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({strerror(status)})")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("hidden_size", ctypes.c_int), ("intermediate_size", ctypes.c_int),
+                ("renormalize", ctypes.c_int), ("use_grouped_topk", ctypes.c_int),
+                ("num_expert_group", ctypes.c_int), ("topk_group", ctypes.c_int),
+                ("routed_scaling_factor", ctypes.c_float),
+                ("num_shared_experts", ctypes.c_int),
+                ("shared_intermediate_size", ctypes.c_int),
+                ("ep_size", ctypes.c_int), ("ep_rank", ctypes.c_int),
+                ("act_dtype", ctypes.c_int), ("router_dtype", ctypes.c_int)]
+
+
+class WorkspaceOffsets(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_size_t), ("topk_ids", ctypes.c_size_t),
+                ("topk_w", ctypes.c_size_t), ("counts", ctypes.c_size_t),
+                ("offsets", ctypes.c_size_t), ("sorted_ids", ctypes.c_size_t),
+                ("inv_pos", ctypes.c_size_t), ("total", ctypes.c_size_t),
+                ("cap", ctypes.c_int), ("block_m", ctypes.c_int)]
+
+
+def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
+                num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
+                num_shared_experts=0, shared_intermediate_size=0, ep_size=1, ep_rank=0,
+                act_dtype="bf16", router_dtype="bf16") -> MoeConfig:
+    dt = {"bf16": MOE_BF16, "f32": MOE_F32}
+    return MoeConfig(num_experts, top_k, hidden_size, intermediate_size, int(bool(renormalize)),
+                     int(num_expert_group > 0), num_expert_group, topk_group,
+                     float(routed_scaling_factor), num_shared_experts,
+                     shared_intermediate_size, ep_size, ep_rank, dt[act_dtype],
+                     dt[router_dtype])
+
+
+_lib = None
+_lock = threading.Lock()
+_VP, _SZ, _I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+_CFG = ctypes.POINTER(MoeConfig)
+
+_SIGS = {
+    "moe_strerror": (ctypes.c_char_p, [_I]),
+    "moe_validate_config": (_I, [_CFG]),
+    "moe_align_cap": (_SZ, [_CFG, _I, _I]),
+    "moe_route_workspace_size": (_SZ, [_CFG, _I]),
+    "moe_route": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_align_workspace_size": (_SZ, [_CFG, _I]),
+    "moe_align_permute": (_I, [_CFG, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
+    "moe_grouped_mlp_workspace_size": (_SZ, [_CFG, _I, _I]),
+    "moe_grouped_mlp": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_combine": (_I, [_CFG, _I, _VP, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_workspace_size": (_SZ, [_CFG, _I]),
+    "moe_workspace_layout": (_I, [_CFG, _I, ctypes.POINTER(WorkspaceOffsets)]),
+    "moe_forward": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "moe_forward_timed": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                               _SZ, _VP, ctypes.POINTER(ctypes.c_void_p),
+                               ctypes.POINTER(ctypes.c_int)]),
+    "moe_get_status": (_I, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32)]),
+}
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/moe.h."""
+    with open(os.path.join(_build.INCLUDE, "moe.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def lib(build: bool = True) -> ctypes.CDLL:
+    """Load libmoe.so (building it in place first if missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build:
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError("libmoe.so is not built; call __graft_entry__.build()")
+            L = ctypes.CDLL(_build.LIB)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(L, name)
+                f.restype, f.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().moe_strerror(status).decode()
+
+
+def _p(t):
+    """Device pointer of a tensor (None -> NULL); integers pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libmoe must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise MoeError(fn, rc)
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def validate_config(cfg: MoeConfig) -> int:
+    return lib().moe_validate_config(ctypes.byref(cfg))
+
+
+def align_cap(cfg, T, block_m) -> int:
+    return lib().moe_align_cap(ctypes.byref(cfg), T, block_m)
+
+
+def route_workspace_size(cfg, T) -> int:
+    return lib().moe_route_workspace_size(ctypes.byref(cfg), T)
+
+
+def align_workspace_size(cfg, T) -> int:
+    return lib().moe_align_workspace_size(ctypes.byref(cfg), T)
+
+
+def grouped_mlp_workspace_size(cfg, T, cap) -> int:
+    return lib().moe_grouped_mlp_workspace_size(ctypes.byref(cfg), T, cap)
+
+
+def workspace_size(cfg, T) -> int:
+    return lib().moe_workspace_size(ctypes.byref(cfg), T)
+
+
+def workspace_layout(cfg, T) -> WorkspaceOffsets:
+    out = WorkspaceOffsets()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(cfg), T,
+                                                             ctypes.byref(out)))
+    return out
+
+
+def moe_route(cfg, T, x, router_w, router_bias, topk_ids, topk_w, ws, stream=None):
+    _check("moe_route", lib().moe_route(ctypes.byref(cfg), T, _p(x), _p(router_w),
+                                        _p(router_bias), _p(topk_ids), _p(topk_w), _p(ws),
+                                        _nbytes(ws), _stream(stream)))
+
+
+def moe_align_permute(cfg, T, topk_ids, expert_map, block_m, counts, offsets, sorted_ids,
+                      inv_pos, cap, ws, stream=None):
+    _check("moe_align_permute", lib().moe_align_permute(
+        ctypes.byref(cfg), T, _p(topk_ids), _p(expert_map), block_m, _p(counts), _p(offsets),
+        _p(sorted_ids), _p(inv_pos), cap, _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_grouped_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm, ws,
+                    stream=None):
+    _check("moe_grouped_mlp", lib().moe_grouped_mlp(
+        ctypes.byref(cfg), T, _p(x), _p(sorted_ids), _p(counts), _p(offsets), cap, _p(w13),
+        _p(w2), _p(y_perm), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_combine(cfg, T, y_perm, cap, inv_pos, topk_w, shared_out, out, ws=None, stream=None):
+    _check("moe_combine", lib().moe_combine(
+        ctypes.byref(cfg), T, _p(y_perm), cap, _p(inv_pos), _p(topk_w), _p(shared_out),
+        _p(out), _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_forward(cfg, T, x, router_w, router_bias, w13, w2, shared_w13, shared_w2, expert_map,
+                out, ws, stream=None):
+    _check("moe_forward", lib().moe_forward(
+        ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias), _p(w13), _p(w2),
+        _p(shared_w13), _p(shared_w2), _p(expert_map), _p(out), _p(ws), _nbytes(ws),
+        _stream(stream)))
+
+
+def moe_forward_timed(cfg, T, x, router_w, router_bias, w13, w2, shared_w13, shared_w2,
+                      expert_map, out, ws, events, stream=None) -> int:
+    """moe_forward that records 8 torch.cuda.Event objects (or None) at the
+    stage boundaries on the stream; returns the number of kernels launched."""
+    handles = (ctypes.c_void_p * 8)()
+    for i, ev in enumerate(events):
+        handles[i] = None if ev is None else ev.cuda_event
+    n = ctypes.c_int(0)
+    _check("moe_forward_timed", lib().moe_forward_timed(
+        ctypes.byref(cfg), T, _p(x), _p(router_w), _p(router_bias), _p(w13), _p(w2),
+        _p(shared_w13), _p(shared_w2), _p(expert_map), _p(out), _p(ws), _nbytes(ws),
+        _stream(stream), handles, ctypes.byref(n)))
+    return n.value
+
+
+def moe_get_status(ws, stream=None) -> tuple[int, int]:
+    """(status code, raw MOE_DEV_* flags); synchronises the stream."""
+    flags = ctypes.c_uint32(0)
+    rc = lib().moe_get_status(_p(ws), _stream(stream), ctypes.byref(flags))
+    return rc, flags.value

@@ -1,0 +1,86 @@
+// Host-side launch helpers shared between the translation units of libmoe.
+// All launches are asynchronous on `st` and return cudaGetLastError().
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+// One GEMM work tile: `count` token rows of one expert's segment.
+//   x = expert (weight slab index), y = first B row, z = first output row,
+//   w = rows (1..nmax).
+using Tile = int4;
+
+struct GemmArgs {
+  const CUtensorMap* mapA;     // weights, 2-D [slabs*rows_per_slab, K]
+  const CUtensorMap* mapB;     // token rows, 2-D [rows, K]
+  const Tile* tiles;           // tile table
+  const int* num_tiles_dev;    // tile count on the device, or nullptr
+  int num_tiles_host;          // used when num_tiles_dev == nullptr
+  int m_tiles;                 // 128-row weight tiles per expert
+  int k_blocks;                // K / (128 bytes of K)
+  int a_rows_per_expert;       // weight rows per expert slab
+  int a_up_offset;             // row offset of the "up" half (SiLU mode)
+  int b_from_out;              // 1: B row = tile.z instead of tile.y
+  void* out;                   // output rows
+  long out_ld;                 // output row stride (elements)
+  int m_valid;                 // weight rows with an output (router: E)
+  unsigned* status;
+};
+
+enum GemmMode { kGemmSiluUp = 0, kGemmPlain = 1, kGemmLogits = 2 };
+
+// tcgen05 grouped GEMM, D[w_row, token] = sum_k W[w_row, k] * B[token, k].
+//   kGemmSiluUp: W = w13 rows, out = silu(gate) * up (act dtype)
+//   kGemmPlain : W = w2 rows,  out = D (act dtype)
+//   kGemmLogits: W = router rows (bf16), out = D (fp32)
+cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a,
+                        int num_sms, cudaStream_t st);
+
+// Shared-memory bytes a GEMM variant needs (for validation/tests).
+size_t gemm_smem_bytes(GemmMode mode, int nmax);
+
+// Router logits on CUDA cores: logits[t,e] = x[t].Wg[e] (fp32 accumulation).
+cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
+                                 const void* wg, float* logits, int T, int E, int H,
+                                 cudaStream_t st);
+
+// Softmax + (grouped) top-k + renormalise on fp32 logits (+ bias if given).
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int K,
+                        int renorm, int n_group, int topk_group, int32_t* ids,
+                        float* w, unsigned* status, cudaStream_t st);
+
+// Alignment / permutation. hist has n_warps*E_l ints, n_warps = align_warps(T*K).
+int align_warps(long n_items);
+cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, int E,
+                         int E_l, int ep_start, int block_m, int* hist, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
+                         unsigned* status, cudaStream_t st);
+
+// Tile tables.
+cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l,
+                               int nmax, Tile* tiles, int* num_tiles, int max_tiles,
+                               unsigned* status, cudaStream_t st);
+cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, cudaStream_t st);
+inline int dense_tile_count(int T, int S, int nmax) { return S * ((T + nmax - 1) / nmax); }
+inline long routed_tile_bound(long n_items, int E_l, int nmax) {
+  return n_items / nmax + E_l + 1;
+}
+
+// x_perm[r] = x[sorted_ids[r] / K] for rows holding an item.
+cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
+                          const int32_t* offsets_end, int cap, long n_items, int K, int H,
+                          void* x_perm, cudaStream_t st);
+
+// out[t] = rsf * sum_k w[t,k] y_perm[inv_pos[t,k]] + sum_s shared[s][t].
+cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
+                           const float* topk_w, int K, const void* shared, int n_shared,
+                           long shared_stride, float rsf, void* out, int T, int H,
+                           unsigned* status, cudaStream_t st);
+
+}  // namespace moe

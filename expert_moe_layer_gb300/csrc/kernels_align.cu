@@ -1,0 +1,387 @@
+// Token alignment / permutation by local expert, GEMM tile tables, row gather
+// and the weighted combine.
+//
+// Work item i = t*K + k (token t, slot k) is the flattening of
+// ep_fused_moe_patch.py _ep_forward step 2. Segments are a stable counting
+// sort of the items by local expert id. A warp owns kItemsPerWarp
+// consecutive items. Pass 1 counts them per expert (match_any groups the
+// lanes with equal keys). Pass 2 turns the counts into padded offsets and
+// into a base row per (warp, expert). Pass 3 replays the same walk in the
+// same order and writes each item to base + rank, so the order inside a
+// segment is ascending item order with no atomics on global memory.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kItemsPerWarp = 256;
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ emap, int E,
+                                            int E_l, int ep_start, unsigned* status) {
+  if (id < 0 || id >= E) {
+    if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    return -1;
+  }
+  int le;
+  if (emap) {
+    le = emap[id];
+    if (le < -1 || le >= E_l) {
+      if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+      return -1;
+    }
+  } else {
+    le = id - ep_start;
+    if (le < 0 || le >= E_l) le = -1;
+  }
+  return le;
+}
+
+// Pass 1: per-warp expert counts; also fills sorted_ids with the sentinel.
+__global__ void __launch_bounds__(256) align_count_kernel(
+    const int32_t* __restrict__ ids, long n_items, const int32_t* __restrict__ emap, int E,
+    int E_l, int ep_start, int* __restrict__ hist, int n_warps, int32_t* __restrict__ sorted_ids,
+    int cap, unsigned* status) {
+  extern __shared__ int cnt[];  // [kWarpsPerBlock][E_l]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (long r = blockIdx.x * 256L + threadIdx.x; r < cap; r += 256L * gridDim.x)
+    sorted_ids[r] = static_cast<int32_t>(n_items);
+  for (int i = threadIdx.x; i < kWarpsPerBlock * E_l; i += 256) cnt[i] = 0;
+  __syncthreads();
+  const int gw = blockIdx.x * kWarpsPerBlock + warp;
+  if (gw >= n_warps) return;
+  int* my = cnt + warp * E_l;
+  const long base = static_cast<long>(gw) * kItemsPerWarp;
+  for (int r = 0; r < kItemsPerWarp; r += 32) {
+    const long item = base + r + lane;
+    int le = -1;
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+  for (int e = lane; e < E_l; e += 32) hist[static_cast<long>(gw) * E_l + e] = my[e];
+}
+
+// Pass 2 (one CTA): counts, padded exclusive offsets, and per-warp base rows
+// written back into hist.
+__global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist, int n_warps,
+                                                          int E_l, int block_m,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int cap, unsigned* status) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E_l)
+    for (int w = 0; w < n_warps; ++w) c += hist[static_cast<long>(w) * E_l + e];
+  const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
+  // block-wide inclusive scan of padded
+  int v = padded;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
+  if (e < E_l) {
+    const int start = incl - padded;
+    counts[e] = c;
+    offsets[e] = start;
+    if (e == E_l - 1) {
+      offsets[E_l] = incl;
+      if (incl > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+    }
+    int run = start;
+    for (int w = 0; w < n_warps; ++w) {
+      const long idx = static_cast<long>(w) * E_l + e;
+      const int h = hist[idx];
+      hist[idx] = run;
+      run += h;
+    }
+  }
+}
+
+// Pass 3: stable scatter of item ids into their segments.
+__global__ void __launch_bounds__(256) align_scatter_kernel(
+    const int32_t* __restrict__ ids, long n_items, const int32_t* __restrict__ emap, int E,
+    int E_l, int ep_start, const int* __restrict__ hist, int n_warps,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
+    unsigned* status) {
+  extern __shared__ int run[];  // [kWarpsPerBlock][E_l]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kWarpsPerBlock + warp;
+  if (gw >= n_warps) return;
+  int* my = run + warp * E_l;
+  for (int e = lane; e < E_l; e += 32) my[e] = hist[static_cast<long>(gw) * E_l + e];
+  __syncwarp();
+  const long base = static_cast<long>(gw) * kItemsPerWarp;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < kItemsPerWarp; r += 32) {
+    const long item = base + r + lane;
+    int le = -1;
+    // status already recorded by pass 1 for bad ids
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (item < n_items) {
+      int pos = -1;
+      if (le >= 0) {
+        pos = my[le] + __popc(peers & lt);
+        if (pos < cap) {
+          sorted_ids[pos] = static_cast<int32_t>(item);
+        } else {
+          if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+          pos = -1;
+        }
+      }
+      inv_pos[item] = pos;
+    }
+    __syncwarp();
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Tile table of the routed experts: each segment's rows in chunks of nmax.
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ counts,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int E_l, int nmax, Tile* __restrict__ tiles,
+                                                           int* __restrict__ num_tiles,
+                                                           int max_tiles, unsigned* status) {
+  __shared__ int warp_sums[32];
+  const int e = threadIdx.x;
+  int n = 0, c = 0, off = 0;
+  if (e < E_l) {
+    c = counts[e];
+    off = offsets[e];
+    if (c < 0 || (e + 1 <= E_l && off + c > offsets[e + 1])) {
+      if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
+      c = 0;
+    }
+    n = (c + nmax - 1) / nmax;
+  }
+  int v = n;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += x;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += x;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
+  const int start = incl - n;
+  for (int j = 0; j < n; ++j) {
+    const int idx = start + j;
+    if (idx < max_tiles) {
+      const int r0 = off + j * nmax;
+      const int rows = c - j * nmax < nmax ? c - j * nmax : nmax;
+      tiles[idx] = make_int4(e, r0, r0, rows);
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) {
+    const int total = incl;
+    if (total > max_tiles && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+    *num_tiles = total < max_tiles ? total : max_tiles;
+  }
+}
+
+// Tile table over all T tokens for each of S weight slabs (shared experts,
+// router): slab s, tokens [t0, t0+rows): B row t0, output row s*T + t0.
+__global__ void dense_tiles_kernel(int T, int S, int nmax, Tile* __restrict__ tiles) {
+  const int per = (T + nmax - 1) / nmax;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= S * per) return;
+  const int s = i / per, j = i - s * per;
+  const int t0 = j * nmax;
+  const int rows = T - t0 < nmax ? T - t0 : nmax;
+  tiles[i] = make_int4(s, t0, s * T + t0, rows);
+}
+
+// x_perm[r] = x[sorted_ids[r] / K], one warp per row, 16-byte vectors.
+template <typename TE>
+__global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
+                                                     const int32_t* __restrict__ sorted_ids,
+                                                     const int32_t* __restrict__ offsets_end,
+                                                     int cap, long n_items, int K, int H,
+                                                     TE* __restrict__ x_perm) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int rows = *offsets_end;
+  if (rows > cap) rows = cap;
+  constexpr int kVec = 16 / sizeof(TE);
+  for (long r = blockIdx.x * 8L + warp; r < rows; r += 8L * gridDim.x) {
+    const int id = sorted_ids[r];
+    if (id < 0 || id >= n_items) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (id / K) * static_cast<long>(H));
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
+    for (int c = lane; c < H / kVec; c += 32) dst[c] = src[c];
+  }
+}
+
+// out[t] = rsf * sum_k w[t,k] * y_perm[inv_pos[t,k]] + sum_s shared[s][t]
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 r;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = r;
+}
+__device__ __forceinline__ void st8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+template <typename TE>
+__global__ void __launch_bounds__(256) combine_kernel(
+    const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
+    const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
+    long shared_stride, float rsf, TE* __restrict__ out, int T, int H, unsigned* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (long t = blockIdx.x * 8L + warp; t < T; t += 8L * gridDim.x) {
+    for (int c = lane * 8; c < H; c += 256) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int k = 0; k < K; ++k) {
+        const int p = inv_pos[t * K + k];
+        if (p < 0) continue;
+        if (p >= cap) {
+          if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
+          continue;
+        }
+        const float w = topk_w[t * K + k];
+        float y[8];
+        ld8(y_perm + static_cast<long>(p) * H + c, y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= rsf;
+      for (int s = 0; s < n_shared; ++s) {
+        float y[8];
+        ld8(shared + s * shared_stride + t * H + c, y);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += y[i];
+      }
+      st8(out + t * H + c, acc);
+    }
+  }
+}
+
+int grid_for(long work, int per_block, int cap_blocks) {
+  long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap_blocks) g = cap_blocks;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+int align_warps(long n_items) {
+  long w = (n_items + kItemsPerWarp - 1) / kItemsPerWarp;
+  return static_cast<int>(w < 1 ? 1 : w);
+}
+
+cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, int E, int E_l,
+                         int ep_start, int block_m, int* hist, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
+                         unsigned* status, cudaStream_t st) {
+  const int n_warps = align_warps(n_items);
+  const int blocks = (n_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const size_t smem = sizeof(int) * kWarpsPerBlock * E_l;
+  align_count_kernel<<<blocks, 256, smem, st>>>(ids, n_items, emap, E, E_l, ep_start, hist,
+                                                n_warps, sorted_ids, cap, status);
+  align_scan_kernel<<<1, 1024, 0, st>>>(hist, n_warps, E_l, block_m, counts, offsets, cap,
+                                        status);
+  align_scatter_kernel<<<blocks, 256, smem, st>>>(ids, n_items, emap, E, E_l, ep_start, hist,
+                                                  n_warps, sorted_ids, inv_pos, cap, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l, int nmax,
+                               Tile* tiles, int* num_tiles, int max_tiles, unsigned* status,
+                               cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(counts, offsets, E_l, nmax, tiles, num_tiles,
+                                         max_tiles, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, cudaStream_t st) {
+  const int n = dense_tile_count(T, S, nmax);
+  if (n <= 0) return cudaSuccess;
+  dense_tiles_kernel<<<(n + 255) / 256, 256, 0, st>>>(T, S, nmax, tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
+                          const int32_t* offsets_end, int cap, long n_items, int K, int H,
+                          void* x_perm, cudaStream_t st) {
+  const int grid = grid_for(cap, 8, 8 * 152);
+  if (bf16)
+    gather_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), sorted_ids,
+                                        offsets_end, cap, n_items, K, H,
+                                        static_cast<__nv_bfloat16*>(x_perm));
+  else
+    gather_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x), sorted_ids, offsets_end,
+                                        cap, n_items, K, H, static_cast<float*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
+                           const float* topk_w, int K, const void* shared, int n_shared,
+                           long shared_stride, float rsf, void* out, int T, int H,
+                           unsigned* status, cudaStream_t st) {
+  const int grid = grid_for(T, 8, 8 * 152);
+  if (bf16)
+    combine_kernel<<<grid, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), cap, inv_pos, topk_w, K,
+        static_cast<const __nv_bfloat16*>(shared), n_shared, shared_stride, rsf,
+        static_cast<__nv_bfloat16*>(out), T, H, status);
+  else
+    combine_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), cap, inv_pos,
+                                         topk_w, K, static_cast<const float*>(shared), n_shared,
+                                         shared_stride, rsf, static_cast<float*>(out), T, H,
+                                         status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

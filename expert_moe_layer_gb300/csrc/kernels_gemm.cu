@@ -1,0 +1,304 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Orientation: the weight rows are the MMA's M side (128 rows per tile) and
+// the token rows of one expert segment are the N side (16..nmax per tile).
+// The accumulator holds D[w_row, token] = sum_k W[w_row, k] * X[token, k].
+// The same kernel serves prefill (segments of hundreds of rows, nmax = 128)
+// and decode (a few rows per expert, nmax = 32). Only the N of the
+// instruction changes.
+//
+// Per CTA (persistent, one per SM, 192 threads):
+//   warp 0      TMA producer: weights (A) and token rows (B) into a ring of
+//               shared-memory stages with the 128-byte swizzle
+//   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of
+//               K = 128 bytes per stage; in SiLU mode a second accumulator for
+//               the "up" rows shares the same B stage
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns one
+//               32-lane quarter), SiLU(gate)*up or plain, store to global
+// Accumulators are double-buffered in TMEM, so the epilogue of one work unit
+// overlaps the main loop of the next.
+//
+// Work unit u -> (m = u / num_tiles, tile = u % num_tiles): all token tiles
+// of one weight tile are adjacent in u, so concurrently running CTAs share
+// each weight tile through L2.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
+
+template <int MODE, int NMAX>
+struct GemmShape {
+  static constexpr int kNA = (MODE == kGemmSiluUp) ? 2 : 1;  // weight boxes per stage
+  static constexpr int kBBytes = NMAX * 128;
+  static constexpr int kStageBytes = kNA * kABytes + kBBytes;
+  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kAccCols = kNA * NMAX;           // fp32 columns per buffer
+  static constexpr int kNAcc = 2;                        // TMEM accumulator buffers
+  static constexpr int kTmemNeed = kAccCols * kNAcc;
+  static constexpr int kTmemCols = kTmemNeed <= 32    ? 32
+                                   : kTmemNeed <= 64  ? 64
+                                   : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256
+                                                      : 512;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static_assert(kTmemNeed <= 512, "TMEM overflow");
+  static_assert(kStages >= 2, "need at least two stages");
+  static_assert(NMAX % 16 == 0 && NMAX <= 256, "bad NMAX");
+};
+
+template <typename T>
+__device__ __forceinline__ T to_out(float v);
+template <>
+__device__ __forceinline__ float to_out<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int MODE, bool TF32, typename TOut, int NMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_tc(const __grid_constant__ CUtensorMap mapA,
+                const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
+                const int* __restrict__ num_tiles_dev, int num_tiles_host, int m_tiles,
+                int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
+                TOut* __restrict__ out, long out_ld, int m_valid, unsigned* status) {
+  using S = GemmShape<MODE, NMAX>;
+  constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
+  constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
+
+  const int num_tiles = num_tiles_dev ? *num_tiles_dev : num_tiles_host;
+  const int total = num_tiles * m_tiles;
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * S::kStages;
+  const uint32_t tfull0 = empty0 + 8 * S::kStages;
+  const uint32_t tempty0 = tfull0 + 8 * S::kNAcc;
+  const uint32_t drain = tempty0 + 8 * S::kNAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 2 * S::kNAcc + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < S::kNAcc; ++b) {
+      ptx::mbar_init(tfull0 + 8 * b, 1);
+      ptx::mbar_init(tempty0 + 8 * b, 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async();
+    ptx::tma_prefetch_map(&mapA);
+    ptx::tma_prefetch_map(&mapB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), S::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const int m = u / num_tiles;
+        const Tile tl = tiles[u - m * num_tiles];
+        const int a_row = tl.x * a_rows_per_expert + m * 128;
+        const int b_row = b_from_out ? tl.z : tl.y;
+        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+          const int s = it % S::kStages;
+          const uint32_t ph = (it / S::kStages) & 1;
+          if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + s * S::kStageBytes;
+          ptx::mbar_arrive_expect_tx(full0 + 8 * s, S::kStageBytes);
+          ptx::tma_load_2d(st, &mapA, full0 + 8 * s, kb * kKe, a_row);
+          if (MODE == kGemmSiluUp)
+            ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, kb * kKe,
+                             a_row + a_up_offset);
+          ptx::tma_load_2d(st + S::kNA * kABytes, &mapB, full0 + 8 * s, kb * kKe, b_row);
+        }
+      }
+      if (!ok) {
+        // unwinding: let every load this thread issued land before exit
+        const int n = it < S::kStages ? it : S::kStages;
+        for (int i = 0; i < n; ++i) {
+          const int j = it - 1 - i;
+          ptx::mbar_wait_drain(full0 + 8 * (j % S::kStages), (j / S::kStages) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int it = 0, ai = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
+        const int m = u / num_tiles;
+        const Tile tl = tiles[u - m * num_tiles];
+        const int n_mma = (tl.w + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_make(kAB, 128, n_mma);
+        const int b = ai % S::kNAcc;
+        const uint32_t aph = (ai / S::kNAcc) & 1;
+        if (!ptx::mbar_wait(tempty0 + 8 * b, aph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + b * S::kAccCols;
+        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+          const int s = it % S::kStages;
+          const uint32_t ph = (it / S::kStages) & 1;
+          if (!ptx::mbar_wait(full0 + 8 * s, ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = sbase + s * S::kStageBytes;
+          const uint64_t da = ptx::sdesc_sw128(st);
+          const uint64_t db = ptx::sdesc_sw128(st + S::kNA * kABytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            ptx::tc_mma<TF32>(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+            if (MODE == kGemmSiluUp) {
+              const uint64_t du = ptx::sdesc_sw128(st + kABytes);
+              ptx::tc_mma<TF32>(d + NMAX, du + 2 * kk, db + 2 * kk, idesc, acc);
+            }
+          }
+          ptx::tc_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        ptx::tc_commit(tfull0 + 8 * b);
+      }
+      if (!ok) {
+        // unwinding: wait for the MMAs already issued
+        ptx::tc_commit(drain);
+        ptx::mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int ai = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
+      const int m = u / num_tiles;
+      const Tile tl = tiles[u - m * num_tiles];
+      const int b = ai % S::kNAcc;
+      const uint32_t aph = (ai / S::kNAcc) & 1;
+      if (!ptx::mbar_wait(tfull0 + 8 * b, aph, abort_flag, status)) break;
+      ptx::tc_fence_after();
+      const int row = m * 128 + q * 32 + lane;
+      const bool row_ok = row < m_valid;
+      const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+      TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
+      for (int c0 = 0; c0 < tl.w; c0 += 16) {
+        float v[16];
+        if constexpr (MODE == kGemmSiluUp) {
+          float w[16];
+          ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = silu_f(v[j]) * w[j];
+        } else {
+          ptx::tmem_ld16(tb + c0, v);
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * out_ld] = to_out<TOut>(v[j]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty0 + 8 * b);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+template <int MODE, bool TF32, typename TOut, int NMAX>
+cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
+  using S = GemmShape<MODE, NMAX>;
+  auto kern = moe_gemm_tc<MODE, TF32, TOut, NMAX>;
+  static bool configured = false;  // per process; attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         S::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  kern<<<num_sms, kThreads, S::kSmemBytes, st>>>(
+      *a.mapA, *a.mapB, a.tiles, a.num_tiles_dev, a.num_tiles_host, a.m_tiles, a.k_blocks,
+      a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out), a.out_ld,
+      a.m_valid, a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(GemmMode mode, int nmax) {
+  if (mode == kGemmSiluUp) return nmax == 128 ? GemmShape<0, 128>::kSmemBytes
+                                              : GemmShape<0, 32>::kSmemBytes;
+  return nmax == 128 ? GemmShape<1, 128>::kSmemBytes : GemmShape<1, 32>::kSmemBytes;
+}
+
+cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
+                        cudaStream_t st) {
+  if (nmax != 32 && nmax != 128) return cudaErrorInvalidValue;
+  const bool big = nmax == 128;
+  switch (mode) {
+    case kGemmSiluUp:
+      if (tf32)
+        return big ? launch_variant<kGemmSiluUp, true, float, 128>(a, num_sms, st)
+                   : launch_variant<kGemmSiluUp, true, float, 32>(a, num_sms, st);
+      return big ? launch_variant<kGemmSiluUp, false, __nv_bfloat16, 128>(a, num_sms, st)
+                 : launch_variant<kGemmSiluUp, false, __nv_bfloat16, 32>(a, num_sms, st);
+    case kGemmPlain:
+      if (tf32)
+        return big ? launch_variant<kGemmPlain, true, float, 128>(a, num_sms, st)
+                   : launch_variant<kGemmPlain, true, float, 32>(a, num_sms, st);
+      return big ? launch_variant<kGemmPlain, false, __nv_bfloat16, 128>(a, num_sms, st)
+                 : launch_variant<kGemmPlain, false, __nv_bfloat16, 32>(a, num_sms, st);
+    case kGemmLogits:
+      if (tf32) return cudaErrorInvalidValue;
+      return big ? launch_variant<kGemmPlain, false, float, 128>(a, num_sms, st)
+                 : launch_variant<kGemmPlain, false, float, 32>(a, num_sms, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,546 @@
+// C ABI of the fused MoE layer forward: host validation, workspace layout,
+// TMA tensor maps and the stream-ordered launch sequence. See include/moe.h
+// for the contract of each entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "moe.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxT = 1 << 18;
+constexpr int kForwardBlock = 16;   // segment padding used by moe_forward
+constexpr size_t kAlignBytes = 256;
+
+size_t rup(size_t v) { return (v + kAlignBytes - 1) / kAlignBytes * kAlignBytes; }
+int ebytes(moe_dtype d) { return d == MOE_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->router_dtype != MOE_F32 && c->router_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  const int E = c->num_experts, K = c->top_k, H = c->hidden_size, I = c->intermediate_size;
+  if (E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
+  if (H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->ep_size < 1 || E % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if (c->ep_rank < 0 || c->ep_rank >= c->ep_size) return MOE_ERR_INVALID_ARG;
+  if (c->use_grouped_topk) {
+    const int g = c->num_expert_group, tg = c->topk_group;
+    if (g < 1 || E % g != 0 || tg < 1 || tg > g) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long>(K) > static_cast<long>(tg) * (E / g)) return MOE_ERR_INVALID_ARG;
+  }
+  if (c->num_shared_experts < 0) return MOE_ERR_INVALID_ARG;
+  if (c->num_shared_experts > 0) {
+    const int Is = c->shared_intermediate_size;
+    if (Is < 128 || Is % 128 != 0) return MOE_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(c->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  // kernel coverage
+  if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->use_grouped_topk && c->num_expert_group > 32) return MOE_ERR_UNSUPPORTED;
+  if (E / c->ep_size > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype == MOE_F32 && c->router_dtype == MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int validate_T(int T) { return (T < 0 || T > kMaxT) ? MOE_ERR_INVALID_ARG : MOE_OK; }
+
+int n_local(const moe_config* c) { return c->num_experts / c->ep_size; }
+
+// Token tile (MMA N) of the routed GEMMs: 128 when segments average at least
+// 48 rows, else 32.
+int routed_nmax(const moe_config* c, int T) {
+  const long avg = static_cast<long>(T) * c->top_k / c->num_experts;
+  return avg >= 48 ? 128 : 32;
+}
+int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
+
+// The router runs as a tcgen05 GEMM when its operands are bf16 and there are
+// enough tokens to fill the machine; otherwise on CUDA cores.
+bool router_on_tensor_cores(const moe_config* c, int T) {
+  return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16 && T >= 256;
+}
+
+long max_routed_tiles(const moe_config* c, int T) {
+  return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
+}
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// -------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major [rows, cols] map; box = 128 bytes of a row x box_rows rows,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long cols,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int eb = ebytes(dt);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / eb), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType t =
+      dt == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  return fn(m, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One grouped GEMM launch. A = weights [slabs*rows_per_slab, Kdim]; B = token
+// rows [b_rows, Kdim].
+int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, const void* B,
+             long b_rows, int Kdim, const Tile* tiles, const int* nt_dev, int nt_host,
+             int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
+             int m_valid, unsigned* status, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, dt, a_rows, Kdim, 128)) return MOE_ERR_CUDA;
+  if (!make_map(&mb, B, dt, b_rows, Kdim, nmax)) return MOE_ERR_CUDA;
+  GemmArgs g;
+  g.mapA = &ma;
+  g.mapB = &mb;
+  g.tiles = tiles;
+  g.num_tiles_dev = nt_dev;
+  g.num_tiles_host = nt_host;
+  g.m_tiles = m_tiles;
+  g.k_blocks = Kdim * ebytes(dt) / 128;
+  g.a_rows_per_expert = rows_per_slab;
+  g.a_up_offset = up_off;
+  g.b_from_out = b_from_out;
+  g.out = out;
+  g.out_ld = out_ld;
+  g.m_valid = m_valid;
+  g.status = status;
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  return launch_gemm(mode, dt == MOE_F32, nmax, g, sms, st) == cudaSuccess ? MOE_OK
+                                                                           : MOE_ERR_CUDA;
+}
+
+// -------------------------------------------------------------- layouts
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = rup(off + bytes);
+    return o;
+  }
+};
+
+struct RouteLayout {
+  size_t status, logits, rtiles, total;
+};
+RouteLayout route_layout(const moe_config* c, int T) {
+  Carver cv;
+  RouteLayout L;
+  L.status = cv.take(4);
+  L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
+  L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
+  L.total = cv.off;
+  return L;
+}
+
+struct AlignLayout {
+  size_t status, hist, total;
+};
+AlignLayout align_layout(const moe_config* c, int T) {
+  Carver cv;
+  AlignLayout L;
+  L.status = cv.take(4);
+  L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(static_cast<long>(T) * c->top_k)) *
+                   n_local(c));
+  L.total = cv.off;
+  return L;
+}
+
+struct MlpLayout {
+  size_t status, tiles, ntiles, x_perm, h_perm, total;
+};
+MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
+  Carver cv;
+  MlpLayout L;
+  const size_t eb = ebytes(c->act_dtype);
+  L.status = cv.take(4);
+  L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
+  L.ntiles = cv.take(sizeof(int));
+  L.x_perm = cv.take(eb * static_cast<size_t>(cap) * c->hidden_size);
+  L.h_perm = cv.take(eb * static_cast<size_t>(cap) * c->intermediate_size);
+  L.total = cv.off;
+  return L;
+}
+
+struct FwdLayout {
+  size_t status, topk_ids, topk_w, logits, rtiles, hist, counts, offsets, sorted_ids, inv_pos;
+  size_t tiles, ntiles, stiles, x_perm, h_perm, y_perm, h_sh, y_sh, total;
+  int cap;
+};
+FwdLayout fwd_layout(const moe_config* c, int T) {
+  Carver cv;
+  FwdLayout L;
+  const size_t eb = ebytes(c->act_dtype);
+  const size_t TK = static_cast<size_t>(T) * c->top_k;
+  const int El = n_local(c);
+  const int S = c->num_shared_experts;
+  L.cap = static_cast<int>(TK + static_cast<size_t>(El) * (kForwardBlock - 1));
+  L.status = cv.take(4);
+  L.topk_ids = cv.take(4 * TK);
+  L.topk_w = cv.take(4 * TK);
+  L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
+  L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
+  L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(TK)) * El);
+  L.counts = cv.take(4 * static_cast<size_t>(El));
+  L.offsets = cv.take(4 * static_cast<size_t>(El + 1));
+  L.sorted_ids = cv.take(4 * static_cast<size_t>(L.cap));
+  L.inv_pos = cv.take(4 * TK);
+  L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
+  L.ntiles = cv.take(sizeof(int));
+  L.stiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, S, dense_nmax(T))));
+  L.x_perm = cv.take(eb * L.cap * c->hidden_size);
+  L.h_perm = cv.take(eb * L.cap * c->intermediate_size);
+  L.y_perm = cv.take(eb * L.cap * c->hidden_size);
+  L.h_sh = cv.take(eb * static_cast<size_t>(S) * T * (S ? c->shared_intermediate_size : 0));
+  L.y_sh = cv.take(eb * static_cast<size_t>(S) * T * c->hidden_size);
+  L.total = cv.off;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+int cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(x)              \
+  do {                          \
+    const int _rc = (x);        \
+    if (_rc != MOE_OK) return _rc; \
+  } while (0)
+
+// ------------------------------------------------------------- stage bodies
+int do_route(const moe_config* c, int T, const void* x, const void* router_w,
+             const float* bias, int32_t* ids, float* w, float* logits, Tile* rtiles,
+             unsigned* status, cudaStream_t st) {
+  const int E = c->num_experts, H = c->hidden_size;
+  if (router_on_tensor_cores(c, T)) {
+    MOE_TRY(cuda_ok(launch_dense_tiles(T, 1, 128, rtiles, st)));
+    MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, 128, router_w, E, x, T, H, rtiles, nullptr,
+                     dense_tile_count(T, 1, 128), (E + 127) / 128, 0, 0, 0, logits, E, E,
+                     status, st));
+  } else {
+    MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
+                                         x, router_w, logits, T, E, H, st)));
+  }
+  return cuda_ok(launch_topk(logits, bias, T, E, c->top_k, c->renormalize ? 1 : 0,
+                             c->use_grouped_topk ? c->num_expert_group : 0,
+                             c->use_grouped_topk ? c->topk_group : 0, ids, w, status, st));
+}
+
+int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
+           const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
+           const void* w2, void* y_perm, Tile* tiles, int* ntiles, void* x_perm, void* h_perm,
+           unsigned* status, cudaStream_t st, void* const* ev = nullptr) {
+  const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
+  const int nmax = routed_nmax(c, T);
+  const long n_items = static_cast<long>(T) * K;
+  MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, ntiles,
+                                     static_cast<int>(max_routed_tiles(c, T)), status, st)));
+  MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
+                                n_items, K, H, x_perm, st)));
+  if (ev && ev[0]) MOE_TRY(cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st)));
+  MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
+                   cap, H, tiles, ntiles, 0, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
+  if (ev && ev[1]) MOE_TRY(cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), st)));
+  MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
+                   tiles, ntiles, 0, H / 128, H, 0, 0, y_perm, H, H, status, st));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_strerror(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace or capacity too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_STATUS: return "device status flag set";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_validate_config(const moe_config* cfg) { return validate_cfg(cfg); }
+
+size_t moe_align_cap(const moe_config* cfg, int T, int block_m) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK || block_m < 1) return 0;
+  return static_cast<size_t>(T) * cfg->top_k +
+         static_cast<size_t>(n_local(cfg)) * (block_m - 1);
+}
+
+size_t moe_route_workspace_size(const moe_config* cfg, int T) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK) return 0;
+  return route_layout(cfg, T).total;
+}
+
+int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
+              const float* router_bias, int32_t* topk_ids, float* topk_w, void* ws,
+              size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w)) return MOE_ERR_INVALID_ARG;
+  const RouteLayout L = route_layout(cfg, T);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = at<unsigned>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  return do_route(cfg, T, x, router_w, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
+                  at<Tile>(ws, L.rtiles), status, st);
+}
+
+size_t moe_align_workspace_size(const moe_config* cfg, int T) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK) return 0;
+  return align_layout(cfg, T).total;
+}
+
+int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
+                      const int32_t* expert_map, int block_m, int32_t* counts, int32_t* offsets,
+                      int32_t* sorted_ids, int32_t* inv_pos, int cap, void* ws, size_t ws_bytes,
+                      void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (block_m < 1 || block_m > 4096) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !counts || !offsets || !sorted_ids || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (cap < 0 || static_cast<size_t>(cap) < moe_align_cap(cfg, T, block_m))
+    return MOE_ERR_WORKSPACE;
+  const AlignLayout L = align_layout(cfg, T);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = at<unsigned>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  const int El = n_local(cfg);
+  return cuda_ok(launch_align(topk_ids, static_cast<long>(T) * cfg->top_k, expert_map,
+                              cfg->num_experts, El, cfg->ep_rank * El, block_m,
+                              at<int>(ws, L.hist), counts, offsets, sorted_ids, inv_pos, cap,
+                              status, st));
+}
+
+size_t moe_grouped_mlp_workspace_size(const moe_config* cfg, int T, int cap) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK || cap < 0) return 0;
+  return mlp_layout(cfg, T, cap).total;
+}
+
+int moe_grouped_mlp(const moe_config* cfg, int T, const void* x, const int32_t* sorted_ids,
+                    const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
+                    const void* w2, void* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (T == 0) return MOE_OK;
+  if (!x || !sorted_ids || !counts || !offsets || !w13 || !w2 || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (cap < 1) return MOE_ERR_WORKSPACE;
+  const MlpLayout L = mlp_layout(cfg, T, cap);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = at<unsigned>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  return do_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm,
+                at<Tile>(ws, L.tiles), at<int>(ws, L.ntiles), at<void>(ws, L.x_perm),
+                at<void>(ws, L.h_perm), status, st);
+}
+
+int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const int32_t* inv_pos,
+                const float* topk_w, const void* shared_out, void* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !inv_pos || !topk_w || !out || cap < 0) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws && ws_bytes < 4) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = ws ? static_cast<unsigned*>(ws) : nullptr;
+  if (status) MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  return cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, y_perm, cap, inv_pos, topk_w,
+                                cfg->top_k, shared_out, shared_out ? 1 : 0, 0,
+                                cfg->routed_scaling_factor, out, T, cfg->hidden_size, status,
+                                st));
+}
+
+size_t moe_workspace_size(const moe_config* cfg, int T) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK) return 0;
+  return fwd_layout(cfg, T).total;
+}
+
+int moe_workspace_layout(const moe_config* cfg, int T, moe_workspace_offsets* out) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(cfg, T);
+  out->status = L.status;
+  out->topk_ids = L.topk_ids;
+  out->topk_w = L.topk_w;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->sorted_ids = L.sorted_ids;
+  out->inv_pos = L.inv_pos;
+  out->total = L.total;
+  out->cap = L.cap;
+  out->block_m = kForwardBlock;
+  return MOE_OK;
+}
+
+static int forward_impl(const moe_config* cfg, int T, const void* x, const void* router_w,
+                        const float* router_bias, const void* w13, const void* w2,
+                        const void* shared_w13, const void* shared_w2,
+                        const int32_t* expert_map, void* out, void* ws, size_t ws_bytes,
+                        void* stream, void* const* events, int* kernels) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (kernels) *kernels = 0;
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(w13) || !aligned16(w2) ||
+      !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const bool with_shared = cfg->num_shared_experts > 0 && shared_w13 && shared_w2;
+  if (with_shared && (!aligned16(shared_w13) || !aligned16(shared_w2)))
+    return MOE_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(cfg, T);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) -> int {
+    if (!events || !events[i]) return MOE_OK;
+    return cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st));
+  };
+  const int El = n_local(cfg), H = cfg->hidden_size, K = cfg->top_k;
+  unsigned* status = at<unsigned>(ws, L.status);
+  int32_t* ids = at<int32_t>(ws, L.topk_ids);
+  float* w = at<float>(ws, L.topk_w);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* sorted_ids = at<int32_t>(ws, L.sorted_ids);
+  int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
+  int n = 0;
+
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  MOE_TRY(mark(0));
+  MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
+                   at<Tile>(ws, L.rtiles), status, st));
+  n += router_on_tensor_cores(cfg, T) ? 3 : 2;
+  MOE_TRY(mark(1));
+  MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts, El,
+                               cfg->ep_rank * El, kForwardBlock, at<int>(ws, L.hist), counts,
+                               offsets, sorted_ids, inv_pos, L.cap, status, st)));
+  n += 3;
+  MOE_TRY(mark(2));
+  MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
+                 at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.ntiles),
+                 at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), status, st,
+                 events ? events + 3 : nullptr));
+  n += 4;
+  MOE_TRY(mark(5));
+  const void* shared_y = nullptr;
+  int S = 0;
+  if (with_shared) {
+    S = cfg->num_shared_experts;
+    const int Is = cfg->shared_intermediate_size;
+    const int nm = dense_nmax(T);
+    const int nt = dense_tile_count(T, S, nm);
+    Tile* stl = at<Tile>(ws, L.stiles);
+    void* h_sh = at<void>(ws, L.h_sh);
+    void* y_sh = at<void>(ws, L.y_sh);
+    MOE_TRY(cuda_ok(launch_dense_tiles(T, S, nm, stl, st)));
+    MOE_TRY(run_gemm(kGemmSiluUp, cfg->act_dtype, nm, shared_w13, static_cast<long>(S) * 2 * Is,
+                     x, T, H, stl, nullptr, nt, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
+                     st));
+    MOE_TRY(run_gemm(kGemmPlain, cfg->act_dtype, nm, shared_w2, static_cast<long>(S) * H, h_sh,
+                     static_cast<long>(S) * T, Is, stl, nullptr, nt, H / 128, H, 0, 1, y_sh, H,
+                     H, status, st));
+    shared_y = y_sh;
+    n += 3;
+  }
+  MOE_TRY(mark(6));
+  MOE_TRY(cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
+                                 inv_pos, w, K, shared_y, S, static_cast<long>(T) * H,
+                                 cfg->routed_scaling_factor, out, T, H, status, st)));
+  n += 1;
+  MOE_TRY(mark(7));
+  if (kernels) *kernels = n;
+  return MOE_OK;
+}
+
+int moe_forward(const moe_config* cfg, int T, const void* x, const void* router_w,
+                const float* router_bias, const void* w13, const void* w2,
+                const void* shared_w13, const void* shared_w2, const int32_t* expert_map,
+                void* out, void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(cfg, T, x, router_w, router_bias, w13, w2, shared_w13, shared_w2,
+                      expert_map, out, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+int moe_forward_timed(const moe_config* cfg, int T, const void* x, const void* router_w,
+                      const float* router_bias, const void* w13, const void* w2,
+                      const void* shared_w13, const void* shared_w2,
+                      const int32_t* expert_map, void* out, void* ws, size_t ws_bytes,
+                      void* stream, void* const* events, int* kernels_launched) {
+  return forward_impl(cfg, T, x, router_w, router_bias, w13, w2, shared_w13, shared_w2,
+                      expert_map, out, ws, ws_bytes, stream, events, kernels_launched);
+}
+
+int moe_get_status(const void* ws, void* stream, uint32_t* flags) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags) *flags = v;
+  if (v == 0) return MOE_OK;
+  return (v & MOE_DEV_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_STATUS;
+}
+
+}  // extern "C"

@@ -1,0 +1,270 @@
+/*
+ * moe.h -- C ABI of the fused Mixture-of-Experts layer forward for sm_103a.
+ *
+ * One layer forward is:
+ *   route         router GEMM, fp32 softmax, (grouped) top-k, renormalise
+ *   align/permute expert_map mask, per-local-expert padded segments
+ *   grouped MLP   gather rows, GEMM1 with the SiLU(gate)*up epilogue, GEMM2
+ *   combine       weighted gather back to token order, routed_scaling_factor,
+ *                 plus the shared-expert output
+ * Each stage is a hand-written CUDA kernel. moe_forward runs all of them.
+ *
+ * Sources of the semantics (the web pages this library restates):
+ *   - SGLang issue "[Feature] Expert parallelism support", MixtralMoE:
+ *     gate = bias-free linear over all experts, softmax in fp32, topk,
+ *     renormalise, sum over experts of weight * expert MLP.
+ *   - ep_fused_moe_patch.py (EP-aware FusedMoE override): _ep_init
+ *     (num_experts % ep_size == 0; local experts [r*E/ep, (r+1)*E/ep)),
+ *     _ep_forward (global routing, flatten (token, slot) work items, local
+ *     expert compute, weighted scatter-add back to tokens).
+ *   - vLLM docs, MoEMixin.recursive_replace: top_k, moe_intermediate_size,
+ *     renormalize = norm_topk_prob, routed_scaling_factor, n_group /
+ *     topk_group (use_grouped_topk), n_shared_experts, router dtype,
+ *     activation "silu", gate_up_proj (E, 2I, H).
+ *   - vllm-omni "Expert Parallel": shared experts are added unweighted on
+ *     every rank; EP size divisibility; contiguous local expert ranges.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device.
+ *     They are row-major and contiguous, with 16-byte-aligned bases. The
+ *     caller owns every buffer. The library allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued asynchronously on it. Only
+ *     moe_get_status synchronises, and only that stream.
+ *   - `ws` is caller-owned device scratch of at least the size reported by
+ *     the matching *_workspace_size call. Its first 4 bytes are the device
+ *     status word (MOE_DEV_* flags). Each call that takes `ws` clears that
+ *     word first, so it reports on the latest call only. Read it with
+ *     moe_get_status.
+ *   - Arguments are validated on the host before any CUDA call. Invalid
+ *     ones return MOE_ERR_INVALID_ARG (or MOE_ERR_UNSUPPORTED, or
+ *     MOE_ERR_WORKSPACE) and enqueue nothing. A launch failure returns
+ *     MOE_ERR_CUDA. Data-dependent faults found on the device (an expert id
+ *     out of range, a full segment buffer, a pipeline wait that timed out)
+ *     never trap. They set a MOE_DEV_* flag and skip the offending access.
+ *   - T == 0 is a valid no-op that returns MOE_OK.
+ *   - Calls that share a `ws` buffer must be ordered, as on one stream.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* bad config, size, pointer or alignment     */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid, but outside what the kernels cover  */
+  MOE_ERR_WORKSPACE = 3,     /* ws too small / NULL, or cap too small      */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed          */
+  MOE_ERR_DEVICE_STATUS = 5, /* moe_get_status: a MOE_DEV_* flag is set    */
+  MOE_ERR_TIMEOUT = 6        /* moe_get_status: MOE_DEV_TIMEOUT is set     */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Device status flags (bit OR, first 4 bytes of ws). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1u /* topk id not in [0,E) or expert_map value
+                                      not in [-1,E_local): item dropped      */
+#define MOE_DEV_CAP_OVERFLOW 0x2u  /* padded segments exceed cap or a tile
+                                      table overflowed: rows dropped        */
+#define MOE_DEV_TIMEOUT 0x4u       /* a GEMM pipeline wait passed its time
+                                      limit; that kernel stopped early      */
+#define MOE_DEV_BAD_SEGMENT 0x8u   /* offsets/counts inconsistent          */
+
+/* Layer description. The field names follow the FusedMoE arguments the
+ * pages pass (num_experts, top_k, hidden_size, intermediate_size,
+ * renormalize, use_grouped_topk, num_expert_group, topk_group,
+ * routed_scaling_factor, shared experts, ep_size / ep_rank). */
+typedef struct {
+  int num_experts;           /* E: global routed experts (router width)      */
+  int top_k;                 /* K: experts per token, 1 <= K <= min(E, 32)   */
+  int hidden_size;           /* H: multiple of 128                           */
+  int intermediate_size;     /* I: per routed expert, multiple of 128        */
+  int renormalize;           /* 1: topk_w /= sum(topk_w) per token           */
+  int use_grouped_topk;      /* 1: group-limited top-k (reading below)       */
+  int num_expert_group;      /* n_group: E % n_group == 0, n_group <= 32     */
+  int topk_group;            /* groups kept per token, 1..n_group            */
+  float routed_scaling_factor; /* rsf: multiplies the routed sum; 1 = off    */
+  int num_shared_experts;    /* S >= 0 shared experts, added unweighted      */
+  int shared_intermediate_size; /* I_s of each shared expert (x128)          */
+  int ep_size;               /* expert-parallel size; E % ep_size == 0       */
+  int ep_rank;               /* this shard, 0 <= ep_rank < ep_size           */
+  moe_dtype act_dtype;       /* x, expert weights, y_perm, out               */
+  moe_dtype router_dtype;    /* router weight storage (logits are fp32)      */
+} moe_config;
+
+/* Grouped top-k reading: the E experts form n_group contiguous groups of
+ * E/n_group. A group's score is the max softmax probability of its members.
+ * The topk_group best groups are kept (ties to the lower group id). Top-k
+ * then runs over the kept experts (ties to the lower expert id), and the
+ * weights are the plain softmax values of the chosen experts. */
+
+/* Human-readable name of a moe_status. Never NULL. */
+const char* moe_strerror(int status);
+
+/* Host-only validation of a config (no CUDA call). Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. Checks: E % ep_size == 0 and
+ * 0 <= ep_rank < ep_size (ep_fused_moe_patch.py _ep_init assert), E_local >= 1
+ * (MixtralMoE "has no experts" error), 1 <= K <= E, grouped constraints
+ * (E % n_group == 0, 1 <= topk_group <= n_group, K <= topk_group*E/n_group),
+ * H and I multiples of 128, S >= 0 with I_s a multiple of 128 when S > 0.
+ * Kernel limits (MOE_ERR_UNSUPPORTED): E <= 512, K <= 32, n_group <= 32,
+ * E_local <= 1024, and act_dtype F32 needs router_dtype F32. */
+int moe_validate_config(const moe_config* cfg);
+
+/* Rows of the padded permutation buffers for T tokens and segment padding
+ * block_m: T*K + E_local*(block_m-1). Returns 0 on an invalid config. */
+size_t moe_align_cap(const moe_config* cfg, int T, int block_m);
+
+/* ------------------------------------------------------------------------ */
+/* moe_route: router logits, fp32 softmax over E, top-k, renormalise.
+ * MixtralMoE.forward (gate, F.softmax(dtype=float), torch.topk, divide by
+ * the sum); ep_fused_moe_patch.py _ep_forward step 1 (global routing: all E
+ * experts on every rank).
+ *   x           [T, H]  act_dtype
+ *   router_w    [E, H]  router_dtype
+ *   router_bias [E]     fp32, nullable. It is added to the logits before the
+ *                       softmax (a per-expert skew of the load).
+ *   topk_ids    [T, K]  int32 out: global expert ids in descending
+ *                       probability, ties to the lower id.
+ *   topk_w      [T, K]  fp32 out: softmax probabilities of those experts
+ *                       (renormalised to sum 1 when cfg->renormalize).
+ *                       routed_scaling_factor is NOT applied here.
+ * ws: moe_route_workspace_size(cfg, T) bytes (status word + fp32 logits). */
+size_t moe_route_workspace_size(const moe_config* cfg, int T);
+int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
+              const float* router_bias, int32_t* topk_ids, float* topk_w,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_align_permute: keep local experts, sort work items by local expert.
+ * Work item i = t*K + k is (token t, slot k), the flattening in
+ * ep_fused_moe_patch.py _ep_forward step 2. expert_map turns global ids
+ * into local ids (-1 = not on this rank: the item is dropped, as step 3
+ * keeps only local ids).
+ *   topk_ids    [T, K] int32 global ids
+ *   expert_map  [E] int32 (values in [-1, E_local)), or NULL for the
+ *               contiguous shard of cfg->ep_rank: id - ep_rank*E/ep_size.
+ *   block_m     segment padding (>= 1). The grouped MLP accepts any value.
+ *   counts      [E_local]   out: items per local expert (unpadded)
+ *   offsets     [E_local+1] out: exclusive prefix of counts, each rounded
+ *               up to a multiple of block_m
+ *   sorted_ids  [cap] out: rows offsets[e] .. offsets[e]+counts[e]-1 hold
+ *               expert e's items in ascending item order (a stable sort).
+ *               Every other row holds the sentinel T*K.
+ *   inv_pos     [T*K] out: row of each item, -1 if dropped
+ *   cap         rows of sorted_ids. Must be >= moe_align_cap(cfg,T,block_m),
+ *               else MOE_ERR_WORKSPACE.
+ * ws: moe_align_workspace_size(cfg, T) bytes. */
+size_t moe_align_workspace_size(const moe_config* cfg, int T);
+int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
+                      const int32_t* expert_map, int block_m, int32_t* counts,
+                      int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
+                      int cap, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_grouped_mlp: the local experts' SiLU-gated MLPs on permuted rows.
+ * For every row r of segment e with sorted_ids[r] < T*K:
+ *   y_perm[r] = W2[e] . ( silu(W13[e][0:I] . x_t) * (W13[e][I:2I] . x_t) ),
+ *   t = sorted_ids[r] / K.
+ * The expert MLP is MixtralMLP with activation "silu" (MoEMixin); w1 = w13,
+ * w2 as passed to fused_experts (ep_fused_moe_patch.py _ep_forward step 3).
+ *   x        [T, H] act_dtype
+ *   sorted_ids, counts, offsets: as produced by moe_align_permute (any
+ *            block_m); cap = rows of sorted_ids and y_perm.
+ *   w13      [E_local, 2*I, H] act_dtype: gate rows [0,I), up rows [I,2I).
+ *   w2       [E_local, H, I]   act_dtype ([out, in]).
+ *   y_perm   [cap, H] act_dtype out. Only rows holding items are written.
+ * Both GEMMs run on the tcgen05 tensor cores (bf16: kind::f16, fp32:
+ * kind::tf32), with fp32 accumulation. The SiLU*up product is rounded to
+ * act_dtype between them.
+ * ws: moe_grouped_mlp_workspace_size(cfg, T, cap) bytes. */
+size_t moe_grouped_mlp_workspace_size(const moe_config* cfg, int T, int cap);
+int moe_grouped_mlp(const moe_config* cfg, int T, const void* x,
+                    const int32_t* sorted_ids, const int32_t* counts,
+                    const int32_t* offsets, int cap, const void* w13,
+                    const void* w2, void* y_perm, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_combine: weighted gather back to token order.
+ *   out[t] = rsf * sum_{k : inv_pos[t*K+k] >= 0} topk_w[t,k] * y_perm[inv_pos]
+ *            + shared_out[t]
+ * This is the scatter_add_ by token of ep_fused_moe_patch.py _ep_forward
+ * step 4, done as a deterministic per-token gather in slot order with fp32
+ * accumulation. rsf = routed_scaling_factor (MoEMixin). The shared output is
+ * added unweighted (vllm-omni "Expert Parallel", Step 5).
+ *   y_perm     [cap, H] act_dtype
+ *   inv_pos    [T*K] int32; entries outside [-1, cap) count as dropped
+ *   topk_w     [T, K] fp32
+ *   shared_out [T, H] act_dtype, nullable
+ *   out        [T, H] act_dtype out
+ * ws: NULL, or >= 4 bytes for the status word. */
+int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap,
+                const int32_t* inv_pos, const float* topk_w,
+                const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* moe_forward: the whole layer (route -> align/permute -> grouped MLP of the
+ * local experts and of the shared experts -> combine), stream-ordered with no
+ * host synchronisation.
+ *   x, router_w, router_bias: as moe_route
+ *   w13, w2:     local experts, as moe_grouped_mlp ([E_local, ...]).
+ *   shared_w13   [S, 2*I_s, H], shared_w2 [S, H, I_s]: nullable. When NULL
+ *                (or S == 0) no shared output is added. With EP, pass them on
+ *                one rank only if the partial outputs are to be summed.
+ *   expert_map   as moe_align_permute (NULL = contiguous shard).
+ *   out          [T, H] act_dtype. With ep_size > 1 this is the partial sum
+ *                over this rank's experts. No collective is made.
+ * Segments are padded to 16 rows. After the call, ws holds topk_ids,
+ * topk_w, counts, offsets, sorted_ids and inv_pos at the byte offsets given
+ * by moe_workspace_layout.
+ * ws: moe_workspace_size(cfg, T) bytes. */
+typedef struct {
+  size_t status, topk_ids, topk_w, counts, offsets, sorted_ids, inv_pos;
+  size_t total;   /* == moe_workspace_size */
+  int cap;        /* rows of sorted_ids */
+  int block_m;    /* segment padding used by moe_forward */
+} moe_workspace_offsets;
+
+size_t moe_workspace_size(const moe_config* cfg, int T);
+int moe_workspace_layout(const moe_config* cfg, int T, moe_workspace_offsets* out);
+int moe_forward(const moe_config* cfg, int T, const void* x,
+                const void* router_w, const float* router_bias,
+                const void* w13, const void* w2, const void* shared_w13,
+                const void* shared_w2, const int32_t* expert_map, void* out,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward plus instrumentation. No page counterpart: this entry point is
+ * there so that each kernel's duration can be measured live on the stream that
+ * runs it. events: 8 caller-created cudaEvent_t (as void*; any may be NULL),
+ * recorded on `stream` at the stage boundaries:
+ *   [0] start  [1] after routing  [2] after align/permute
+ *   [3] after the tile table and row gather  [4] after GEMM1 (SiLU*up)
+ *   [5] after GEMM2  [6] after the shared experts  [7] after combine.
+ * kernels_launched (nullable): number of kernels this call launched. The
+ * results are identical to moe_forward. */
+int moe_forward_timed(const moe_config* cfg, int T, const void* x,
+                      const void* router_w, const float* router_bias,
+                      const void* w13, const void* w2, const void* shared_w13,
+                      const void* shared_w2, const int32_t* expert_map, void* out,
+                      void* ws, size_t ws_bytes, void* stream,
+                      void* const* events, int* kernels_launched);
+
+/* ------------------------------------------------------------------------ */
+/* Synchronises `stream` and reads the device status word at the start of
+ * `ws`. Writes the raw MOE_DEV_* bits to *flags (nullable). Returns MOE_OK if
+ * no flag is set, MOE_ERR_TIMEOUT if MOE_DEV_TIMEOUT is set, else
+ * MOE_ERR_DEVICE_STATUS. MOE_ERR_CUDA if the synchronisation fails. */
+int moe_get_status(const void* ws, void* stream, uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

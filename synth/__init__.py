@@ -123,6 +123,18 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return out
 
 
+class BF16Experts:
+    """Expert-indexed view of bf16 bit patterns [E, R, C] that widens one
+    expert to float32 on access (a host copy at half the memory)."""
+
+    def __init__(self, bits: np.ndarray):
+        self.bits = bits
+        self.shape = bits.shape
+
+    def __getitem__(self, e):
+        return bf16_bits_to_f32(self.bits[e])
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     """Shape and input distribution of one synthetic MoE layer."""

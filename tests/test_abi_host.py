@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+
+import pytest
+
+from expert_moe_layer_gb300 import binding as B
+
+MIX = dict(num_experts=8, top_k=2, hidden_size=4096, intermediate_size=14336)
+
+
+def test_library_exports_every_header_function():
+    L = B.lib()
+    names = B.header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/moe.h but not exported"
+    assert set(names) == set(B._SIGS)
+
+
+def test_strerror_covers_all_codes():
+    for code in range(7):
+        assert B.strerror(code) and B.strerror(code) != "unknown status"
+    assert B.strerror(99) == "unknown status"
+
+
+def _cfg(**kw):
+    base = dict(MIX)
+    base.update(kw)
+    return B.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(), 0),
+    (dict(num_experts=160, top_k=6, hidden_size=5120, intermediate_size=1536,
+          num_expert_group=8, topk_group=3, num_shared_experts=2,
+          shared_intermediate_size=1536, routed_scaling_factor=16.0, renormalize=False), 0),
+    (dict(num_experts=256, top_k=8, hidden_size=2048, intermediate_size=512, ep_size=4,
+          ep_rank=1), 0),
+    (dict(top_k=0), 1), (dict(top_k=9), 1),
+    (dict(hidden_size=100), 1), (dict(intermediate_size=4000), 1),
+    (dict(ep_size=3), 1),                 # E % ep_size != 0 (_ep_init assert)
+    (dict(ep_size=4, ep_rank=4), 1), (dict(ep_size=4, ep_rank=-1), 1),
+    (dict(num_expert_group=3, topk_group=1), 1),   # E % n_group
+    (dict(num_expert_group=4, topk_group=5), 1),
+    (dict(num_expert_group=4, topk_group=1, top_k=3), 1),  # K > kept experts
+    (dict(num_shared_experts=1, shared_intermediate_size=0), 1),
+    (dict(routed_scaling_factor=float("inf")), 1),
+    (dict(num_experts=1024, top_k=2), 2),  # beyond kernel coverage
+    (dict(num_experts=64, top_k=33), 2),
+    (dict(act_dtype="f32", router_dtype="bf16"), 2),
+])
+def test_validate_config(kw, expect):
+    assert B.validate_config(_cfg(**kw)) == expect
+
+
+def test_entry_points_reject_bad_args_without_cuda():
+    cfg = _cfg()
+    bad = _cfg(top_k=0)
+    L = B.lib()
+    null = None
+    # invalid config -> INVALID_ARG before anything touches CUDA
+    assert L.moe_forward(ctypes.byref(bad), 4, 16, 16, null, 16, 16, null, null, null, 16,
+                         16, 1 << 30, null) == 1
+    assert L.moe_route(ctypes.byref(cfg), -1, 16, 16, null, 16, 16, 16, 1 << 30, null) == 1
+    # NULL / misaligned pointers
+    assert L.moe_route(ctypes.byref(cfg), 4, null, 16, null, 16, 16, 16, 1 << 30, null) == 1
+    assert L.moe_forward(ctypes.byref(cfg), 4, 18, 16, null, 16, 16, null, null, null, 16,
+                         16, 1 << 30, null) == 1
+    # workspace too small
+    need = B.workspace_size(cfg, 4)
+    assert need > 0
+    assert L.moe_forward(ctypes.byref(cfg), 4, 16, 16, null, 16, 16, null, null, null, 16,
+                         16, need - 1, null) == 3
+    # cap below T*K + E_l*(block-1)
+    assert L.moe_align_permute(ctypes.byref(cfg), 4, 16, null, 16, 16, 16, 16, 16,
+                               int(B.align_cap(cfg, 4, 16)) - 1, 16, 1 << 30, null) == 3
+    assert L.moe_align_permute(ctypes.byref(cfg), 4, 16, null, 0, 16, 16, 16, 16, 1000, 16,
+                               1 << 30, null) == 1
+    # T == 0 is a no-op
+    assert L.moe_forward(ctypes.byref(cfg), 0, null, null, null, null, null, null, null,
+                         null, null, null, 0, null) == 0
+
+
+def test_workspace_sizes_and_layout():
+    cfg = _cfg()
+    T = 4096
+    assert B.align_cap(cfg, T, 16) == T * 2 + 8 * 15
+    lay = B.workspace_layout(cfg, T)
+    assert lay.total == B.workspace_size(cfg, T)
+    assert lay.cap == T * 2 + 8 * 15 and lay.block_m == 16
+    offs = [lay.status, lay.topk_ids, lay.topk_w, lay.counts, lay.offsets, lay.sorted_ids,
+            lay.inv_pos]
+    assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs)
+    assert B.route_workspace_size(cfg, T) >= 4 + 4 * T * 8
+    assert B.align_workspace_size(cfg, T) > 0
+    assert B.grouped_mlp_workspace_size(cfg, T, lay.cap) >= 2 * lay.cap * (4096 + 14336)
+    assert B.workspace_size(_cfg(top_k=0), T) == 0

@@ -1,0 +1,250 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing ids, counts, offsets, the permutation and inv_pos must match
+bit-exactly. Routing weights must agree within W_RTOL, and layer outputs per
+element within |gpu - ref| <= 2e-2 + 2e-2*|ref|. Small layers are compared
+element by element. The full-size layers are compared on all routing and
+permutation arrays and on a sample of output tokens, run exactly as bench.py
+runs them (moe_forward, one call).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from expert_moe_layer_gb300 import binding as B
+from oracle import moe_oracle as O
+
+from gpu_cases import (ATOL, RTOL, W_ATOL, W_RTOL, DeviceCase, assert_close, sample_tokens,
+                       ws_views)
+
+pytestmark = pytest.mark.gpu
+
+W = synth.Workload
+SMALL = {
+    "tiny_f32": synth.TINY,
+    "ragged_prefill": W("ragged_prefill", T=333, H=384, I=640, E=12, K=3),
+    "ragged_decode": W("ragged_decode", T=77, H=256, I=384, E=16, K=4, router_bias=True),
+    "grouped_shared": synth.DEEPSEEK.with_(name="grouped_shared", T=300, H=512, I=256,
+                                           I_shared=384),
+    "ep_rank1": synth.EP_SHARD.with_(name="ep_rank1", T=500, H=256, I=256),
+    "f32_ragged": W("f32_ragged", T=90, H=256, I=384, E=6, K=2, act="f32", router="f32",
+                    x_std=0.3),
+    "k_equals_e": W("k_equals_e", T=40, H=128, I=128, E=8, K=8),
+    "single_token": W("single_token", T=1, H=256, I=256, E=32, K=4, router_bias=True),
+}
+FULL = {
+    "mixtral_prefill": synth.MIXTRAL,
+    "deepseek_v2_prefill": synth.DEEPSEEK,
+    "ep_shard": synth.EP_SHARD,
+}
+
+_cache = {}
+
+
+def case(name):
+    if name not in _cache:
+        _cache.clear()
+        torch.cuda.empty_cache()
+        wl = {**SMALL, **FULL}.get(name)
+        if wl is None:
+            T = int(name.split("_T")[1])
+            wl = synth.QWEN_DECODE.with_(name=name, T=T)
+        _cache[name] = DeviceCase(wl)
+    return _cache[name]
+
+
+def check_forward(c: DeviceCase, tokens=None):
+    wl = c.wl
+    out, ws = c.forward()
+    rc, flags = B.moe_get_status(ws)
+    assert rc == 0 and flags == 0, (rc, flags)
+    v = ws_views(c.cfg, wl.T, ws)
+    np.testing.assert_array_equal(v["topk_ids"], c.ids)
+    np.testing.assert_allclose(v["topk_w"], c.w, rtol=W_RTOL, atol=W_ATOL)
+    counts, offsets, sorted_ids, inv_pos = c.oracle_align(v["block_m"])
+    np.testing.assert_array_equal(v["counts"], counts)
+    np.testing.assert_array_equal(v["offsets"], offsets)
+    np.testing.assert_array_equal(v["sorted_ids"], sorted_ids)
+    np.testing.assert_array_equal(v["inv_pos"], inv_pos)
+    tok = np.arange(wl.T) if tokens is None else tokens
+    ref = c.oracle_out(tokens=tok)
+    got = out.float().cpu().numpy()[tok]
+    assert_close(got, ref, f"{wl.name} out")
+    return out, ws
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small(name):
+    check_forward(case(name))
+
+
+@pytest.mark.parametrize("T", synth.DECODE_TOKENS)
+def test_forward_decode_full_shape(T):
+    check_forward(case(f"qwen3_decode_T{T}"))
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_forward_full_size_sampled(name):
+    c = case(name)
+    check_forward(c, tokens=sample_tokens(c.wl.T))
+
+
+# ------------------------------------------------------------------ components
+@pytest.mark.parametrize("name", ["ragged_prefill", "grouped_shared", "ragged_decode",
+                                  "tiny_f32", "ep_rank1"])
+def test_route_entry_point(name):
+    c = case(name)
+    wl = c.wl
+    ids = torch.empty(wl.T, wl.K, dtype=torch.int32, device="cuda")
+    w = torch.empty(wl.T, wl.K, dtype=torch.float32, device="cuda")
+    ws = torch.empty(B.route_workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    B.moe_route(c.cfg, wl.T, c.d["x"], c.d["router_w"], c.d["router_b"], ids, w, ws)
+    assert B.moe_get_status(ws) == (0, 0)
+    np.testing.assert_array_equal(ids.cpu().numpy(), c.ids)
+    np.testing.assert_allclose(w.cpu().numpy(), c.w, rtol=W_RTOL, atol=W_ATOL)
+
+
+def _align(c, ids_np, block, emap=None, cap=None):
+    wl = c.wl
+    El = wl.E_local
+    cap = cap or B.align_cap(c.cfg, wl.T, block)
+    ids = torch.from_numpy(ids_np).cuda()
+    counts = torch.empty(El, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(El + 1, dtype=torch.int32, device="cuda")
+    sorted_ids = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    inv_pos = torch.empty(wl.T * wl.K, dtype=torch.int32, device="cuda")
+    ws = torch.empty(B.align_workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    em = None if emap is None else torch.from_numpy(emap).cuda()
+    B.moe_align_permute(c.cfg, wl.T, ids, em, block, counts, offsets, sorted_ids, inv_pos,
+                        cap, ws)
+    st = B.moe_get_status(ws)
+    return (counts.cpu().numpy(), offsets.cpu().numpy(), sorted_ids.cpu().numpy(),
+            inv_pos.cpu().numpy(), st, cap)
+
+
+@pytest.mark.parametrize("block", [1, 7, 16, 64, 128])
+@pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1"])
+def test_align_entry_point(name, block):
+    c = case(name)
+    counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, block)
+    assert st == (0, 0)
+    rc, ro, rs, ri = O.align_permute(c.ids, c.h["emap"], c.wl.E_local, block, cap)
+    np.testing.assert_array_equal(counts, rc)
+    np.testing.assert_array_equal(offsets, ro)
+    np.testing.assert_array_equal(sorted_ids, rs)
+    np.testing.assert_array_equal(inv_pos, ri)
+
+
+def test_align_general_expert_map_and_bad_ids():
+    c = case("ep_rank1")
+    wl = c.wl
+    rng = np.random.default_rng(7)
+    emap = np.full(wl.E, -1, dtype=np.int32)
+    chosen = rng.choice(wl.E, wl.E_local, replace=False)
+    emap[chosen] = rng.permutation(wl.E_local).astype(np.int32)
+    counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, 16, emap)
+    assert st == (0, 0)
+    rc, ro, rs, ri = O.align_permute(c.ids, emap, wl.E_local, 16, cap)
+    np.testing.assert_array_equal(sorted_ids, rs)
+    np.testing.assert_array_equal(inv_pos, ri)
+    # out-of-range ids and map values are dropped and flagged, never read
+    ids = c.ids.copy()
+    ids[0, 0] = wl.E + 5
+    ids[1, 1] = -3
+    emap2 = emap.copy()
+    emap2[ids[2, 0]] = wl.E_local + 9
+    _, _, sorted_ids, inv_pos, st, _ = _align(c, ids, 16, emap2)
+    assert st[0] == 5 and st[1] & B.DEV_BAD_EXPERT_ID
+    assert inv_pos[0] == -1 and inv_pos[1 * wl.K + 1] == -1 and inv_pos[2 * wl.K] == -1
+
+
+@pytest.mark.parametrize("name", ["ragged_prefill", "ragged_decode", "f32_ragged",
+                                  "grouped_shared"])
+def test_grouped_mlp_and_combine_entry_points(name):
+    c = case(name)
+    wl = c.wl
+    block = 16
+    counts, offsets, sorted_ids, inv_pos = c.oracle_align(block)
+    cap = len(sorted_ids)
+    dt = c.d["x"].dtype
+    y = torch.full((cap, wl.H), float("nan"), dtype=dt, device="cuda")
+    ws = torch.empty(B.grouped_mlp_workspace_size(c.cfg, wl.T, cap), dtype=torch.uint8,
+                     device="cuda")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    B.moe_grouped_mlp(c.cfg, wl.T, c.d["x"], dev(sorted_ids), dev(counts), dev(offsets), cap,
+                      c.d["w13"], c.d["w2"], y, ws)
+    assert B.moe_get_status(ws) == (0, 0)
+    rows = np.nonzero(sorted_ids < wl.T * wl.K)[0]
+    ref = O.grouped_mlp(c.h["x"], sorted_ids, offsets, c.h["w13"], c.h["w2"], wl.K, rows)
+    got = y.float().cpu().numpy()
+    assert_close(got[rows], np.stack([ref[int(r)] for r in rows]), f"{name} y_perm")
+    # combine from the oracle's y_perm rounded to the activation dtype
+    yref = np.zeros((cap, wl.H), dtype=np.float32)
+    for r in rows:
+        yref[r] = ref[int(r)]
+    y_dev = torch.from_numpy(yref).to(dt).cuda()
+    shared = None
+    if wl.n_shared:
+        sh = sum(O.expert_mlp(c.h["x"], c.h["shared_w13"][s], c.h["shared_w2"][s])
+                 for s in range(wl.n_shared))
+        shared = torch.from_numpy(sh.astype(np.float32)).to(dt).cuda()
+    out = torch.empty(wl.T, wl.H, dtype=dt, device="cuda")
+    cws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    B.moe_combine(c.cfg, wl.T, y_dev, cap, dev(inv_pos), dev(c.w), shared, out, cws)
+    assert B.moe_get_status(cws) == (0, 0)
+    want = O.combine(y_dev.float().cpu().numpy(), inv_pos, c.w, wl.rsf,
+                     None if shared is None else shared.float().cpu().numpy())
+    assert_close(out.float().cpu().numpy(), want, f"{name} combine", atol=1e-2, rtol=1e-2)
+
+
+# ------------------------------------------------------------------ edge cases
+def test_no_local_items_gives_shared_only():
+    c = case("grouped_shared")
+    wl = c.wl
+    d = c.d
+    emap = torch.full((wl.E,), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    out = torch.empty(wl.T, wl.H, dtype=d["x"].dtype, device="cuda")
+    B.moe_forward(c.cfg, wl.T, d["x"], d["router_w"], None, d["w13"], d["w2"], d["shared_w13"],
+                  d["shared_w2"], emap, out, ws)
+    assert B.moe_get_status(ws) == (0, 0)
+    sh = sum(O.expert_mlp(c.h["x"], c.h["shared_w13"][s], c.h["shared_w2"][s])
+             for s in range(wl.n_shared))
+    assert_close(out.float().cpu().numpy(), sh, "shared only")
+    B.moe_forward(c.cfg, wl.T, d["x"], d["router_w"], None, d["w13"], d["w2"], None, None,
+                  emap, out, ws)
+    assert (out.float() == 0).all()
+
+
+def test_zero_tokens_is_noop_and_repeat_calls_agree():
+    c = case("ragged_decode")
+    wl = c.wl
+    d = c.d
+    ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    out = torch.full((wl.T, wl.H), 3.0, dtype=d["x"].dtype, device="cuda")
+    B.moe_forward(c.cfg, 0, d["x"], d["router_w"], None, d["w13"], d["w2"], None, None, None,
+                  out, ws)
+    torch.cuda.synchronize()
+    assert (out.float() == 3.0).all()
+    a, _ = c.forward()
+    b, _ = c.forward()
+    assert torch.equal(a, b)        # deterministic: no atomics in the reductions
+
+
+def test_skewed_single_expert_segment():
+    """Nearly all tokens choose expert 0 first: one long segment, many short or
+    empty ones. (A much larger bias would leave the other experts' weights in
+    exact ties near zero, which the tie-free inputs rule out.)"""
+    wl = W("skewed", T=300, H=256, I=256, E=16, K=2, router_bias=True)
+    c = DeviceCase(wl)
+    c.h["router_b"] = c.h["router_b"].copy()
+    c.h["router_b"][0] = 6.0
+    c.d["router_b"] = torch.from_numpy(c.h["router_b"]).cuda()
+    from oracle import cases
+    x, _ = cases.gap_checked_x(wl, 0, c.h["router_w"], c.h["router_b"])
+    c.h["x"] = x
+    c.d["x"] = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    c.ids, c.w, c.p = O.route(x, c.h["router_w"], c.h["router_b"], top_k=2, renormalize=True)
+    assert (c.ids[:, 0] == 0).mean() > 0.9
+    check_forward(c)
