@@ -73,6 +73,7 @@ _SIGS = {
     "moe_route": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "moe_align_workspace_size": (_SZ, [_CFG, _I]),
     "moe_align_permute": (_I, [_CFG, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP, _SZ, _VP]),
+    "moe_align_permute_noalloc": (_I, [_CFG, _I, _VP, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP]),
     "moe_grouped_mlp_workspace_size": (_SZ, [_CFG, _I, _I]),
     "moe_grouped_mlp": (_I, [_CFG, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "moe_combine": (_I, [_CFG, _I, _VP, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
@@ -184,6 +185,15 @@ def moe_align_permute(cfg, T, topk_ids, expert_map, block_m, counts, offsets, so
     _check("moe_align_permute", lib().moe_align_permute(
         ctypes.byref(cfg), T, _p(topk_ids), _p(expert_map), block_m, _p(counts), _p(offsets),
         _p(sorted_ids), _p(inv_pos), cap, _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_align_permute_noalloc(cfg, T, topk_ids, expert_map, block_m, counts, offsets,
+                              sorted_ids, inv_pos, cap, stream=None):
+    """moe_align_permute with its scratch in the library's static device array
+    (for callers that cannot allocate a workspace)."""
+    _check("moe_align_permute_noalloc", lib().moe_align_permute_noalloc(
+        ctypes.byref(cfg), T, _p(topk_ids), _p(expert_map), block_m, _p(counts), _p(offsets),
+        _p(sorted_ids), _p(inv_pos), cap, _stream(stream)))
 
 
 def moe_grouped_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm, ws,

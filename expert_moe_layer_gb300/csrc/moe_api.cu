@@ -544,3 +544,60 @@ int moe_get_status(const void* ws, void* stream, uint32_t* flags) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// moe_align_permute_noalloc: the align/permute launch with its scratch in a
+// static device array instead of a caller workspace (see include/moe.h).
+static __device__ __align__(256) unsigned char moe_align_noalloc_scratch
+    [MOE_ALIGN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};
+
+// Device address of the static scratch on the current device. The host-side
+// name of the array is only a stand-in, so the address is looked up once per
+// device with that device current.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, moe_align_noalloc_scratch) != cudaSuccess || !p)
+      return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" int moe_align_permute_noalloc(const moe_config* cfg, int T, const int32_t* topk_ids,
+                                         const int32_t* expert_map, int block_m,
+                                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids,
+                                         int32_t* inv_pos, int cap, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (block_m < 1 || block_m > 4096) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !counts || !offsets || !sorted_ids || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (cap < 0 || static_cast<size_t>(cap) < moe_align_cap(cfg, T, block_m))
+    return MOE_ERR_WORKSPACE;
+  const AlignLayout L = align_layout(cfg, T);
+  if (L.total > MOE_ALIGN_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  MOE_TRY(noalloc_scratch(&scratch));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = at<unsigned>(scratch, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  // the per-warp counts need no clearing: pass 1 writes every entry it reads
+  const int El = n_local(cfg);
+  return cuda_ok(launch_align(topk_ids, static_cast<long>(T) * cfg->top_k, expert_map,
+                              cfg->num_experts, El, cfg->ep_rank * El, block_m,
+                              at<int>(scratch, L.hist), counts, offsets, sorted_ids, inv_pos,
+                              cap, status, st));
+}

@@ -167,6 +167,40 @@ int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
                       int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
                       int cap, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_align_permute_noalloc: moe_align_permute for callers that cannot
+ * allocate device memory. The source pages have no counterpart to this entry
+ * point; it exists for integration. Some hosts own every byte of device memory
+ * through their own pool and forbid side allocations. Some serving loops must
+ * not pay the implicit synchronisation of cudaMalloc. Some embedded callers
+ * fix their memory budget at start-up. None of them can supply `ws`.
+ *
+ * The per-warp counts and the status word live instead in one scratch array
+ * of MOE_ALIGN_NOALLOC_SCRATCH_BYTES, compiled into the library as a static
+ * device array. Every GPU that loads the library holds that array until the
+ * process exits. This call allocates nothing, on the host or on the device.
+ *   - Arguments and outputs are as moe_align_permute, minus ws/ws_bytes.
+ *   - Results are identical to moe_align_permute.
+ *   - It returns MOE_ERR_WORKSPACE, before any CUDA call, when the scratch
+ *     that (T, top_k, E_local) need, moe_align_workspace_size(cfg, T), exceeds
+ *     MOE_ALIGN_NOALLOC_SCRATCH_BYTES. At 256 local experts that is about
+ *     260k (token, slot) items.
+ *   - The first call on each device looks up the array's device address once
+ *     (cudaGetSymbolAddress with that device current). Make that first call
+ *     before any stream capture.
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Each call clears the status word it uses, and every count it reads is
+ *     rewritten first. Calls that can overlap on the GPU (different streams
+ *     without ordering, or several host threads) race on the array and must
+ *     be serialised by the caller.
+ *   - Device flags (MOE_DEV_*) land in the shared array and are not reported.
+ *     Out-of-range expert ids are still dropped, exactly as moe_align_permute
+ *     drops them. */
+#define MOE_ALIGN_NOALLOC_SCRATCH_BYTES (1u << 20)
+int moe_align_permute_noalloc(const moe_config* cfg, int T, const int32_t* topk_ids,
+                              const int32_t* expert_map, int block_m, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
+                              int cap, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* moe_grouped_mlp: the local experts' SiLU-gated MLPs on permuted rows.
  * For every row r of segment e with sorted_ids[r] < T*K:
