@@ -19,9 +19,9 @@ using Tile = int4;
 struct GemmArgs {
   const CUtensorMap* mapA;     // weights, 2-D [slabs*rows_per_slab, K]
   const CUtensorMap* mapB;     // token rows, 2-D [rows, K]
-  const Tile* tiles;           // tile table
-  const int* num_tiles_dev;    // tile count on the device, or nullptr
-  int num_tiles_host;          // used when num_tiles_dev == nullptr
+  const Tile* tiles;           // tile table, grouped (one group per expert / slab)
+  const int* group_start;      // [n_groups+1] first tile of each group; [n_groups] = total
+  int n_groups;                // <= 1024
   int m_tiles;                 // 128-row weight tiles per expert
   int k_blocks;                // K / (128 bytes of K)
   int a_rows_per_expert;       // weight rows per expert slab
@@ -62,11 +62,13 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                          int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
                          unsigned* status, cudaStream_t st);
 
-// Tile tables.
+// Tile tables. group_start gets n_groups+1 ints (the routed table has one
+// group per local expert; the dense table one group per slab).
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l,
-                               int nmax, Tile* tiles, int* num_tiles, int max_tiles,
+                               int nmax, Tile* tiles, int* group_start, int max_tiles,
                                unsigned* status, cudaStream_t st);
-cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, cudaStream_t st);
+cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, int* group_start,
+                               cudaStream_t st);
 inline int dense_tile_count(int T, int S, int nmax) { return S * ((T + nmax - 1) / nmax); }
 inline long routed_tile_bound(long n_items, int E_l, int nmax) {
   return n_items / nmax + E_l + 1;

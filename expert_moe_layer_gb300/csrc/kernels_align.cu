@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ offsets,
                                                            int E_l, int nmax, Tile* __restrict__ tiles,
-                                                           int* __restrict__ num_tiles,
+                                                           int* __restrict__ group_start,
                                                            int max_tiles, unsigned* status) {
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
@@ -204,18 +204,21 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
       tiles[idx] = make_int4(e, r0, r0, rows);
     }
   }
+  if (e < E_l) group_start[e] = start < max_tiles ? start : max_tiles;
   if (threadIdx.x == blockDim.x - 1) {
     const int total = incl;
     if (total > max_tiles && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
-    *num_tiles = total < max_tiles ? total : max_tiles;
+    group_start[E_l] = total < max_tiles ? total : max_tiles;
   }
 }
 
 // Tile table over all T tokens for each of S weight slabs (shared experts,
 // router): slab s, tokens [t0, t0+rows): B row t0, output row s*T + t0.
-__global__ void dense_tiles_kernel(int T, int S, int nmax, Tile* __restrict__ tiles) {
+__global__ void dense_tiles_kernel(int T, int S, int nmax, Tile* __restrict__ tiles,
+                                   int* __restrict__ group_start) {
   const int per = (T + nmax - 1) / nmax;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i <= S) group_start[i] = i * per;
   if (i >= S * per) return;
   const int s = i / per, j = i - s * per;
   const int t0 = j * nmax;
@@ -338,17 +341,19 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
 }
 
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l, int nmax,
-                               Tile* tiles, int* num_tiles, int max_tiles, unsigned* status,
+                               Tile* tiles, int* group_start, int max_tiles, unsigned* status,
                                cudaStream_t st) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(counts, offsets, E_l, nmax, tiles, num_tiles,
+  build_tiles_kernel<<<1, 1024, 0, st>>>(counts, offsets, E_l, nmax, tiles, group_start,
                                          max_tiles, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, cudaStream_t st) {
+cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, int* group_start,
+                               cudaStream_t st) {
   const int n = dense_tile_count(T, S, nmax);
   if (n <= 0) return cudaSuccess;
-  dense_tiles_kernel<<<(n + 255) / 256, 256, 0, st>>>(T, S, nmax, tiles);
+  const int threads = n > S + 1 ? n : S + 1;
+  dense_tiles_kernel<<<(threads + 255) / 256, 256, 0, st>>>(T, S, nmax, tiles, group_start);
   return cudaGetLastError();
 }
 

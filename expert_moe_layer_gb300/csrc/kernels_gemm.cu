@@ -18,9 +18,12 @@
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
 // overlaps the main loop of the next.
 //
-// Work unit u -> (m = u / num_tiles, tile = u % num_tiles): all token tiles
-// of one weight tile are adjacent in u, so concurrently running CTAs share
-// each weight tile through L2.
+// Work units are ordered group by group (a group = one expert's tiles, or one
+// shared-expert slab), then by weight tile m, then by token tile. CTAs running
+// at the same time therefore work on one expert. The 128-row weight tiles of
+// that expert are read from DRAM once and shared by its token tiles through
+// L2. The expert's token rows stay resident in L2 while all its weight tiles
+// stream past them.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -39,15 +42,16 @@ struct GemmShape {
   static constexpr int kStageBytes = kNA * kABytes + kBBytes;
   static constexpr int kStages0 = (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kAccCols = kNA * NMAX;           // fp32 columns per buffer
-  static constexpr int kNAcc = 2;                        // TMEM accumulator buffers
+  static constexpr int kAccCols = kNA * NMAX;            // fp32 columns per buffer
+  static constexpr int kNAcc = kAccCols <= 256 ? 2 : 1;  // TMEM accumulator buffers
   static constexpr int kTmemNeed = kAccCols * kNAcc;
   static constexpr int kTmemCols = kTmemNeed <= 32    ? 32
                                    : kTmemNeed <= 64  ? 64
                                    : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256
                                                       : 512;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16;
+  static constexpr int kMaxGroups = 1024;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16 + 4 * (kMaxGroups + 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
   static_assert(kTmemNeed <= 512, "TMEM overflow");
   static_assert(kStages >= 2, "need at least two stages");
@@ -65,19 +69,35 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// Unit u -> (tile index, weight tile m). gstart (shared memory) holds the
+// first tile of each group and the total at [n_groups]; group g owns units
+// [gstart[g]*m_tiles, gstart[g+1]*m_tiles), ordered m-major inside the group.
+__device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_groups, int m_tiles,
+                                            int& tile, int& m) {
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {  // last group whose first unit is <= u (skips empty groups)
+    const int mid = (lo + hi + 1) >> 1;
+    if (gstart[mid] * m_tiles <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int n = gstart[lo + 1] - gstart[lo];
+  const int r = u - gstart[lo] * m_tiles;
+  m = r / n;
+  tile = gstart[lo] + (r - m * n);
+}
+
 template <int MODE, bool TF32, typename TOut, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap mapA,
                 const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
-                const int* __restrict__ num_tiles_dev, int num_tiles_host, int m_tiles,
+                const int* __restrict__ group_start, int n_groups, int m_tiles,
                 int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
                 TOut* __restrict__ out, long out_ld, int m_valid, unsigned* status) {
   using S = GemmShape<MODE, NMAX>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
 
-  const int num_tiles = num_tiles_dev ? *num_tiles_dev : num_tiles_host;
-  const int total = num_tiles * m_tiles;
+  const int total = group_start[n_groups] * m_tiles;
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
 
   extern __shared__ uint8_t smem_raw[];
@@ -92,6 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain = tempty0 + 8 * S::kNAcc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 2 * S::kNAcc + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
+  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -127,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const int m = u / num_tiles;
-        const Tile tl = tiles[u - m * num_tiles];
-        const int a_row = tl.x * a_rows_per_expert + m * 128;
+        int ti, m;
+        decode_unit(u, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tiles[ti];
         const int b_row = b_from_out ? tl.z : tl.y;
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
           const int s = it % S::kStages;
@@ -140,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t st = sbase + s * S::kStageBytes;
           ptx::mbar_arrive_expect_tx(full0 + 8 * s, S::kStageBytes);
+          const int a_row = tl.x * a_rows_per_expert + m * 128;
           ptx::tma_load_2d(st, &mapA, full0 + 8 * s, kb * kKe, a_row);
           if (MODE == kGemmSiluUp)
             ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, kb * kKe,
@@ -162,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, ai = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
-        const int m = u / num_tiles;
-        const Tile tl = tiles[u - m * num_tiles];
+        int ti, m;
+        decode_unit(u, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tiles[ti];
         const int n_mma = (tl.w + 15) & ~15;
         const uint32_t idesc = ptx::idesc_make(kAB, 128, n_mma);
         const int b = ai % S::kNAcc;
@@ -210,15 +234,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int ai = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
-      const int m = u / num_tiles;
-      const Tile tl = tiles[u - m * num_tiles];
+      int ti, m;
+      decode_unit(u, gstart, n_groups, m_tiles, ti, m);
+      const Tile tl = tiles[ti];
       const int b = ai % S::kNAcc;
       const uint32_t aph = (ai / S::kNAcc) & 1;
       if (!ptx::mbar_wait(tfull0 + 8 * b, aph, abort_flag, status)) break;
       ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       const int row = m * 128 + q * 32 + lane;
       const bool row_ok = row < m_valid;
-      const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
       for (int c0 = 0; c0 < tl.w; c0 += 16) {
         float v[16];
@@ -262,7 +287,7 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
     configured = true;
   }
   kern<<<num_sms, kThreads, S::kSmemBytes, st>>>(
-      *a.mapA, *a.mapB, a.tiles, a.num_tiles_dev, a.num_tiles_host, a.m_tiles, a.k_blocks,
+      *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups, a.m_tiles, a.k_blocks,
       a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out), a.out_ld,
       a.m_valid, a.status);
   return cudaGetLastError();
@@ -271,14 +296,26 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
 }  // namespace
 
 size_t gemm_smem_bytes(GemmMode mode, int nmax) {
-  if (mode == kGemmSiluUp) return nmax == 128 ? GemmShape<0, 128>::kSmemBytes
-                                              : GemmShape<0, 32>::kSmemBytes;
-  return nmax == 128 ? GemmShape<1, 128>::kSmemBytes : GemmShape<1, 32>::kSmemBytes;
+  if (mode == kGemmSiluUp)
+    return nmax == 256   ? GemmShape<0, 256>::kSmemBytes
+           : nmax == 128 ? GemmShape<0, 128>::kSmemBytes
+                         : GemmShape<0, 32>::kSmemBytes;
+  return nmax == 256   ? GemmShape<1, 256>::kSmemBytes
+         : nmax == 128 ? GemmShape<1, 128>::kSmemBytes
+                       : GemmShape<1, 32>::kSmemBytes;
 }
 
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
-  if (nmax != 32 && nmax != 128) return cudaErrorInvalidValue;
+  if (nmax != 32 && nmax != 128 && nmax != 256) return cudaErrorInvalidValue;
+  if (nmax == 256) {  // prefill-sized segments, bf16 only
+    if (tf32) return cudaErrorInvalidValue;
+    if (mode == kGemmSiluUp)
+      return launch_variant<kGemmSiluUp, false, __nv_bfloat16, 256>(a, num_sms, st);
+    if (mode == kGemmPlain)
+      return launch_variant<kGemmPlain, false, __nv_bfloat16, 256>(a, num_sms, st);
+    return cudaErrorInvalidValue;
+  }
   const bool big = nmax == 128;
   switch (mode) {
     case kGemmSiluUp:

@@ -73,6 +73,52 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
   }
 }
 
+// Token-major variant for small E (<= 32): warp = one token, all experts in
+// chunks of 8. The token's row is read once per chunk (once for E <= 8); the
+// router rows stay in L1/L2.
+template <typename TX, typename TW>
+__global__ void __launch_bounds__(256) router_logits_token_kernel(const TX* __restrict__ x,
+                                                                  const TW* __restrict__ wg,
+                                                                  float* __restrict__ logits,
+                                                                  int T, int E, int H) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long t = blockIdx.x * 8L + warp;
+  if (t >= T) return;
+  const TX* xrow = x + t * H;
+  for (int e0 = 0; e0 < E; e0 += 8) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int h = lane * 8; h < H; h += 256) {
+      float xv[8];
+      load8(xrow + h, xv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (e0 + j < E) {
+          float w[8];
+          load8(wg + static_cast<long>(e0 + j) * H + h, w);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[j] = fmaf(xv[i], w[i], acc[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float v = acc[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[j] = v;
+    }
+    if (lane < 8 && e0 + lane < E) {
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j == lane) v = acc[j];
+      logits[t * E + e0 + lane] = v;
+    }
+  }
+}
+
 // --------------------------------------------------------------- top-k
 // One warp per token. Lane l holds experts e = l + 32*j (j < VPL).
 // Ordering: larger value first, equal values -> lower index first.
@@ -204,6 +250,22 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
                                  const void* wg, float* logits, int T, int E, int H,
                                  cudaStream_t st) {
+  if (E <= 32) {
+    const int grid = (T + 7) / 8;
+    if (act_bf16 && router_bf16)
+      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                        static_cast<const __nv_bfloat16*>(wg),
+                                                        logits, T, E, H);
+    else if (act_bf16)
+      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
+                                                        static_cast<const float*>(wg), logits,
+                                                        T, E, H);
+    else
+      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x),
+                                                        static_cast<const float*>(wg), logits,
+                                                        T, E, H);
+    return cudaGetLastError();
+  }
   dim3 grid((E + 7) / 8, (T + kTok - 1) / kTok);
   if (act_bf16 && router_bf16)
     router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),

@@ -47,6 +47,7 @@ int validate_cfg(const moe_config* c) {
   if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED;
   if (c->use_grouped_topk && c->num_expert_group > 32) return MOE_ERR_UNSUPPORTED;
   if (E / c->ep_size > 1024) return MOE_ERR_UNSUPPORTED;
+  if (c->num_shared_experts > 1024) return MOE_ERR_UNSUPPORTED;
   if (c->act_dtype == MOE_F32 && c->router_dtype == MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -55,10 +56,15 @@ int validate_T(int T) { return (T < 0 || T > kMaxT) ? MOE_ERR_INVALID_ARG : MOE_
 
 int n_local(const moe_config* c) { return c->num_experts / c->ep_size; }
 
-// Token tile (MMA N) of the routed GEMMs: 128 when segments average at least
-// 48 rows, else 32.
+// Token tile (MMA N) of the routed GEMMs, from the average segment length:
+// 256 (bf16) from 192 rows when that still leaves >= 512 GEMM1 work units
+// (several per SM), 128 from 48 rows, else 32. A larger N means more FLOPs
+// per byte staged into shared memory; more units mean better balance.
 int routed_nmax(const moe_config* c, int T) {
   const long avg = static_cast<long>(T) * c->top_k / c->num_experts;
+  const long local_items = static_cast<long>(T) * c->top_k / c->ep_size;
+  const long units256 = (local_items / 256) * (c->intermediate_size / 128);
+  if (avg >= 192 && c->act_dtype == MOE_BF16 && units256 >= 512) return 256;
   return avg >= 48 ? 128 : 32;
 }
 int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
@@ -122,7 +128,7 @@ bool make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long co
 // One grouped GEMM launch. A = weights [slabs*rows_per_slab, Kdim]; B = token
 // rows [b_rows, Kdim].
 int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, const void* B,
-             long b_rows, int Kdim, const Tile* tiles, const int* nt_dev, int nt_host,
+             long b_rows, int Kdim, const Tile* tiles, const int* group_start, int n_groups,
              int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
              int m_valid, unsigned* status, cudaStream_t st) {
   CUtensorMap ma, mb;
@@ -132,8 +138,8 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.mapA = &ma;
   g.mapB = &mb;
   g.tiles = tiles;
-  g.num_tiles_dev = nt_dev;
-  g.num_tiles_host = nt_host;
+  g.group_start = group_start;
+  g.n_groups = n_groups;
   g.m_tiles = m_tiles;
   g.k_blocks = Kdim * ebytes(dt) / 128;
   g.a_rows_per_expert = rows_per_slab;
@@ -160,7 +166,7 @@ struct Carver {
 };
 
 struct RouteLayout {
-  size_t status, logits, rtiles, total;
+  size_t status, logits, rtiles, rgroups, total;
 };
 RouteLayout route_layout(const moe_config* c, int T) {
   Carver cv;
@@ -168,6 +174,7 @@ RouteLayout route_layout(const moe_config* c, int T) {
   L.status = cv.take(4);
   L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
   L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
+  L.rgroups = cv.take(sizeof(int) * 2);
   L.total = cv.off;
   return L;
 }
@@ -186,7 +193,7 @@ AlignLayout align_layout(const moe_config* c, int T) {
 }
 
 struct MlpLayout {
-  size_t status, tiles, ntiles, x_perm, h_perm, total;
+  size_t status, tiles, groups, x_perm, h_perm, total;
 };
 MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   Carver cv;
@@ -194,7 +201,7 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   const size_t eb = ebytes(c->act_dtype);
   L.status = cv.take(4);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
-  L.ntiles = cv.take(sizeof(int));
+  L.groups = cv.take(sizeof(int) * static_cast<size_t>(n_local(c) + 1));
   L.x_perm = cv.take(eb * static_cast<size_t>(cap) * c->hidden_size);
   L.h_perm = cv.take(eb * static_cast<size_t>(cap) * c->intermediate_size);
   L.total = cv.off;
@@ -202,8 +209,8 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
 }
 
 struct FwdLayout {
-  size_t status, topk_ids, topk_w, logits, rtiles, hist, counts, offsets, sorted_ids, inv_pos;
-  size_t tiles, ntiles, stiles, x_perm, h_perm, y_perm, h_sh, y_sh, total;
+  size_t status, topk_ids, topk_w, logits, rtiles, rgroups, hist, counts, offsets, sorted_ids;
+  size_t inv_pos, tiles, groups, stiles, sgroups, x_perm, h_perm, y_perm, h_sh, y_sh, total;
   int cap;
 };
 FwdLayout fwd_layout(const moe_config* c, int T) {
@@ -219,14 +226,16 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.topk_w = cv.take(4 * TK);
   L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
   L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
+  L.rgroups = cv.take(sizeof(int) * 2);
   L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(TK)) * El);
   L.counts = cv.take(4 * static_cast<size_t>(El));
   L.offsets = cv.take(4 * static_cast<size_t>(El + 1));
   L.sorted_ids = cv.take(4 * static_cast<size_t>(L.cap));
   L.inv_pos = cv.take(4 * TK);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
-  L.ntiles = cv.take(sizeof(int));
+  L.groups = cv.take(sizeof(int) * static_cast<size_t>(El + 1));
   L.stiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, S, dense_nmax(T))));
+  L.sgroups = cv.take(sizeof(int) * static_cast<size_t>(S + 1));
   L.x_perm = cv.take(eb * L.cap * c->hidden_size);
   L.h_perm = cv.take(eb * L.cap * c->intermediate_size);
   L.y_perm = cv.take(eb * L.cap * c->hidden_size);
@@ -243,6 +252,19 @@ P* at(void* ws, size_t off) {
 
 int cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Record a caller's timing event on `st`. Under stream capture the event
+// becomes an event-record node, so a replayed graph still timestamps stages.
+int record_event(void* ev, cudaStream_t st) {
+  if (!ev) return MOE_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t e =
+      cs == cudaStreamCaptureStatusActive
+          ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, cudaEventRecordExternal)
+          : cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 #define MOE_TRY(x)              \
   do {                          \
     const int _rc = (x);        \
@@ -251,14 +273,13 @@ int cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // ------------------------------------------------------------- stage bodies
 int do_route(const moe_config* c, int T, const void* x, const void* router_w,
-             const float* bias, int32_t* ids, float* w, float* logits, Tile* rtiles,
+             const float* bias, int32_t* ids, float* w, float* logits, Tile* rtiles, int* rgroups,
              unsigned* status, cudaStream_t st) {
   const int E = c->num_experts, H = c->hidden_size;
   if (router_on_tensor_cores(c, T)) {
-    MOE_TRY(cuda_ok(launch_dense_tiles(T, 1, 128, rtiles, st)));
-    MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, 128, router_w, E, x, T, H, rtiles, nullptr,
-                     dense_tile_count(T, 1, 128), (E + 127) / 128, 0, 0, 0, logits, E, E,
-                     status, st));
+    MOE_TRY(cuda_ok(launch_dense_tiles(T, 1, 128, rtiles, rgroups, st)));
+    MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, 128, router_w, E, x, T, H, rtiles, rgroups, 1,
+                     (E + 127) / 128, 0, 0, 0, logits, E, E, status, st));
   } else {
     MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
                                          x, router_w, logits, T, E, H, st)));
@@ -270,21 +291,21 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
 
 int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
-           const void* w2, void* y_perm, Tile* tiles, int* ntiles, void* x_perm, void* h_perm,
+           const void* w2, void* y_perm, Tile* tiles, int* groups, void* x_perm, void* h_perm,
            unsigned* status, cudaStream_t st, void* const* ev = nullptr) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
-  MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, ntiles,
+  MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
                                      static_cast<int>(max_routed_tiles(c, T)), status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
                                 n_items, K, H, x_perm, st)));
-  if (ev && ev[0]) MOE_TRY(cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st)));
+  if (ev) MOE_TRY(record_event(ev[0], st));
   MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
-                   cap, H, tiles, ntiles, 0, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
-  if (ev && ev[1]) MOE_TRY(cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), st)));
+                   cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
+  if (ev) MOE_TRY(record_event(ev[1], st));
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
-                   tiles, ntiles, 0, H / 128, H, 0, 0, y_perm, H, H, status, st));
+                   tiles, groups, El, H / 128, H, 0, 0, y_perm, H, H, status, st));
   return MOE_OK;
 }
 
@@ -335,7 +356,7 @@ int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
   unsigned* status = at<unsigned>(ws, L.status);
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return do_route(cfg, T, x, router_w, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
-                  at<Tile>(ws, L.rtiles), status, st);
+                  at<Tile>(ws, L.rtiles), at<int>(ws, L.rgroups), status, st);
 }
 
 size_t moe_align_workspace_size(const moe_config* cfg, int T) {
@@ -388,7 +409,7 @@ int moe_grouped_mlp(const moe_config* cfg, int T, const void* x, const int32_t* 
   unsigned* status = at<unsigned>(ws, L.status);
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return do_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm,
-                at<Tile>(ws, L.tiles), at<int>(ws, L.ntiles), at<void>(ws, L.x_perm),
+                at<Tile>(ws, L.tiles), at<int>(ws, L.groups), at<void>(ws, L.x_perm),
                 at<void>(ws, L.h_perm), status, st);
 }
 
@@ -454,10 +475,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  auto mark = [&](int i) -> int {
-    if (!events || !events[i]) return MOE_OK;
-    return cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st));
-  };
+  auto mark = [&](int i) -> int { return events ? record_event(events[i], st) : MOE_OK; };
   const int El = n_local(cfg), H = cfg->hidden_size, K = cfg->top_k;
   unsigned* status = at<unsigned>(ws, L.status);
   int32_t* ids = at<int32_t>(ws, L.topk_ids);
@@ -471,7 +489,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   MOE_TRY(mark(0));
   MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
-                   at<Tile>(ws, L.rtiles), status, st));
+                   at<Tile>(ws, L.rtiles), at<int>(ws, L.rgroups), status, st));
   n += router_on_tensor_cores(cfg, T) ? 3 : 2;
   MOE_TRY(mark(1));
   MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts, El,
@@ -480,7 +498,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   n += 3;
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
-                 at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.ntiles),
+                 at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
                  at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), status, st,
                  events ? events + 3 : nullptr));
   n += 4;
@@ -491,16 +509,16 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     S = cfg->num_shared_experts;
     const int Is = cfg->shared_intermediate_size;
     const int nm = dense_nmax(T);
-    const int nt = dense_tile_count(T, S, nm);
     Tile* stl = at<Tile>(ws, L.stiles);
+    int* sgr = at<int>(ws, L.sgroups);
     void* h_sh = at<void>(ws, L.h_sh);
     void* y_sh = at<void>(ws, L.y_sh);
-    MOE_TRY(cuda_ok(launch_dense_tiles(T, S, nm, stl, st)));
+    MOE_TRY(cuda_ok(launch_dense_tiles(T, S, nm, stl, sgr, st)));
     MOE_TRY(run_gemm(kGemmSiluUp, cfg->act_dtype, nm, shared_w13, static_cast<long>(S) * 2 * Is,
-                     x, T, H, stl, nullptr, nt, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
+                     x, T, H, stl, sgr, S, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
                      st));
     MOE_TRY(run_gemm(kGemmPlain, cfg->act_dtype, nm, shared_w2, static_cast<long>(S) * H, h_sh,
-                     static_cast<long>(S) * T, Is, stl, nullptr, nt, H / 128, H, 0, 1, y_sh, H,
+                     static_cast<long>(S) * T, Is, stl, sgr, S, H / 128, H, 0, 1, y_sh, H,
                      H, status, st));
     shared_y = y_sh;
     n += 3;

@@ -114,7 +114,7 @@ const char* moe_strerror(int status);
  * (E % n_group == 0, 1 <= topk_group <= n_group, K <= topk_group*E/n_group),
  * H and I multiples of 128, S >= 0 with I_s a multiple of 128 when S > 0.
  * Kernel limits (MOE_ERR_UNSUPPORTED): E <= 512, K <= 32, n_group <= 32,
- * E_local <= 1024, and act_dtype F32 needs router_dtype F32. */
+ * E_local <= 1024, S <= 1024, and act_dtype F32 needs router_dtype F32. */
 int moe_validate_config(const moe_config* cfg);
 
 /* Rows of the padded permutation buffers for T tokens and segment padding
@@ -283,7 +283,9 @@ int moe_forward(const moe_config* cfg, int T, const void* x,
  *   [3] after the tile table and row gather  [4] after GEMM1 (SiLU*up)
  *   [5] after GEMM2  [6] after the shared experts  [7] after combine.
  * kernels_launched (nullable): number of kernels this call launched. The
- * results are identical to moe_forward. */
+ * results are identical to moe_forward. When `stream` is being captured into a
+ * CUDA graph, the events are recorded as external event nodes
+ * (cudaEventRecordExternal), so every replay timestamps the stages. */
 int moe_forward_timed(const moe_config* cfg, int T, const void* x,
                       const void* router_w, const float* router_bias,
                       const void* w13, const void* w2, const void* shared_w13,

@@ -32,6 +32,8 @@ SMALL = {
                     x_std=0.3),
     "k_equals_e": W("k_equals_e", T=40, H=128, I=128, E=8, K=8),
     "single_token": W("single_token", T=1, H=256, I=256, E=32, K=4, router_bias=True),
+    # segments averaging >= 192 rows: the 256-row token tiles
+    "wide_prefill": W("wide_prefill", T=1100, H=256, I=384, E=5, K=1),
 }
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
@@ -248,3 +250,26 @@ def test_skewed_single_expert_segment():
     c.ids, c.w, c.p = O.route(x, c.h["router_w"], c.h["router_b"], top_k=2, renormalize=True)
     assert (c.ids[:, 0] == 0).mean() > 0.9
     check_forward(c)
+
+
+@pytest.mark.parametrize("name", ["ragged_decode", "grouped_shared"])
+def test_forward_captured_in_cuda_graph_matches_eager(name):
+    """moe_forward enqueues only stream work (no host sync, no allocation), so
+    it can be captured once and replayed; replays must equal the eager call."""
+    c = case(name)
+    wl, d = c.wl, c.d
+    eager, _ = c.forward()
+    ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    out = torch.zeros_like(eager)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        B.moe_forward(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"], d["w2"],
+                      d["shared_w13"], d["shared_w2"], None, out, ws, s)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert B.moe_get_status(ws) == (0, 0)
