@@ -344,13 +344,18 @@ def run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world):
 
 
 def traffic_from_profile(workload):
-    """DRAM bytes per GEMM1 launch from the committed ncu summary, if any."""
+    """DRAM bytes per GEMM1 launch from the committed ncu summary, or None when
+    there is none for this workload or the GEMM source changed since."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    v = d.get(workload)
+    with open(os.path.join(ROOT, d["kernel_source"]), "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != d["kernel_sha256"]:
+            return None
+    v = d["workloads"].get(workload)
     return None if v is None else v.get("dram_bytes_per_launch")
 
 
