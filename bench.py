@@ -209,21 +209,25 @@ def run_ours(args, wl, rank, world, device):
     eager_ms = statistics.mean(eager_ev[i][0].elapsed_time(eager_ev[i][7])
                                for i in range(args.steps))
 
-    # Timed region: the K steps (L2 flush + layer forward) are captured into one
-    # CUDA graph and replayed once, as a serving engine replays its layers.
-    # The library records each step's stage events as graph nodes.
-    events = new_events(args.steps)
-    graph = torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream(device)
-    cap_stream.wait_stream(stream)
-    torch.cuda.synchronize(device)
-    launches = 0
-    with torch.cuda.graph(graph, stream=cap_stream):
-        for i in range(args.steps):
-            flush.zero_()
-            launches += fwd(events[i])
-    torch.cuda.synchronize(device)
+    def capture(evs):
+        g = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream(device)
+        cap_stream.wait_stream(stream)
+        torch.cuda.synchronize(device)
+        n = 0
+        with torch.cuda.graph(g, stream=cap_stream):
+            for i in range(args.steps):
+                flush.zero_()
+                n += fwd(evs[i])
+        torch.cuda.synchronize(device)
+        return g, n
 
+    # Timed region: the K steps (L2 flush + layer forward) are captured into one
+    # CUDA graph and replayed once, as a serving engine replays its layers. The
+    # library records only each step's start and end events, as graph nodes.
+    events = new_events(args.steps)
+    edges = [[ev[0], None, None, None, None, None, None, ev[7]] for ev in events]
+    graph, launches = capture(edges)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
@@ -236,11 +240,20 @@ def run_ours(args, wl, rank, world, device):
     rc, flags = B.moe_get_status(ws, stream)
     if rc != 0:
         raise RuntimeError(f"device status {rc} flags {flags:#x} in the timed region")
+    step_ms = [events[i][0].elapsed_time(events[i][7]) for i in range(args.steps)]
+    del graph
+
+    # Per-stage breakdown (and the dominant kernel's live duration): a second
+    # graph of the same K steps with events at every stage boundary.
+    sevents = new_events(args.steps)
+    sgraph, _ = capture(sevents)
+    sgraph.replay()
+    torch.cuda.synchronize(device)
+    del sgraph
 
     def span(a, b):
-        return [events[i][a].elapsed_time(events[i][b]) for i in range(args.steps)]
+        return [sevents[i][a].elapsed_time(sevents[i][b]) for i in range(args.steps)]
 
-    step_ms = span(0, 7)
     total_ms = sum(step_ms)
     stage_names = ["route", "align", "tiles_gather", "gemm1_silu", "gemm2", "shared", "combine"]
     stages = {n: statistics.mean(span(i, i + 1)) for i, n in enumerate(stage_names)}
@@ -300,8 +313,10 @@ def run_ours(args, wl, rank, world, device):
         "gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
         "alg_flops_per_step": flops, "alg_bytes_per_step": alg_bytes,
         "stages_ms": {k: round(v, 4) for k, v in stages.items()},
-        "timing": "one CUDA graph of the K steps replayed once; stage and step times from "
-                  "CUDA events recorded by the library on the launching stream",
+        "timing": "one CUDA graph of the K steps replayed once; step times from CUDA events "
+                  "the library records at each step's start and end; stage times from a "
+                  "second graph with events at every stage boundary",
+        "staged_ms_per_step": round(statistics.mean(span(0, 7)), 4),
         "eager_ms_per_step": round(eager_ms, 4),
         "roofline": roof,
         "e2e": e2e,

@@ -19,11 +19,15 @@ using Tile = int4;
 struct GemmArgs {
   const CUtensorMap* mapA;     // weights, 2-D [slabs*rows_per_slab, K]
   const CUtensorMap* mapB;     // token rows, 2-D [rows, K]
-  const Tile* tiles;           // tile table, grouped (one group per expert / slab)
+  const Tile* tiles;           // tile table, grouped (one group per expert), or nullptr:
+                               //   dense tiles over dense_T tokens per slab, implicit
   const int* group_start;      // [n_groups+1] first tile of each group; [n_groups] = total
-  int n_groups;                // <= 1024
+  int n_groups;                // <= 1024 (experts, or dense slabs)
+  int dense_T = 0;             // tokens per slab when tiles == nullptr
   int m_tiles;                 // 128-row weight tiles per expert
   int k_blocks;                // K / (128 bytes of K)
+  int k_split = 1;             // K ranges per tile (router logits only); partial
+  long split_stride = 0;       //   sums go to out + ks * split_stride
   int a_rows_per_expert;       // weight rows per expert slab
   int a_up_offset;             // row offset of the "up" half (SiLU mode)
   int b_from_out;              // 1: B row = tile.z instead of tile.y
@@ -51,24 +55,30 @@ cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
                                  cudaStream_t st);
 
 // Softmax + (grouped) top-k + renormalise on fp32 logits (+ bias if given).
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int K,
+// logits = sum of n_part partial slabs, partial_stride floats apart.
+cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
+                        const float* bias, int T, int E, int K,
                         int renorm, int n_group, int topk_group, int32_t* ids,
                         float* w, unsigned* status, cudaStream_t st);
 
 // Alignment / permutation. hist has n_warps*E_l ints, n_warps = align_warps(T*K).
+// Small inputs run as one fused kernel (hist unused), larger ones as three.
+int align_kernel_count(long n_items, int E_l);
 int align_warps(long n_items);
+// With tiles != nullptr the align kernels also write the routed tile table
+// (token chunks of nmax per local expert) and its group_start, as
+// launch_build_tiles would.
 cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, int E,
                          int E_l, int ep_start, int block_m, int* hist, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
-                         unsigned* status, cudaStream_t st);
+                         unsigned* status, cudaStream_t st, Tile* tiles = nullptr,
+                         int* group_start = nullptr, int nmax = 0, int max_tiles = 0);
 
-// Tile tables. group_start gets n_groups+1 ints (the routed table has one
-// group per local expert; the dense table one group per slab).
+// Routed tile table: group_start gets E_l+1 ints, one group per local expert.
+// (Dense problems need no table: the GEMM derives their tiles from T.)
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l,
                                int nmax, Tile* tiles, int* group_start, int max_tiles,
                                unsigned* status, cudaStream_t st);
-cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, int* group_start,
-                               cudaStream_t st);
 inline int dense_tile_count(int T, int S, int nmax) { return S * ((T + nmax - 1) / nmax); }
 inline long routed_tile_bound(long n_items, int E_l, int nmax) {
   return n_items / nmax + E_l + 1;

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -39,11 +40,61 @@ __device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ 
   return le;
 }
 
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  __syncthreads();  // warp_sums may still be read by a previous scan
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  return incl - v;
+}
+
+// Block-wide: the routed tile table from each expert's count c and first
+// row off (thread e < E_l; other threads pass c = 0). Called by every thread.
+__device__ __forceinline__ void write_tile_table(int e, int E_l, int c, int off, int nmax,
+                                                 Tile* __restrict__ tiles,
+                                                 int* __restrict__ group_start, int max_tiles,
+                                                 int* warp_sums, unsigned* status) {
+  const int n = e < E_l ? (c + nmax - 1) / nmax : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(n, warp_sums, total);
+  for (int j = 0; j < n; ++j) {
+    const int idx = start + j;
+    if (idx < max_tiles) {
+      const int r0 = off + j * nmax;
+      tiles[idx] = make_int4(e, r0, r0, min(nmax, c - j * nmax));
+    }
+  }
+  if (e < E_l) group_start[e] = min(start, max_tiles);
+  if (threadIdx.x == 0) {
+    group_start[E_l] = min(total, max_tiles);
+    if (total > max_tiles && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+  }
+}
+
 // Pass 1: per-warp expert counts; also fills sorted_ids with the sentinel.
 __global__ void __launch_bounds__(256) align_count_kernel(
     const int32_t* __restrict__ ids, long n_items, const int32_t* __restrict__ emap, int E,
     int E_l, int ep_start, int* __restrict__ hist, int n_warps, int32_t* __restrict__ sorted_ids,
     int cap, unsigned* status) {
+  pdl_enter();
   extern __shared__ int cnt[];  // [kWarpsPerBlock][E_l]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (long r = blockIdx.x * 256L + threadIdx.x; r < cap; r += 256L * gridDim.x)
@@ -71,12 +122,18 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
                                                           int E_l, int block_m,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets,
-                                                          int cap, unsigned* status) {
+                                                          int cap, unsigned* status,
+                                                          Tile* __restrict__ tiles,
+                                                          int* __restrict__ group_start,
+                                                          int nmax, int max_tiles) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
   int c = 0;
-  if (e < E_l)
+  if (e < E_l) {
+#pragma unroll 8
     for (int w = 0; w < n_warps; ++w) c += hist[static_cast<long>(w) * E_l + e];
+  }
   const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
   // block-wide inclusive scan of padded
   int v = padded;
@@ -108,6 +165,7 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
       if (incl > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
     }
     int run = start;
+#pragma unroll 8
     for (int w = 0; w < n_warps; ++w) {
       const long idx = static_cast<long>(w) * E_l + e;
       const int h = hist[idx];
@@ -115,6 +173,9 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
       run += h;
     }
   }
+  if (tiles)
+    write_tile_table(e, E_l, e < E_l ? c : 0, incl - padded, nmax, tiles, group_start,
+                     max_tiles, warp_sums, status);
 }
 
 // Pass 3: stable scatter of item ids into their segments.
@@ -123,6 +184,7 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
     int E_l, int ep_start, const int* __restrict__ hist, int n_warps,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
     unsigned* status) {
+  pdl_enter();
   extern __shared__ int run[];  // [kWarpsPerBlock][E_l]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kWarpsPerBlock + warp;
@@ -157,12 +219,95 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
   }
 }
 
+// Small inputs (n_items <= kSmallItems, E_l <= kSmallExperts): the three
+// passes above in one CTA of 32 warps, counts kept in shared memory. The same
+// walk order gives the same stable result.
+constexpr int kSmallItems = 32 * 256;
+constexpr int kSmallExperts = 256;
+
+__global__ void __launch_bounds__(1024) align_small_kernel(
+    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
+    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
+    int* __restrict__ group_start, int nmax, int max_tiles) {
+  pdl_enter();
+  __shared__ int hist[32 * kSmallExperts];  // [warp][expert], then base rows
+  __shared__ int warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ipw = ((n_items + 31) / 32 + 31) / 32 * 32;  // items per warp, multiple of 32
+  for (int r = threadIdx.x; r < cap; r += 1024) sorted_ids[r] = n_items;
+  for (int i = threadIdx.x; i < 32 * E_l; i += 1024) hist[i] = 0;
+  __syncthreads();
+  int* my = hist + warp * E_l;
+  const int base = warp * ipw;
+  for (int r = 0; r < ipw; r += 32) {
+    const int item = base + r + lane;
+    int le = -1;
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // counts, padded offsets, per-warp base rows
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E_l)
+    for (int w = 0; w < 32; ++w) c += hist[w * E_l + e];
+  const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(padded, warp_sums, total);
+  if (e < E_l) {
+    counts[e] = c;
+    offsets[e] = start;
+    int run = start;
+    for (int w = 0; w < 32; ++w) {
+      const int h = hist[w * E_l + e];
+      hist[w * E_l + e] = run;
+      run += h;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[E_l] = total;
+    if (total > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+  }
+  if (tiles)
+    write_tile_table(e, E_l, e < E_l ? c : 0, start, nmax, tiles, group_start, max_tiles,
+                     warp_sums, status);
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < ipw; r += 32) {
+    const int item = base + r + lane;
+    int le = -1;
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (item < n_items) {
+      int pos = -1;
+      if (le >= 0) {
+        pos = my[le] + __popc(peers & lt);
+        if (pos < cap) {
+          sorted_ids[pos] = item;
+        } else {
+          if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+          pos = -1;
+        }
+      }
+      inv_pos[item] = pos;
+    }
+    __syncwarp();
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 // Tile table of the routed experts: each segment's rows in chunks of nmax.
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ counts,
                                                            const int32_t* __restrict__ offsets,
                                                            int E_l, int nmax, Tile* __restrict__ tiles,
                                                            int* __restrict__ group_start,
                                                            int max_tiles, unsigned* status) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
   int n = 0, c = 0, off = 0;
@@ -212,20 +357,6 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
   }
 }
 
-// Tile table over all T tokens for each of S weight slabs (shared experts,
-// router): slab s, tokens [t0, t0+rows): B row t0, output row s*T + t0.
-__global__ void dense_tiles_kernel(int T, int S, int nmax, Tile* __restrict__ tiles,
-                                   int* __restrict__ group_start) {
-  const int per = (T + nmax - 1) / nmax;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i <= S) group_start[i] = i * per;
-  if (i >= S * per) return;
-  const int s = i / per, j = i - s * per;
-  const int t0 = j * nmax;
-  const int rows = T - t0 < nmax ? T - t0 : nmax;
-  tiles[i] = make_int4(s, t0, s * T + t0, rows);
-}
-
 // x_perm[r] = x[sorted_ids[r] / K], one warp per row, 16-byte vectors.
 template <typename TE>
 __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
@@ -233,6 +364,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
                                                      const int32_t* __restrict__ offsets_end,
                                                      int cap, long n_items, int K, int H,
                                                      TE* __restrict__ x_perm) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rows = *offsets_end;
   if (rows > cap) rows = cap;
@@ -275,38 +407,64 @@ __device__ __forceinline__ void st8(float* p, const float (&v)[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-template <typename TE>
+// One warp task = one token x one 256-column chunk (8 columns per lane), so
+// small batches still spread over many warps. Lane k holds slot k's row and
+// weight; the rows of KB slots are loaded together before the fixed-order
+// accumulation k = 0..K-1 (KB = K rounded up to a power of two, at most 8).
+template <typename TE, int KB>
 __global__ void __launch_bounds__(256) combine_kernel(
     const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
     const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
     long shared_stride, float rsf, TE* __restrict__ out, int T, int H, unsigned* status) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (long t = blockIdx.x * 8L + warp; t < T; t += 8L * gridDim.x) {
-    for (int c = lane * 8; c < H; c += 256) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int k = 0; k < K; ++k) {
-        const int p = inv_pos[t * K + k];
-        if (p < 0) continue;
-        if (p >= cap) {
-          if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
-          continue;
-        }
-        const float w = topk_w[t * K + k];
-        float y[8];
-        ld8(y_perm + static_cast<long>(p) * H + c, y);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, y[i], acc[i]);
+  const int chunks = (H + 255) / 256;
+  const long tasks = static_cast<long>(T) * chunks;
+  for (long task = blockIdx.x * 8L + warp; task < tasks; task += 8L * gridDim.x) {
+    const long t = task / chunks;
+    const int c = static_cast<int>(task - t * chunks) * 256 + lane * 8;
+    int p_l = -1;
+    float w_l = 0.f;
+    if (lane < K) {
+      p_l = inv_pos[t * K + lane];
+      w_l = topk_w[t * K + lane];
+      if (p_l >= cap) {
+        if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
+        p_l = -1;
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] *= rsf;
-      for (int s = 0; s < n_shared; ++s) {
-        float y[8];
-        ld8(shared + s * shared_stride + t * H + c, y);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += y[i];
-      }
-      st8(out + t * H + c, acc);
     }
+    const bool col_ok = c < H;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < K; k0 += KB) {
+      float y[KB][8];
+      float wk[KB];
+      bool ok[KB];
+#pragma unroll
+      for (int j = 0; j < KB; ++j) {
+        const int k = k0 + j;
+        const int p = __shfl_sync(0xffffffffu, p_l, k & 31);
+        wk[j] = __shfl_sync(0xffffffffu, w_l, k & 31);
+        ok[j] = col_ok && k < K && p >= 0;
+        if (ok[j]) ld8(y_perm + static_cast<long>(p) * H + c, y[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < KB; ++j) {
+        if (ok[j]) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[j], y[j][i], acc[i]);
+        }
+      }
+    }
+    if (!col_ok) continue;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] *= rsf;
+    for (int s = 0; s < n_shared; ++s) {
+      float y[8];
+      ld8(shared + s * shared_stride + t * H + c, y);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += y[i];
+    }
+    st8(out + t * H + c, acc);
   }
 }
 
@@ -319,6 +477,10 @@ int grid_for(long work, int per_block, int cap_blocks) {
 
 }  // namespace
 
+int align_kernel_count(long n_items, int E_l) {
+  return (n_items <= kSmallItems && E_l <= kSmallExperts) ? 1 : 3;
+}
+
 int align_warps(long n_items) {
   long w = (n_items + kItemsPerWarp - 1) / kItemsPerWarp;
   return static_cast<int>(w < 1 ? 1 : w);
@@ -327,34 +489,33 @@ int align_warps(long n_items) {
 cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, int E, int E_l,
                          int ep_start, int block_m, int* hist, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
-                         unsigned* status, cudaStream_t st) {
+                         unsigned* status, cudaStream_t st, Tile* tiles, int* group_start,
+                         int nmax, int max_tiles) {
+  if (n_items <= kSmallItems && E_l <= kSmallExperts) {
+    return launch_pdl(align_small_kernel, dim3(1), dim3(1024), 0, st, ids,
+                      static_cast<int>(n_items), emap, E, E_l, ep_start, block_m, counts,
+                      offsets, sorted_ids, inv_pos, cap, status, tiles, group_start, nmax,
+                      max_tiles);
+  }
   const int n_warps = align_warps(n_items);
   const int blocks = (n_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const size_t smem = sizeof(int) * kWarpsPerBlock * E_l;
-  align_count_kernel<<<blocks, 256, smem, st>>>(ids, n_items, emap, E, E_l, ep_start, hist,
-                                                n_warps, sorted_ids, cap, status);
-  align_scan_kernel<<<1, 1024, 0, st>>>(hist, n_warps, E_l, block_m, counts, offsets, cap,
-                                        status);
-  align_scatter_kernel<<<blocks, 256, smem, st>>>(ids, n_items, emap, E, E_l, ep_start, hist,
-                                                  n_warps, sorted_ids, inv_pos, cap, status);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(align_count_kernel, dim3(blocks), dim3(256), smem, st, ids, n_items,
+                             emap, E, E_l, ep_start, hist, n_warps, sorted_ids, cap, status);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, st, hist, n_warps, E_l, block_m,
+                 counts, offsets, cap, status, tiles, group_start, nmax, max_tiles);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(align_scatter_kernel, dim3(blocks), dim3(256), smem, st, ids, n_items, emap,
+                    E, E_l, ep_start, static_cast<const int*>(hist), n_warps, sorted_ids, inv_pos,
+                    cap, status);
 }
 
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l, int nmax,
                                Tile* tiles, int* group_start, int max_tiles, unsigned* status,
                                cudaStream_t st) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(counts, offsets, E_l, nmax, tiles, group_start,
-                                         max_tiles, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dense_tiles(int T, int S, int nmax, Tile* tiles, int* group_start,
-                               cudaStream_t st) {
-  const int n = dense_tile_count(T, S, nmax);
-  if (n <= 0) return cudaSuccess;
-  const int threads = n > S + 1 ? n : S + 1;
-  dense_tiles_kernel<<<(threads + 255) / 256, 256, 0, st>>>(T, S, nmax, tiles, group_start);
-  return cudaGetLastError();
+  return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E_l, nmax,
+                    tiles, group_start, max_tiles, status);
 }
 
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
@@ -362,30 +523,34 @@ cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
                           void* x_perm, cudaStream_t st) {
   const int grid = grid_for(cap, 8, 8 * 152);
   if (bf16)
-    gather_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), sorted_ids,
-                                        offsets_end, cap, n_items, K, H,
-                                        static_cast<__nv_bfloat16*>(x_perm));
-  else
-    gather_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x), sorted_ids, offsets_end,
-                                        cap, n_items, K, H, static_cast<float*>(x_perm));
-  return cudaGetLastError();
+    return launch_pdl(gather_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), sorted_ids, offsets_end, cap, n_items,
+                      K, H, static_cast<__nv_bfloat16*>(x_perm));
+  return launch_pdl(gather_kernel<float>, dim3(grid), dim3(256), 0, st,
+                    static_cast<const float*>(x), sorted_ids, offsets_end, cap, n_items, K, H,
+                    static_cast<float*>(x_perm));
 }
 
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
                            const float* topk_w, int K, const void* shared, int n_shared,
                            long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st) {
-  const int grid = grid_for(T, 8, 8 * 152);
-  if (bf16)
-    combine_kernel<<<grid, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), cap, inv_pos, topk_w, K,
-        static_cast<const __nv_bfloat16*>(shared), n_shared, shared_stride, rsf,
-        static_cast<__nv_bfloat16*>(out), T, H, status);
-  else
-    combine_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(y_perm), cap, inv_pos,
-                                         topk_w, K, static_cast<const float*>(shared), n_shared,
-                                         shared_stride, rsf, static_cast<float*>(out), T, H,
-                                         status);
+  const int grid = grid_for(static_cast<long>(T) * ((H + 255) / 256), 8, 16 * 152);
+#define MOE_COMBINE(TE, KB)                                                                \
+  return launch_pdl(combine_kernel<TE, KB>, dim3(grid), dim3(256), 0, st,                  \
+                    static_cast<const TE*>(y_perm), cap, inv_pos, topk_w, K,               \
+                    static_cast<const TE*>(shared), n_shared, shared_stride, rsf,          \
+                    static_cast<TE*>(out), T, H, status)
+  if (bf16) {
+    if (K <= 1) MOE_COMBINE(__nv_bfloat16, 1);
+    else if (K <= 2) MOE_COMBINE(__nv_bfloat16, 2);
+    else if (K <= 4) MOE_COMBINE(__nv_bfloat16, 4);
+    else MOE_COMBINE(__nv_bfloat16, 8);
+  } else {
+    if (K <= 2) MOE_COMBINE(float, 2);
+    else MOE_COMBINE(float, 8);
+  }
+#undef MOE_COMBINE
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -90,14 +91,22 @@ template <int MODE, bool TF32, typename TOut, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap mapA,
                 const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
-                const int* __restrict__ group_start, int n_groups, int m_tiles,
-                int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
-                TOut* __restrict__ out, long out_ld, int m_valid, unsigned* status) {
+                const int* __restrict__ group_start, int n_groups, int dense_T, int m_tiles,
+                int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
+                int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
+                int m_valid, unsigned* status) {
+  pdl_enter();
   using S = GemmShape<MODE, NMAX>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
 
-  const int total = group_start[n_groups] * m_tiles;
+  // With k_split > 1 a unit covers one K range and writes its fp32 partial
+  // sums to the slab out + ks * split_stride (plain modes only).
+  // Dense problems (router, shared experts: every token of T for each of
+  // n_groups weight slabs) pass no tile table; their tiles are implicit.
+  const int dense_per = (dense_T + NMAX - 1) / NMAX;
+  const int total = (tiles ? group_start[n_groups] : n_groups * dense_per) * m_tiles * k_split;
+  const int kb_per = (k_blocks + k_split - 1) / k_split;
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
 
   extern __shared__ uint8_t smem_raw[];
@@ -113,7 +122,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 2 * S::kNAcc + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
-  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
+  for (int i = threadIdx.x; i <= n_groups; i += kThreads)
+    gstart[i] = tiles ? group_start[i] : i * dense_per;
+  auto tile_at = [&](int ti) -> Tile {
+    if (tiles) return tiles[ti];
+    const int s = ti / dense_per, t0 = (ti - s * dense_per) * NMAX;
+    return make_int4(s, t0, s * dense_T + t0, min(NMAX, dense_T - t0));
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -150,10 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         int ti, m;
-        decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-        const Tile tl = tiles[ti];
+        const int ks = u % k_split;
+        decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tile_at(ti);
         const int b_row = b_from_out ? tl.z : tl.y;
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+        const int kb1 = min(k_blocks, (ks + 1) * kb_per);
+        for (int kb = ks * kb_per; kb < kb1; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
@@ -186,9 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
         int ti, m;
-        decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-        const Tile tl = tiles[ti];
+        const int ks = u % k_split;
+        decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tile_at(ti);
         const int n_mma = (tl.w + 15) & ~15;
+        const int kb0 = ks * kb_per, kb1 = min(k_blocks, kb0 + kb_per);
         const uint32_t idesc = ptx::idesc_make(kAB, 128, n_mma);
         const int b = ai % S::kNAcc;
         const uint32_t aph = (ai / S::kNAcc) & 1;
@@ -198,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + b * S::kAccCols;
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           if (!ptx::mbar_wait(full0 + 8 * s, ph, abort_flag, status)) {
@@ -211,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t db = ptx::sdesc_sw128(st + S::kNA * kABytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
+            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
             ptx::tc_mma<TF32>(d, da + 2 * kk, db + 2 * kk, idesc, acc);
             if (MODE == kGemmSiluUp) {
               const uint64_t du = ptx::sdesc_sw128(st + kABytes);
@@ -235,8 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ai = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
       int ti, m;
-      decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-      const Tile tl = tiles[ti];
+      const int ks = u % k_split;
+      decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+      const Tile tl = tile_at(ti);
       const int b = ai % S::kNAcc;
       const uint32_t aph = (ai / S::kNAcc) & 1;
       if (!ptx::mbar_wait(tfull0 + 8 * b, aph, abort_flag, status)) break;
@@ -244,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       const int row = m * 128 + q * 32 + lane;
       const bool row_ok = row < m_valid;
-      TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
+      TOut* orow = out + ks * split_stride + static_cast<long>(tl.z) * out_ld + row;
       for (int c0 = 0; c0 < tl.w; c0 += 16) {
         float v[16];
         if constexpr (MODE == kGemmSiluUp) {
@@ -286,11 +306,10 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<num_sms, kThreads, S::kSmemBytes, st>>>(
-      *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups, a.m_tiles, a.k_blocks,
-      a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out), a.out_ld,
-      a.m_valid, a.status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(num_sms), dim3(kThreads), S::kSmemBytes, st, *a.mapA, *a.mapB,
+                    a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
+                    a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),
+                    a.out_ld, a.split_stride, a.m_valid, a.status);
 }
 
 }  // namespace
@@ -307,6 +326,7 @@ size_t gemm_smem_bytes(GemmMode mode, int nmax) {
 
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
+  if (a.k_split < 1 || (a.k_split > 1 && mode != kGemmLogits)) return cudaErrorInvalidValue;
   if (nmax != 32 && nmax != 128 && nmax != 256) return cudaErrorInvalidValue;
   if (nmax == 256) {  // prefill-sized segments, bf16 only
     if (tf32) return cudaErrorInvalidValue;

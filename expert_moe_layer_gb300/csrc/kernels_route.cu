@@ -4,6 +4,7 @@
 #include <math_constants.h>
 
 #include "internal.h"
+#include "launch.cuh"
 
 namespace moe {
 namespace {
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
                                                             const TW* __restrict__ wg,
                                                             float* __restrict__ logits, int T,
                                                             int E, int H) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + warp;
   const int t0 = blockIdx.y * kTok;
@@ -44,6 +46,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
 #pragma unroll
   for (int j = 0; j < kTok; ++j) acc[j] = 0.f;
   const TW* wrow = wg + static_cast<long>(e) * H;
+#pragma unroll 4
   for (int h = lane * 8; h < H; h += 256) {
     float w[8];
     load8(wrow + h, w);
@@ -73,49 +76,66 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
   }
 }
 
-// Token-major variant for small E (<= 32): warp = one token, all experts in
-// chunks of 8. The token's row is read once per chunk (once for E <= 8); the
-// router rows stay in L1/L2.
+// Token-major variant for small E (<= 32): a warp takes kTokW tokens and all
+// experts in chunks of 8. Each router row chunk loaded from L1 serves kTokW
+// tokens, and each token row is read once per expert chunk (once for E <= 8).
+constexpr int kTokW = 1;
+
 template <typename TX, typename TW>
 __global__ void __launch_bounds__(256) router_logits_token_kernel(const TX* __restrict__ x,
                                                                   const TW* __restrict__ wg,
                                                                   float* __restrict__ logits,
                                                                   int T, int E, int H) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long t = blockIdx.x * 8L + warp;
-  if (t >= T) return;
-  const TX* xrow = x + t * H;
+  const long t0 = (blockIdx.x * 8L + warp) * kTokW;
+  if (t0 >= T) return;
   for (int e0 = 0; e0 < E; e0 += 8) {
-    float acc[8];
+    float acc[kTokW][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int a = 0; a < kTokW; ++a)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
     for (int h = lane * 8; h < H; h += 256) {
-      float xv[8];
-      load8(xrow + h, xv);
+      float xv[kTokW][8];
+#pragma unroll
+      for (int a = 0; a < kTokW; ++a) {
+        if (t0 + a < T) load8(x + (t0 + a) * H + h, xv[a]);
+        else
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xv[a][i] = 0.f;
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         if (e0 + j < E) {
           float w[8];
           load8(wg + static_cast<long>(e0 + j) * H + h, w);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[j] = fmaf(xv[i], w[i], acc[j]);
+          for (int a = 0; a < kTokW; ++a)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[a][j] = fmaf(xv[a][i], w[i], acc[a][j]);
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float v = acc[j];
+    for (int a = 0; a < kTokW; ++a) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      acc[j] = v;
-    }
-    if (lane < 8 && e0 + lane < E) {
-      float v = 0.f;
+      for (int j = 0; j < 8; ++j) {
+        float v = acc[a][j];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j == lane) v = acc[j];
-      logits[t * E + e0 + lane] = v;
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[a][j] = v;
+      }
     }
+    // lane = a*8 + j writes logit (t0+a, e0+j)
+    const int a = lane >> 3, j = lane & 7;
+    float v = 0.f;
+#pragma unroll
+    for (int aa = 0; aa < kTokW; ++aa)
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj)
+        if (aa == a && jj == j) v = acc[aa][jj];
+    if (a < kTokW && t0 + a < T && e0 + j < E) logits[(t0 + a) * E + e0 + j] = v;
   }
 }
 
@@ -138,28 +158,17 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   }
 }
 
+// The warp-level routing decision for one token. p[j] holds the logit (with
+// bias) of expert lane + 32*j, or -inf beyond E. Softmax, the optional group
+// limit, K rounds of argmax and the renormalisation all run on this warp.
 template <int VPL>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
-                                                   const float* __restrict__ bias, int T,
-                                                   int E, int K, int renorm, int n_group,
-                                                   int topk_group, int32_t* __restrict__ ids,
-                                                   float* __restrict__ wout) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  const float* row = logits + static_cast<long>(t) * E;
-
-  float p[VPL];
+__device__ __forceinline__ void topk_warp(float (&p)[VPL], int lane, int E, int K, int renorm,
+                                          int n_group, int topk_group,
+                                          int32_t* __restrict__ ids_row,
+                                          float* __restrict__ w_row) {
   float mx = -CUDART_INF_F;
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    p[j] = -CUDART_INF_F;
-    if (e < E) {
-      p[j] = row[e] + (bias ? bias[e] : 0.f);
-      mx = fmaxf(mx, p[j]);
-    }
-  }
+  for (int j = 0; j < VPL; ++j) mx = fmaxf(mx, p[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
@@ -231,7 +240,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
         c[j] = -CUDART_INF_F;
       }
     }
-    if (((i & 31) != lane)) pw = 0.f;
     pw = __shfl_sync(0xffffffffu, pw, i & 31);
     wsum += pw;
     if (lane == k) {
@@ -240,63 +248,120 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
   }
   if (lane < K) {
-    ids[static_cast<long>(t) * K + lane] = my_id;
-    wout[static_cast<long>(t) * K + lane] = renorm ? my_w / wsum : my_w;
+    ids_row[lane] = my_id;
+    w_row[lane] = renorm ? my_w / wsum : my_w;
   }
+}
+
+// One warp per token (large batches): logits = sum of n_part partial slabs.
+template <int VPL>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
+                                                   int n_part, long partial_stride,
+                                                   const float* __restrict__ bias, int T,
+                                                   int E, int K, int renorm, int n_group,
+                                                   int topk_group, int32_t* __restrict__ ids,
+                                                   float* __restrict__ wout) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float* row = logits + static_cast<long>(t) * E;
+  float p[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    p[j] = -CUDART_INF_F;
+    if (e < E) {
+      float l = row[e];
+      for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
+      p[j] = l + (bias ? bias[e] : 0.f);
+    }
+  }
+  topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + static_cast<long>(t) * K,
+                 wout + static_cast<long>(t) * K);
+}
+
+// One CTA per token (small batches): all threads sum the partial slabs into
+// shared memory in parallel, then warp 0 takes the decision.
+template <int VPL>
+__global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__ logits,
+                                                       int n_part, long partial_stride,
+                                                       const float* __restrict__ bias, int T,
+                                                       int E, int K, int renorm, int n_group,
+                                                       int topk_group,
+                                                       int32_t* __restrict__ ids,
+                                                       float* __restrict__ wout) {
+  pdl_enter();
+  __shared__ float sl[32 * VPL];
+  const long t = blockIdx.x;
+  const float* row = logits + t * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float l = row[e];
+    for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
+    sl[e] = l + (bias ? bias[e] : 0.f);
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  float p[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    p[j] = e < E ? sl[e] : -CUDART_INF_F;
+  }
+  topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + t * K, wout + t * K);
 }
 
 }  // namespace
 
+template <typename TX, typename TW>
+cudaError_t logits_launch(const void* x, const void* wg, float* logits, int T, int E, int H,
+                          cudaStream_t st) {
+  const TX* xp = static_cast<const TX*>(x);
+  const TW* wp = static_cast<const TW*>(wg);
+  if (E <= 32)
+    return launch_pdl(router_logits_token_kernel<TX, TW>, dim3((T + 8 * kTokW - 1) / (8 * kTokW)),
+                      dim3(256), 0, st, xp, wp, logits, T, E, H);
+  return launch_pdl(router_logits_kernel<TX, TW>, dim3((E + 7) / 8, (T + kTok - 1) / kTok),
+                    dim3(256), 0, st, xp, wp, logits, T, E, H);
+}
+
 cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
                                  const void* wg, float* logits, int T, int E, int H,
                                  cudaStream_t st) {
-  if (E <= 32) {
-    const int grid = (T + 7) / 8;
-    if (act_bf16 && router_bf16)
-      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                        static_cast<const __nv_bfloat16*>(wg),
-                                                        logits, T, E, H);
-    else if (act_bf16)
-      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                        static_cast<const float*>(wg), logits,
-                                                        T, E, H);
-    else
-      router_logits_token_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x),
-                                                        static_cast<const float*>(wg), logits,
-                                                        T, E, H);
-    return cudaGetLastError();
-  }
-  dim3 grid((E + 7) / 8, (T + kTok - 1) / kTok);
   if (act_bf16 && router_bf16)
-    router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                static_cast<const __nv_bfloat16*>(wg), logits,
-                                                T, E, H);
-  else if (act_bf16)
-    router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x),
-                                                static_cast<const float*>(wg), logits, T, E,
-                                                H);
-  else
-    router_logits_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x),
-                                                static_cast<const float*>(wg), logits, T, E,
-                                                H);
-  return cudaGetLastError();
+    return logits_launch<__nv_bfloat16, __nv_bfloat16>(x, wg, logits, T, E, H, st);
+  if (act_bf16) return logits_launch<__nv_bfloat16, float>(x, wg, logits, T, E, H, st);
+  return logits_launch<float, float>(x, wg, logits, T, E, H, st);
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int K,
-                        int renorm, int n_group, int topk_group, int32_t* ids, float* w,
-                        unsigned* /*status*/, cudaStream_t st) {
-  const int grid = (T + 7) / 8;
+template <int V>
+cudaError_t topk_launch(const float* logits, int n_part, long partial_stride, const float* bias,
+                        int T, int E, int K, int renorm, int n_group, int topk_group,
+                        int32_t* ids, float* w, cudaStream_t st) {
+  if (T < 256)
+    return launch_pdl(topk_cta_kernel<V>, dim3(T), dim3(256), 0, st, logits, n_part,
+                      partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
+  return launch_pdl(topk_kernel<V>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
+                    partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
+}
+
+cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
+                        const float* bias, int T, int E, int K, int renorm, int n_group,
+                        int topk_group, int32_t* ids, float* w, unsigned* /*status*/,
+                        cudaStream_t st) {
   const int vpl = (E + 31) / 32;
-#define MOE_TOPK(V) \
-  topk_kernel<V><<<grid, 256, 0, st>>>(logits, bias, T, E, K, renorm, n_group, topk_group, ids, w)
-  if (vpl <= 1) MOE_TOPK(1);
-  else if (vpl <= 2) MOE_TOPK(2);
-  else if (vpl <= 4) MOE_TOPK(4);
-  else if (vpl <= 8) MOE_TOPK(8);
-  else if (vpl <= 16) MOE_TOPK(16);
-  else return cudaErrorInvalidValue;
-#undef MOE_TOPK
-  return cudaGetLastError();
+  if (vpl <= 1) return topk_launch<1>(logits, n_part, partial_stride, bias, T, E, K, renorm,
+                                      n_group, topk_group, ids, w, st);
+  if (vpl <= 2) return topk_launch<2>(logits, n_part, partial_stride, bias, T, E, K, renorm,
+                                      n_group, topk_group, ids, w, st);
+  if (vpl <= 4) return topk_launch<4>(logits, n_part, partial_stride, bias, T, E, K, renorm,
+                                      n_group, topk_group, ids, w, st);
+  if (vpl <= 8) return topk_launch<8>(logits, n_part, partial_stride, bias, T, E, K, renorm,
+                                      n_group, topk_group, ids, w, st);
+  if (vpl <= 16) return topk_launch<16>(logits, n_part, partial_stride, bias, T, E, K, renorm,
+                                        n_group, topk_group, ids, w, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

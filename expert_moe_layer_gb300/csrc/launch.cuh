@@ -1,0 +1,37 @@
+// Programmatic dependent launch (PDL) for every kernel of the library.
+//
+// Kernels are launched with programmatic stream serialisation, so the next
+// kernel of the layer can be scheduled while the current one finishes. Each
+// kernel's first statement is pdl_enter(): it waits until the preceding grid
+// has completed and its memory is visible, then allows the following grid to
+// launch. Consumers never read a producer's output before that wait.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <utility>
+
+namespace moe {
+
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+}  // namespace moe

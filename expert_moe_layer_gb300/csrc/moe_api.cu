@@ -69,10 +69,25 @@ int routed_nmax(const moe_config* c, int T) {
 }
 int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
 
-// The router runs as a tcgen05 GEMM when its operands are bf16 and there are
-// enough tokens to fill the machine; otherwise on CUDA cores.
-bool router_on_tensor_cores(const moe_config* c, int T) {
-  return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16 && T >= 256;
+// The router runs as a tcgen05 GEMM whenever x and the router weights are
+// bf16 (fp32 routers run on CUDA cores). Batches under 256 tokens split K = H
+// so that ~2 units per SM exist; the top-k kernel sums the fp32 partials in a
+// fixed order.
+bool router_on_tensor_cores(const moe_config* c, int /*T*/) {
+  return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16;
+}
+int router_nmax(int T) { return T >= 256 ? 128 : 32; }
+int router_ksplit(const moe_config* c, int T) {
+  if (!router_on_tensor_cores(c, T) || T >= 256) return 1;
+  const int k_blocks = c->hidden_size / 64;
+  const long base = static_cast<long>((c->num_experts + 127) / 128) *
+                    dense_tile_count(T, 1, router_nmax(T));
+  long ks = (304 + base - 1) / base;
+  if (ks > 16) ks = 16;
+  if (ks > k_blocks) ks = k_blocks;
+  if (ks < 1) ks = 1;
+  const long kb_per = (k_blocks + ks - 1) / ks;
+  return static_cast<int>((k_blocks + kb_per - 1) / kb_per);
 }
 
 long max_routed_tiles(const moe_config* c, int T) {
@@ -130,7 +145,8 @@ bool make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long co
 int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, const void* B,
              long b_rows, int Kdim, const Tile* tiles, const int* group_start, int n_groups,
              int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
-             int m_valid, unsigned* status, cudaStream_t st) {
+             int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
+             long split_stride = 0, int dense_T = 0) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, dt, a_rows, Kdim, 128)) return MOE_ERR_CUDA;
   if (!make_map(&mb, B, dt, b_rows, Kdim, nmax)) return MOE_ERR_CUDA;
@@ -142,6 +158,9 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.n_groups = n_groups;
   g.m_tiles = m_tiles;
   g.k_blocks = Kdim * ebytes(dt) / 128;
+  g.k_split = k_split;
+  g.split_stride = split_stride;
+  g.dense_T = dense_T;
   g.a_rows_per_expert = rows_per_slab;
   g.a_up_offset = up_off;
   g.b_from_out = b_from_out;
@@ -166,15 +185,14 @@ struct Carver {
 };
 
 struct RouteLayout {
-  size_t status, logits, rtiles, rgroups, total;
+  size_t status, logits, total;
 };
 RouteLayout route_layout(const moe_config* c, int T) {
   Carver cv;
   RouteLayout L;
   L.status = cv.take(4);
-  L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
-  L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
-  L.rgroups = cv.take(sizeof(int) * 2);
+  L.logits = cv.take(sizeof(float) * static_cast<size_t>(router_ksplit(c, T)) * T *
+                     c->num_experts);
   L.total = cv.off;
   return L;
 }
@@ -209,8 +227,8 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
 }
 
 struct FwdLayout {
-  size_t status, topk_ids, topk_w, logits, rtiles, rgroups, hist, counts, offsets, sorted_ids;
-  size_t inv_pos, tiles, groups, stiles, sgroups, x_perm, h_perm, y_perm, h_sh, y_sh, total;
+  size_t status, topk_ids, topk_w, logits, hist, counts, offsets, sorted_ids, inv_pos;
+  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, total;
   int cap;
 };
 FwdLayout fwd_layout(const moe_config* c, int T) {
@@ -224,9 +242,8 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.status = cv.take(4);
   L.topk_ids = cv.take(4 * TK);
   L.topk_w = cv.take(4 * TK);
-  L.logits = cv.take(sizeof(float) * static_cast<size_t>(T) * c->num_experts);
-  L.rtiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, 1, 128)));
-  L.rgroups = cv.take(sizeof(int) * 2);
+  L.logits = cv.take(sizeof(float) * static_cast<size_t>(router_ksplit(c, T)) * T *
+                     c->num_experts);
   L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(TK)) * El);
   L.counts = cv.take(4 * static_cast<size_t>(El));
   L.offsets = cv.take(4 * static_cast<size_t>(El + 1));
@@ -234,8 +251,6 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.inv_pos = cv.take(4 * TK);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(El + 1));
-  L.stiles = cv.take(sizeof(Tile) * static_cast<size_t>(dense_tile_count(T, S, dense_nmax(T))));
-  L.sgroups = cv.take(sizeof(int) * static_cast<size_t>(S + 1));
   L.x_perm = cv.take(eb * L.cap * c->hidden_size);
   L.h_perm = cv.take(eb * L.cap * c->intermediate_size);
   L.y_perm = cv.take(eb * L.cap * c->hidden_size);
@@ -273,18 +288,22 @@ int record_event(void* ev, cudaStream_t st) {
 
 // ------------------------------------------------------------- stage bodies
 int do_route(const moe_config* c, int T, const void* x, const void* router_w,
-             const float* bias, int32_t* ids, float* w, float* logits, Tile* rtiles, int* rgroups,
+             const float* bias, int32_t* ids, float* w, float* logits,
              unsigned* status, cudaStream_t st) {
   const int E = c->num_experts, H = c->hidden_size;
+  int n_part = 1;
   if (router_on_tensor_cores(c, T)) {
-    MOE_TRY(cuda_ok(launch_dense_tiles(T, 1, 128, rtiles, rgroups, st)));
-    MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, 128, router_w, E, x, T, H, rtiles, rgroups, 1,
-                     (E + 127) / 128, 0, 0, 0, logits, E, E, status, st));
+    const int nm = router_nmax(T);
+    n_part = router_ksplit(c, T);
+    MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, nm, router_w, E, x, T, H, nullptr, nullptr, 1,
+                     (E + 127) / 128, 0, 0, 0, logits, E, E, status, st, n_part,
+                     static_cast<long>(T) * E, T));
   } else {
     MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
                                          x, router_w, logits, T, E, H, st)));
   }
-  return cuda_ok(launch_topk(logits, bias, T, E, c->top_k, c->renormalize ? 1 : 0,
+  return cuda_ok(launch_topk(logits, n_part, static_cast<long>(T) * E, bias, T, E, c->top_k,
+                             c->renormalize ? 1 : 0,
                              c->use_grouped_topk ? c->num_expert_group : 0,
                              c->use_grouped_topk ? c->topk_group : 0, ids, w, status, st));
 }
@@ -292,12 +311,14 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
 int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
            const void* w2, void* y_perm, Tile* tiles, int* groups, void* x_perm, void* h_perm,
-           unsigned* status, cudaStream_t st, void* const* ev = nullptr) {
+           unsigned* status, cudaStream_t st, void* const* ev = nullptr,
+           bool tiles_ready = false) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
-  MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
-                                     static_cast<int>(max_routed_tiles(c, T)), status, st)));
+  if (!tiles_ready)
+    MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
+                                       static_cast<int>(max_routed_tiles(c, T)), status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
                                 n_items, K, H, x_perm, st)));
   if (ev) MOE_TRY(record_event(ev[0], st));
@@ -356,7 +377,7 @@ int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
   unsigned* status = at<unsigned>(ws, L.status);
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return do_route(cfg, T, x, router_w, router_bias, topk_ids, topk_w, at<float>(ws, L.logits),
-                  at<Tile>(ws, L.rtiles), at<int>(ws, L.rgroups), status, st);
+                  status, st);
 }
 
 size_t moe_align_workspace_size(const moe_config* cfg, int T) {
@@ -489,19 +510,22 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   MOE_TRY(mark(0));
   MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
-                   at<Tile>(ws, L.rtiles), at<int>(ws, L.rgroups), status, st));
-  n += router_on_tensor_cores(cfg, T) ? 3 : 2;
+                   status, st));
+  n += 2;  // logits + top-k
   MOE_TRY(mark(1));
   MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts, El,
                                cfg->ep_rank * El, kForwardBlock, at<int>(ws, L.hist), counts,
-                               offsets, sorted_ids, inv_pos, L.cap, status, st)));
-  n += 3;
+                               offsets, sorted_ids, inv_pos, L.cap, status, st,
+                               at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
+                               routed_nmax(cfg, T),
+                               static_cast<int>(max_routed_tiles(cfg, T)))));
+  n += align_kernel_count(static_cast<long>(T) * K, El);
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
                  at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), status, st,
-                 events ? events + 3 : nullptr));
-  n += 4;
+                 events ? events + 3 : nullptr, true));
+  n += 3;  // gather, GEMM1, GEMM2 (the tile table came with align)
   MOE_TRY(mark(5));
   const void* shared_y = nullptr;
   int S = 0;
@@ -509,19 +533,16 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     S = cfg->num_shared_experts;
     const int Is = cfg->shared_intermediate_size;
     const int nm = dense_nmax(T);
-    Tile* stl = at<Tile>(ws, L.stiles);
-    int* sgr = at<int>(ws, L.sgroups);
     void* h_sh = at<void>(ws, L.h_sh);
     void* y_sh = at<void>(ws, L.y_sh);
-    MOE_TRY(cuda_ok(launch_dense_tiles(T, S, nm, stl, sgr, st)));
     MOE_TRY(run_gemm(kGemmSiluUp, cfg->act_dtype, nm, shared_w13, static_cast<long>(S) * 2 * Is,
-                     x, T, H, stl, sgr, S, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
-                     st));
+                     x, T, H, nullptr, nullptr, S, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
+                     st, 1, 0, T));
     MOE_TRY(run_gemm(kGemmPlain, cfg->act_dtype, nm, shared_w2, static_cast<long>(S) * H, h_sh,
-                     static_cast<long>(S) * T, Is, stl, sgr, S, H / 128, H, 0, 1, y_sh, H,
-                     H, status, st));
+                     static_cast<long>(S) * T, Is, nullptr, nullptr, S, H / 128, H, 0, 1, y_sh,
+                     H, H, status, st, 1, 0, T));
     shared_y = y_sh;
-    n += 3;
+    n += 2;
   }
   MOE_TRY(mark(6));
   MOE_TRY(cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
