@@ -7,14 +7,15 @@
 // and decode (a few rows per expert, nmax = 32). Only the N of the
 // instruction changes.
 //
-// Per CTA (persistent, one per SM, 192 threads):
+// Per CTA (persistent, one per SM, 320 threads):
 //   warp 0      TMA producer: weights (A) and token rows (B) into a ring of
 //               shared-memory stages with the 128-byte swizzle
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of
 //               K = 128 bytes per stage; in SiLU mode a second accumulator for
 //               the "up" rows shares the same B stage
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns one
-//               32-lane quarter), SiLU(gate)*up or plain, store to global
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (two warps per 32-lane
+//               TMEM quarter, alternating 16-column chunks), SiLU(gate)*up or
+//               plain, store to global
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
 // overlaps the main loop of the next.
 //
@@ -33,7 +34,8 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kEpiThreads = 256;    // warps 2..9
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
 
 template <int MODE, int NMAX>
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < S::kNAcc; ++b) {
       ptx::mbar_init(tfull0 + 8 * b, 1);
-      ptx::mbar_init(tempty0 + 8 * b, 128);
+      ptx::mbar_init(tempty0 + 8 * b, kEpiThreads);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -250,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;    // two warps per quarter split the columns
     int ai = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
       int ti, m;
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = m * 128 + q * 32 + lane;
       const bool row_ok = row < m_valid;
       TOut* orow = out + ks * split_stride + static_cast<long>(tl.z) * out_ld + row;
-      for (int c0 = 0; c0 < tl.w; c0 += 16) {
+      for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
         float v[16];
         if constexpr (MODE == kGemmSiluUp) {
           float w[16];
