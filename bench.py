@@ -153,6 +153,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --------------------------------------------------------------------------- ranks
+def aggregate_over_ranks(local_ms, tokens_per_rank, steps, world, device=None):
+    """Whole-job numbers of a replicated run: the slowest rank's time over the
+    K steps, and every rank's tokens. Returns (max total ms, tokens/s)."""
+    total = float(local_ms)
+    if world > 1:
+        t = torch.tensor([total], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    return total, world * tokens_per_rank * steps / (total / 1e3)
+
+
 # --------------------------------------------------------------------------- our arm
 def run_ours(args, wl, rank, world, device):
     from expert_moe_layer_gb300 import binding as B
@@ -254,15 +266,10 @@ def run_ours(args, wl, rank, world, device):
     def span(a, b):
         return [sevents[i][a].elapsed_time(sevents[i][b]) for i in range(args.steps)]
 
-    total_ms = sum(step_ms)
+    total_ms, tokens_per_s = aggregate_over_ranks(sum(step_ms), T, args.steps, world, device)
     stage_names = ["route", "align", "tiles_gather", "gemm1_silu", "gemm2", "shared", "combine"]
     stages = {n: statistics.mean(span(i, i + 1)) for i, n in enumerate(stage_names)}
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    tokens_per_s = world * T * args.steps / (total_ms / 1e3)
 
     # algorithmic work per step
     rb = 2 if wl.router == "bf16" else 4
