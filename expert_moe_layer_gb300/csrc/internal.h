@@ -46,6 +46,12 @@ enum GemmMode { kGemmSiluUp = 0, kGemmPlain = 1, kGemmLogits = 2 };
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a,
                         int num_sms, cudaStream_t st);
 
+// The same grouped GEMM on CTA pairs (cta_group::2, M = 256 weight rows per
+// pair unit, 128 per CTA): bf16, nmax = 256 token tiles, routed tile table,
+// m_tiles counted in 256-row tiles, B tensor map boxes of nmax/2 rows.
+cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num_sms,
+                             cudaStream_t st);
+
 // Shared-memory bytes a GEMM variant needs (for validation/tests).
 size_t gemm_smem_bytes(GemmMode mode, int nmax);
 

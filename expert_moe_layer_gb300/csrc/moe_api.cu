@@ -94,6 +94,14 @@ long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
 
+// With 256-token tiles, GEMM2 (one accumulator, double-buffered in TMEM) runs
+// on CTA pairs: one M = 256 MMA over two SMs halves the token bytes each SM
+// stages. GEMM1 keeps single-CTA tiles: its gate and up accumulators already
+// fill TMEM, and on pairs it measured slower.
+bool gemm2_on_pairs(const moe_config* c, int T) {
+  return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
+}
+
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -146,10 +154,10 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              long b_rows, int Kdim, const Tile* tiles, const int* group_start, int n_groups,
              int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
-             long split_stride = 0, int dense_T = 0) {
+             long split_stride = 0, int dense_T = 0, bool pair = false) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, dt, a_rows, Kdim, 128)) return MOE_ERR_CUDA;
-  if (!make_map(&mb, B, dt, b_rows, Kdim, nmax)) return MOE_ERR_CUDA;
+  if (!make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax)) return MOE_ERR_CUDA;
   GemmArgs g;
   g.mapA = &ma;
   g.mapB = &mb;
@@ -170,6 +178,7 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.status = status;
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
+  if (pair) return launch_gemm_pair(mode, nmax, g, sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   return launch_gemm(mode, dt == MOE_F32, nmax, g, sms, st) == cudaSuccess ? MOE_OK
                                                                            : MOE_ERR_CUDA;
 }
@@ -316,6 +325,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
+  const bool pair2 = gemm2_on_pairs(c, T);
   if (!tiles_ready)
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
                                        static_cast<int>(max_routed_tiles(c, T)), status, st)));
@@ -326,7 +336,8 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
                    cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
   if (ev) MOE_TRY(record_event(ev[1], st));
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
-                   tiles, groups, El, H / 128, H, 0, 0, y_perm, H, H, status, st));
+                   tiles, groups, El, H / (pair2 ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
+                   1, 0, 0, pair2));
   return MOE_OK;
 }
 

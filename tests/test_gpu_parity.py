@@ -32,8 +32,10 @@ SMALL = {
                     x_std=0.3),
     "k_equals_e": W("k_equals_e", T=40, H=128, I=128, E=8, K=8),
     "single_token": W("single_token", T=1, H=256, I=256, E=32, K=4, router_bias=True),
-    # segments averaging >= 192 rows: the 256-row token tiles
+    # segments averaging >= 192 rows
     "wide_prefill": W("wide_prefill", T=1100, H=256, I=384, E=5, K=1),
+    # long segments with enough work units: 256-token tiles on CTA pairs
+    "pair_prefill": W("pair_prefill", T=4096, H=256, I=2048, E=8, K=2),
 }
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
