@@ -26,8 +26,9 @@ struct GemmArgs {
   int dense_T = 0;             // tokens per slab when tiles == nullptr
   int m_tiles;                 // 128-row weight tiles per expert
   int k_blocks;                // K / (128 bytes of K)
-  int k_split = 1;             // K ranges per tile (router logits only); partial
-  long split_stride = 0;       //   sums go to out + ks * split_stride
+  int k_split = 1;             // K ranges per tile; with k_split > 1 the raw fp32
+  long split_stride = 0;       //   accumulators go to part + ks * split_stride
+  float* part = nullptr;
   int a_rows_per_expert;       // weight rows per expert slab
   int a_up_offset;             // row offset of the "up" half (SiLU mode)
   int b_from_out;              // 1: B row = tile.z instead of tile.y
@@ -89,6 +90,13 @@ inline int dense_tile_count(int T, int S, int nmax) { return S * ((T + nmax - 1)
 inline long routed_tile_bound(long n_items, int E_l, int nmax) {
   return n_items / nmax + E_l + 1;
 }
+
+// h[r][i] = silu(sum_s g_s[r][i]) * sum_s u_s[r][i] over n_part fp32 slabs
+// (gate at column i, up at column I + i, row stride 2I), rows below
+// min(*rows_dev, cap).
+cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long part_stride,
+                                 const int32_t* rows_dev, int cap, int I, void* h,
+                                 cudaStream_t st);
 
 // x_perm[r] = x[sorted_ids[r] / K] for rows holding an item.
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,

@@ -407,6 +407,43 @@ __device__ __forceinline__ void st8(float* p, const float (&v)[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// The SiLU*up epilogue of a GEMM1 split over K: sums the fp32 partial gate
+// and up accumulators in slab order. One warp per (row, 256-column chunk).
+template <typename TE>
+__global__ void __launch_bounds__(256) silu_finalize_kernel(const float* __restrict__ part,
+                                                            int n_part, long part_stride,
+                                                            const int32_t* __restrict__ rows_dev,
+                                                            int cap, int I, TE* __restrict__ h) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int rows = *rows_dev;
+  if (rows > cap) rows = cap;
+  const int chunks = (I + 255) / 256;
+  const long tasks = static_cast<long>(rows) * chunks;
+  for (long task = blockIdx.x * 8L + warp; task < tasks; task += 8L * gridDim.x) {
+    const long r = task / chunks;
+    const int c = static_cast<int>(task - r * chunks) * 256 + lane * 8;
+    if (c >= I) continue;
+    float g[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float u[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < n_part; ++s) {
+      const float* src = part + s * part_stride + r * (2L * I) + c;
+      float a[8], b[8];
+      ld8(src, a);
+      ld8(src + I, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        g[i] += a[i];
+        u[i] += b[i];
+      }
+    }
+    float o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+    st8(h + r * I + c, o);
+  }
+}
+
 // One warp task = one token x one 256-column chunk (8 columns per lane), so
 // small batches still spread over many warps. Lane k holds slot k's row and
 // weight; the rows of KB slots are loaded together before the fixed-order
@@ -529,6 +566,17 @@ cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
   return launch_pdl(gather_kernel<float>, dim3(grid), dim3(256), 0, st,
                     static_cast<const float*>(x), sorted_ids, offsets_end, cap, n_items, K, H,
                     static_cast<float*>(x_perm));
+}
+
+cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long part_stride,
+                                 const int32_t* rows_dev, int cap, int I, void* h,
+                                 cudaStream_t st) {
+  const int grid = grid_for(static_cast<long>(cap) * ((I + 255) / 256), 8, 16 * 152);
+  if (bf16)
+    return launch_pdl(silu_finalize_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st, part,
+                      n_part, part_stride, rows_dev, cap, I, static_cast<__nv_bfloat16*>(h));
+  return launch_pdl(silu_finalize_kernel<float>, dim3(grid), dim3(256), 0, st, part, n_part,
+                    part_stride, rows_dev, cap, I, static_cast<float*>(h));
 }
 
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,

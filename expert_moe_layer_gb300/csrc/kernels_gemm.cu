@@ -96,14 +96,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int* __restrict__ group_start, int n_groups, int dense_T, int m_tiles,
                 int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
-                int m_valid, unsigned* status) {
+                float* __restrict__ part, int m_valid, unsigned* status) {
   pdl_enter();
   using S = GemmShape<MODE, NMAX>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
 
-  // With k_split > 1 a unit covers one K range and writes its fp32 partial
-  // sums to the slab out + ks * split_stride (plain modes only).
+  // With k_split > 1 a unit covers one K range and writes its raw fp32
+  // accumulator to the slab part + ks * split_stride (row stride out_ld; in
+  // SiLU mode gate at column i and up at column a_up_offset + i). The caller
+  // sums the slabs in order and applies the epilogue.
   // Dense problems (router, shared experts: every token of T for each of
   // n_groups weight slabs) pass no tile table; their tiles are implicit.
   const int dense_per = (dense_T + NMAX - 1) / NMAX;
@@ -267,7 +269,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       const int row = m * 128 + q * 32 + lane;
       const bool row_ok = row < m_valid;
-      TOut* orow = out + ks * split_stride + static_cast<long>(tl.z) * out_ld + row;
+      if (k_split > 1) {
+        float* prow = part + ks * split_stride + static_cast<long>(tl.z) * out_ld + row;
+        for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
+          float v[16];
+          if constexpr (MODE == kGemmSiluUp) {
+            float w[16];
+            ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
+            if (row_ok) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (c0 + j < tl.w) {
+                  prow[static_cast<long>(c0 + j) * out_ld] = v[j];
+                  prow[static_cast<long>(c0 + j) * out_ld + a_up_offset] = w[j];
+                }
+              }
+            }
+          } else {
+            ptx::tmem_ld16(tb + c0, v);
+            if (row_ok) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < tl.w) prow[static_cast<long>(c0 + j) * out_ld] = v[j];
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty0 + 8 * b);
+        continue;
+      }
+      TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
       for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
         float v[16];
         if constexpr (MODE == kGemmSiluUp) {
@@ -312,7 +343,7 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
   return launch_pdl(kern, dim3(num_sms), dim3(kThreads), S::kSmemBytes, st, *a.mapA, *a.mapB,
                     a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
                     a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),
-                    a.out_ld, a.split_stride, a.m_valid, a.status);
+                    a.out_ld, a.split_stride, a.part, a.m_valid, a.status);
 }
 
 }  // namespace
@@ -329,7 +360,7 @@ size_t gemm_smem_bytes(GemmMode mode, int nmax) {
 
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
-  if (a.k_split < 1 || (a.k_split > 1 && mode != kGemmLogits)) return cudaErrorInvalidValue;
+  if (a.k_split < 1 || (a.k_split > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
   if (nmax != 32 && nmax != 128 && nmax != 256) return cudaErrorInvalidValue;
   if (nmax == 256) {  // prefill-sized segments, bf16 only
     if (tf32) return cudaErrorInvalidValue;

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     p[j] = -CUDART_INF_F;
     if (e < E) {
       float l = row[e];
+#pragma unroll 8
       for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
       p[j] = l + (bias ? bias[e] : 0.f);
     }
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__
   const float* row = logits + t * E;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float l = row[e];
+#pragma unroll 8
     for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
     sl[e] = l + (bias ? bias[e] : 0.f);
   }

@@ -16,7 +16,8 @@ namespace moe {
 namespace {
 
 constexpr int kMaxT = 1 << 18;
-constexpr int kForwardBlock = 16;   // segment padding used by moe_forward
+constexpr int kForwardBlock = 1;    // moe_forward leaves segments unpadded (the GEMMs
+                                    // read past a segment's end but never store there)
 constexpr size_t kAlignBytes = 256;
 
 size_t rup(size_t v) { return (v + kAlignBytes - 1) / kAlignBytes * kAlignBytes; }
@@ -90,6 +91,22 @@ int router_ksplit(const moe_config* c, int T) {
   return static_cast<int>((k_blocks + kb_per - 1) / kb_per);
 }
 
+// Decode batches leave few GEMM1 units (token tiles x I/128): split K = H
+// so that ~2 units per SM exist. Estimate tiles as one per touched expert.
+int gemm1_ksplit(const moe_config* c, int T) {
+  const long local_items = static_cast<long>(T) * c->top_k / c->ep_size;
+  long tiles = local_items < n_local(c) ? local_items : n_local(c);
+  if (tiles < 1) tiles = 1;
+  const long units = tiles * (c->intermediate_size / 128);
+  if (units >= 152) return 1;
+  const int k_blocks = c->hidden_size * (c->act_dtype == MOE_BF16 ? 2 : 4) / 128;
+  long ks = (304 + units - 1) / units;
+  if (ks > 8) ks = 8;
+  if (ks > k_blocks) ks = k_blocks;
+  const long kb_per = (k_blocks + ks - 1) / ks;
+  return static_cast<int>((k_blocks + kb_per - 1) / kb_per);
+}
+
 long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
@@ -154,7 +171,8 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              long b_rows, int Kdim, const Tile* tiles, const int* group_start, int n_groups,
              int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
-             long split_stride = 0, int dense_T = 0, bool pair = false) {
+             long split_stride = 0, int dense_T = 0, bool pair = false,
+             float* part = nullptr) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, dt, a_rows, Kdim, 128)) return MOE_ERR_CUDA;
   if (!make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax)) return MOE_ERR_CUDA;
@@ -169,6 +187,7 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.k_split = k_split;
   g.split_stride = split_stride;
   g.dense_T = dense_T;
+  g.part = part;
   g.a_rows_per_expert = rows_per_slab;
   g.a_up_offset = up_off;
   g.b_from_out = b_from_out;
@@ -220,7 +239,7 @@ AlignLayout align_layout(const moe_config* c, int T) {
 }
 
 struct MlpLayout {
-  size_t status, tiles, groups, x_perm, h_perm, total;
+  size_t status, tiles, groups, x_perm, h_perm, part1, total;
 };
 MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   Carver cv;
@@ -231,13 +250,16 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(n_local(c) + 1));
   L.x_perm = cv.take(eb * static_cast<size_t>(cap) * c->hidden_size);
   L.h_perm = cv.take(eb * static_cast<size_t>(cap) * c->intermediate_size);
+  L.part1 = cv.take(gemm1_ksplit(c, T) > 1 ? sizeof(float) * gemm1_ksplit(c, T) * cap * 2 *
+                                                 static_cast<size_t>(c->intermediate_size)
+                                           : 0);
   L.total = cv.off;
   return L;
 }
 
 struct FwdLayout {
   size_t status, topk_ids, topk_w, logits, hist, counts, offsets, sorted_ids, inv_pos;
-  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, total;
+  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
   int cap;
 };
 FwdLayout fwd_layout(const moe_config* c, int T) {
@@ -265,6 +287,9 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.y_perm = cv.take(eb * L.cap * c->hidden_size);
   L.h_sh = cv.take(eb * static_cast<size_t>(S) * T * (S ? c->shared_intermediate_size : 0));
   L.y_sh = cv.take(eb * static_cast<size_t>(S) * T * c->hidden_size);
+  L.part1 = cv.take(gemm1_ksplit(c, T) > 1 ? sizeof(float) * gemm1_ksplit(c, T) * L.cap * 2 *
+                                                 static_cast<size_t>(c->intermediate_size)
+                                           : 0);
   L.total = cv.off;
   return L;
 }
@@ -306,7 +331,7 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
     n_part = router_ksplit(c, T);
     MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, nm, router_w, E, x, T, H, nullptr, nullptr, 1,
                      (E + 127) / 128, 0, 0, 0, logits, E, E, status, st, n_part,
-                     static_cast<long>(T) * E, T));
+                     static_cast<long>(T) * E, T, false, logits));
   } else {
     MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
                                          x, router_w, logits, T, E, H, st)));
@@ -320,7 +345,7 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
 int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
            const void* w2, void* y_perm, Tile* tiles, int* groups, void* x_perm, void* h_perm,
-           unsigned* status, cudaStream_t st, void* const* ev = nullptr,
+           float* part1, unsigned* status, cudaStream_t st, void* const* ev = nullptr,
            bool tiles_ready = false) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
@@ -332,8 +357,19 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
                                 n_items, K, H, x_perm, st)));
   if (ev) MOE_TRY(record_event(ev[0], st));
-  MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
-                   cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
+  const int ks1 = gemm1_ksplit(c, T);
+  if (ks1 > 1) {
+    // split over K: raw gate/up partials, then the SiLU*up epilogue
+    MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
+                     cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, 2 * I, I, status,
+                     st, ks1, static_cast<long>(cap) * 2 * I, 0, false, part1));
+    MOE_TRY(cuda_ok(launch_silu_finalize(c->act_dtype == MOE_BF16, part1, ks1,
+                                         static_cast<long>(cap) * 2 * I, offsets + El, cap, I,
+                                         h_perm, st)));
+  } else {
+    MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
+                     cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
+  }
   if (ev) MOE_TRY(record_event(ev[1], st));
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
                    tiles, groups, El, H / (pair2 ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
@@ -442,7 +478,7 @@ int moe_grouped_mlp(const moe_config* cfg, int T, const void* x, const int32_t* 
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return do_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm,
                 at<Tile>(ws, L.tiles), at<int>(ws, L.groups), at<void>(ws, L.x_perm),
-                at<void>(ws, L.h_perm), status, st);
+                at<void>(ws, L.h_perm), at<float>(ws, L.part1), status, st);
 }
 
 int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const int32_t* inv_pos,
@@ -534,9 +570,9 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
-                 at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), status, st,
-                 events ? events + 3 : nullptr, true));
-  n += 3;  // gather, GEMM1, GEMM2 (the tile table came with align)
+                 at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
+                 st, events ? events + 3 : nullptr, true));
+  n += gemm1_ksplit(cfg, T) > 1 ? 4 : 3;  // gather, GEMM1 [+ SiLU finalize], GEMM2
   MOE_TRY(mark(5));
   const void* shared_y = nullptr;
   int S = 0;

@@ -88,7 +88,7 @@ def test_workspace_sizes_and_layout():
     assert B.align_cap(cfg, T, 16) == T * 2 + 8 * 15
     lay = B.workspace_layout(cfg, T)
     assert lay.total == B.workspace_size(cfg, T)
-    assert lay.cap == T * 2 + 8 * 15 and lay.block_m == 16
+    assert lay.block_m == 1 and lay.cap == B.align_cap(cfg, T, lay.block_m) == T * 2
     offs = [lay.status, lay.topk_ids, lay.topk_w, lay.counts, lay.offsets, lay.sorted_ids,
             lay.inv_pos]
     assert all(o % 256 == 0 for o in offs) and len(set(offs)) == len(offs)
