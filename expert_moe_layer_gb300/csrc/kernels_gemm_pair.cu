@@ -1,19 +1,30 @@
 // Grouped GEMM on CTA pairs: one tcgen05 MMA of M = 256 weight rows spans two
 // SMs (cta_group::2). Each CTA of a cluster pair stages its own 128 weight rows
 // and half of the token rows, and keeps its 128 accumulator lanes in its own
-// TMEM. So each SM stages fewer bytes per FLOP than in moe_gemm_tc: for
-// 256-token tiles in SiLU mode, 8.4 MFLOP per 48 KB stage.
+// TMEM. So each SM stages fewer bytes per FLOP than in moe_gemm_tc: 131 FLOPs
+// per byte with 256-token tiles, with the accumulator double-buffered.
+//
+//   plain mode (GEMM2): the pair's 256 rows are 256 consecutive output rows.
+//   SiLU mode (GEMM1):  rank 0 holds 128 gate rows and rank 1 the matching
+//                       128 up rows, so the pair computes gate and up for the
+//                       same 128 intermediate indices. Rank 1's epilogue sends
+//                       its up values to rank 0 over distributed shared memory
+//                       in 32-column chunks. Two slots alternate: st.async
+//                       completes bytes on rank 0's full barrier, and rank 0
+//                       frees a slot with a relaxed arrive. Rank 0 then applies
+//                       SiLU(gate)*up and stores.
 //
 // Roles per CTA (persistent, 320 threads), as in moe_gemm_tc:
-//   warp 0      TMA producer of this CTA's halves. Bytes are counted on the
-//               full barrier of rank 0, which alone issues MMAs.
+//   warp 0      TMA producer of this CTA's rows. The bytes of both CTAs are
+//               counted on rank 0's full barrier (rank 0 declares them).
 //   warp 1      TMEM allocation (both CTAs, cta_group::2). On rank 0 also the
-//               MMA issuer: it waits for both CTAs' bytes. Its commits arrive
-//               on the stage-free and accumulator-full barriers of both CTAs.
-//   warps 2..9  epilogue on this CTA's accumulator lanes. Each thread then
-//               arrives on rank 0's accumulator-free barrier.
-// Work units (pair tile m of 256 weight rows x one token tile) are ordered as
-// in moe_gemm_tc: expert by expert.
+//               MMA issuer. Its commits arrive on the stage-free and
+//               accumulator-full barriers of both CTAs.
+//   warps 2..9  epilogue on this CTA's 128 accumulator lanes (two warps per
+//               lane quarter, 16 columns each per 32-column chunk). Each warp
+//               then arrives once on rank 0's accumulator-free barrier.
+// Work units (one 256-row pair tile x one token tile) are ordered as in
+// moe_gemm_tc: expert by expert.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -24,26 +35,27 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 8;
 constexpr int kABytes = 128 * 128;
+constexpr int kChunk = 32;                       // columns per SiLU exchange chunk
+constexpr int kXSlotBytes = 128 * kChunk * 4;    // one chunk of up values, fp32
 
 template <int MODE, int NMAX>
 struct PairShape {
-  static constexpr int kNA = (MODE == kGemmSiluUp) ? 2 : 1;
   static constexpr int kBRows = NMAX / 2;  // token rows staged per CTA
   static constexpr int kBBytes = kBRows * 128;
-  static constexpr int kStageBytes = kNA * kABytes + kBBytes;
-  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kXBytes = (MODE == kGemmSiluUp) ? 2 * kXSlotBytes : 0;
+  static constexpr int kStages0 = (200 * 1024 - kXBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kAccCols = kNA * NMAX;
-  static constexpr int kNAcc = kAccCols <= 256 ? 2 : 1;
-  static constexpr int kTmemNeed = kAccCols * kNAcc;
-  static constexpr int kTmemCols = kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kAccCols = NMAX;
+  static constexpr int kNAcc = 2;
+  static constexpr int kTmemCols = kAccCols * kNAcc <= 256 ? 256 : 512;
   static constexpr int kMaxGroups = 1024;
-  static constexpr int kBarBytes =
-      8 * (2 * kStages + 2 * kNAcc + 1) + 16 + 4 * (kMaxGroups + 1);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
-  static_assert(kTmemNeed <= 512, "TMEM overflow");
+  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4;  // + xfull[2], xempty[2]
+  static constexpr int kBarBytes = 8 * kNBars + 16 + 4 * (kMaxGroups + 1);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kXBytes + kBarBytes;
+  static_assert(kAccCols * kNAcc <= 512, "TMEM overflow");
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(NMAX % 32 == 0 && NMAX <= 256, "bad NMAX");
 };
@@ -91,13 +103,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
+  const uint32_t xbase = sbase + S::kStages * S::kStageBytes;  // SiLU exchange slots
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes + S::kXBytes);
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S::kStages;
   const uint32_t tfull0 = empty0 + 8 * S::kStages;
   const uint32_t tempty0 = tfull0 + 8 * S::kNAcc;
   const uint32_t drain = tempty0 + 8 * S::kNAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 2 * S::kNAcc + 1);
+  const uint32_t xfull0 = drain + 8;     // on rank 0: rank 1 wrote a chunk
+  const uint32_t xempty0 = xfull0 + 16;  // on rank 1: rank 0 consumed a chunk
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kNBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
   for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
@@ -112,9 +128,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < S::kNAcc; ++b) {
       ptx::mbar_init(tfull0 + 8 * b, 1);
-      ptx::mbar_init(tempty0 + 8 * b, 2 * (kEpiThreads / 32));  // one per epilogue warp of each CTA
+      ptx::mbar_init(tempty0 + 8 * b, 2 * kEpiWarps);  // one per epilogue warp of each CTA
     }
     ptx::mbar_init(drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      ptx::mbar_init(xfull0 + 8 * x, 1);          // rank 0 arms it with the chunk's bytes
+      ptx::mbar_init(xempty0 + 8 * x, kEpiWarps);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async();
@@ -142,7 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tiles[ti];
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
-        const int a_row = tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128;
+        const int a_row =
+            MODE == kGemmSiluUp
+                ? tl.x * a_rows_per_expert + static_cast<int>(rank) * a_up_offset + m * 128
+                : tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
@@ -158,9 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // never land in an older phase.
           if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * S::kStageBytes);
           ptx::tma_load_2d_pair(st, &mapA, fb, kb * 64, a_row);
-          if (MODE == kGemmSiluUp)
-            ptx::tma_load_2d_pair(st + kABytes, &mapA, fb, kb * 64, a_row + a_up_offset);
-          ptx::tma_load_2d_pair(st + S::kNA * kABytes, &mapB, fb, kb * 64, b_row);
+          ptx::tma_load_2d_pair(st + kABytes, &mapB, fb, kb * 64, b_row);
         }
       }
       if (!ok) settle(200000);
@@ -194,16 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           const uint32_t st = sbase + s * S::kStageBytes;
           const uint64_t da = ptx::sdesc_sw128(st);
-          const uint64_t db = ptx::sdesc_sw128(st + S::kNA * kABytes);
+          const uint64_t db = ptx::sdesc_sw128(st + kABytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb | kk) ? 1u : 0u;
-            ptx::tc_mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, acc);
-            if (MODE == kGemmSiluUp) {
-              const uint64_t du = ptx::sdesc_sw128(st + kABytes);
-              ptx::tc_mma_pair(d + NMAX, du + 2 * kk, db + 2 * kk, idesc, acc);
-            }
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            ptx::tc_mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
           ptx::tc_commit_pair(empty0 + 8 * s);
         }
         if (!ok) break;
@@ -219,8 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t tempty_r0 = ptx::map_to_rank(tempty0, 0);
-    int ai = 0;
-    for (int u = pair; u < total; u += n_pairs, ++ai) {
+    const uint32_t xfull_r0 = ptx::map_to_rank(xfull0, 0);
+    const uint32_t xempty_r1 = ptx::map_to_rank(xempty0, 1);
+    const int row_l = q * 32 + lane;  // accumulator lane of this thread
+    int ai = 0, cc = 0;
+    bool ok = true;
+    for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
       int ti, m;
       decode_unit(u, gstart, n_groups, m_tiles, ti, m);
       const Tile tl = tiles[ti];
@@ -229,21 +248,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ptx::mbar_wait_cluster(tfull0 + 8 * b, aph, abort_flag, status)) break;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
-      const int row = m * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
-      __nv_bfloat16* orow = out + static_cast<long>(tl.z) * out_ld + row;
-      for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
-        float v[16];
-        if constexpr (MODE == kGemmSiluUp) {
-          float w[16];
-          ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
+      if constexpr (MODE == kGemmSiluUp) {
+        const int i = m * 128 + row_l;
+        __nv_bfloat16* orow = out + static_cast<long>(tl.z) * out_ld + i;
+        for (int c0 = 0; c0 < tl.w; c0 += kChunk, ++cc) {
+          const int slot = cc & 1;
+          const uint32_t xph = (cc >> 1) & 1;
+          const int col = c0 + 16 * half;
+          const uint32_t xrow = xbase + slot * kXSlotBytes + (row_l * kChunk + 16 * half) * 4;
+          float v[16];
+          ptx::tmem_ld16(tb + col, v);
+          if (rank == 1) {
+            // up values -> rank 0's slot, once rank 0 has drained it; the
+            // asynchronous stores complete bytes on rank 0's xfull barrier
+            if (!ptx::mbar_wait_cluster(xempty0 + 8 * slot, xph ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = ptx::map_to_rank(xrow, 0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = silu_f(v[j]) * w[j];
-        } else {
-          ptx::tmem_ld16(tb + c0, v);
+            for (int j = 0; j < 16; j += 4)
+              ptx::st_async_v4(dst + 4 * j, v[j], v[j + 1], v[j + 2], v[j + 3],
+                               xfull_r0 + 8 * slot);
+          } else {
+            if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(xfull0 + 8 * slot, kXSlotBytes);
+            if (!ptx::mbar_wait_cluster(xfull0 + 8 * slot, xph, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            const float* up = reinterpret_cast<const float*>(smem + (xrow - sbase));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (col + j < tl.w)
+                orow[static_cast<long>(col + j) * out_ld] = __float2bfloat16_rn(silu_f(v[j]) * up[j]);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(xempty_r1 + 8 * slot);
+          }
         }
+        if (!ok) break;
+      } else {
+        const int row = m * 256 + static_cast<int>(rank) * 128 + row_l;
+        __nv_bfloat16* orow = out + static_cast<long>(tl.z) * out_ld + row;
+        for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
+          float v[16];
+          ptx::tmem_ld16(tb + c0, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * out_ld] = __float2bfloat16_rn(v[j]);
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * out_ld] = __float2bfloat16_rn(v[j]);
+          }
         }
       }
       ptx::tc_fence_before();
@@ -297,10 +350,10 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
 cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num_sms,
                              cudaStream_t st) {
   if (a.tiles == nullptr || a.k_split != 1) return cudaErrorInvalidValue;
-  // Only GEMM2 runs on pairs: GEMM1 (two accumulators) measured faster on
-  // single CTAs.
   if (nmax == 256 && mode == kGemmPlain)
     return launch_pair_variant<kGemmPlain, 256>(a, num_sms, st);
+  if (nmax == 256 && mode == kGemmSiluUp)
+    return launch_pair_variant<kGemmSiluUp, 256>(a, num_sms, st);
   return cudaErrorInvalidValue;
 }
 

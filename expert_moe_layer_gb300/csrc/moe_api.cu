@@ -111,11 +111,11 @@ long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
 
-// With 256-token tiles, GEMM2 (one accumulator, double-buffered in TMEM) runs
-// on CTA pairs: one M = 256 MMA over two SMs halves the token bytes each SM
-// stages. GEMM1 keeps single-CTA tiles: its gate and up accumulators already
-// fill TMEM, and on pairs it measured slower.
-bool gemm2_on_pairs(const moe_config* c, int T) {
+// With 256-token tiles both GEMMs run on CTA pairs: one M = 256 MMA over two
+// SMs, each SM staging half of the token rows. GEMM1 puts the 128 gate rows on
+// rank 0 and the matching 128 up rows on rank 1 (one double-buffered
+// accumulator per CTA); GEMM2 puts 256 consecutive output rows on the pair.
+bool gemms_on_pairs(const moe_config* c, int T) {
   return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
 }
 
@@ -350,7 +350,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
-  const bool pair2 = gemm2_on_pairs(c, T);
+  const bool pairs = gemms_on_pairs(c, T);
   if (!tiles_ready)
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
                                        static_cast<int>(max_routed_tiles(c, T)), status, st)));
@@ -368,12 +368,13 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
                                          h_perm, st)));
   } else {
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
-                     cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st));
+                     cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st,
+                     1, 0, 0, pairs));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
-                   tiles, groups, El, H / (pair2 ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
-                   1, 0, 0, pair2));
+                   tiles, groups, El, H / (pairs ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
+                   1, 0, 0, pairs));
   return MOE_OK;
 }
 

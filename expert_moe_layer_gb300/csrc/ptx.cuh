@@ -289,6 +289,31 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// Store four floats to shared memory of any CTA in the cluster.
+__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+// Asynchronous store of four floats into another CTA's shared memory; the
+// 16 bytes complete a transaction on that CTA's mbarrier (no fence needed).
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float a, float b, float c, float d,
+                                            uint32_t cbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(caddr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cbar)
+      : "memory");
+}
+
+// Arrive on a cluster mbarrier without release ordering (the caller's reads
+// have already been consumed by dependent instructions).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
+               : "memory");
+}
+
 // TMA load whose completion is counted on an mbarrier that may live in the
 // peer CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
