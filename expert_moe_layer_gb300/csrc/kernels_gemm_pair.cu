@@ -9,7 +9,7 @@
 //                       128 up rows, so the pair computes gate and up for the
 //                       same 128 intermediate indices. Rank 1's epilogue sends
 //                       its up values to rank 0 over distributed shared memory
-//                       in 32-column chunks. Two slots alternate: st.async
+//                       in 16-column chunks. Two slots alternate: st.async
 //                       completes bytes on rank 0's full barrier, and rank 0
 //                       frees a slot with a relaxed arrive. Rank 0 then applies
 //                       SiLU(gate)*up and stores.
@@ -21,7 +21,8 @@
 //               MMA issuer. Its commits arrive on the stage-free and
 //               accumulator-full barriers of both CTAs.
 //   warps 2..9  epilogue on this CTA's 128 accumulator lanes (two warps per
-//               lane quarter, 16 columns each per 32-column chunk). Each warp
+//               lane quarter: 8 columns each of a 16-column SiLU chunk, or
+//               alternate 16-column blocks in plain mode). Each warp
 //               then arrives once on rank 0's accumulator-free barrier.
 // Work units (one 256-row pair tile x one token tile) are ordered as in
 // moe_gemm_tc: expert by expert.
@@ -37,7 +38,8 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kABytes = 128 * 128;
-constexpr int kChunk = 32;                       // columns per SiLU exchange chunk
+constexpr int kChunk = 16;                       // columns per SiLU exchange chunk
+constexpr int kHalfCols = kChunk / 2;            // columns of a chunk per epilogue warp
 constexpr int kXSlotBytes = 128 * kChunk * 4;    // one chunk of up values, fp32
 
 template <int MODE, int NMAX>
@@ -46,7 +48,7 @@ struct PairShape {
   static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kXBytes = (MODE == kGemmSiluUp) ? 2 * kXSlotBytes : 0;
-  static constexpr int kStages0 = (200 * 1024 - kXBytes) / kStageBytes;
+  static constexpr int kStages0 = (216 * 1024 - kXBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kAccCols = NMAX;
   static constexpr int kNAcc = 2;
@@ -254,10 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 0; c0 < tl.w; c0 += kChunk, ++cc) {
           const int slot = cc & 1;
           const uint32_t xph = (cc >> 1) & 1;
-          const int col = c0 + 16 * half;
-          const uint32_t xrow = xbase + slot * kXSlotBytes + (row_l * kChunk + 16 * half) * 4;
-          float v[16];
-          ptx::tmem_ld16(tb + col, v);
+          const int col = c0 + kHalfCols * half;
+          // slot layout [column group of 4][row][4]: eight lanes' 16-byte
+          // accesses cover 128 contiguous bytes, free of bank conflicts
+          const uint32_t xg = xbase + slot * kXSlotBytes + (2 * half * 128 + row_l) * 16;
+          float v[kHalfCols];
+          ptx::tmem_ld8(tb + col, v);
           if (rank == 1) {
             // up values -> rank 0's slot, once rank 0 has drained it; the
             // asynchronous stores complete bytes on rank 0's xfull barrier
@@ -265,10 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const uint32_t dst = ptx::map_to_rank(xrow, 0);
+            const uint32_t dst = ptx::map_to_rank(xg, 0);
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-              ptx::st_async_v4(dst + 4 * j, v[j], v[j + 1], v[j + 2], v[j + 3],
+            for (int j = 0; j < kHalfCols; j += 4)
+              ptx::st_async_v4(dst + (j / 4) * 128 * 16, v[j], v[j + 1], v[j + 2], v[j + 3],
                                xfull_r0 + 8 * slot);
           } else {
             if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(xfull0 + 8 * slot, kXSlotBytes);
@@ -276,11 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const float* up = reinterpret_cast<const float*>(smem + (xrow - sbase));
+            const float4* up = reinterpret_cast<const float4*>(smem + (xg - sbase));
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (col + j < tl.w)
-                orow[static_cast<long>(col + j) * out_ld] = __float2bfloat16_rn(silu_f(v[j]) * up[j]);
+            for (int j = 0; j < kHalfCols; j += 4) {
+              const float4 u4 = up[(j / 4) * 128];
+              const float uj[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                if (col + j + t < tl.w)
+                  orow[static_cast<long>(col + j + t) * out_ld] =
+                      __float2bfloat16_rn(silu_f(v[j + t]) * uj[t]);
+              }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster_relaxed(xempty_r1 + 8 * slot);
