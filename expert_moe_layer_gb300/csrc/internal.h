@@ -57,6 +57,12 @@ cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num
 size_t gemm_smem_bytes(GemmMode mode, int nmax);
 
 // Router logits on CUDA cores: logits[t,e] = x[t].Wg[e] (fp32 accumulation).
+// For E <= 32 the sum over H is split into slices of kRouterSplitCols
+// columns, each written to its own partial slab (T*E floats apart); larger E
+// writes one slab.
+constexpr int kRouterSplitCols = 256;
+inline int router_split_slabs(int H) { return (H + kRouterSplitCols - 1) / kRouterSplitCols; }
+inline int router_cuda_core_slabs(int E, int H) { return E <= 32 ? router_split_slabs(H) : 1; }
 cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
                                  const void* wg, float* logits, int T, int E, int H,
                                  cudaStream_t st);

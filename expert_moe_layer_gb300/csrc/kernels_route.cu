@@ -76,66 +76,89 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
   }
 }
 
-// Token-major variant for small E (<= 32): a warp takes kTokW tokens and all
-// experts in chunks of 8. Each router row chunk loaded from L1 serves kTokW
-// tokens, and each token row is read once per expert chunk (once for E <= 8).
-constexpr int kTokW = 1;
+// Split-H variant for small E (<= 32). A CTA covers 64 tokens (8 per warp),
+// one kRouterSplitCols-wide slice of H and up to 8 experts (blockIdx.z picks
+// the expert octet). Each lane keeps its 8 columns of those experts' router
+// rows in registers, so the router weights are read once per warp and every
+// token row once per octet. The slice sums go to partial slab blockIdx.y; the
+// top-k kernel adds the slabs in slab order.
+constexpr int kSplitTokWarp = 8;
+
+// Sum acc[0..7] over the 32 lanes; lane l ends up with the total of entry
+// (l >> 2) & 7. Each halving step keeps half of the entries and hands the
+// other half to the partner lane: 4 + 2 + 1 + 1 + 1 shuffles.
+__device__ __forceinline__ float warp_sum8(const float (&acc)[8], int lane) {
+  float r[4], s[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 16;
+    const float keep = hi ? acc[i + 4] : acc[i];
+    const float give = hi ? acc[i] : acc[i + 4];
+    r[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 8;
+    const float keep = hi ? r[i + 2] : r[i];
+    const float give = hi ? r[i] : r[i + 2];
+    s[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+  }
+  const bool hi = lane & 4;
+  float u = (hi ? s[1] : s[0]) + __shfl_xor_sync(0xffffffffu, hi ? s[0] : s[1], 4);
+  u += __shfl_xor_sync(0xffffffffu, u, 2);
+  u += __shfl_xor_sync(0xffffffffu, u, 1);
+  return u;
+}
 
 template <typename TX, typename TW>
-__global__ void __launch_bounds__(256) router_logits_token_kernel(const TX* __restrict__ x,
+__global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __restrict__ x,
                                                                   const TW* __restrict__ wg,
                                                                   float* __restrict__ logits,
                                                                   int T, int E, int H) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long t0 = (blockIdx.x * 8L + warp) * kTokW;
-  if (t0 >= T) return;
-  for (int e0 = 0; e0 < E; e0 += 8) {
-    float acc[kTokW][8];
+  const int h = blockIdx.y * kRouterSplitCols + lane * 8;
+  const bool hv = h < H;  // H is a multiple of 128
+  const int e0 = blockIdx.z * 8;
+  float w[8][8];
 #pragma unroll
-    for (int a = 0; a < kTokW; ++a)
+  for (int j = 0; j < 8; ++j) {
+    if (hv && e0 + j < E) {
+      load8(wg + static_cast<long>(e0 + j) * H + h, w[j]);
+    } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
-    for (int h = lane * 8; h < H; h += 256) {
-      float xv[kTokW][8];
+      for (int i = 0; i < 8; ++i) w[j][i] = 0.f;
+    }
+  }
+  float* slab = logits + static_cast<long>(blockIdx.y) * T * E;
+  const long tw = (static_cast<long>(blockIdx.x) * 8 + warp) * kSplitTokWarp;
+  const int ex = (lane >> 2) & 7;
 #pragma unroll
-      for (int a = 0; a < kTokW; ++a) {
-        if (t0 + a < T) load8(x + (t0 + a) * H + h, xv[a]);
-        else
+  for (int a = 0; a < kSplitTokWarp; a += 4) {
+    float xv[4][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xv[a][i] = 0.f;
-      }
+    for (int b = 0; b < 4; ++b) {
+      if (hv && tw + a + b < T) {
+        load8(x + (tw + a + b) * H + h, xv[b]);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (e0 + j < E) {
-          float w[8];
-          load8(wg + static_cast<long>(e0 + j) * H + h, w);
-#pragma unroll
-          for (int a = 0; a < kTokW; ++a)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[a][j] = fmaf(xv[a][i], w[i], acc[a][j]);
-        }
+        for (int i = 0; i < 8; ++i) xv[b][i] = 0.f;
       }
     }
 #pragma unroll
-    for (int a = 0; a < kTokW; ++a) {
+    for (int b = 0; b < 4; ++b) {
+      float acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float v = acc[a][j];
+        float d = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[a][j] = v;
+        for (int i = 0; i < 8; ++i) d = fmaf(xv[b][i], w[j][i], d);
+        acc[j] = d;
       }
+      const float v = warp_sum8(acc, lane);
+      const long t = tw + a + b;
+      if ((lane & 3) == 0 && t < T && e0 + ex < E) slab[t * E + e0 + ex] = v;
     }
-    // lane = a*8 + j writes logit (t0+a, e0+j)
-    const int a = lane >> 3, j = lane & 7;
-    float v = 0.f;
-#pragma unroll
-    for (int aa = 0; aa < kTokW; ++aa)
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj)
-        if (aa == a && jj == j) v = acc[aa][jj];
-    if (a < kTokW && t0 + a < T && e0 + j < E) logits[(t0 + a) * E + e0 + j] = v;
   }
 }
 
@@ -322,7 +345,9 @@ cudaError_t logits_launch(const void* x, const void* wg, float* logits, int T, i
   const TX* xp = static_cast<const TX*>(x);
   const TW* wp = static_cast<const TW*>(wg);
   if (E <= 32)
-    return launch_pdl(router_logits_token_kernel<TX, TW>, dim3((T + 8 * kTokW - 1) / (8 * kTokW)),
+    return launch_pdl(router_logits_split_kernel<TX, TW>,
+                      dim3((T + 8 * kSplitTokWarp - 1) / (8 * kSplitTokWarp),
+                           router_split_slabs(H), (E + 7) / 8),
                       dim3(256), 0, st, xp, wp, logits, T, E, H);
   return launch_pdl(router_logits_kernel<TX, TW>, dim3((E + 7) / 8, (T + kTok - 1) / kTok),
                     dim3(256), 0, st, xp, wp, logits, T, E, H);

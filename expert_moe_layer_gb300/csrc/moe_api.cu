@@ -71,7 +71,8 @@ int routed_nmax(const moe_config* c, int T) {
 int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
 
 // The router runs as a tcgen05 GEMM whenever x and the router weights are
-// bf16 (fp32 routers run on CUDA cores). Batches under 256 tokens split K = H
+// bf16 (fp32 routers run on CUDA cores, split over H into 256-column slices
+// when E <= 32). Tensor-core batches under 256 tokens split K = H
 // so that ~2 units per SM exist; the top-k kernel sums the fp32 partials in a
 // fixed order.
 bool router_on_tensor_cores(const moe_config* c, int /*T*/) {
@@ -79,7 +80,8 @@ bool router_on_tensor_cores(const moe_config* c, int /*T*/) {
 }
 int router_nmax(int T) { return T >= 256 ? 128 : 32; }
 int router_ksplit(const moe_config* c, int T) {
-  if (!router_on_tensor_cores(c, T) || T >= 256) return 1;
+  if (!router_on_tensor_cores(c, T)) return router_cuda_core_slabs(c->num_experts, c->hidden_size);
+  if (T >= 256) return 1;
   const int k_blocks = c->hidden_size / 64;
   const long base = static_cast<long>((c->num_experts + 127) / 128) *
                     dense_tile_count(T, 1, router_nmax(T));
@@ -333,6 +335,7 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
                      (E + 127) / 128, 0, 0, 0, logits, E, E, status, st, n_part,
                      static_cast<long>(T) * E, T, false, logits));
   } else {
+    n_part = router_ksplit(c, T);
     MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
                                          x, router_w, logits, T, E, H, st)));
   }
