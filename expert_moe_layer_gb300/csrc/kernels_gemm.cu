@@ -97,7 +97,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
                 float* __restrict__ part, int m_valid, unsigned* status) {
-  pdl_enter();
   using S = GemmShape<MODE, NMAX>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
@@ -165,6 +164,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Operand A (weights) of the first kStages stages before the
+      // dependency wait; operand B (token rows) only after it.
+      int pre = 0;
+      for (int u = blockIdx.x; u < total && pre < S::kStages; u += gridDim.x) {
+        int ti, m;
+        const int ks = u % k_split;
+        decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tile_at(ti);
+        const int a_row = tl.x * a_rows_per_expert + m * 128;
+        const int kb1 = min(k_blocks, (ks + 1) * kb_per);
+        for (int kb = ks * kb_per; kb < kb1 && pre < S::kStages; ++kb, ++pre) {
+          const uint32_t st = sbase + pre * S::kStageBytes;
+          ptx::mbar_arrive_expect_tx(full0 + 8 * pre, S::kStageBytes);
+          ptx::tma_load_2d(st, &mapA, full0 + 8 * pre, kb * kKe, a_row);
+          if (MODE == kGemmSiluUp)
+            ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * pre, kb * kKe,
+                             a_row + a_up_offset);
+        }
+      }
+      pdl_enter();
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -177,31 +196,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = ks * kb_per; kb < kb1; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
-          if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
-            ok = false;
-            break;
-          }
           const uint32_t st = sbase + s * S::kStageBytes;
-          ptx::mbar_arrive_expect_tx(full0 + 8 * s, S::kStageBytes);
-          const int a_row = tl.x * a_rows_per_expert + m * 128;
-          ptx::tma_load_2d(st, &mapA, full0 + 8 * s, kb * kKe, a_row);
-          if (MODE == kGemmSiluUp)
-            ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, kb * kKe,
-                             a_row + a_up_offset);
+          if (it >= pre) {  // stages of the early loads are fresh: no empty wait
+            if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(full0 + 8 * s, S::kStageBytes);
+            const int a_row = tl.x * a_rows_per_expert + m * 128;
+            ptx::tma_load_2d(st, &mapA, full0 + 8 * s, kb * kKe, a_row);
+            if (MODE == kGemmSiluUp)
+              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, kb * kKe,
+                               a_row + a_up_offset);
+          }
           ptx::tma_load_2d(st + S::kNA * kABytes, &mapB, full0 + 8 * s, kb * kKe, b_row);
         }
       }
       if (!ok) {
         // unwinding: let every load this thread issued land before exit
+        // (a failed empty wait implies it >= pre: every early stage got its B)
         const int n = it < S::kStages ? it : S::kStages;
         for (int i = 0; i < n; ++i) {
           const int j = it - 1 - i;
           ptx::mbar_wait_drain(full0 + 8 * (j % S::kStages), (j / S::kStages) & 1);
         }
       }
+    } else {
+      pdl_enter();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    pdl_enter();
     if (lane == 0) {
       int it = 0, ai = 0;
       bool ok = true;
@@ -254,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_enter();
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // two warps per quarter split the columns
     int ai = 0;

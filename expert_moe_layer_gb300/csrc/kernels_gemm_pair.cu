@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int* __restrict__ group_start, int n_groups, int m_tiles, int k_blocks,
                   int a_rows_per_expert, int a_up_offset, int b_from_out,
                   __nv_bfloat16* __restrict__ out, long out_ld, unsigned* status) {
-  pdl_enter();
   using S = PairShape<MODE, NMAX>;
   const uint32_t rank = ptx::cluster_rank();
   const int pair = blockIdx.x >> 1;
@@ -156,6 +155,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint32_t full_r0 = ptx::map_to_rank(full0, 0);  // rank 0's full barriers
+      // Operand A (weights) of the first kStages stages before the
+      // dependency wait; operand B (token rows) only after it.
+      int pre = 0;
+      for (int u = pair; u < total && pre < S::kStages; u += n_pairs) {
+        int ti, m;
+        decode_unit(u, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tiles[ti];
+        const int a_row =
+            MODE == kGemmSiluUp
+                ? tl.x * a_rows_per_expert + static_cast<int>(rank) * a_up_offset + m * 128
+                : tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < k_blocks && pre < S::kStages; ++kb, ++pre) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * pre, 2 * S::kStageBytes);
+          ptx::tma_load_2d_pair(sbase + pre * S::kStageBytes, &mapA, full_r0 + 8 * pre,
+                                kb * 64, a_row);
+        }
+      }
+      pdl_enter();
       int it = 0;
       bool ok = true;
       for (int u = pair; u < total && ok; u += n_pairs) {
@@ -171,25 +188,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
-          if (!ptx::mbar_wait_cluster(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
-            ok = false;
-            break;
-          }
           const uint32_t st = sbase + s * S::kStageBytes;
           const uint32_t fb = full_r0 + 8 * s;
-          // Rank 0 declares the bytes of both CTAs on its own barrier; the
-          // peer's copies only complete transactions on it. The peer loads
-          // stage s again only after rank 0's MMAs freed it, so its bytes
-          // never land in an older phase.
-          if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * S::kStageBytes);
-          ptx::tma_load_2d_pair(st, &mapA, fb, kb * 64, a_row);
+          if (it >= pre) {  // stages of the early loads are fresh: no empty wait
+            if (!ptx::mbar_wait_cluster(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            // Rank 0 declares the bytes of both CTAs on its own barrier; the
+            // peer's copies only complete transactions on it. The peer loads
+            // stage s again only after rank 0's MMAs freed it, so its bytes
+            // never land in an older phase.
+            if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * S::kStageBytes);
+            ptx::tma_load_2d_pair(st, &mapA, fb, kb * 64, a_row);
+          }
           ptx::tma_load_2d_pair(st + kABytes, &mapB, fb, kb * 64, b_row);
         }
       }
       if (!ok) settle(200000);
+    } else {
+      pdl_enter();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
+    pdl_enter();
     if (lane == 0 && rank == 0) {
       int it = 0, ai = 0;
       bool ok = true;
@@ -233,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_enter();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t tempty_r0 = ptx::map_to_rank(tempty0, 0);

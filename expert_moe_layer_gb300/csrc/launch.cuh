@@ -5,6 +5,13 @@
 // kernel's first statement is pdl_enter(): it waits until the preceding grid
 // has completed and its memory is visible, then allows the following grid to
 // launch. Consumers never read a producer's output before that wait.
+//
+// Since every kernel allows its dependents only after its own wait, a kernel
+// that has launched may assume that the kernel two places before it has
+// completed. The GEMM kernels use this: their tile tables (written at least
+// two kernels earlier) and their weight operands (never written by the
+// library) are read before the wait, so the first weight tiles stream in
+// while the preceding kernel finishes.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -13,9 +20,13 @@
 
 namespace moe {
 
-__device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
 }
 
 template <typename... KArgs, typename... Args>
