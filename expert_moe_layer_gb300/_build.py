@@ -22,8 +22,8 @@ BUILD = os.path.join(ROOT, "_build", "libmoe")
 LIB = os.path.join(PKG, "libmoe.so")
 STAMP = LIB + ".stamp"
 
-SOURCES = ["moe_api.cu", "kernels_gemm.cu", "kernels_gemm_pair.cu", "kernels_route.cu",
-           "kernels_align.cu"]
+SOURCES = ["moe_api.cu", "kernels_gemm.cu", "kernels_gemm_pair.cu", "kernels_mlp_fused.cu",
+           "kernels_route.cu", "kernels_align.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "launch.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",

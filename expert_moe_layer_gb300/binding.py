@@ -48,6 +48,13 @@ class WorkspaceOffsets(ctypes.Structure):
                 ("cap", ctypes.c_int), ("block_m", ctypes.c_int)]
 
 
+class Plan(ctypes.Structure):
+    _fields_ = [("kernels", ctypes.c_int), ("router_tensor_cores", ctypes.c_int),
+                ("router_partials", ctypes.c_int), ("align_kernels", ctypes.c_int),
+                ("tile_rows", ctypes.c_int), ("gemm1_k_split", ctypes.c_int),
+                ("cta_pairs", ctypes.c_int), ("fused_mlp", ctypes.c_int)]
+
+
 def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,
                 num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
                 num_shared_experts=0, shared_intermediate_size=0, ep_size=1, ep_rank=0,
@@ -84,6 +91,7 @@ _SIGS = {
                                _SZ, _VP, ctypes.POINTER(ctypes.c_void_p),
                                ctypes.POINTER(ctypes.c_int)]),
     "moe_get_status": (_I, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_forward_plan": (_I, [_CFG, _I, ctypes.POINTER(Plan)]),
 }
 
 
@@ -171,6 +179,12 @@ def workspace_layout(cfg, T) -> WorkspaceOffsets:
     out = WorkspaceOffsets()
     _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(cfg), T,
                                                              ctypes.byref(out)))
+    return out
+
+
+def forward_plan(cfg, T) -> Plan:
+    out = Plan()
+    _check("moe_forward_plan", lib().moe_forward_plan(ctypes.byref(cfg), T, ctypes.byref(out)))
     return out
 
 

@@ -1,0 +1,409 @@
+// Both expert GEMMs of a decode-sized batch in one persistent tcgen05 kernel.
+//
+// The routed expert MLP (MixtralMoE expert forward: w2(silu(w1 x) * w3 x)) is
+// two grouped GEMMs: h = silu(gate) * up over w13, then y = h w2^T. Launched
+// one after the other, the second waits for the first one's slowest CTA. At
+// decode sizes both are short and bound by weight reads, so that wait, plus
+// the wave quantisation of the first GEMM's few hundred units, costs a
+// sizeable share of the layer. Here one grid walks a single unit list:
+//
+//   units [0, U1)        GEMM1: (tile, 128 rows of w13's gate and up halves)
+//   units [U1, U1 + U2)  GEMM2: (tile, 128 rows of w2)
+//
+// Each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... in order. The
+// epilogue warps of a GEMM1 unit store their h rows, then add 1 to the
+// tile's ready counter (8 warps x I/128 units = the count a GEMM2 unit of
+// that tile waits for). A GEMM2 unit's producer streams its w2 tiles first,
+// then waits (bounded) for the counter, then loads the h rows. All GEMM1
+// units precede all GEMM2 units in every CTA's sequence, so all GEMM1 work
+// runs without waiting and no wait can deadlock once every CTA is resident
+// (one CTA per SM; a wait that runs out sets MOE_DEV_TIMEOUT).
+//
+// Stage layout (40 KB): two 128-row weight boxes and two token-row boxes of
+// nmax rows, each box 128 bytes of K with the 128-byte swizzle.
+//   GEMM1 stage: A0 = gate rows, A1 = up rows, B0 = x rows (one K block);
+//                gate accumulates in columns [0, nmax), up in [nmax, 2 nmax)
+//   GEMM2 stage: A0/B0 = K block 2j, A1/B1 = K block 2j+1, one accumulator
+// Warp roles as in moe_gemm_tc: warp 0 TMA producer, warp 1 TMEM owner and
+// MMA issuer, warps 2..9 epilogue (two per TMEM lane quarter).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "launch.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 8;
+constexpr int kABytes = 128 * 128;
+constexpr int kNmax = 32;                          // token rows per tile
+constexpr int kBBytes = kNmax * 128;
+constexpr int kStageBytes = 2 * kABytes + 2 * kBBytes;
+constexpr int kStages = 5;
+constexpr int kAccCols = 2 * kNmax;                // gate + up
+constexpr int kNAcc = 2;
+constexpr int kTmemCols = 128;
+constexpr int kMaxGroups = 1024;
+constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16 + 4 * (kMaxGroups + 1);
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+static_assert(kAccCols * kNAcc <= kTmemCols, "TMEM overflow");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_groups, int m_tiles,
+                                            int& tile, int& m) {
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (gstart[mid] * m_tiles <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  const int n = gstart[lo + 1] - gstart[lo];
+  const int r = u - gstart[lo] * m_tiles;
+  m = r / n;
+  tile = gstart[lo] + (r - m * n);
+}
+
+struct UnitInfo {
+  bool g2;     // GEMM2 unit
+  int ti, m;   // tile index, weight tile
+  int n_st;    // pipeline stages of the unit
+};
+
+__device__ __forceinline__ UnitInfo unit_info(int u, int U1, const int* gstart, int n_groups,
+                                              int m1, int m2, int kb1, int kb2) {
+  UnitInfo r;
+  r.g2 = u >= U1;
+  if (!r.g2) {
+    decode_unit(u, gstart, n_groups, m1, r.ti, r.m);
+    r.n_st = kb1;
+  } else {
+    decode_unit(u - U1, gstart, n_groups, m2, r.ti, r.m);
+    r.n_st = (kb2 + 1) >> 1;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *p >= target, bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort,
+                                           unsigned* status) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (ld_acquire(p) >= target) return true;
+    if ((n & 15u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+        *abort = 1;
+        if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_mlp_fused(const __grid_constant__ CUtensorMap mapW13,
+                  const __grid_constant__ CUtensorMap mapX,
+                  const __grid_constant__ CUtensorMap mapW2,
+                  const __grid_constant__ CUtensorMap mapH, const Tile* __restrict__ tiles,
+                  const int* __restrict__ group_start, int n_groups, int H, int I,
+                  int* __restrict__ ready, __nv_bfloat16* __restrict__ h_out,
+                  __nv_bfloat16* __restrict__ y_out, unsigned* status) {
+  const int m1 = I / 128, m2 = H / 128;
+  const int kb1 = H / 64, kb2 = I / 64;
+  const int n_tiles = group_start[n_groups];
+  const int U1 = n_tiles * m1;
+  const int total = U1 + n_tiles * m2;
+  const int ready_target = kEpiWarps * m1;
+  if (static_cast<int>(blockIdx.x) >= total) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t full0 = ptx::smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  const uint32_t tfull0 = empty0 + 8 * kStages;
+  const uint32_t tempty0 = tfull0 + 8 * kNAcc;
+  const uint32_t drain = tempty0 + 8 * kNAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kNAcc + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
+  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < kNAcc; ++b) {
+      ptx::mbar_init(tfull0 + 8 * b, 1);
+      ptx::mbar_init(tempty0 + 8 * b, kEpiThreads);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async();
+    ptx::tma_prefetch_map(&mapW13);
+    ptx::tma_prefetch_map(&mapX);
+    ptx::tma_prefetch_map(&mapW2);
+    ptx::tma_prefetch_map(&mapH);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      // weight boxes of one stage (the tile table was written two kernels back)
+      auto load_a = [&](const UnitInfo& ui, const Tile& tl, int j, uint32_t st, uint32_t fb) {
+        if (!ui.g2) {
+          const int row = tl.x * 2 * I + ui.m * 128;
+          ptx::tma_load_2d(st, &mapW13, fb, j * 64, row);
+          ptx::tma_load_2d(st + kABytes, &mapW13, fb, j * 64, row + I);
+        } else {
+          const int row = tl.x * H + ui.m * 128;
+          ptx::tma_load_2d(st, &mapW2, fb, 2 * j * 64, row);
+          if (2 * j + 1 < kb2) ptx::tma_load_2d(st + kABytes, &mapW2, fb, (2 * j + 1) * 64, row);
+        }
+      };
+      auto load_b = [&](const UnitInfo& ui, const Tile& tl, int j, uint32_t st, uint32_t fb) {
+        if (!ui.g2) {
+          ptx::tma_load_2d(st + 2 * kABytes, &mapX, fb, j * 64, tl.y);
+        } else {
+          ptx::tma_load_2d(st + 2 * kABytes, &mapH, fb, 2 * j * 64, tl.z);
+          if (2 * j + 1 < kb2)
+            ptx::tma_load_2d(st + 2 * kABytes + kBBytes, &mapH, fb, (2 * j + 1) * 64, tl.z);
+        }
+      };
+      auto stage_bytes = [&](const UnitInfo& ui, int j) -> uint32_t {
+        if (!ui.g2) return 2 * kABytes + kBBytes;
+        return (2 * j + 1 < kb2) ? 2 * (kABytes + kBBytes) : kABytes + kBBytes;
+      };
+
+      // weights of the first stages before the dependency wait
+      int pre = 0;
+      for (int u = blockIdx.x; u < total && pre < kStages; u += gridDim.x) {
+        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+        const Tile tl = tiles[ui.ti];
+        for (int j = 0; j < ui.n_st && pre < kStages; ++j, ++pre) {
+          const uint32_t fb = full0 + 8 * pre;
+          ptx::mbar_arrive_expect_tx(fb, stage_bytes(ui, j));
+          load_a(ui, tl, j, sbase + pre * kStageBytes, fb);
+        }
+      }
+      pdl_enter();
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+        const Tile tl = tiles[ui.ti];
+        // GEMM2: stream the unit's first weight boxes, then wait for its h rows
+        const int n_a = ui.g2 ? min(ui.n_st, kStages) : 0;
+        int j = 0;
+        for (; j < n_a; ++j) {
+          const int i2 = it + j;
+          if (i2 >= pre) {
+            const int s = i2 % kStages;
+            const uint32_t ph = (i2 / kStages) & 1;
+            if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes(ui, j));
+            load_a(ui, tl, j, sbase + s * kStageBytes, full0 + 8 * s);
+          }
+        }
+        if (!ok) {
+          it += j;
+          break;
+        }
+        if (ui.g2) {
+          if (!wait_count(ready + ui.ti, ready_target, abort_flag, status)) {
+            ok = false;
+            it += n_a;
+            // the issued weight boxes still land; their stages never fill
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        for (j = 0; j < ui.n_st; ++j, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          const uint32_t st = sbase + s * kStageBytes;
+          if (j >= n_a && it >= pre) {
+            if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes(ui, j));
+            load_a(ui, tl, j, st, full0 + 8 * s);
+          }
+          load_b(ui, tl, j, st, full0 + 8 * s);
+        }
+      }
+      if (!ok) {
+        // unwinding: give in-flight copies time to land before the CTA exits
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 200000) {
+        }
+      }
+    } else {
+      pdl_enter();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    pdl_enter();
+    if (lane == 0) {
+      int it = 0, ai = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
+        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+        const Tile tl = tiles[ui.ti];
+        const int n_mma = (tl.w + 15) & ~15;
+        const uint32_t idesc = ptx::idesc_make(1u, 128, n_mma);
+        const int b = ai % kNAcc;
+        const uint32_t aph = (ai / kNAcc) & 1;
+        if (!ptx::mbar_wait(tempty0 + 8 * b, aph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + b * kAccCols;
+        for (int j = 0; j < ui.n_st; ++j, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!ptx::mbar_wait(full0 + 8 * s, ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t st = sbase + s * kStageBytes;
+          const uint64_t da0 = ptx::sdesc_sw128(st);
+          const uint64_t da1 = ptx::sdesc_sw128(st + kABytes);
+          const uint64_t db0 = ptx::sdesc_sw128(st + 2 * kABytes);
+          const uint64_t db1 = ptx::sdesc_sw128(st + 2 * kABytes + kBBytes);
+          if (!ui.g2) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+              ptx::tc_mma<false>(d, da0 + 2 * kk, db0 + 2 * kk, idesc, acc);
+              ptx::tc_mma<false>(d + kNmax, da1 + 2 * kk, db0 + 2 * kk, idesc, acc);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::tc_mma<false>(d, da0 + 2 * kk, db0 + 2 * kk, idesc,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+            if (2 * j + 1 < kb2) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::tc_mma<false>(d, da1 + 2 * kk, db1 + 2 * kk, idesc, 1u);
+            }
+          }
+          ptx::tc_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        ptx::tc_commit(tfull0 + 8 * b);
+      }
+      if (!ok) {
+        ptx::tc_commit(drain);
+        ptx::mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_enter();
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int ai = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
+      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+      const Tile tl = tiles[ui.ti];
+      const int b = ai % kNAcc;
+      const uint32_t aph = (ai / kNAcc) & 1;
+      if (!ptx::mbar_wait(tfull0 + 8 * b, aph, abort_flag, status)) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+      const int row = ui.m * 128 + q * 32 + lane;  // h column (GEMM1) or y column (GEMM2)
+      const int c0 = 16 * half;                     // this warp's 16 token columns
+      float v[16];
+      if (!ui.g2) {
+        float w[16];
+        ptx::tmem_ld16x2(tb + c0, tb + kNmax + c0, v, w);
+        __nv_bfloat16* orow = h_out + static_cast<long>(tl.z) * I + row;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(v[j]) * w[j]);
+      } else {
+        ptx::tmem_ld16(tb + c0, v);
+        __nv_bfloat16* orow = y_out + static_cast<long>(tl.z) * H + row;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * H] = __float2bfloat16_rn(v[j]);
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty0 + 8 * b);
+      if (!ui.g2) {
+        // publish this warp's h block: generic stores -> async-proxy readers
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(ready + ui.ti, 1);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t mlp_fused_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(moe_mlp_fused,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups) return cudaErrorInvalidValue;
+  return launch_pdl(moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st, *a.mapW13,
+                    *a.mapX, *a.mapW2, *a.mapH, a.tiles, a.group_start, a.n_groups, a.H, a.I,
+                    a.ready, static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y),
+                    a.status);
+}
+
+}  // namespace moe

@@ -113,6 +113,13 @@ long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
 
+// Decode-sized bf16 batches (32-token tiles, GEMM1 not split over K) run
+// both routed GEMMs in one persistent kernel with per-tile ready counters.
+bool mlp_fused(const moe_config* c, int T) {
+  return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && gemm1_ksplit(c, T) == 1 &&
+         n_local(c) <= 1024;
+}
+
 // With 256-token tiles both GEMMs run on CTA pairs: one M = 256 MMA over two
 // SMs, each SM staging half of the token rows. GEMM1 puts the 128 gate rows on
 // rank 0 and the matching 128 up rows on rank 1 (one double-buffered
@@ -241,7 +248,7 @@ AlignLayout align_layout(const moe_config* c, int T) {
 }
 
 struct MlpLayout {
-  size_t status, tiles, groups, x_perm, h_perm, part1, total;
+  size_t status, tiles, groups, ready, x_perm, h_perm, part1, total;
 };
 MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   Carver cv;
@@ -250,6 +257,7 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   L.status = cv.take(4);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(n_local(c) + 1));
+  L.ready = cv.take(sizeof(int) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.x_perm = cv.take(eb * static_cast<size_t>(cap) * c->hidden_size);
   L.h_perm = cv.take(eb * static_cast<size_t>(cap) * c->intermediate_size);
   L.part1 = cv.take(gemm1_ksplit(c, T) > 1 ? sizeof(float) * gemm1_ksplit(c, T) * cap * 2 *
@@ -261,7 +269,7 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
 
 struct FwdLayout {
   size_t status, topk_ids, topk_w, logits, hist, counts, offsets, sorted_ids, inv_pos;
-  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
+  size_t tiles, groups, ready, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
   int cap;
 };
 FwdLayout fwd_layout(const moe_config* c, int T) {
@@ -284,6 +292,7 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.inv_pos = cv.take(4 * TK);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(El + 1));
+  L.ready = cv.take(sizeof(int) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.x_perm = cv.take(eb * L.cap * c->hidden_size);
   L.h_perm = cv.take(eb * L.cap * c->intermediate_size);
   L.y_perm = cv.take(eb * L.cap * c->hidden_size);
@@ -347,19 +356,49 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
 
 int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
-           const void* w2, void* y_perm, Tile* tiles, int* groups, void* x_perm, void* h_perm,
-           float* part1, unsigned* status, cudaStream_t st, void* const* ev = nullptr,
-           bool tiles_ready = false) {
+           const void* w2, void* y_perm, Tile* tiles, int* groups, int* ready, void* x_perm,
+           void* h_perm, float* part1, unsigned* status, cudaStream_t st,
+           void* const* ev = nullptr, bool tiles_ready = false) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
   const bool pairs = gemms_on_pairs(c, T);
+  const bool fused = mlp_fused(c, T);
+  const int max_tiles = static_cast<int>(max_routed_tiles(c, T));
   if (!tiles_ready)
-    MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups,
-                                       static_cast<int>(max_routed_tiles(c, T)), status, st)));
+    MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
+                                       status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
-                                n_items, K, H, x_perm, st)));
+                                n_items, K, H, x_perm, st, fused ? ready : nullptr,
+                                fused ? max_tiles : 0)));
   if (ev) MOE_TRY(record_event(ev[0], st));
+  if (fused) {
+    CUtensorMap m13, mx, m2, mh;
+    if (!make_map(&m13, w13, c->act_dtype, static_cast<long>(El) * 2 * I, H, 128) ||
+        !make_map(&mx, x_perm, c->act_dtype, cap, H, 32) ||
+        !make_map(&m2, w2, c->act_dtype, static_cast<long>(El) * H, I, 128) ||
+        !make_map(&mh, h_perm, c->act_dtype, cap, I, 32))
+      return MOE_ERR_CUDA;
+    MlpFusedArgs a;
+    a.mapW13 = &m13;
+    a.mapX = &mx;
+    a.mapW2 = &m2;
+    a.mapH = &mh;
+    a.tiles = tiles;
+    a.group_start = groups;
+    a.n_groups = El;
+    a.H = H;
+    a.I = I;
+    a.ready = ready;
+    a.h = h_perm;
+    a.y = y_perm;
+    a.status = status;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    MOE_TRY(cuda_ok(launch_mlp_fused(a, sms, st)));
+    if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
+    return MOE_OK;
+  }
   const int ks1 = gemm1_ksplit(c, T);
   if (ks1 > 1) {
     // split over K: raw gate/up partials, then the SiLU*up epilogue
@@ -481,8 +520,9 @@ int moe_grouped_mlp(const moe_config* cfg, int T, const void* x, const int32_t* 
   unsigned* status = at<unsigned>(ws, L.status);
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return do_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm,
-                at<Tile>(ws, L.tiles), at<int>(ws, L.groups), at<void>(ws, L.x_perm),
-                at<void>(ws, L.h_perm), at<float>(ws, L.part1), status, st);
+                at<Tile>(ws, L.tiles), at<int>(ws, L.groups), at<int>(ws, L.ready),
+                at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
+                st);
 }
 
 int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const int32_t* inv_pos,
@@ -524,6 +564,28 @@ int moe_workspace_layout(const moe_config* cfg, int T, moe_workspace_offsets* ou
   out->total = L.total;
   out->cap = L.cap;
   out->block_m = kForwardBlock;
+  return MOE_OK;
+}
+
+int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (!out) return MOE_ERR_INVALID_ARG;
+  moe_plan p;
+  p.router_tensor_cores = router_on_tensor_cores(cfg, T) ? 1 : 0;
+  p.router_partials = router_ksplit(cfg, T);
+  p.align_kernels = align_kernel_count(static_cast<long>(T) * cfg->top_k, n_local(cfg));
+  p.tile_rows = routed_nmax(cfg, T);
+  p.fused_mlp = mlp_fused(cfg, T) ? 1 : 0;
+  p.gemm1_k_split = gemm1_ksplit(cfg, T);
+  p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
+  p.kernels = 0;
+  if (T > 0) {
+    // logits + top-k, align, gather + routed GEMMs, shared GEMMs, combine
+    p.kernels = 2 + p.align_kernels + (p.fused_mlp ? 2 : p.gemm1_k_split > 1 ? 4 : 3) +
+                (cfg->num_shared_experts > 0 ? 2 : 0) + 1;
+  }
+  *out = p;
   return MOE_OK;
 }
 
@@ -574,9 +636,10 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
-                 at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
-                 st, events ? events + 3 : nullptr, true));
-  n += gemm1_ksplit(cfg, T) > 1 ? 4 : 3;  // gather, GEMM1 [+ SiLU finalize], GEMM2
+                 at<int>(ws, L.ready), at<void>(ws, L.x_perm), at<void>(ws, L.h_perm),
+                 at<float>(ws, L.part1), status, st, events ? events + 3 : nullptr, true));
+  // gather, then GEMM1 [+ SiLU finalize] and GEMM2, or the fused MLP kernel
+  n += mlp_fused(cfg, T) ? 2 : gemm1_ksplit(cfg, T) > 1 ? 4 : 3;
   MOE_TRY(mark(5));
   const void* shared_y = nullptr;
   int S = 0;

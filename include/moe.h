@@ -293,6 +293,23 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
                       void* ws, size_t ws_bytes, void* stream,
                       void* const* events, int* kernels_launched);
 
+/* The kernel plan moe_forward follows for (cfg, T): which variant runs each
+ * stage. No page counterpart; it describes this library's own kernels, for
+ * instrumentation and tests. Host-only (no device work); returns the
+ * validation status of (cfg, T). The plan assumes shared-expert weights are
+ * passed when cfg->num_shared_experts > 0. */
+typedef struct {
+  int kernels;             /* kernels one moe_forward call launches           */
+  int router_tensor_cores; /* 1: router GEMM on tcgen05, 0: CUDA cores        */
+  int router_partials;     /* partial logit slabs the top-k kernel sums       */
+  int align_kernels;       /* 1 (one CTA) or 3 (count, scan, scatter)         */
+  int tile_rows;           /* token rows per routed GEMM tile: 32, 128 or 256 */
+  int gemm1_k_split;       /* 1, or K ranges of GEMM1 summed by a finalize    */
+  int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */
+  int fused_mlp;           /* 1: GEMM1 and GEMM2 in one persistent kernel     */
+} moe_plan;
+int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
+
 /* ------------------------------------------------------------------------ */
 /* Synchronises `stream` and reads the device status word at the start of
  * `ws`. Writes the raw MOE_DEV_* bits to *flags (nullable). Returns MOE_OK if

@@ -96,3 +96,40 @@ def test_workspace_sizes_and_layout():
     assert B.align_workspace_size(cfg, T) > 0
     assert B.grouped_mlp_workspace_size(cfg, T, lay.cap) >= 2 * lay.cap * (4096 + 14336)
     assert B.workspace_size(_cfg(top_k=0), T) == 0
+
+
+def _plan(wl, T=None):
+    from gpu_cases import cfg_of
+    return B.forward_plan(cfg_of(wl), wl.T if T is None else T)
+
+
+def test_forward_plan_per_workload():
+    import synth
+    # Mixtral-shape prefill: bf16 routed GEMMs on CTA pairs, 256-token tiles,
+    # fp32 router on CUDA cores split into 256-column slices of H
+    p = _plan(synth.MIXTRAL)
+    assert (p.tile_rows, p.cta_pairs, p.fused_mlp, p.gemm1_k_split) == (256, 1, 0, 1)
+    assert (p.router_tensor_cores, p.router_partials) == (0, 4096 // 256)
+    # route 2, align 1, gather + GEMM1 + GEMM2, combine
+    assert p.kernels == 2 + 1 + 3 + 1
+    # decode: 32-token tiles; T=8 and T=64 run both GEMMs in the fused kernel,
+    # T=1 leaves too few GEMM1 units and splits GEMM1 over K instead
+    for T in (8, 64):
+        p = _plan(synth.QWEN_DECODE, T)
+        assert (p.tile_rows, p.fused_mlp, p.gemm1_k_split, p.cta_pairs) == (32, 1, 1, 0)
+        assert p.router_tensor_cores == 1 and p.router_partials > 1
+        assert p.kernels == 2 + 1 + 2 + 1  # gather + fused MLP
+    p = _plan(synth.QWEN_DECODE, 1)
+    assert (p.fused_mlp, p.tile_rows) == (0, 32) and p.gemm1_k_split > 1
+    assert p.kernels == 2 + 1 + 4 + 1  # gather, GEMM1, SiLU finalize, GEMM2
+    # DeepSeek-V2 shape: three-pass align, shared experts add two GEMMs
+    p = _plan(synth.DEEPSEEK)
+    assert p.align_kernels == 3 and p.fused_mlp == 0
+    assert p.kernels == 2 + 3 + 3 + 2 + 1
+    # fp32 layers never take the bf16-only fused or pair kernels
+    p = _plan(synth.TINY)
+    assert (p.fused_mlp, p.cta_pairs, p.router_tensor_cores) == (0, 0, 0)
+    # T = 0 launches nothing; bad configs are refused
+    assert _plan(synth.TINY, 0).kernels == 0
+    with pytest.raises(B.MoeError):
+        B.forward_plan(_cfg(top_k=0), 16)

@@ -36,7 +36,12 @@ SMALL = {
     "wide_prefill": W("wide_prefill", T=1100, H=256, I=384, E=5, K=1),
     # long segments with enough work units: 256-token tiles on CTA pairs
     "pair_prefill": W("pair_prefill", T=4096, H=256, I=2048, E=8, K=2),
+    # decode-sized segments with >= 152 GEMM1 units: both GEMMs in the fused
+    # kernel (one tile per expert; then up to two ragged tiles per expert)
+    "fused_decode": W("fused_decode", T=64, H=256, I=512, E=64, K=8, router_bias=True),
+    "fused_two_tiles": W("fused_two_tiles", T=150, H=384, I=2048, E=16, K=4),
 }
+FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
     "deepseek_v2_prefill": synth.DEEPSEEK,
@@ -164,7 +169,7 @@ def test_align_general_expert_map_and_bad_ids():
 
 
 @pytest.mark.parametrize("name", ["ragged_prefill", "ragged_decode", "f32_ragged",
-                                  "grouped_shared"])
+                                  "grouped_shared", "fused_two_tiles"])
 def test_grouped_mlp_and_combine_entry_points(name):
     c = case(name)
     wl = c.wl
@@ -254,7 +259,7 @@ def test_skewed_single_expert_segment():
     check_forward(c)
 
 
-@pytest.mark.parametrize("name", ["ragged_decode", "grouped_shared"])
+@pytest.mark.parametrize("name", ["ragged_decode", "grouped_shared", "fused_decode"])
 def test_forward_captured_in_cuda_graph_matches_eager(name):
     """moe_forward enqueues only stream work (no host sync, no allocation), so
     it can be captured once and replayed; replays must equal the eager call."""
@@ -275,3 +280,22 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert B.moe_get_status(ws) == (0, 0)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "ragged_decode", "pair_prefill", *FUSED])
+def test_plan_matches_the_kernels_launched(name):
+    """moe_forward_plan (host only) names the path; moe_forward_timed counts
+    the kernels that path launched. The fused cases must take the fused
+    kernel, or their parity tests would not cover it."""
+    c = case(name)
+    wl, d = c.wl, c.d
+    plan = B.forward_plan(c.cfg, wl.T)
+    if name in FUSED:
+        assert plan.fused_mlp == 1 and plan.tile_rows == 32
+    ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
+    out = torch.empty(wl.T, wl.H, dtype=d["x"].dtype, device="cuda")
+    n = B.moe_forward_timed(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"],
+                            d["w2"], d["shared_w13"], d["shared_w2"], None, out, ws,
+                            [None] * 8)
+    assert B.moe_get_status(ws) == (0, 0)
+    assert n == plan.kernels
