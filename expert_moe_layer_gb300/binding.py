@@ -49,7 +49,8 @@ class WorkspaceOffsets(ctypes.Structure):
 
 
 class Plan(ctypes.Structure):
-    _fields_ = [("kernels", ctypes.c_int), ("router_tensor_cores", ctypes.c_int),
+    _fields_ = [("kernels", ctypes.c_int), ("fused_route", ctypes.c_int),
+                ("router_tensor_cores", ctypes.c_int),
                 ("router_partials", ctypes.c_int), ("align_kernels", ctypes.c_int),
                 ("tile_rows", ctypes.c_int), ("gemm1_k_split", ctypes.c_int),
                 ("cta_pairs", ctypes.c_int), ("fused_mlp", ctypes.c_int)]

@@ -1,0 +1,166 @@
+// Block-level pieces of token alignment shared by the align kernels and the
+// fused small-batch route kernel: expert-id mapping, a block-wide exclusive
+// scan, the routed tile table and the single-CTA counting sort.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace moe {
+
+__device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ emap, int E,
+                                            int E_l, int ep_start, unsigned* status) {
+  if (id < 0 || id >= E) {
+    if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+    return -1;
+  }
+  int le;
+  if (emap) {
+    le = emap[id];
+    if (le < -1 || le >= E_l) {
+      if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+      return -1;
+    }
+  } else {
+    le = id - ep_start;
+    if (le < 0 || le >= E_l) le = -1;
+  }
+  return le;
+}
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  __syncthreads();  // warp_sums may still be read by a previous scan
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_sums[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < (blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+  total = warp_sums[(blockDim.x >> 5) - 1];
+  return incl - v;
+}
+
+// Block-wide: the routed tile table from each expert's count c and first
+// row off (thread e < E_l; other threads pass c = 0). Called by every thread.
+__device__ __forceinline__ void write_tile_table(int e, int E_l, int c, int off, int nmax,
+                                                 Tile* __restrict__ tiles,
+                                                 int* __restrict__ group_start, int max_tiles,
+                                                 int* warp_sums, unsigned* status) {
+  const int n = e < E_l ? (c + nmax - 1) / nmax : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(n, warp_sums, total);
+  for (int j = 0; j < n; ++j) {
+    const int idx = start + j;
+    if (idx < max_tiles) {
+      const int r0 = off + j * nmax;
+      tiles[idx] = make_int4(e, r0, r0, min(nmax, c - j * nmax));
+    }
+  }
+  if (e < E_l) group_start[e] = min(start, max_tiles);
+  if (threadIdx.x == 0) {
+    group_start[E_l] = min(total, max_tiles);
+    if (total > max_tiles && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+  }
+}
+
+// Single-CTA alignment for n_items <= kSmallItems and E_l <= kSmallExperts,
+// run by a CTA of exactly 1024 threads (32 warps). A warp owns a run of
+// consecutive items; per-warp counts live in hist ([warp][expert], 32*E_l
+// ints of shared memory), which then become each warp's base rows, and the
+// walk is replayed in the same order, so the order inside a segment is
+// ascending item order (a stable counting sort). warp_sums: 32 ints of
+// shared memory. ids may have been written by this CTA before a
+// __syncthreads().
+constexpr int kSmallItems = 32 * 256;
+constexpr int kSmallExperts = 256;
+
+__device__ __forceinline__ void align_small_block(
+    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
+    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
+    int* __restrict__ group_start, int nmax, int max_tiles, int* hist, int* warp_sums) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ipw = ((n_items + 31) / 32 + 31) / 32 * 32;  // items per warp, multiple of 32
+  for (int r = threadIdx.x; r < cap; r += 1024) sorted_ids[r] = n_items;
+  for (int i = threadIdx.x; i < 32 * E_l; i += 1024) hist[i] = 0;
+  __syncthreads();
+  int* my = hist + warp * E_l;
+  const int base = warp * ipw;
+  for (int r = 0; r < ipw; r += 32) {
+    const int item = base + r + lane;
+    int le = -1;
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // counts, padded offsets, per-warp base rows
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E_l)
+    for (int w = 0; w < 32; ++w) c += hist[w * E_l + e];
+  const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(padded, warp_sums, total);
+  if (e < E_l) {
+    counts[e] = c;
+    offsets[e] = start;
+    int run = start;
+    for (int w = 0; w < 32; ++w) {
+      const int h = hist[w * E_l + e];
+      hist[w * E_l + e] = run;
+      run += h;
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[E_l] = total;
+    if (total > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+  }
+  if (tiles)
+    write_tile_table(e, E_l, e < E_l ? c : 0, start, nmax, tiles, group_start, max_tiles,
+                     warp_sums, status);
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < ipw; r += 32) {
+    const int item = base + r + lane;
+    int le = -1;
+    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (item < n_items) {
+      int pos = -1;
+      if (le >= 0) {
+        pos = my[le] + __popc(peers & lt);
+        if (pos < cap) {
+          sorted_ids[pos] = item;
+        } else {
+          if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+          pos = -1;
+        }
+      }
+      inv_pos[item] = pos;
+    }
+    __syncwarp();
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+
+}  // namespace moe

@@ -74,6 +74,38 @@ cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
                         int renorm, int n_group, int topk_group, int32_t* ids,
                         float* w, unsigned* status, cudaStream_t st);
 
+// Routing and single-CTA alignment of a small batch in one kernel: router
+// logits ([T, E] fp32 into logits), fp32 softmax, (grouped) top-k and
+// renormalise into ids / w, then the counting sort into segments and the
+// routed tile table, as launch_topk + launch_align would. tickets:
+// kRouteTickets ints, zero before the call (the kernel leaves them zero).
+constexpr int kRouteSmallTokens = 128;
+constexpr int kRouteTickets = kRouteSmallTokens / 16 + 1;
+struct RouteAlignArgs {
+  const void* x;
+  const void* wg;
+  const float* bias;
+  int T, E, H, K, renorm, n_group, topk_group;
+  float* logits;
+  int* tickets;
+  int32_t* ids;
+  float* w;
+  const int32_t* emap;
+  int E_l, ep_start, block_m;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_ids;
+  int32_t* inv_pos;
+  int cap;
+  unsigned* status;
+  Tile* tiles;
+  int* group_start;
+  int nmax, max_tiles;
+};
+bool route_align_small_ok(int T, int K, int E_l);
+cudaError_t launch_route_align_small(const RouteAlignArgs& a, bool act_bf16, bool router_bf16,
+                                     cudaStream_t st);
+
 // Alignment / permutation. hist has n_warps*E_l ints, n_warps = align_warps(T*K).
 // Small inputs run as one fused kernel (hist unused), larger ones as three.
 int align_kernel_count(long n_items, int E_l);

@@ -3,8 +3,11 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include "align_block.cuh"
 #include "internal.h"
 #include "launch.cuh"
+#include "ptx.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 namespace {
@@ -163,119 +166,6 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __re
 }
 
 // --------------------------------------------------------------- top-k
-// One warp per token. Lane l holds experts e = l + 32*j (j < VPL).
-// Ordering: larger value first, equal values -> lower index first.
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (better(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-}
-
-// The warp-level routing decision for one token. p[j] holds the logit (with
-// bias) of expert lane + 32*j, or -inf beyond E. Softmax, the optional group
-// limit, K rounds of argmax and the renormalisation all run on this warp.
-template <int VPL>
-__device__ __forceinline__ void topk_warp(float (&p)[VPL], int lane, int E, int K, int renorm,
-                                          int n_group, int topk_group,
-                                          int32_t* __restrict__ ids_row,
-                                          float* __restrict__ w_row) {
-  float mx = -CUDART_INF_F;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) mx = fmaxf(mx, p[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    p[j] = (e < E) ? expf(p[j] - mx) : 0.f;
-    sum += p[j];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] / sum : -CUDART_INF_F;
-
-  // candidate values: p, or -inf outside the kept groups
-  float c[VPL];
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) c[j] = p[j];
-  if (n_group > 0) {
-    const int gs = E / n_group;
-    float my_score = -CUDART_INF_F;  // lane g holds the score of group g
-    for (int g = 0; g < n_group; ++g) {
-      float m = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && e / gs == g) m = fmaxf(m, p[j]);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == g) my_score = m;
-    }
-    bool taken = false;
-    for (int r = 0; r < topk_group; ++r) {
-      float v = (lane < n_group && !taken) ? my_score : -CUDART_INF_F;
-      int i = (lane < n_group && !taken) ? lane : 0x7fffffff;
-      warp_argmax(v, i);
-      if (lane == i) taken = true;
-    }
-    const unsigned keep = __ballot_sync(0xffffffffu, taken);
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((keep >> (e / gs)) & 1u)) c[j] = -CUDART_INF_F;
-    }
-  }
-
-  float my_w = 0.f;
-  int my_id = 0;
-  float wsum = 0.f;
-  for (int k = 0; k < K; ++k) {
-    float v = -CUDART_INF_F;
-    int i = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && better(c[j], e, v, i)) {
-        v = c[j];
-        i = e;
-      }
-    }
-    warp_argmax(v, i);
-    // owner lane marks the winner as taken and publishes its probability
-    float pw = 0.f;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      if (lane + 32 * j == i) {
-        pw = p[j];
-        c[j] = -CUDART_INF_F;
-      }
-    }
-    pw = __shfl_sync(0xffffffffu, pw, i & 31);
-    wsum += pw;
-    if (lane == k) {
-      my_w = pw;
-      my_id = i;
-    }
-  }
-  if (lane < K) {
-    ids_row[lane] = my_id;
-    w_row[lane] = renorm ? my_w / wsum : my_w;
-  }
-}
-
 // One warp per token (large batches): logits = sum of n_part partial slabs.
 template <int VPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
@@ -337,6 +227,219 @@ __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__
   topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + t * K, wout + t * K);
 }
 
+// ------------------------------------------------- small batches: fused
+// Routing and alignment of a small batch in one launch (T <= kRouteSmallTokens
+// and the single-CTA align applies). Grid (E/8 expert octets, T/16 token
+// blocks), CTAs of 1024 threads.
+//   phase 1, every CTA: logits of its 8 experts x 16 tokens. Thread 0 bulk
+//     copies the 8 router rows and 16 token rows (in chunks of kHC columns,
+//     rows padded by 16 bytes) into shared memory, all in flight at once on
+//     one mbarrier. bf16 x bf16: each warp takes a share of the 16-column K
+//     steps on mma.sync m16n8k16 (fp32 accumulation) and the 32 partial
+//     16x8 tiles are summed in warp order. Otherwise warp w takes expert
+//     w & 7 and tokens 4*(w >> 3) .. +3 with fp32 FMA and a butterfly sum.
+//   the last CTA of a token block (ticket per block) takes the decision for
+//     its 16 tokens (topk_warp, one warp per token); the last of those
+//     (block ticket) runs the single-CTA alignment and tile table. Each
+//     ticket is reset by the CTA that drew the last number. A ticket is drawn
+//     after a __syncthreads by one thread with an acquire-release atomic, so
+//     the CTA's writes are published and the other CTAs' writes observed.
+// A copy that does not complete in time sets MOE_DEV_TIMEOUT; the CTA still
+// draws its tickets, so the tables downstream are always well formed.
+constexpr int kRouteTokBlock = 16;
+
+template <typename TX, typename TW>
+struct RouteSmem {
+  static constexpr int kHC = sizeof(TX) == 4 ? 1024 : 2048;  // columns per chunk
+  static constexpr int kRW = kHC + 16 / static_cast<int>(sizeof(TW));  // padded row strides
+  static constexpr int kRX = kHC + 16 / static_cast<int>(sizeof(TX));
+  static constexpr int kW = 8 * kRW * static_cast<int>(sizeof(TW));
+  static constexpr int kX = kRouteTokBlock * kRX * static_cast<int>(sizeof(TX));
+  static constexpr int kHist = 4 * 32 * kSmallExperts;  // align counts, or MMA partials
+  static constexpr int kBytes = kW + kX + kHist + 4 * 32 + 16 + 128;
+  static constexpr bool kMma = sizeof(TX) == 2 && sizeof(TW) == 2;
+};
+
+__device__ __forceinline__ int ticket_acq_rel(int* p) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                               const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+template <typename TX, typename TW, int VPL>
+__global__ void __launch_bounds__(1024) route_align_small_kernel(
+    const TX* __restrict__ x, const TW* __restrict__ wg, const float* __restrict__ bias, int T,
+    int E, int H, int K, int renorm, int n_group, int topk_group, float* __restrict__ logits,
+    int* __restrict__ tickets, int32_t* __restrict__ ids, float* __restrict__ wout,
+    const int32_t* __restrict__ emap, int E_l, int ep_start, int block_m,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
+    unsigned* status, Tile* __restrict__ tiles, int* __restrict__ group_start, int nmax,
+    int max_tiles) {
+  using S = RouteSmem<TX, TW>;
+  pdl_enter();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  TW* wbuf = reinterpret_cast<TW*>(smem);
+  TX* xbuf = reinterpret_cast<TX*>(smem + S::kW);
+  int* hist = reinterpret_cast<int*>(smem + S::kW + S::kX);
+  int* warp_sums = hist + 32 * kSmallExperts;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(warp_sums + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
+  __shared__ int is_last;
+  const uint32_t bar_a = ptx::smem_u32(bar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * 8, tb0 = blockIdx.y * kRouteTokBlock;
+  const int ne = min(8, E - e0), nt = min(kRouteTokBlock, T - tb0);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_a, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+
+  // the router bias of the decision warps, fetched while the logits are made
+  float bv[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int ex = lane + 32 * j;
+    bv[j] = (bias && warp < nt && ex < E) ? bias[ex] : 0.f;
+  }
+
+  const int el = warp & 7, ta = 4 * (warp >> 3);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int hc0 = 0; hc0 < H && ok; hc0 += S::kHC, phase ^= 1) {
+    const int hc = min(S::kHC, H - hc0);
+    if (threadIdx.x == 0) {
+      const uint32_t wrow = hc * sizeof(TW), xrow = hc * sizeof(TX);
+      ptx::mbar_arrive_expect_tx(bar_a, ne * wrow + nt * xrow);
+      for (int j = 0; j < ne; ++j)
+        ptx::bulk_load(ptx::smem_u32(wbuf + j * S::kRW), wg + static_cast<long>(e0 + j) * H + hc0,
+                       wrow, bar_a);
+      for (int a = 0; a < nt; ++a)
+        ptx::bulk_load(ptx::smem_u32(xbuf + a * S::kRX), x + static_cast<long>(tb0 + a) * H + hc0,
+                       xrow, bar_a);
+    }
+    ok = __syncthreads_and(ptx::mbar_wait(bar_a, phase, abort_flag, status));
+    if (ok) {
+      if constexpr (S::kMma) {
+        // acc = this warp's partial D[token][expert] over its K steps
+        const uint32_t xa = ptx::smem_u32(xbuf) +
+                            ((lane & 15) * S::kRX + (lane >> 4) * 8) * 2;
+        const uint32_t wa = ptx::smem_u32(wbuf) + ((lane & 7) * S::kRW + ((lane >> 3) & 1) * 8) * 2;
+        for (int ks = warp; ks < hc / 16; ks += 32) {
+          uint32_t a[4], b[2];
+          ldsm_x4(xa + ks * 32, a);
+          ldsm_x2(wa + ks * 32, b);
+          mma_bf16_16816(acc, a, b);
+        }
+      } else if (el < ne && ta < nt) {
+        const TW* wr = wbuf + el * S::kRW;
+        for (int h = lane * 8; h < hc; h += 256) {
+          float wv[8], xv[8];
+          load8(wr + h, wv);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            if (ta + a < nt) {
+              load8(xbuf + (ta + a) * S::kRX + h, xv);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[a] = fmaf(xv[i], wv[i], acc[a]);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // the next chunk overwrites the buffers
+  }
+  if (!ok && threadIdx.x == 0) ptx::mbar_wait_drain(bar_a, phase);  // let late copies land
+  if (ok) {
+    if constexpr (S::kMma) {
+      // partial tiles -> shared memory (the align counts area), then a fixed
+      // order sum over the 32 warps; lane holds D rows g, g+8, columns 2c, 2c+1
+      float* red = reinterpret_cast<float*>(hist);
+      const int g = lane >> 2, c = 2 * (lane & 3);
+      red[warp * 128 + g * 8 + c] = acc[0];
+      red[warp * 128 + g * 8 + c + 1] = acc[1];
+      red[warp * 128 + (g + 8) * 8 + c] = acc[2];
+      red[warp * 128 + (g + 8) * 8 + c + 1] = acc[3];
+      __syncthreads();
+      if (threadIdx.x < 128) {
+        const int r = threadIdx.x >> 3, col = threadIdx.x & 7;
+        float v = 0.f;
+        for (int w2 = 0; w2 < 32; ++w2) v += red[w2 * 128 + threadIdx.x];
+        if (r < nt && col < ne) logits[static_cast<long>(tb0 + r) * E + e0 + col] = v;
+      }
+    } else if (el < ne && ta < nt) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[a] += __shfl_xor_sync(0xffffffffu, acc[a], o);
+      }
+      if (lane < 4 && ta + lane < nt) {
+        float v = acc[0];
+#pragma unroll
+        for (int a = 1; a < 4; ++a)
+          if (lane == a) v = acc[a];
+        logits[static_cast<long>(tb0 + ta + lane) * E + e0 + el] = v;
+      }
+    }
+  }
+
+  // last CTA of this token block: the routing decisions of its tokens
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    is_last = ticket_acq_rel(tickets + blockIdx.y) == static_cast<int>(gridDim.x) - 1;
+    if (is_last) tickets[blockIdx.y] = 0;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  if (warp < nt) {
+    const int t = tb0 + warp;
+    float p[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int ex = lane + 32 * j;
+      p[j] = ex < E ? __ldcg(logits + static_cast<long>(t) * E + ex) + bv[j] : -CUDART_INF_F;
+    }
+    topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + static_cast<long>(t) * K,
+                   wout + static_cast<long>(t) * K);
+  }
+
+  // last token block: alignment of all T*K items
+  __syncthreads();
+  int* block_ticket = tickets + gridDim.y;
+  if (threadIdx.x == 0) {
+    is_last = ticket_acq_rel(block_ticket) == static_cast<int>(gridDim.y) - 1;
+    if (is_last) *block_ticket = 0;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  align_small_block(ids, T * K, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
+                    inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
+}
+
 }  // namespace
 
 template <typename TX, typename TW>
@@ -371,6 +474,50 @@ cudaError_t topk_launch(const float* logits, int n_part, long partial_stride, co
                       partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
   return launch_pdl(topk_kernel<V>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
                     partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
+}
+
+template <typename TX, typename TW, int VPL>
+cudaError_t route_align_launch(const RouteAlignArgs& a, cudaStream_t st) {
+  using S = RouteSmem<TX, TW>;
+  auto kern = route_align_small_kernel<TX, TW, VPL>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  return launch_pdl(kern, dim3((a.E + 7) / 8, (a.T + kRouteTokBlock - 1) / kRouteTokBlock),
+                    dim3(1024), S::kBytes, st, static_cast<const TX*>(a.x),
+                    static_cast<const TW*>(a.wg), a.bias, a.T,
+                    a.E, a.H, a.K, a.renorm, a.n_group, a.topk_group, a.logits, a.tickets, a.ids,
+                    a.w, a.emap, a.E_l, a.ep_start, a.block_m, a.counts, a.offsets,
+                    a.sorted_ids, a.inv_pos, a.cap, a.status, a.tiles, a.group_start, a.nmax,
+                    a.max_tiles);
+}
+
+template <typename TX, typename TW>
+cudaError_t route_align_vpl(const RouteAlignArgs& a, cudaStream_t st) {
+  const int vpl = (a.E + 31) / 32;
+  if (vpl <= 1) return route_align_launch<TX, TW, 1>(a, st);
+  if (vpl <= 2) return route_align_launch<TX, TW, 2>(a, st);
+  if (vpl <= 4) return route_align_launch<TX, TW, 4>(a, st);
+  if (vpl <= 8) return route_align_launch<TX, TW, 8>(a, st);
+  if (vpl <= 16) return route_align_launch<TX, TW, 16>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+bool route_align_small_ok(int T, int K, int E_l) {
+  return T >= 1 && T <= kRouteSmallTokens && static_cast<long>(T) * K <= kSmallItems &&
+         E_l <= kSmallExperts;
+}
+
+cudaError_t launch_route_align_small(const RouteAlignArgs& a, bool act_bf16, bool router_bf16,
+                                     cudaStream_t st) {
+  if (!route_align_small_ok(a.T, a.K, a.E_l)) return cudaErrorInvalidValue;
+  if (act_bf16 && router_bf16) return route_align_vpl<__nv_bfloat16, __nv_bfloat16>(a, st);
+  if (act_bf16) return route_align_vpl<__nv_bfloat16, float>(a, st);
+  return route_align_vpl<float, float>(a, st);
 }
 
 cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,

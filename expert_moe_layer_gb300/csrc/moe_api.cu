@@ -280,7 +280,7 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   const int El = n_local(c);
   const int S = c->num_shared_experts;
   L.cap = static_cast<int>(TK + static_cast<size_t>(El) * (kForwardBlock - 1));
-  L.status = cv.take(4);
+  L.status = cv.take(4 + 4 * kRouteTickets);  // status word, small-batch route tickets
   L.topk_ids = cv.take(4 * TK);
   L.topk_w = cv.take(4 * TK);
   L.logits = cv.take(sizeof(float) * static_cast<size_t>(router_ksplit(c, T)) * T *
@@ -572,17 +572,21 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   MOE_TRY(validate_T(T));
   if (!out) return MOE_ERR_INVALID_ARG;
   moe_plan p;
-  p.router_tensor_cores = router_on_tensor_cores(cfg, T) ? 1 : 0;
-  p.router_partials = router_ksplit(cfg, T);
-  p.align_kernels = align_kernel_count(static_cast<long>(T) * cfg->top_k, n_local(cfg));
+  p.fused_route = route_align_small_ok(T, cfg->top_k, n_local(cfg)) ? 1 : 0;
+  p.router_tensor_cores = !p.fused_route && router_on_tensor_cores(cfg, T) ? 1 : 0;
+  p.router_partials = p.fused_route ? 1 : router_ksplit(cfg, T);
+  p.align_kernels =
+      p.fused_route ? 0 : align_kernel_count(static_cast<long>(T) * cfg->top_k, n_local(cfg));
   p.tile_rows = routed_nmax(cfg, T);
   p.fused_mlp = mlp_fused(cfg, T) ? 1 : 0;
   p.gemm1_k_split = gemm1_ksplit(cfg, T);
   p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
   p.kernels = 0;
   if (T > 0) {
-    // logits + top-k, align, gather + routed GEMMs, shared GEMMs, combine
-    p.kernels = 2 + p.align_kernels + (p.fused_mlp ? 2 : p.gemm1_k_split > 1 ? 4 : 3) +
+    // logits + top-k and align (or the fused route kernel), gather + routed
+    // GEMMs, shared GEMMs, combine
+    p.kernels = (p.fused_route ? 1 : 2 + p.align_kernels) +
+                (p.fused_mlp ? 2 : p.gemm1_k_split > 1 ? 4 : 3) +
                 (cfg->num_shared_experts > 0 ? 2 : 0) + 1;
   }
   *out = p;
@@ -620,19 +624,55 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
   int n = 0;
 
-  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4 + 4 * kRouteTickets, st)));
   MOE_TRY(mark(0));
-  MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
-                   status, st));
-  n += 2;  // logits + top-k
-  MOE_TRY(mark(1));
-  MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts, El,
-                               cfg->ep_rank * El, kForwardBlock, at<int>(ws, L.hist), counts,
-                               offsets, sorted_ids, inv_pos, L.cap, status, st,
-                               at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
-                               routed_nmax(cfg, T),
-                               static_cast<int>(max_routed_tiles(cfg, T)))));
-  n += align_kernel_count(static_cast<long>(T) * K, El);
+  if (route_align_small_ok(T, K, El)) {
+    RouteAlignArgs a;
+    a.x = x;
+    a.wg = router_w;
+    a.bias = router_bias;
+    a.T = T;
+    a.E = cfg->num_experts;
+    a.H = H;
+    a.K = K;
+    a.renorm = cfg->renormalize ? 1 : 0;
+    a.n_group = cfg->use_grouped_topk ? cfg->num_expert_group : 0;
+    a.topk_group = cfg->use_grouped_topk ? cfg->topk_group : 0;
+    a.logits = at<float>(ws, L.logits);
+    a.tickets = reinterpret_cast<int*>(status + 1);
+    a.ids = ids;
+    a.w = w;
+    a.emap = expert_map;
+    a.E_l = El;
+    a.ep_start = cfg->ep_rank * El;
+    a.block_m = kForwardBlock;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.sorted_ids = sorted_ids;
+    a.inv_pos = inv_pos;
+    a.cap = L.cap;
+    a.status = status;
+    a.tiles = at<Tile>(ws, L.tiles);
+    a.group_start = at<int>(ws, L.groups);
+    a.nmax = routed_nmax(cfg, T);
+    a.max_tiles = static_cast<int>(max_routed_tiles(cfg, T));
+    MOE_TRY(cuda_ok(launch_route_align_small(a, cfg->act_dtype == MOE_BF16,
+                                             cfg->router_dtype == MOE_BF16, st)));
+    n += 1;
+    MOE_TRY(mark(1));  // routing and align share one kernel
+  } else {
+    MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
+                     status, st));
+    n += 2;  // logits + top-k
+    MOE_TRY(mark(1));
+    MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts,
+                                 El, cfg->ep_rank * El, kForwardBlock, at<int>(ws, L.hist),
+                                 counts, offsets, sorted_ids, inv_pos, L.cap, status, st,
+                                 at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
+                                 routed_nmax(cfg, T),
+                                 static_cast<int>(max_routed_tiles(cfg, T)))));
+    n += align_kernel_count(static_cast<long>(T) * K, El);
+  }
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),

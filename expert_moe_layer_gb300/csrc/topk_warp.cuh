@@ -1,0 +1,156 @@
+// The per-token routing decision on one warp: fp32 softmax over the logits,
+// the optional group limit, top-k and renormalisation (MixtralMoE.forward;
+// FusedMoE select_experts / grouped_topk arguments).
+//
+// Order: larger probability first, equal probabilities -> lower expert id.
+// Every argmax is two single-instruction warp reductions (redux.sync) on an
+// order-preserving 32-bit key of the float: the largest key, then the lowest
+// expert id among the lanes that hold it. Each lane sorts its own candidates
+// once, so a selection round only pops the winner's head.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+namespace moe {
+
+// Unsigned key with key(a) > key(b) <=> a > b for non-NaN floats (-0 sorts
+// just below +0; probabilities are never -0). NaN maps to 0, below every
+// number, so it is never chosen over one.
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t b = __float_as_uint(v);
+  if (v != v) return 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Warp argmax of (key, id) with ties to the lower id; every lane gets both.
+__device__ __forceinline__ void warp_argmax_key(uint32_t& key, int& id) {
+  const uint32_t m = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t cand = key == m ? static_cast<uint32_t>(id) : 0x7fffffffu;
+  id = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+  key = m;
+}
+
+// The warp-level routing decision for one token. p[j] holds the logit (with
+// bias) of expert lane + 32*j, or -inf beyond E. Softmax, the optional group
+// limit, K selections and the renormalisation all run on this warp. Lane k < K
+// writes ids_row[k] and w_row[k].
+template <int VPL>
+__device__ __forceinline__ void topk_warp(float (&p)[VPL], int lane, int E, int K, int renorm,
+                                          int n_group, int topk_group,
+                                          int32_t* __restrict__ ids_row,
+                                          float* __restrict__ w_row) {
+  // softmax in fp32: max, exp, sum, divide
+  float lmx = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) lmx = fmaxf(lmx, p[j]);
+  const float mx = fkey_inv(__reduce_max_sync(0xffffffffu, fkey(lmx)));
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    p[j] = (e < E) ? expf(p[j] - mx) : 0.f;
+    sum += p[j];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] / sum : -CUDART_INF_F;
+
+  // candidate keys: p, or -inf outside the kept groups (group score = the
+  // largest p in the group; topk_group groups by score, ties to lower group)
+  uint32_t ck[VPL];
+  int ci[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    ck[j] = fkey(p[j]);
+    ci[j] = lane + 32 * j;
+  }
+  if (n_group > 0) {
+    const int gs = E / n_group;
+    uint32_t my_score = 0;  // lane g holds the key of group g's score
+    for (int g = 0; g < n_group; ++g) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && e / gs == g) m = max(m, ck[j]);
+      }
+      m = __reduce_max_sync(0xffffffffu, m);
+      if (lane == g) my_score = m;
+    }
+    bool taken = false;
+    for (int r = 0; r < topk_group; ++r) {
+      uint32_t key = (lane < n_group && !taken) ? my_score : 0u;
+      int id = (lane < n_group && !taken) ? lane : 0x7fffffff;
+      warp_argmax_key(key, id);
+      if (lane == id) taken = true;
+    }
+    const unsigned keep = __ballot_sync(0xffffffffu, taken);
+    const uint32_t ninf = fkey(-CUDART_INF_F);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && !((keep >> (e / gs)) & 1u)) ck[j] = ninf;
+    }
+  }
+
+  // this lane's candidates in decision order (odd-even transposition sort)
+#pragma unroll
+  for (int r = 0; r < VPL; ++r) {
+#pragma unroll
+    for (int j = r & 1; j + 1 < VPL; j += 2) {
+      const bool swap = ck[j + 1] > ck[j] || (ck[j + 1] == ck[j] && ci[j + 1] < ci[j]);
+      if (swap) {
+        const uint32_t tk = ck[j];
+        ck[j] = ck[j + 1];
+        ck[j + 1] = tk;
+        const int ti = ci[j];
+        ci[j] = ci[j + 1];
+        ci[j + 1] = ti;
+      }
+    }
+  }
+  // lanes beyond E hold -inf entries with ids >= E; they never win while a
+  // real expert remains
+  int head = 0;
+  uint32_t hk = ck[0];
+  int hi = ci[0];
+  float my_w = 0.f;
+  int my_id = 0;
+  float wsum = 0.f;
+  for (int k = 0; k < K; ++k) {
+    uint32_t key = hk;
+    int id = hi;
+    warp_argmax_key(key, id);
+    const float pw = fkey_inv(key);
+    if (hi == id) {  // the owner pops its head
+      ++head;
+      hk = 0u;
+      hi = 0x7fffffff;
+#pragma unroll
+      for (int j = 1; j < VPL; ++j) {
+        if (j == head) {
+          hk = ck[j];
+          hi = ci[j];
+        }
+      }
+    }
+    wsum += pw;
+    if (lane == k) {
+      my_w = pw;
+      my_id = id;
+    }
+  }
+  if (lane < K) {
+    ids_row[lane] = my_id;
+    w_row[lane] = renorm ? my_w / wsum : my_w;
+  }
+}
+
+}  // namespace moe

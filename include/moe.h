@@ -300,9 +300,10 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
  * passed when cfg->num_shared_experts > 0. */
 typedef struct {
   int kernels;             /* kernels one moe_forward call launches           */
+  int fused_route;         /* 1: logits, top-k and align in one kernel        */
   int router_tensor_cores; /* 1: router GEMM on tcgen05, 0: CUDA cores        */
   int router_partials;     /* partial logit slabs the top-k kernel sums       */
-  int align_kernels;       /* 1 (one CTA) or 3 (count, scan, scatter)         */
+  int align_kernels;       /* 0 (fused route), 1 (one CTA) or 3 (3 passes)    */
   int tile_rows;           /* token rows per routed GEMM tile: 32, 128 or 256 */
   int gemm1_k_split;       /* 1, or K ranges of GEMM1 summed by a finalize    */
   int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */

@@ -40,8 +40,18 @@ SMALL = {
     # kernel (one tile per expert; then up to two ragged tiles per expert)
     "fused_decode": W("fused_decode", T=64, H=256, I=512, E=64, K=8, router_bias=True),
     "fused_two_tiles": W("fused_two_tiles", T=150, H=384, I=2048, E=16, K=4),
+    # small batches route and align in one kernel: bf16 x with an fp32 router,
+    # group-limited top-k with shared experts, an EP shard, and E > 256
+    "f32_router_decode": W("f32_router_decode", T=16, H=256, I=256, E=8, K=2, router="f32"),
+    "grouped_decode": synth.DEEPSEEK.with_(name="grouped_decode", T=24, H=256, I=256,
+                                           I_shared=256),
+    "ep_decode": synth.EP_SHARD.with_(name="ep_decode", T=32, H=256, I=256),
+    "wide_router": W("wide_router", T=12, H=128, I=128, E=320, K=4, ep_size=2, ep_rank=1,
+                     router_bias=True),
 }
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
+ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
+               "grouped_decode", "ep_decode", "wide_router")
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
     "deepseek_v2_prefill": synth.DEEPSEEK,
@@ -282,7 +292,7 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
     assert B.moe_get_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "ragged_decode", "pair_prefill", *FUSED])
+@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED])
 def test_plan_matches_the_kernels_launched(name):
     """moe_forward_plan (host only) names the path; moe_forward_timed counts
     the kernels that path launched. The fused cases must take the fused
@@ -292,6 +302,10 @@ def test_plan_matches_the_kernels_launched(name):
     plan = B.forward_plan(c.cfg, wl.T)
     if name in FUSED:
         assert plan.fused_mlp == 1 and plan.tile_rows == 32
+    if name in ROUTE_FUSED:
+        assert plan.fused_route == 1
+    if name in ("pair_prefill", "ragged_prefill"):
+        assert plan.fused_route == 0 and plan.align_kernels == 1
     ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
     out = torch.empty(wl.T, wl.H, dtype=d["x"].dtype, device="cuda")
     n = B.moe_forward_timed(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"],
