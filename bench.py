@@ -293,28 +293,43 @@ def run_ours(args, wl, rank, world, device):
     alg_bytes = (touched * 3 * wl.H * wl.I * eb + wl.E * wl.H * rb
                  + wl.n_shared * 3 * wl.H * wl.I_shared * eb + 2 * T * wl.H * eb)
 
-    # dominant kernel: GEMM1 (gate/up, SiLU epilogue)
-    g1_ms = stages["gemm1_silu"]
-    g1_flops = 4 * A * wl.H * wl.I
-    g1_bytes = touched * 2 * wl.I * wl.H * eb + A * wl.H * eb + A * wl.I * eb
+    # dominant kernel: GEMM1 (gate/up, SiLU epilogue), or for decode-sized
+    # batches the fused kernel that runs GEMM1 and GEMM2 together
+    plan = B.forward_plan(cfg, T)
+    w13_bytes = touched * 2 * wl.I * wl.H * eb
+    w2_bytes = touched * wl.H * wl.I * eb
+    if plan.fused_mlp:
+        kname, ksrc = "moe_mlp_fused (GEMM1 + GEMM2)", "kernels_mlp_fused.cu"
+        k_ms = stages["gemm1_silu"]
+        k_flops = 6 * A * wl.H * wl.I
+        # weights once; x rows in, h out and back in, y out
+        k_bytes = w13_bytes + w2_bytes + (2 * A * wl.H + 2 * A * wl.I) * eb
+    else:
+        kname, ksrc = (("moe_gemm_pair<SiLU> (GEMM1, CTA pairs)", "kernels_gemm_pair.cu")
+                       if plan.cta_pairs else
+                       ("moe_gemm_tc<SiLU> (GEMM1)", "kernels_gemm.cu"))
+        k_ms = stages["gemm1_silu"]
+        k_flops = 4 * A * wl.H * wl.I
+        k_bytes = w13_bytes + A * wl.H * eb + A * wl.I * eb
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    tensor_bound = g1_flops / max(g1_bytes, 1) >= ridge
+    tensor_bound = k_flops / max(k_bytes, 1) >= ridge
     if tensor_bound:
-        ach = g1_flops / (g1_ms / 1e3) / 1e12
+        ach = k_flops / (k_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 4),
                 "peak_basis": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
                 "frac_of_burst": round(ach / peaks["bf16_tflops"], 4)}
     else:
-        ach = g1_bytes / (g1_ms / 1e3) / 1e9
+        ach = k_bytes / (k_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_basis": f"{peaks['source']} HBM copy",
                 "frac_of_nominal_8TBs": round(ach / 8000.0, 4)}
-    roof.update({"kernel": "moe_gemm_tc<SiLU-up> (GEMM1)", "ms_per_launch": round(g1_ms, 4),
-                 "algorithmic_flops": g1_flops, "algorithmic_bytes": g1_bytes,
-                 "traffic": traffic_from_profile(wl.name)})
+    roof.update({"kernel": kname, "ms_per_launch": round(k_ms, 4),
+                 "algorithmic_flops": k_flops, "algorithmic_bytes": k_bytes,
+                 "traffic": traffic_from_profile(wl.name, ksrc)})
+    path = {f: getattr(plan, f) for f, _ in B.Plan._fields_}
 
     # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world)
@@ -343,6 +358,7 @@ def run_ours(args, wl, rank, world, device):
         "staged_ms_per_step": round(statistics.mean(span(0, 7)), 4),
         "eager_ms_per_step": round(eager_ms, 4),
         "roofline": roof,
+        "path": path,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -382,20 +398,23 @@ def run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world):
             "ms_per_step": round(ms, 4), "steps": n}
 
 
-def traffic_from_profile(workload):
-    """DRAM bytes per GEMM1 launch from the committed ncu summary, or None when
-    there is none for this workload or the GEMM source changed since."""
+def traffic_from_profile(workload, kernel_source):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when there is none for this workload or the kernel's
+    source changed since the capture."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    p = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh)
-    with open(os.path.join(ROOT, d["kernel_source"]), "rb") as fh:
-        if hashlib.sha256(fh.read()).hexdigest() != d["kernel_sha256"]:
-            return None
     v = d["workloads"].get(workload)
-    return None if v is None else v.get("dram_bytes_per_launch")
+    if v is None or os.path.basename(v["kernel_source"]) != kernel_source:
+        return None
+    with open(os.path.join(ROOT, v["kernel_source"]), "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest() != v["kernel_sha256"]:
+            return None
+    return v.get("dram_bytes_per_launch")
 
 
 # --------------------------------------------------------------------------- oracle arms

@@ -137,26 +137,29 @@ cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long 
                                  cudaStream_t st);
 
 // x_perm[r] = x[sorted_ids[r] / K] for rows holding an item.
-// ready (optional, n_ready ints) is zeroed for the fused MLP kernel that
-// follows the gather.
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
                           const int32_t* offsets_end, int cap, long n_items, int K, int H,
-                          void* x_perm, cudaStream_t st, int* ready = nullptr,
-                          int n_ready = 0);
+                          void* x_perm, cudaStream_t st);
 
 // Both routed GEMMs of a decode-sized batch (32-token tiles, bf16) in one
 // persistent kernel: h = silu(x W_gate^T) * (x W_up^T) per tile, then
-// y = h W2^T, GEMM2 units waiting on per-tile ready counters (zeroed by the
-// gather kernel that precedes it).
+// y = h W2^T, GEMM2 units
+// waiting on per-tile ready counters. GEMM1 may be split over K (ks1 > 1):
+// fp32 partial slabs in part, finished by the last warp of each block
+// (split_cnt). ready and split_cnt must be zero before the launch.
 struct MlpFusedArgs {
   const CUtensorMap* mapW13;  // [E_l*2I, H], box 128 x 64
-  const CUtensorMap* mapX;    // x_perm [cap, H], box 32 x 64
   const CUtensorMap* mapW2;   // [E_l*H, I], box 128 x 64
   const CUtensorMap* mapH;    // h_perm [cap, I], box 32 x 64
+  const CUtensorMap* mapX;    // x_perm [cap, H], box 32 x 64 (gathered rows)
   const Tile* tiles;
   const int* group_start;
   int n_groups;
   int H, I;
+  int ks1;                    // K ranges of GEMM1
+  float* part;                // ks1 slabs of [cap, 2I] fp32 (ks1 > 1)
+  long part_stride;           // floats per slab
+  int* split_cnt;             // max tiles x I/128 x 8 counters (ks1 > 1)
   int* ready;                 // one counter per tile
   void* h;                    // h_perm
   void* y;                    // y_perm

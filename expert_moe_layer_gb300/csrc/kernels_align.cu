@@ -228,10 +228,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
                                                      const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets_end,
                                                      int cap, long n_items, int K, int H,
-                                                     TE* __restrict__ x_perm,
-                                                     int* __restrict__ ready, int n_ready) {
+                                                     TE* __restrict__ x_perm) {
   pdl_enter();
-  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_ready; i += 256 * gridDim.x) ready[i] = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rows = *offsets_end;
   if (rows > cap) rows = cap;
@@ -424,16 +422,15 @@ cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, in
 
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
                           const int32_t* offsets_end, int cap, long n_items, int K, int H,
-                          void* x_perm, cudaStream_t st, int* ready, int n_ready) {
+                          void* x_perm, cudaStream_t st) {
   const int grid = grid_for(cap, 8, 8 * 152);
-  if (!ready) n_ready = 0;
   if (bf16)
     return launch_pdl(gather_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
                       static_cast<const __nv_bfloat16*>(x), sorted_ids, offsets_end, cap, n_items,
-                      K, H, static_cast<__nv_bfloat16*>(x_perm), ready, n_ready);
+                      K, H, static_cast<__nv_bfloat16*>(x_perm));
   return launch_pdl(gather_kernel<float>, dim3(grid), dim3(256), 0, st,
                     static_cast<const float*>(x), sorted_ids, offsets_end, cap, n_items, K, H,
-                    static_cast<float*>(x_perm), ready, n_ready);
+                    static_cast<float*>(x_perm));
 }
 
 cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long part_stride,

@@ -372,10 +372,10 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
+  return counted(cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
                             a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
                             a.b_from_out, static_cast<__nv_bfloat16*>(a.out), a.out_ld,
-                            a.status);
+                            a.status));
 }
 
 }  // namespace

@@ -4,25 +4,35 @@
 // two grouped GEMMs: h = silu(gate) * up over w13, then y = h w2^T. Launched
 // one after the other, the second waits for the first one's slowest CTA. At
 // decode sizes both are short and bound by weight reads, so that wait, plus
-// the wave quantisation of the first GEMM's few hundred units, costs a
-// sizeable share of the layer. Here one grid walks a single unit list:
+// the wave quantisation of the first GEMM's units and the launches around
+// them, costs a sizeable share of the layer. Here one grid walks a single
+// unit list:
 //
-//   units [0, U1)        GEMM1: (tile, 128 rows of w13's gate and up halves)
+//   units [0, U1)        GEMM1: (tile, 128 rows of w13's gate and up halves,
+//                        K range ks of ks1)
 //   units [U1, U1 + U2)  GEMM2: (tile, 128 rows of w2)
 //
-// Each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... in order. The
-// epilogue warps of a GEMM1 unit store their h rows, then add 1 to the
-// tile's ready counter (8 warps x I/128 units = the count a GEMM2 unit of
-// that tile waits for). A GEMM2 unit's producer streams its w2 tiles first,
-// then waits (bounded) for the counter, then loads the h rows. All GEMM1
-// units precede all GEMM2 units in every CTA's sequence, so all GEMM1 work
-// runs without waiting and no wait can deadlock once every CTA is resident
-// (one CTA per SM; a wait that runs out sets MOE_DEV_TIMEOUT).
+// Token rows are TMA boxes of x_perm, gathered by the kernel before this one.
+// The tile table is therefore two kernels old, so the weight boxes of each
+// CTA's first stages are issued before the dependency wait and stream in
+// while the gather runs.
+//
+// Each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ... in order.
+// With ks1 = 1 the epilogue warps of a GEMM1 unit store their block of h and
+// add 1 to the tile's ready counter. With ks1 > 1 they store raw fp32 gate and
+// up partials. The last of the ks1 warps that cover the same 32 rows x 16
+// columns (a counter per block) sums the partials in slab order, applies
+// SiLU*up, stores h and adds 1 to the ready counter. A GEMM2 unit's producer
+// streams its w2 tiles first, then waits (bounded) until the counter reaches
+// 8 blocks x I/128, then loads the h rows. All GEMM1 units precede all GEMM2
+// units in every CTA's sequence, so GEMM1 work never waits and no wait can
+// deadlock once every CTA is resident (one CTA per SM; a wait that runs out
+// sets MOE_DEV_TIMEOUT). The counters are zeroed before the kernel.
 //
 // Stage layout (40 KB): two 128-row weight boxes and two token-row boxes of
-// nmax rows, each box 128 bytes of K with the 128-byte swizzle.
+// 32 rows, each box 128 bytes of K with the 128-byte swizzle.
 //   GEMM1 stage: A0 = gate rows, A1 = up rows, B0 = x rows (one K block);
-//                gate accumulates in columns [0, nmax), up in [nmax, 2 nmax)
+//                gate accumulates in columns [0, 32), up in [32, 64)
 //   GEMM2 stage: A0/B0 = K block 2j, A1/B1 = K block 2j+1, one accumulator
 // Warp roles as in moe_gemm_tc: warp 0 TMA producer, warp 1 TMEM owner and
 // MMA issuer, warps 2..9 epilogue (two per TMEM lane quarter).
@@ -47,6 +57,7 @@ constexpr int kAccCols = 2 * kNmax;                // gate + up
 constexpr int kNAcc = 2;
 constexpr int kTmemCols = 128;
 constexpr int kMaxGroups = 1024;
+constexpr int kMaxSplit = 8;                       // K ranges of GEMM1 at most
 constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16 + 4 * (kMaxGroups + 1);
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 static_assert(kAccCols * kNAcc <= kTmemCols, "TMEM overflow");
@@ -69,19 +80,26 @@ __device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_grou
 }
 
 struct UnitInfo {
-  bool g2;     // GEMM2 unit
-  int ti, m;   // tile index, weight tile
-  int n_st;    // pipeline stages of the unit
+  bool g2;      // GEMM2 unit
+  int ti, m;    // tile index, weight tile
+  int ks;       // K range (GEMM1)
+  int kb0;      // first K block (GEMM1)
+  int n_st;     // pipeline stages of the unit
 };
 
 __device__ __forceinline__ UnitInfo unit_info(int u, int U1, const int* gstart, int n_groups,
-                                              int m1, int m2, int kb1, int kb2) {
+                                              int m1, int m2, int kb1, int kb2, int ks1,
+                                              int kb_per) {
   UnitInfo r;
   r.g2 = u >= U1;
   if (!r.g2) {
-    decode_unit(u, gstart, n_groups, m1, r.ti, r.m);
-    r.n_st = kb1;
+    r.ks = u % ks1;
+    decode_unit(u / ks1, gstart, n_groups, m1, r.ti, r.m);
+    r.kb0 = r.ks * kb_per;
+    r.n_st = min(kb1, r.kb0 + kb_per) - r.kb0;
   } else {
+    r.ks = 0;
+    r.kb0 = 0;
     decode_unit(u - U1, gstart, n_groups, m2, r.ti, r.m);
     r.n_st = (kb2 + 1) >> 1;
   }
@@ -92,6 +110,15 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ int add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -117,21 +144,28 @@ __device__ __forceinline__ bool wait_count(const int* p, int target, volatile in
   }
 }
 
+// Publish a warp's block of h (generic stores) to the GEMM2 producers, which
+// read it through the async proxy.
+__device__ __forceinline__ void publish_h(int* ready, int lane) {
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) add_acq_rel(ready, 1);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     moe_mlp_fused(const __grid_constant__ CUtensorMap mapW13,
-                  const __grid_constant__ CUtensorMap mapX,
                   const __grid_constant__ CUtensorMap mapW2,
-                  const __grid_constant__ CUtensorMap mapH, const Tile* __restrict__ tiles,
+                  const __grid_constant__ CUtensorMap mapH,
+                  const __grid_constant__ CUtensorMap mapX, const Tile* __restrict__ tiles,
                   const int* __restrict__ group_start, int n_groups, int H, int I,
-                  int* __restrict__ ready, __nv_bfloat16* __restrict__ h_out,
-                  __nv_bfloat16* __restrict__ y_out, unsigned* status) {
+                  int ks1, float* __restrict__ part, long part_stride,
+                  int* __restrict__ split_cnt, int* __restrict__ ready,
+                  __nv_bfloat16* __restrict__ h_out, __nv_bfloat16* __restrict__ y_out,
+                  unsigned* status) {
   const int m1 = I / 128, m2 = H / 128;
   const int kb1 = H / 64, kb2 = I / 64;
-  const int n_tiles = group_start[n_groups];
-  const int U1 = n_tiles * m1;
-  const int total = U1 + n_tiles * m2;
+  const int kb_per = (kb1 + ks1 - 1) / ks1;
   const int ready_target = kEpiWarps * m1;
-  if (static_cast<int>(blockIdx.x) >= total) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -146,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2 * kNAcc + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
-  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -164,126 +197,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_barrier_init();
     ptx::fence_proxy_async();
     ptx::tma_prefetch_map(&mapW13);
-    ptx::tma_prefetch_map(&mapX);
     ptx::tma_prefetch_map(&mapW2);
     ptx::tma_prefetch_map(&mapH);
+    ptx::tma_prefetch_map(&mapX);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
     ptx::tmem_relinquish();
   }
+  // the tile table is two kernels old: read before the dependency wait
+  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int n_tiles = gstart[n_groups];
+  const int U1 = n_tiles * m1 * ks1;
+  const int total = U1 + n_tiles * m2;
+
+  // weight boxes of the first stages before the wait
+  int pre = 0;
+  {
+    if (warp == 0 && lane == 0) {
+      for (int u = blockIdx.x; u < U1 && pre < kStages; u += gridDim.x) {
+        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+        const Tile tl = tiles[ui.ti];
+        const int arow = tl.x * 2 * I + ui.m * 128;
+        for (int j = 0; j < ui.n_st && pre < kStages; ++j, ++pre) {
+          const uint32_t st = sbase + pre * kStageBytes, fb = full0 + 8 * pre;
+          const int kx = (ui.kb0 + j) * 64;
+          ptx::mbar_arrive_expect_tx(fb, 2 * kABytes + kBBytes);
+          ptx::tma_load_2d(st, &mapW13, fb, kx, arow);
+          ptx::tma_load_2d(st + kABytes, &mapW13, fb, kx, arow + I);
+        }
+      }
+    }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
+    pdl_enter();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // weight boxes of one stage (the tile table was written two kernels back)
-      auto load_a = [&](const UnitInfo& ui, const Tile& tl, int j, uint32_t st, uint32_t fb) {
-        if (!ui.g2) {
-          const int row = tl.x * 2 * I + ui.m * 128;
-          ptx::tma_load_2d(st, &mapW13, fb, j * 64, row);
-          ptx::tma_load_2d(st + kABytes, &mapW13, fb, j * 64, row + I);
-        } else {
-          const int row = tl.x * H + ui.m * 128;
-          ptx::tma_load_2d(st, &mapW2, fb, 2 * j * 64, row);
-          if (2 * j + 1 < kb2) ptx::tma_load_2d(st + kABytes, &mapW2, fb, (2 * j + 1) * 64, row);
+    // lane 0 issues; the warp keeps the unit walk and the status in step
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+      const Tile tl = tiles[ui.ti];
+      if (!ui.g2) {
+        // token rows from x_perm (segment rows tl.y ..) with TMA
+        if (lane == 0) {
+          const int arow = tl.x * 2 * I + ui.m * 128;
+          for (int j = 0; j < ui.n_st; ++j) {
+            const int i2 = it + j;
+            const int s = i2 % kStages;
+            const uint32_t ph = (i2 / kStages) & 1;
+            const uint32_t st = sbase + s * kStageBytes, fb = full0 + 8 * s;
+            const int kx = (ui.kb0 + j) * 64;
+            if (i2 >= pre) {  // stages of the early loads are fresh: no empty wait
+              if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+                ok = false;
+                break;
+              }
+              ptx::mbar_arrive_expect_tx(fb, 2 * kABytes + kBBytes);
+              ptx::tma_load_2d(st, &mapW13, fb, kx, arow);
+              ptx::tma_load_2d(st + kABytes, &mapW13, fb, kx, arow + I);
+            }
+            ptx::tma_load_2d(st + 2 * kABytes, &mapX, fb, kx, tl.y);
+          }
         }
-      };
-      auto load_b = [&](const UnitInfo& ui, const Tile& tl, int j, uint32_t st, uint32_t fb) {
-        if (!ui.g2) {
-          ptx::tma_load_2d(st + 2 * kABytes, &mapX, fb, j * 64, tl.y);
-        } else {
-          ptx::tma_load_2d(st + 2 * kABytes, &mapH, fb, 2 * j * 64, tl.z);
-          if (2 * j + 1 < kb2)
-            ptx::tma_load_2d(st + 2 * kABytes + kBBytes, &mapH, fb, (2 * j + 1) * 64, tl.z);
-        }
-      };
-      auto stage_bytes = [&](const UnitInfo& ui, int j) -> uint32_t {
-        if (!ui.g2) return 2 * kABytes + kBBytes;
-        return (2 * j + 1 < kb2) ? 2 * (kABytes + kBBytes) : kABytes + kBBytes;
-      };
-
-      // weights of the first stages before the dependency wait
-      int pre = 0;
-      for (int u = blockIdx.x; u < total && pre < kStages; u += gridDim.x) {
-        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
-        const Tile tl = tiles[ui.ti];
-        for (int j = 0; j < ui.n_st && pre < kStages; ++j, ++pre) {
-          const uint32_t fb = full0 + 8 * pre;
-          ptx::mbar_arrive_expect_tx(fb, stage_bytes(ui, j));
-          load_a(ui, tl, j, sbase + pre * kStageBytes, fb);
-        }
-      }
-      pdl_enter();
-      int it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
-        const Tile tl = tiles[ui.ti];
-        // GEMM2: stream the unit's first weight boxes, then wait for its h rows
-        const int n_a = ui.g2 ? min(ui.n_st, kStages) : 0;
-        int j = 0;
-        for (; j < n_a; ++j) {
-          const int i2 = it + j;
-          if (i2 >= pre) {
+        it += ui.n_st;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      } else {
+        // GEMM2: the unit's first weight boxes, then wait for its h rows
+        if (lane == 0) {
+          const int arow = tl.x * H + ui.m * 128;
+          const int n_a = min(ui.n_st, kStages);
+          int j = 0;
+          for (; j < n_a; ++j) {
+            const int i2 = it + j;
             const int s = i2 % kStages;
             const uint32_t ph = (i2 / kStages) & 1;
             if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes(ui, j));
-            load_a(ui, tl, j, sbase + s * kStageBytes, full0 + 8 * s);
+            const uint32_t st = sbase + s * kStageBytes, fb = full0 + 8 * s;
+            const bool two = 2 * j + 1 < kb2;
+            ptx::mbar_arrive_expect_tx(fb, two ? 2 * (kABytes + kBBytes) : kABytes + kBBytes);
+            ptx::tma_load_2d(st, &mapW2, fb, 2 * j * 64, arow);
+            if (two) ptx::tma_load_2d(st + kABytes, &mapW2, fb, (2 * j + 1) * 64, arow);
           }
-        }
-        if (!ok) {
-          it += j;
-          break;
-        }
-        if (ui.g2) {
-          if (!wait_count(ready + ui.ti, ready_target, abort_flag, status)) {
-            ok = false;
-            it += n_a;
-            // the issued weight boxes still land; their stages never fill
-            break;
-          }
-          fence_proxy_async_global();
-        }
-        for (j = 0; j < ui.n_st; ++j, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          const uint32_t st = sbase + s * kStageBytes;
-          if (j >= n_a && it >= pre) {
-            if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
-              ok = false;
-              break;
+          // on failure the issued weight boxes still land; their stages never fill
+          if (ok && !wait_count(ready + ui.ti, ready_target, abort_flag, status)) ok = false;
+          if (ok) fence_proxy_async_global();
+          for (j = 0; j < ui.n_st && ok; ++j) {
+            const int i2 = it + j;
+            const int s = i2 % kStages;
+            const uint32_t ph = (i2 / kStages) & 1;
+            const uint32_t st = sbase + s * kStageBytes, fb = full0 + 8 * s;
+            const bool two = 2 * j + 1 < kb2;
+            if (j >= n_a) {
+              if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+                ok = false;
+                break;
+              }
+              ptx::mbar_arrive_expect_tx(fb, two ? 2 * (kABytes + kBBytes) : kABytes + kBBytes);
+              ptx::tma_load_2d(st, &mapW2, fb, 2 * j * 64, arow);
+              if (two) ptx::tma_load_2d(st + kABytes, &mapW2, fb, (2 * j + 1) * 64, arow);
             }
-            ptx::mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes(ui, j));
-            load_a(ui, tl, j, st, full0 + 8 * s);
+            ptx::tma_load_2d(st + 2 * kABytes, &mapH, fb, 2 * j * 64, tl.z);
+            if (two) ptx::tma_load_2d(st + 2 * kABytes + kBBytes, &mapH, fb, (2 * j + 1) * 64, tl.z);
           }
-          load_b(ui, tl, j, st, full0 + 8 * s);
         }
+        it += ui.n_st;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      if (!ok) {
-        // unwinding: give in-flight copies time to land before the CTA exits
-        const uint64_t t0 = ptx::globaltimer();
-        while (ptx::globaltimer() - t0 < 200000) {
-        }
+    }
+    if (!ok) {
+      // unwinding: give in-flight copies time to land before the CTA exits
+      const uint64_t t0 = ptx::globaltimer();
+      while (ptx::globaltimer() - t0 < 200000) {
       }
-    } else {
-      pdl_enter();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    pdl_enter();
     if (lane == 0) {
       int it = 0, ai = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
-        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
         const Tile tl = tiles[ui.ti];
         const int n_mma = (tl.w + 15) & ~15;
         const uint32_t idesc = ptx::idesc_make(1u, 128, n_mma);
@@ -338,12 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_enter();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
+    const int blk = warp - 2;                     // this warp's 32 x 16 block of a unit
     int ai = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
-      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2);
+      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
       const Tile tl = tiles[ui.ti];
       const int b = ai % kNAcc;
       const uint32_t aph = (ai / kNAcc) & 1;
@@ -353,29 +396,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = ui.m * 128 + q * 32 + lane;  // h column (GEMM1) or y column (GEMM2)
       const int c0 = 16 * half;                     // this warp's 16 token columns
       float v[16];
-      if (!ui.g2) {
-        float w[16];
-        ptx::tmem_ld16x2(tb + c0, tb + kNmax + c0, v, w);
-        __nv_bfloat16* orow = h_out + static_cast<long>(tl.z) * I + row;
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(v[j]) * w[j]);
-      } else {
+      if (ui.g2) {
         ptx::tmem_ld16(tb + c0, v);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty0 + 8 * b);
         __nv_bfloat16* orow = y_out + static_cast<long>(tl.z) * H + row;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * H] = __float2bfloat16_rn(v[j]);
+        continue;
       }
+      float w[16];
+      ptx::tmem_ld16x2(tb + c0, tb + kNmax + c0, v, w);
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty0 + 8 * b);
-      if (!ui.g2) {
-        // publish this warp's h block: generic stores -> async-proxy readers
-        fence_proxy_async_global();
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(ready + ui.ti, 1);
+      __nv_bfloat16* hrow = h_out + static_cast<long>(tl.z) * I + row;
+      if (ks1 == 1) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < tl.w) hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(v[j]) * w[j]);
+        publish_h(ready + ui.ti, lane);
+        continue;
       }
+      // K split: raw partials of this slab ([row][gate I | up I] fp32), then
+      // the last of the ks1 warps on this block finishes it
+      float* prow = part + ui.ks * part_stride + static_cast<long>(tl.z) * 2 * I + row;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j < tl.w) {
+          prow[static_cast<long>(c0 + j) * 2 * I] = v[j];
+          prow[static_cast<long>(c0 + j) * 2 * I + I] = w[j];
+        }
+      }
+      __syncwarp();
+      int old = 0;
+      if (lane == 0) old = add_acq_rel(split_cnt + (ui.ti * m1 + ui.m) * kEpiWarps + blk, 1);
+      old = __shfl_sync(0xffffffffu, old, 0);
+      if (old != ks1 - 1) continue;
+      // every slab's value is loaded before the sum, which runs in slab order
+      const float* qrow = part + static_cast<long>(tl.z) * 2 * I + row;
+      for (int j = 0; j < 16 && c0 + j < tl.w; ++j) {
+        const float* pc = qrow + static_cast<long>(c0 + j) * 2 * I;
+        float gs[kMaxSplit], us[kMaxSplit];
+#pragma unroll
+        for (int s = 0; s < kMaxSplit; ++s) {
+          gs[s] = s < ks1 ? __ldcg(pc + s * part_stride) : 0.f;
+          us[s] = s < ks1 ? __ldcg(pc + s * part_stride + I) : 0.f;
+        }
+        float g = gs[0], up = us[0];
+#pragma unroll
+        for (int s = 1; s < kMaxSplit; ++s) {
+          if (s < ks1) {
+            g += gs[s];
+            up += us[s];
+          }
+        }
+        hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(g) * up);
+      }
+      publish_h(ready + ui.ti, lane);
     }
   }
 
@@ -399,11 +477,13 @@ cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups) return cudaErrorInvalidValue;
+  if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups || a.ks1 < 1 ||
+      a.ks1 > kMaxSplit || (a.ks1 > 1 && (!a.part || !a.split_cnt)))
+    return cudaErrorInvalidValue;
   return launch_pdl(moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st, *a.mapW13,
-                    *a.mapX, *a.mapW2, *a.mapH, a.tiles, a.group_start, a.n_groups, a.H, a.I,
-                    a.ready, static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y),
-                    a.status);
+                    *a.mapW2, *a.mapH, *a.mapX, a.tiles, a.group_start, a.n_groups, a.H, a.I,
+                    a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
+                    static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y), a.status);
 }
 
 }  // namespace moe

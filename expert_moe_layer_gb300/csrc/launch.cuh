@@ -29,6 +29,15 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_launch_dependents();
 }
 
+// Kernels this host thread has launched (successfully) through the library;
+// moe_forward_timed reports the difference across one call.
+inline thread_local long g_kernel_launches = 0;
+
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) ++g_kernel_launches;
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t st, Args&&... args) {
@@ -42,7 +51,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  return counted(cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...));
 }
 
 }  // namespace moe

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "launch.cuh"
 #include "moe.h"
 
 namespace moe {
@@ -113,11 +114,30 @@ long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
 
-// Decode-sized bf16 batches (32-token tiles, GEMM1 not split over K) run
-// both routed GEMMs in one persistent kernel with per-tile ready counters.
+// Decode-sized bf16 batches (32-token tiles) run both routed GEMMs in one
+// persistent kernel that gathers its token rows from x itself.
 bool mlp_fused(const moe_config* c, int T) {
-  return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && gemm1_ksplit(c, T) == 1 &&
-         n_local(c) <= 1024;
+  return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && n_local(c) <= 1024;
+}
+
+// Zeroed at the start of every call (one memset): the status word, the
+// small-batch route tickets and, on the fused MLP path, its per-tile ready
+// counters and per-block split counters. Offsets from the start of ws.
+struct SyncRegion {
+  size_t bytes, ready, split;
+};
+SyncRegion sync_region(const moe_config* c, int T) {
+  SyncRegion r;
+  size_t off = 4 + 4 * static_cast<size_t>(kRouteTickets);
+  r.ready = r.split = off;
+  if (mlp_fused(c, T)) {
+    const size_t tiles = static_cast<size_t>(max_routed_tiles(c, T));
+    off += 4 * tiles;
+    r.split = off;
+    if (gemm1_ksplit(c, T) > 1) off += 4 * tiles * (c->intermediate_size / 128) * 8;
+  }
+  r.bytes = off;
+  return r;
 }
 
 // With 256-token tiles both GEMMs run on CTA pairs: one M = 256 MMA over two
@@ -248,16 +268,17 @@ AlignLayout align_layout(const moe_config* c, int T) {
 }
 
 struct MlpLayout {
-  size_t status, tiles, groups, ready, x_perm, h_perm, part1, total;
+  size_t status, tiles, groups, x_perm, h_perm, part1, total;
+  SyncRegion sync;
 };
 MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
   Carver cv;
   MlpLayout L;
   const size_t eb = ebytes(c->act_dtype);
-  L.status = cv.take(4);
+  L.sync = sync_region(c, T);
+  L.status = cv.take(L.sync.bytes);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(n_local(c) + 1));
-  L.ready = cv.take(sizeof(int) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.x_perm = cv.take(eb * static_cast<size_t>(cap) * c->hidden_size);
   L.h_perm = cv.take(eb * static_cast<size_t>(cap) * c->intermediate_size);
   L.part1 = cv.take(gemm1_ksplit(c, T) > 1 ? sizeof(float) * gemm1_ksplit(c, T) * cap * 2 *
@@ -269,8 +290,9 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
 
 struct FwdLayout {
   size_t status, topk_ids, topk_w, logits, hist, counts, offsets, sorted_ids, inv_pos;
-  size_t tiles, groups, ready, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
+  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
   int cap;
+  SyncRegion sync;
 };
 FwdLayout fwd_layout(const moe_config* c, int T) {
   Carver cv;
@@ -280,7 +302,8 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   const int El = n_local(c);
   const int S = c->num_shared_experts;
   L.cap = static_cast<int>(TK + static_cast<size_t>(El) * (kForwardBlock - 1));
-  L.status = cv.take(4 + 4 * kRouteTickets);  // status word, small-batch route tickets
+  L.sync = sync_region(c, T);
+  L.status = cv.take(L.sync.bytes);
   L.topk_ids = cv.take(4 * TK);
   L.topk_w = cv.take(4 * TK);
   L.logits = cv.take(sizeof(float) * static_cast<size_t>(router_ksplit(c, T)) * T *
@@ -292,7 +315,6 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.inv_pos = cv.take(4 * TK);
   L.tiles = cv.take(sizeof(Tile) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.groups = cv.take(sizeof(int) * static_cast<size_t>(El + 1));
-  L.ready = cv.take(sizeof(int) * static_cast<size_t>(max_routed_tiles(c, T)));
   L.x_perm = cv.take(eb * L.cap * c->hidden_size);
   L.h_perm = cv.take(eb * L.cap * c->intermediate_size);
   L.y_perm = cv.take(eb * L.cap * c->hidden_size);
@@ -356,8 +378,8 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
 
 int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
-           const void* w2, void* y_perm, Tile* tiles, int* groups, int* ready, void* x_perm,
-           void* h_perm, float* part1, unsigned* status, cudaStream_t st,
+           const void* w2, void* y_perm, Tile* tiles, int* groups, const SyncRegion& sync,
+           void* x_perm, void* h_perm, float* part1, unsigned* status, cudaStream_t st,
            void* const* ev = nullptr, bool tiles_ready = false) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
@@ -369,27 +391,31 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
                                        status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
-                                n_items, K, H, x_perm, st, fused ? ready : nullptr,
-                                fused ? max_tiles : 0)));
+                                n_items, K, H, x_perm, st)));
   if (ev) MOE_TRY(record_event(ev[0], st));
   if (fused) {
-    CUtensorMap m13, mx, m2, mh;
+    const int ks = gemm1_ksplit(c, T);
+    CUtensorMap m13, m2, mh, mx;
     if (!make_map(&m13, w13, c->act_dtype, static_cast<long>(El) * 2 * I, H, 128) ||
-        !make_map(&mx, x_perm, c->act_dtype, cap, H, 32) ||
         !make_map(&m2, w2, c->act_dtype, static_cast<long>(El) * H, I, 128) ||
-        !make_map(&mh, h_perm, c->act_dtype, cap, I, 32))
+        !make_map(&mh, h_perm, c->act_dtype, cap, I, 32) ||
+        !make_map(&mx, x_perm, c->act_dtype, cap, H, 32))
       return MOE_ERR_CUDA;
     MlpFusedArgs a;
     a.mapW13 = &m13;
-    a.mapX = &mx;
     a.mapW2 = &m2;
     a.mapH = &mh;
+    a.mapX = &mx;
     a.tiles = tiles;
     a.group_start = groups;
     a.n_groups = El;
     a.H = H;
     a.I = I;
-    a.ready = ready;
+    a.ks1 = ks;
+    a.part = ks > 1 ? part1 : nullptr;
+    a.part_stride = static_cast<long>(cap) * 2 * I;
+    a.split_cnt = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + sync.split);
+    a.ready = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + sync.ready);
     a.h = h_perm;
     a.y = y_perm;
     a.status = status;
@@ -518,11 +544,10 @@ int moe_grouped_mlp(const moe_config* cfg, int T, const void* x, const int32_t* 
   if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned* status = at<unsigned>(ws, L.status);
-  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.sync.bytes, st)));
   return do_mlp(cfg, T, x, sorted_ids, counts, offsets, cap, w13, w2, y_perm,
-                at<Tile>(ws, L.tiles), at<int>(ws, L.groups), at<int>(ws, L.ready),
-                at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
-                st);
+                at<Tile>(ws, L.tiles), at<int>(ws, L.groups), L.sync, at<void>(ws, L.x_perm),
+                at<void>(ws, L.h_perm), at<float>(ws, L.part1), status, st);
 }
 
 int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const int32_t* inv_pos,
@@ -583,8 +608,8 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
   p.kernels = 0;
   if (T > 0) {
-    // logits + top-k and align (or the fused route kernel), gather + routed
-    // GEMMs, shared GEMMs, combine
+    // logits + top-k and align (or the fused route kernel), the routed MLP
+    // (fused kernel, or gather + GEMMs), shared GEMMs, combine
     p.kernels = (p.fused_route ? 1 : 2 + p.align_kernels) +
                 (p.fused_mlp ? 2 : p.gemm1_k_split > 1 ? 4 : 3) +
                 (cfg->num_shared_experts > 0 ? 2 : 0) + 1;
@@ -622,9 +647,9 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* sorted_ids = at<int32_t>(ws, L.sorted_ids);
   int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
-  int n = 0;
+  const long launches0 = g_kernel_launches;
 
-  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4 + 4 * kRouteTickets, st)));
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.sync.bytes, st)));
   MOE_TRY(mark(0));
   if (route_align_small_ok(T, K, El)) {
     RouteAlignArgs a;
@@ -658,12 +683,10 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     a.max_tiles = static_cast<int>(max_routed_tiles(cfg, T));
     MOE_TRY(cuda_ok(launch_route_align_small(a, cfg->act_dtype == MOE_BF16,
                                              cfg->router_dtype == MOE_BF16, st)));
-    n += 1;
     MOE_TRY(mark(1));  // routing and align share one kernel
   } else {
     MOE_TRY(do_route(cfg, T, x, router_w, router_bias, ids, w, at<float>(ws, L.logits),
                      status, st));
-    n += 2;  // logits + top-k
     MOE_TRY(mark(1));
     MOE_TRY(cuda_ok(launch_align(ids, static_cast<long>(T) * K, expert_map, cfg->num_experts,
                                  El, cfg->ep_rank * El, kForwardBlock, at<int>(ws, L.hist),
@@ -671,15 +694,12 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
                                  at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
                                  routed_nmax(cfg, T),
                                  static_cast<int>(max_routed_tiles(cfg, T)))));
-    n += align_kernel_count(static_cast<long>(T) * K, El);
   }
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
-                 at<int>(ws, L.ready), at<void>(ws, L.x_perm), at<void>(ws, L.h_perm),
+                 L.sync, at<void>(ws, L.x_perm), at<void>(ws, L.h_perm),
                  at<float>(ws, L.part1), status, st, events ? events + 3 : nullptr, true));
-  // gather, then GEMM1 [+ SiLU finalize] and GEMM2, or the fused MLP kernel
-  n += mlp_fused(cfg, T) ? 2 : gemm1_ksplit(cfg, T) > 1 ? 4 : 3;
   MOE_TRY(mark(5));
   const void* shared_y = nullptr;
   int S = 0;
@@ -696,15 +716,13 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
                      static_cast<long>(S) * T, Is, nullptr, nullptr, S, H / 128, H, 0, 1, y_sh,
                      H, H, status, st, 1, 0, T));
     shared_y = y_sh;
-    n += 2;
   }
   MOE_TRY(mark(6));
   MOE_TRY(cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
                                  inv_pos, w, K, shared_y, S, static_cast<long>(T) * H,
                                  cfg->routed_scaling_factor, out, T, H, status, st)));
-  n += 1;
   MOE_TRY(mark(7));
-  if (kernels) *kernels = n;
+  if (kernels) *kernels = static_cast<int>(g_kernel_launches - launches0);
   return MOE_OK;
 }
 

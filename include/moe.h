@@ -305,9 +305,11 @@ typedef struct {
   int router_partials;     /* partial logit slabs the top-k kernel sums       */
   int align_kernels;       /* 0 (fused route), 1 (one CTA) or 3 (3 passes)    */
   int tile_rows;           /* token rows per routed GEMM tile: 32, 128 or 256 */
-  int gemm1_k_split;       /* 1, or K ranges of GEMM1 summed by a finalize    */
+  int gemm1_k_split;       /* 1, or K ranges of GEMM1 whose fp32 partials are
+                              summed by a finalize kernel or, fused, in-kernel */
   int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */
-  int fused_mlp;           /* 1: GEMM1 and GEMM2 in one persistent kernel     */
+  int fused_mlp;           /* 1: token gather, GEMM1 and GEMM2 in one
+                              persistent kernel                               */
 } moe_plan;
 int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 

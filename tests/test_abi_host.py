@@ -113,17 +113,17 @@ def test_forward_plan_per_workload():
     # route 2, align 1, gather + GEMM1 + GEMM2, combine
     assert p.kernels == 2 + 1 + 3 + 1
     assert p.fused_route == 0 and p.align_kernels == 1
-    # decode: routing and align in one kernel; 32-token tiles; T=8 and T=64
-    # run both GEMMs in the fused kernel, T=1 leaves too few GEMM1 units and
-    # splits GEMM1 over K instead
+    # decode: routing and align in one kernel; 32-token tiles; gather, GEMM1
+    # and GEMM2 in the fused kernel; T=1 leaves few GEMM1 units, so GEMM1 is
+    # also split over K (finished inside the fused kernel)
     for T in (8, 64):
         p = _plan(synth.QWEN_DECODE, T)
         assert (p.tile_rows, p.fused_mlp, p.gemm1_k_split, p.cta_pairs) == (32, 1, 1, 0)
         assert (p.fused_route, p.align_kernels, p.router_partials) == (1, 0, 1)
         assert p.kernels == 1 + 2 + 1  # route+align, gather + fused MLP, combine
     p = _plan(synth.QWEN_DECODE, 1)
-    assert (p.fused_mlp, p.tile_rows, p.fused_route) == (0, 32, 1) and p.gemm1_k_split > 1
-    assert p.kernels == 1 + 4 + 1  # gather, GEMM1, SiLU finalize, GEMM2
+    assert (p.fused_mlp, p.tile_rows, p.fused_route) == (1, 32, 1) and p.gemm1_k_split > 1
+    assert p.kernels == 1 + 2 + 1
     # the fused route kernel stops at 128 tokens
     assert _plan(synth.QWEN_DECODE, 128).fused_route == 1
     assert _plan(synth.QWEN_DECODE, 129).fused_route == 0
