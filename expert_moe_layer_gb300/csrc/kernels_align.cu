@@ -309,64 +309,133 @@ __global__ void __launch_bounds__(256) silu_finalize_kernel(const float* __restr
   }
 }
 
-// One warp task = one token x one 256-column chunk (8 columns per lane), so
-// small batches still spread over many warps. Lane k holds slot k's row and
-// weight; the rows of KB slots are loaded together before the fixed-order
-// accumulation k = 0..K-1 (KB = K rounded up to a power of two, at most 8).
+// A CTA takes tpc consecutive tokens (at most kCombTok). Its warps first
+// stage each token's slots into shared memory: position and weight of the
+// slots whose row is local, compacted in slot order so the accumulation keeps
+// the fixed order k = 0..K-1. Then one warp step = one token x U consecutive
+// 256-column chunks (8 columns per lane per chunk), U = 4 / KB for KB < 4:
+// the rows of up to KB slots for all U chunks (plus, with U = 1, up to two
+// shared experts) are loaded together as raw 16-byte vectors, so at least
+// four loads per lane are in flight whatever top_k is, then summed in slot
+// order.
+constexpr int kCombTok = 8;
+
+__device__ __forceinline__ void raw8_add(float (&acc)[8], const uint4& r, float w) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+  }
+}
+__device__ __forceinline__ void raw8_add(float (&acc)[8], const float4 (&r)[2], float w) {
+  acc[0] = fmaf(w, r[0].x, acc[0]); acc[1] = fmaf(w, r[0].y, acc[1]);
+  acc[2] = fmaf(w, r[0].z, acc[2]); acc[3] = fmaf(w, r[0].w, acc[3]);
+  acc[4] = fmaf(w, r[1].x, acc[4]); acc[5] = fmaf(w, r[1].y, acc[5]);
+  acc[6] = fmaf(w, r[1].z, acc[6]); acc[7] = fmaf(w, r[1].w, acc[7]);
+}
+template <typename TE> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void add_to(float (&acc)[8], float w) const { raw8_add(acc, v, w); }
+};
+template <> struct Raw8<float> {
+  float4 v[2];
+  __device__ __forceinline__ void load(const float* p) {
+    v[0] = *reinterpret_cast<const float4*>(p);
+    v[1] = *reinterpret_cast<const float4*>(p + 4);
+  }
+  __device__ __forceinline__ void add_to(float (&acc)[8], float w) const { raw8_add(acc, v, w); }
+};
+
 template <typename TE, int KB>
-__global__ void __launch_bounds__(256) combine_kernel(
+__global__ void __launch_bounds__(256, KB > 4 ? 3 : 4) combine_kernel(
     const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
     const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
-    long shared_stride, float rsf, TE* __restrict__ out, int T, int H, unsigned* status) {
+    long shared_stride, float rsf, TE* __restrict__ out, int T, int H, int tpc,
+    unsigned* status) {
+  constexpr int U = KB >= 4 ? 1 : 4 / KB;  // chunks per warp step
   pdl_enter();
+  __shared__ int s_pos[kCombTok][32];
+  __shared__ float s_w[kCombTok][32];
+  __shared__ int s_n[kCombTok];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int chunks = (H + 255) / 256;
-  const long tasks = static_cast<long>(T) * chunks;
-  for (long task = blockIdx.x * 8L + warp; task < tasks; task += 8L * gridDim.x) {
-    const long t = task / chunks;
-    const int c = static_cast<int>(task - t * chunks) * 256 + lane * 8;
-    int p_l = -1;
-    float w_l = 0.f;
-    if (lane < K) {
-      p_l = inv_pos[t * K + lane];
-      w_l = topk_w[t * K + lane];
-      if (p_l >= cap) {
+  const long t0 = static_cast<long>(blockIdx.x) * tpc;
+  for (int tt = warp; tt < tpc; tt += 8) {
+    const long t = t0 + tt;
+    int p = -1;
+    float w = 0.f;
+    if (t < T && lane < K) {
+      p = inv_pos[t * K + lane];
+      w = topk_w[t * K + lane];
+      if (p >= cap) {
         if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
-        p_l = -1;
+        p = -1;
       }
     }
-    const bool col_ok = c < H;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k0 = 0; k0 < K; k0 += KB) {
-      float y[KB][8];
-      float wk[KB];
-      bool ok[KB];
+    const unsigned local = __ballot_sync(0xffffffffu, p >= 0);
+    if (p >= 0) {
+      const int j = __popc(local & ((1u << lane) - 1u));
+      s_pos[tt][j] = p;
+      s_w[tt][j] = w;
+    }
+    if (lane == 0) s_n[tt] = __popc(local);
+  }
+  __syncthreads();
+  const int chunks = (H + 255) / 256;
+  const int steps = (chunks + U - 1) / U;  // warp steps per token
+  for (int task = warp; task < tpc * steps; task += 8) {
+    const int tt = task / steps;
+    const long t = t0 + tt;
+    if (t >= T) continue;
+    const int cb = (task - tt * steps) * U * 256 + lane * 8;
+    const int n = s_n[tt];
+    Raw8<TE> sh[2];
+    const int ns0 = U == 1 ? (n_shared < 2 ? n_shared : 2) : 0;
+    if (cb < H)
+      for (int s = 0; s < ns0; ++s) sh[s].load(shared + s * shared_stride + t * H + cb);
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += KB) {
+      Raw8<TE> y[KB][U];
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
-        const int k = k0 + j;
-        const int p = __shfl_sync(0xffffffffu, p_l, k & 31);
-        wk[j] = __shfl_sync(0xffffffffu, w_l, k & 31);
-        ok[j] = col_ok && k < K && p >= 0;
-        if (ok[j]) ld8(y_perm + static_cast<long>(p) * H + c, y[j]);
+        if (j0 + j < n) {
+          const TE* row = y_perm + static_cast<long>(s_pos[tt][j0 + j]) * H;
+#pragma unroll
+          for (int u = 0; u < U; ++u)
+            if (cb + u * 256 < H) y[j][u].load(row + cb + u * 256);
+        }
       }
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
-        if (ok[j]) {
+        if (j0 + j < n) {
+          const float w = s_w[tt][j0 + j];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[j], y[j][i], acc[i]);
+          for (int u = 0; u < U; ++u)
+            if (cb + u * 256 < H) y[j][u].add_to(acc[u], w);
         }
       }
     }
-    if (!col_ok) continue;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] *= rsf;
-    for (int s = 0; s < n_shared; ++s) {
-      float y[8];
-      ld8(shared + s * shared_stride + t * H + c, y);
+    for (int u = 0; u < U; ++u) {
+      const int c = cb + u * 256;
+      if (c >= H) continue;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += y[i];
+      for (int i = 0; i < 8; ++i) acc[u][i] *= rsf;
+      for (int s = 0; s < ns0; ++s) sh[s].add_to(acc[u], 1.f);
+      for (int s = ns0; s < n_shared; ++s) {
+        Raw8<TE> r;
+        r.load(shared + s * shared_stride + t * H + c);
+        r.add_to(acc[u], 1.f);
+      }
+      st8(out + t * H + c, acc[u]);
     }
-    st8(out + t * H + c, acc);
   }
 }
 
@@ -448,12 +517,21 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
                            const float* topk_w, int K, const void* shared, int n_shared,
                            long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st) {
-  const int grid = grid_for(static_cast<long>(T) * ((H + 255) / 256), 8, 16 * 152);
+  // up to kCombTok tokens per CTA, about four warp steps per warp, and at
+  // least two CTAs per SM where the batch allows
+  const int kb = bf16 ? (K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : 8) : (K <= 2 ? 2 : 8);
+  const int chunks = (H + 255) / 256;
+  const int u = kb >= 4 ? 1 : 4 / kb;
+  const int steps = (chunks + u - 1) / u;
+  int tpc = 32 / steps;
+  if (tpc > T / 304) tpc = T / 304;
+  tpc = tpc < 1 ? 1 : tpc > kCombTok ? kCombTok : tpc;
+  const int grid = (T + tpc - 1) / tpc;
 #define MOE_COMBINE(TE, KB)                                                                \
   return launch_pdl(combine_kernel<TE, KB>, dim3(grid), dim3(256), 0, st,                  \
                     static_cast<const TE*>(y_perm), cap, inv_pos, topk_w, K,               \
                     static_cast<const TE*>(shared), n_shared, shared_stride, rsf,          \
-                    static_cast<TE*>(out), T, H, status)
+                    static_cast<TE*>(out), T, H, tpc, status)
   if (bf16) {
     if (K <= 1) MOE_COMBINE(__nv_bfloat16, 1);
     else if (K <= 2) MOE_COMBINE(__nv_bfloat16, 2);
