@@ -102,10 +102,21 @@ __device__ __forceinline__ void align_small_block(
   __syncthreads();
   int* my = hist + warp * E_l;
   const int base = warp * ipw;
-  for (int r = 0; r < ipw; r += 32) {
-    const int item = base + r + lane;
-    int le = -1;
-    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, status);
+  // this lane's items (at most 8): ids loaded together, local ids kept for
+  // the second walk
+  constexpr int kRuns = kSmallItems / 32 / 32;
+  int lev[kRuns];
+#pragma unroll
+  for (int i = 0; i < kRuns; ++i) {
+    const int item = base + 32 * i + lane;
+    lev[i] = (32 * i < ipw && item < n_items) ? ids[item] : -1;
+  }
+#pragma unroll
+  for (int i = 0; i < kRuns; ++i) {
+    if (32 * i >= ipw) break;
+    const int item = base + 32 * i + lane;
+    lev[i] = item < n_items ? local_expert(lev[i], emap, E, E_l, ep_start, status) : -1;
+    const int le = lev[i];
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
     __syncwarp();
@@ -138,10 +149,11 @@ __device__ __forceinline__ void align_small_block(
                      warp_sums, status);
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
-  for (int r = 0; r < ipw; r += 32) {
-    const int item = base + r + lane;
-    int le = -1;
-    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, nullptr);
+#pragma unroll
+  for (int i = 0; i < kRuns; ++i) {
+    if (32 * i >= ipw) break;
+    const int item = base + 32 * i + lane;
+    const int le = lev[i];
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (item < n_items) {
       int pos = -1;

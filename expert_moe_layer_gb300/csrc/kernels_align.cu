@@ -37,10 +37,17 @@ __global__ void __launch_bounds__(256) align_count_kernel(
   if (gw >= n_warps) return;
   int* my = cnt + warp * E_l;
   const long base = static_cast<long>(gw) * kItemsPerWarp;
-  for (int r = 0; r < kItemsPerWarp; r += 32) {
-    const long item = base + r + lane;
+  int idv[kItemsPerWarp / 32];  // all of this lane's ids in flight at once
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    idv[i] = item < n_items ? ids[item] : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
     int le = -1;
-    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, status);
+    if (item < n_items) le = local_expert(idv[i], emap, E, E_l, ep_start, status);
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
     __syncwarp();
@@ -49,7 +56,9 @@ __global__ void __launch_bounds__(256) align_count_kernel(
 }
 
 // Pass 2 (one CTA): counts, padded exclusive offsets, and per-warp base rows
-// written back into hist.
+// written back into hist. G = 1024 / E_l threads share each expert's column
+// of hist: thread (g, e) sums warps [g*R, (g+1)*R), the partial sums are
+// turned into per-group prefixes, and each thread then rewrites its own range.
 __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist, int n_warps,
                                                           int E_l, int block_m,
                                                           int32_t* __restrict__ counts,
@@ -60,11 +69,28 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
                                                           int nmax, int max_tiles) {
   pdl_enter();
   __shared__ int warp_sums[32];
+  __shared__ int part[1024];   // per-(group, expert) sums, then their exclusive prefixes
+  __shared__ int sbase[1024];  // each expert's first row
+  const int G = E_l >= 1024 ? 1 : 1024 / E_l;
+  const bool active = threadIdx.x < G * E_l;
+  const int ge = active ? threadIdx.x % E_l : 0, g = active ? threadIdx.x / E_l : 0;
+  const int R = (n_warps + G - 1) / G;
+  const int w0 = min(n_warps, g * R), w1 = min(n_warps, w0 + R);
+  int sum = 0;
+  if (active) {
+#pragma unroll 8
+    for (int w = w0; w < w1; ++w) sum += hist[static_cast<long>(w) * E_l + ge];
+    part[threadIdx.x] = sum;
+  }
+  __syncthreads();
   const int e = threadIdx.x;
   int c = 0;
   if (e < E_l) {
-#pragma unroll 8
-    for (int w = 0; w < n_warps; ++w) c += hist[static_cast<long>(w) * E_l + e];
+    for (int gg = 0; gg < G; ++gg) {
+      const int v = part[gg * E_l + e];
+      part[gg * E_l + e] = c;
+      c += v;
+    }
   }
   const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
   // block-wide inclusive scan of padded
@@ -78,13 +104,13 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
   if (lane == 31) warp_sums[wid] = v;
   __syncthreads();
   if (wid == 0) {
-    int s = warp_sums[lane];
+    int s2 = warp_sums[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += n;
+      const int n = __shfl_up_sync(0xffffffffu, s2, o);
+      if (lane >= o) s2 += n;
     }
-    warp_sums[lane] = s;
+    warp_sums[lane] = s2;
   }
   __syncthreads();
   const int incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
@@ -92,14 +118,18 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
     const int start = incl - padded;
     counts[e] = c;
     offsets[e] = start;
+    sbase[e] = start;
     if (e == E_l - 1) {
       offsets[E_l] = incl;
       if (incl > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
     }
-    int run = start;
+  }
+  __syncthreads();
+  if (active) {
+    int run = sbase[ge] + part[threadIdx.x];
 #pragma unroll 8
-    for (int w = 0; w < n_warps; ++w) {
-      const long idx = static_cast<long>(w) * E_l + e;
+    for (int w = w0; w < w1; ++w) {
+      const long idx = static_cast<long>(w) * E_l + ge;
       const int h = hist[idx];
       hist[idx] = run;
       run += h;
@@ -122,15 +152,22 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
   const int gw = blockIdx.x * kWarpsPerBlock + warp;
   if (gw >= n_warps) return;
   int* my = run + warp * E_l;
+  const long base = static_cast<long>(gw) * kItemsPerWarp;
+  int idv[kItemsPerWarp / 32];  // all of this lane's ids in flight at once
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    idv[i] = item < n_items ? ids[item] : 0;
+  }
   for (int e = lane; e < E_l; e += 32) my[e] = hist[static_cast<long>(gw) * E_l + e];
   __syncwarp();
-  const long base = static_cast<long>(gw) * kItemsPerWarp;
   const unsigned lt = (1u << lane) - 1u;
-  for (int r = 0; r < kItemsPerWarp; r += 32) {
-    const long item = base + r + lane;
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
     int le = -1;
     // status already recorded by pass 1 for bad ids
-    if (item < n_items) le = local_expert(ids[item], emap, E, E_l, ep_start, nullptr);
+    if (item < n_items) le = local_expert(idv[i], emap, E, E_l, ep_start, nullptr);
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (item < n_items) {
       int pos = -1;
