@@ -73,19 +73,19 @@ int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
 
 // The router runs as a tcgen05 GEMM whenever x and the router weights are
 // bf16 (fp32 routers run on CUDA cores, split over H into 256-column slices
-// when E <= 32). Tensor-core batches under 256 tokens split K = H
-// so that ~2 units per SM exist; the top-k kernel sums the fp32 partials in a
-// fixed order.
+// when E <= 32). Tensor-core routers whose units (expert tiles x token tiles)
+// fill less than half the SMs split K = H so that ~2 units per SM exist; the
+// top-k kernel sums the fp32 partials in a fixed order.
 bool router_on_tensor_cores(const moe_config* c, int /*T*/) {
   return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16;
 }
 int router_nmax(int T) { return T >= 256 ? 128 : 32; }
 int router_ksplit(const moe_config* c, int T) {
   if (!router_on_tensor_cores(c, T)) return router_cuda_core_slabs(c->num_experts, c->hidden_size);
-  if (T >= 256) return 1;
   const int k_blocks = c->hidden_size / 64;
   const long base = static_cast<long>((c->num_experts + 127) / 128) *
                     dense_tile_count(T, 1, router_nmax(T));
+  if (2 * base >= 152) return 1;  // fills half the SMs: fp32 partials would cost more
   long ks = (304 + base - 1) / base;
   if (ks > 16) ks = 16;
   if (ks > k_blocks) ks = k_blocks;
