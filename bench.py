@@ -446,7 +446,8 @@ def oracle_step(wl, inputs):
     return O.moe_forward(x, rw, w13, w2, top_k=wl.K, renormalize=wl.renormalize,
                          n_group=wl.n_group, topk_group=wl.topk_group, rsf=wl.rsf, router_b=rb,
                          shared_w13=s13, shared_w2=s2,
-                         emap=O.expert_map(wl.E, wl.ep_size, wl.ep_rank))
+                         emap=O.expert_map(wl.E, wl.ep_size, wl.ep_rank),
+                         scoring=wl.scoring, bias_mode=wl.bias_mode)
 
 
 def oracle_tokens(wl):

@@ -69,9 +69,11 @@ cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
 
 // Softmax + (grouped) top-k + renormalise on fp32 logits (+ bias if given).
 // logits = sum of n_part partial slabs, partial_stride floats apart.
+// flags: kRouteSigmoid / kRouteBiasSelect (topk_warp.cuh); bias, if given, is
+// added to the logits, or with kRouteBiasSelect to the scores for the choice.
 cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
                         const float* bias, int T, int E, int K,
-                        int renorm, int n_group, int topk_group, int32_t* ids,
+                        int renorm, int flags, int n_group, int topk_group, int32_t* ids,
                         float* w, unsigned* status, cudaStream_t st);
 
 // Routing and single-CTA alignment of a small batch in one kernel: router
@@ -85,7 +87,7 @@ struct RouteAlignArgs {
   const void* x;
   const void* wg;
   const float* bias;
-  int T, E, H, K, renorm, n_group, topk_group;
+  int T, E, H, K, renorm, flags, n_group, topk_group;
   float* logits;
   int* tickets;
   int32_t* ids;

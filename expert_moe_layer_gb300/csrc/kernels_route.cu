@@ -171,28 +171,33 @@ template <int VPL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
                                                    int n_part, long partial_stride,
                                                    const float* __restrict__ bias, int T,
-                                                   int E, int K, int renorm, int n_group,
-                                                   int topk_group, int32_t* __restrict__ ids,
+                                                   int E, int K, int renorm, int flags,
+                                                   int n_group, int topk_group,
+                                                   int32_t* __restrict__ ids,
                                                    float* __restrict__ wout) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const float* row = logits + static_cast<long>(t) * E;
-  float p[VPL];
+  float p[VPL], sb[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
     p[j] = -CUDART_INF_F;
+    sb[j] = 0.f;
     if (e < E) {
       float l = row[e];
 #pragma unroll 8
       for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
-      p[j] = l + (bias ? bias[e] : 0.f);
+      const float b = bias ? bias[e] : 0.f;
+      if (flags & kRouteBiasSelect) sb[j] = b;
+      else l += b;
+      p[j] = l;
     }
   }
-  topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + static_cast<long>(t) * K,
-                 wout + static_cast<long>(t) * K);
+  topk_warp<VPL>(p, sb, lane, E, K, renorm, flags, n_group, topk_group,
+                 ids + static_cast<long>(t) * K, wout + static_cast<long>(t) * K);
 }
 
 // One CTA per token (small batches): all threads sum the partial slabs into
@@ -201,8 +206,8 @@ template <int VPL>
 __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__ logits,
                                                        int n_part, long partial_stride,
                                                        const float* __restrict__ bias, int T,
-                                                       int E, int K, int renorm, int n_group,
-                                                       int topk_group,
+                                                       int E, int K, int renorm, int flags,
+                                                       int n_group, int topk_group,
                                                        int32_t* __restrict__ ids,
                                                        float* __restrict__ wout) {
   pdl_enter();
@@ -213,18 +218,20 @@ __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__
     float l = row[e];
 #pragma unroll 8
     for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
-    sl[e] = l + (bias ? bias[e] : 0.f);
+    sl[e] = l + ((bias && !(flags & kRouteBiasSelect)) ? bias[e] : 0.f);
   }
   __syncthreads();
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
-  float p[VPL];
+  float p[VPL], sb[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
     p[j] = e < E ? sl[e] : -CUDART_INF_F;
+    sb[j] = (e < E && bias && (flags & kRouteBiasSelect)) ? bias[e] : 0.f;
   }
-  topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + t * K, wout + t * K);
+  topk_warp<VPL>(p, sb, lane, E, K, renorm, flags, n_group, topk_group, ids + t * K,
+                 wout + t * K);
 }
 
 // ------------------------------------------------- small batches: fused
@@ -288,7 +295,8 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 template <typename TX, typename TW, int VPL>
 __global__ void __launch_bounds__(1024) route_align_small_kernel(
     const TX* __restrict__ x, const TW* __restrict__ wg, const float* __restrict__ bias, int T,
-    int E, int H, int K, int renorm, int n_group, int topk_group, float* __restrict__ logits,
+    int E, int H, int K, int renorm, int flags, int n_group, int topk_group,
+    float* __restrict__ logits,
     int* __restrict__ tickets, int32_t* __restrict__ ids, float* __restrict__ wout,
     const int32_t* __restrict__ emap, int E_l, int ep_start, int block_m,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -417,14 +425,17 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(
   if (!is_last) return;
   if (warp < nt) {
     const int t = tb0 + warp;
-    float p[VPL];
+    float p[VPL], sb[VPL];
+    const bool sel = flags & kRouteBiasSelect;
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int ex = lane + 32 * j;
-      p[j] = ex < E ? __ldcg(logits + static_cast<long>(t) * E + ex) + bv[j] : -CUDART_INF_F;
+      p[j] = ex < E ? __ldcg(logits + static_cast<long>(t) * E + ex) + (sel ? 0.f : bv[j])
+                    : -CUDART_INF_F;
+      sb[j] = sel ? bv[j] : 0.f;
     }
-    topk_warp<VPL>(p, lane, E, K, renorm, n_group, topk_group, ids + static_cast<long>(t) * K,
-                   wout + static_cast<long>(t) * K);
+    topk_warp<VPL>(p, sb, lane, E, K, renorm, flags, n_group, topk_group,
+                   ids + static_cast<long>(t) * K, wout + static_cast<long>(t) * K);
   }
 
   // last token block: alignment of all T*K items
@@ -467,13 +478,14 @@ cudaError_t launch_router_logits(bool act_bf16, bool router_bf16, const void* x,
 
 template <int V>
 cudaError_t topk_launch(const float* logits, int n_part, long partial_stride, const float* bias,
-                        int T, int E, int K, int renorm, int n_group, int topk_group,
-                        int32_t* ids, float* w, cudaStream_t st) {
+                        int T, int E, int K, int renorm, int flags, int n_group,
+                        int topk_group, int32_t* ids, float* w, cudaStream_t st) {
   if (T < 256)
     return launch_pdl(topk_cta_kernel<V>, dim3(T), dim3(256), 0, st, logits, n_part,
-                      partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
+                      partial_stride, bias, T, E, K, renorm, flags, n_group, topk_group, ids,
+                      w);
   return launch_pdl(topk_kernel<V>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
-                    partial_stride, bias, T, E, K, renorm, n_group, topk_group, ids, w);
+                    partial_stride, bias, T, E, K, renorm, flags, n_group, topk_group, ids, w);
 }
 
 template <typename TX, typename TW, int VPL>
@@ -490,7 +502,8 @@ cudaError_t route_align_launch(const RouteAlignArgs& a, cudaStream_t st) {
   return launch_pdl(kern, dim3((a.E + 7) / 8, (a.T + kRouteTokBlock - 1) / kRouteTokBlock),
                     dim3(1024), S::kBytes, st, static_cast<const TX*>(a.x),
                     static_cast<const TW*>(a.wg), a.bias, a.T,
-                    a.E, a.H, a.K, a.renorm, a.n_group, a.topk_group, a.logits, a.tickets, a.ids,
+                    a.E, a.H, a.K, a.renorm, a.flags, a.n_group, a.topk_group, a.logits,
+                    a.tickets, a.ids,
                     a.w, a.emap, a.E_l, a.ep_start, a.block_m, a.counts, a.offsets,
                     a.sorted_ids, a.inv_pos, a.cap, a.status, a.tiles, a.group_start, a.nmax,
                     a.max_tiles);
@@ -521,20 +534,20 @@ cudaError_t launch_route_align_small(const RouteAlignArgs& a, bool act_bf16, boo
 }
 
 cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
-                        const float* bias, int T, int E, int K, int renorm, int n_group,
-                        int topk_group, int32_t* ids, float* w, unsigned* /*status*/,
-                        cudaStream_t st) {
+                        const float* bias, int T, int E, int K, int renorm, int flags,
+                        int n_group, int topk_group, int32_t* ids, float* w,
+                        unsigned* /*status*/, cudaStream_t st) {
   const int vpl = (E + 31) / 32;
   if (vpl <= 1) return topk_launch<1>(logits, n_part, partial_stride, bias, T, E, K, renorm,
-                                      n_group, topk_group, ids, w, st);
+                                      flags, n_group, topk_group, ids, w, st);
   if (vpl <= 2) return topk_launch<2>(logits, n_part, partial_stride, bias, T, E, K, renorm,
-                                      n_group, topk_group, ids, w, st);
+                                      flags, n_group, topk_group, ids, w, st);
   if (vpl <= 4) return topk_launch<4>(logits, n_part, partial_stride, bias, T, E, K, renorm,
-                                      n_group, topk_group, ids, w, st);
+                                      flags, n_group, topk_group, ids, w, st);
   if (vpl <= 8) return topk_launch<8>(logits, n_part, partial_stride, bias, T, E, K, renorm,
-                                      n_group, topk_group, ids, w, st);
+                                      flags, n_group, topk_group, ids, w, st);
   if (vpl <= 16) return topk_launch<16>(logits, n_part, partial_stride, bias, T, E, K, renorm,
-                                        n_group, topk_group, ids, w, st);
+                                        flags, n_group, topk_group, ids, w, st);
   return cudaErrorInvalidValue;
 }
 

@@ -11,6 +11,7 @@
 
 #include "internal.h"
 #include "launch.cuh"
+#include "topk_warp.cuh"
 #include "moe.h"
 
 namespace moe {
@@ -45,6 +46,10 @@ int validate_cfg(const moe_config* c) {
     if (Is < 128 || Is % 128 != 0) return MOE_ERR_INVALID_ARG;
   }
   if (!std::isfinite(c->routed_scaling_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->scoring_func != MOE_SCORE_SOFTMAX && c->scoring_func != MOE_SCORE_SIGMOID)
+    return MOE_ERR_INVALID_ARG;
+  if (c->bias_mode != MOE_BIAS_LOGIT && c->bias_mode != MOE_BIAS_SELECT)
+    return MOE_ERR_INVALID_ARG;
   // kernel coverage
   if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED;
   if (c->use_grouped_topk && c->num_expert_group > 32) return MOE_ERR_UNSUPPORTED;
@@ -76,6 +81,11 @@ int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
 // when E <= 32). Tensor-core routers whose units (expert tiles x token tiles)
 // fill less than half the SMs split K = H so that ~2 units per SM exist; the
 // top-k kernel sums the fp32 partials in a fixed order.
+int route_flags(const moe_config* c) {
+  return (c->scoring_func == MOE_SCORE_SIGMOID ? kRouteSigmoid : 0) |
+         (c->bias_mode == MOE_BIAS_SELECT ? kRouteBiasSelect : 0);
+}
+
 bool router_on_tensor_cores(const moe_config* c, int /*T*/) {
   return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16;
 }
@@ -371,7 +381,7 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
                                          x, router_w, logits, T, E, H, st)));
   }
   return cuda_ok(launch_topk(logits, n_part, static_cast<long>(T) * E, bias, T, E, c->top_k,
-                             c->renormalize ? 1 : 0,
+                             c->renormalize ? 1 : 0, route_flags(c),
                              c->use_grouped_topk ? c->num_expert_group : 0,
                              c->use_grouped_topk ? c->topk_group : 0, ids, w, status, st));
 }
@@ -661,6 +671,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     a.H = H;
     a.K = K;
     a.renorm = cfg->renormalize ? 1 : 0;
+    a.flags = route_flags(cfg);
     a.n_group = cfg->use_grouped_topk ? cfg->num_expert_group : 0;
     a.topk_group = cfg->use_grouped_topk ? cfg->topk_group : 0;
     a.logits = at<float>(ws, L.logits);

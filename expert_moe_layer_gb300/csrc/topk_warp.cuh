@@ -1,8 +1,10 @@
-// The per-token routing decision on one warp: fp32 softmax over the logits,
-// the optional group limit, top-k and renormalisation (MixtralMoE.forward;
-// FusedMoE select_experts / grouped_topk arguments).
+// The per-token routing decision on one warp: fp32 scores over the logits
+// (softmax, or per-expert sigmoid), the optional selection-only score
+// correction and group limit, top-k and renormalisation (MixtralMoE.forward;
+// FusedMoE select_experts / grouped_topk / scoring_func /
+// e_score_correction_bias arguments).
 //
-// Order: larger probability first, equal probabilities -> lower expert id.
+// Order: larger selection score first, equal scores -> lower expert id.
 // Every argmax is two single-instruction warp reductions (redux.sync) on an
 // order-preserving 32-bit key of the float: the largest key, then the lowest
 // expert id among the lanes that hold it. Each lane sorts its own candidates
@@ -15,6 +17,10 @@
 #include <cstdint>
 
 namespace moe {
+
+// flags of the routing kernels
+constexpr int kRouteSigmoid = 1;     // scores = sigmoid(logit) instead of softmax
+constexpr int kRouteBiasSelect = 2;  // the per-expert bias corrects the selection only
 
 // Unsigned key with key(a) > key(b) <=> a > b for non-NaN floats (-0 sorts
 // just below +0; probabilities are never -0). NaN maps to 0, below every
@@ -36,39 +42,48 @@ __device__ __forceinline__ void warp_argmax_key(uint32_t& key, int& id) {
   key = m;
 }
 
-// The warp-level routing decision for one token. p[j] holds the logit (with
-// bias) of expert lane + 32*j, or -inf beyond E. Softmax, the optional group
-// limit, K selections and the renormalisation all run on this warp. Lane k < K
-// writes ids_row[k] and w_row[k].
+// The warp-level routing decision for one token. p[j] holds the logit of
+// expert lane + 32*j, or -inf beyond E; sb[j] its selection-only correction
+// (0 without one). Scoring, the optional group limit, K selections and the
+// renormalisation all run on this warp. Lane k < K writes ids_row[k] and
+// w_row[k].
 template <int VPL>
-__device__ __forceinline__ void topk_warp(float (&p)[VPL], int lane, int E, int K, int renorm,
-                                          int n_group, int topk_group,
-                                          int32_t* __restrict__ ids_row,
+__device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL], int lane,
+                                          int E, int K, int renorm, int flags, int n_group,
+                                          int topk_group, int32_t* __restrict__ ids_row,
                                           float* __restrict__ w_row) {
-  // softmax in fp32: max, exp, sum, divide
-  float lmx = -CUDART_INF_F;
+  if (flags & kRouteSigmoid) {
+    // per-expert logistic in fp32
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) lmx = fmaxf(lmx, p[j]);
-  const float mx = fkey_inv(__reduce_max_sync(0xffffffffu, fkey(lmx)));
-  float sum = 0.f;
+    for (int j = 0; j < VPL; ++j)
+      p[j] = (lane + 32 * j < E) ? 1.0f / (1.0f + expf(-p[j])) : -CUDART_INF_F;
+  } else {
+    // softmax in fp32: max, exp, sum, divide
+    float lmx = -CUDART_INF_F;
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = lane + 32 * j;
-    p[j] = (e < E) ? expf(p[j] - mx) : 0.f;
-    sum += p[j];
+    for (int j = 0; j < VPL; ++j) lmx = fmaxf(lmx, p[j]);
+    const float mx = fkey_inv(__reduce_max_sync(0xffffffffu, fkey(lmx)));
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      p[j] = (e < E) ? expf(p[j] - mx) : 0.f;
+      sum += p[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] / sum : -CUDART_INF_F;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-#pragma unroll
-  for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] / sum : -CUDART_INF_F;
 
-  // candidate keys: p, or -inf outside the kept groups (group score = the
-  // largest p in the group; topk_group groups by score, ties to lower group)
+  // candidate keys: p + correction, or -inf outside the kept groups (group
+  // score = the largest corrected score in the group; topk_group groups by
+  // score, ties to lower group)
   uint32_t ck[VPL];
   int ci[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
-    ck[j] = fkey(p[j]);
+    ck[j] = fkey(lane + 32 * j < E ? p[j] + sb[j] : -CUDART_INF_F);
     ci[j] = lane + 32 * j;
   }
   if (n_group > 0) {
@@ -128,7 +143,16 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], int lane, int E, int 
     uint32_t key = hk;
     int id = hi;
     warp_argmax_key(key, id);
-    const float pw = fkey_inv(key);
+    // the winner's score: the key itself, or with a selection correction the
+    // uncorrected score from the lane that holds it
+    float pw = fkey_inv(key);
+    if (flags & kRouteBiasSelect) {
+      float mine = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j)
+        if ((hi >> 5) == j) mine = p[j];
+      pw = __shfl_sync(0xffffffffu, mine, id & 31);
+    }
     if (hi == id) {  // the owner pops its head
       ++head;
       hk = 0u;

@@ -96,13 +96,31 @@ typedef struct {
   int ep_rank;               /* this shard, 0 <= ep_rank < ep_size           */
   moe_dtype act_dtype;       /* x, expert weights, y_perm, out               */
   moe_dtype router_dtype;    /* router weight storage (logits are fp32)      */
+  int scoring_func;          /* MOE_SCORE_SOFTMAX (0) or MOE_SCORE_SIGMOID (1) */
+  int bias_mode;             /* role of router_bias: MOE_BIAS_LOGIT (0) or
+                                MOE_BIAS_SELECT (1), reading below          */
 } moe_config;
 
-/* Grouped top-k reading: the E experts form n_group contiguous groups of
- * E/n_group. A group's score is the max softmax probability of its members.
+/* Routing scores p: fp32 softmax over the E logits (MixtralMoE.forward), or,
+ * with MOE_SCORE_SIGMOID, 1 / (1 + exp(-logit)) per expert. The pages name a
+ * non-softmax scoring_func among the FusedMoE routing arguments without
+ * defining it; the elementwise logistic is the reading taken.
+ *
+ * router_bias (nullable, fp32 [E]): with MOE_BIAS_LOGIT it is added to the
+ * logits before scoring (a skew input of this library). With MOE_BIAS_SELECT
+ * it is the per-expert score correction the pages name as
+ * e_score_correction_bias: it is added to p only to choose the groups and
+ * the top-k, and the weights are the uncorrected p of the chosen experts.
+ *
+ * Grouped top-k reading: the E experts form n_group contiguous groups of
+ * E/n_group. A group's score is the max selection score of its members.
  * The topk_group best groups are kept (ties to the lower group id). Top-k
  * then runs over the kept experts (ties to the lower expert id), and the
- * weights are the plain softmax values of the chosen experts. */
+ * weights are the scores p of the chosen experts. */
+#define MOE_SCORE_SOFTMAX 0
+#define MOE_SCORE_SIGMOID 1
+#define MOE_BIAS_LOGIT 0
+#define MOE_BIAS_SELECT 1
 
 /* Human-readable name of a moe_status. Never NULL. */
 const char* moe_strerror(int status);

@@ -3,7 +3,7 @@
 Bit-exact routing comparisons are only well posed when no top-k decision sits
 on a near tie. This module draws a workload's inputs from ``synth``. It then
 redraws any token row whose smallest routing decision gap, measured on the
-oracle's fp32 softmax, is below ``min_gap`` (1e-5). A redraw uses the row's
+oracle's fp32 selection scores, is below ``min_gap`` (1e-5). A redraw uses the row's
 next attempt counter, so the final inputs are reproducible from
 (seed, attempts). Only the token rows are redrawn; the weights are never
 touched.
@@ -29,10 +29,11 @@ def gap_checked_x(wl, seed=0, router_w=None, router_b=None, min_gap=MIN_GAP,
     x = synth.draw_tensor(wl, synth.X, seed, attempts)
     todo = np.arange(wl.T)
     for _ in range(max_rounds):
-        _, _, p = route(x[todo], router_w, router_b, top_k=wl.K,
-                        renormalize=wl.renormalize, n_group=wl.n_group,
-                        topk_group=wl.topk_group)
-        gap = routing_min_gap(p, wl.K, wl.n_group, wl.topk_group)
+        _, _, sel = route(x[todo], router_w, router_b, top_k=wl.K,
+                          renormalize=wl.renormalize, n_group=wl.n_group,
+                          topk_group=wl.topk_group, scoring=wl.scoring,
+                          bias_mode=wl.bias_mode)
+        gap = routing_min_gap(sel, wl.K, wl.n_group, wl.topk_group)
         bad = todo[gap < min_gap]
         if bad.size == 0:
             return x, attempts
@@ -53,7 +54,8 @@ def build_case(wl, seed=0, min_gap=MIN_GAP, local=True):
     d["emap"] = expert_map(wl.E, wl.ep_size, wl.ep_rank)
     ids, w, p = route(d["x"], d["router_w"], d["router_b"], top_k=wl.K,
                       renormalize=wl.renormalize, n_group=wl.n_group,
-                      topk_group=wl.topk_group)
+                      topk_group=wl.topk_group, scoring=wl.scoring,
+                      bias_mode=wl.bias_mode)
     d["topk_ids"], d["topk_w"], d["p"] = ids, w, p
     d["wl"] = wl
     return d

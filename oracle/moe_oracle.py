@@ -14,6 +14,9 @@ product per (token, expert), rounded once to fp32.
 Pins (checked by ``tests/test_oracle_pins.py``):
   * routing, top-k, renormalise: pinned by the full-softmax closed form
     (top_k = E), brute-force top-k on tiny inputs, and scipy's softmax;
+  * sigmoid scoring and the selection-only score correction: pinned by
+    hand-computed examples, by the monotonicity of the sigmoid and by the
+    zero-correction identity;
   * grouped top-k: pinned by its reductions to plain top-k and by brute force
     over all group subsets;
   * expert MLP: pinned by the SiLU closed form and the gate/up role test;
@@ -76,6 +79,27 @@ def softmax_fp32(logits32: np.ndarray) -> np.ndarray:
     return (e / e.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
 
 
+def sigmoid_fp32(logits32: np.ndarray) -> np.ndarray:
+    """Per-expert sigmoid scores in fp32: 1 / (1 + exp(-l)).
+
+    ``scoring_func`` is named among the FusedMoE routing arguments the pages
+    list but not defined there (SURVEY reading: the non-softmax scoring is an
+    elementwise logistic of each logit, in the same fp32 as the softmax).
+    """
+    l = np.asarray(logits32, np.float32)
+    with np.errstate(over="ignore"):
+        return (np.float32(1.0) / (np.float32(1.0) + np.exp(-l))).astype(np.float32)
+
+
+def scores_fp32(logits32: np.ndarray, scoring: str = "softmax") -> np.ndarray:
+    """Routing scores p: fp32 softmax over experts, or per-expert sigmoid."""
+    if scoring == "softmax":
+        return softmax_fp32(logits32)
+    if scoring == "sigmoid":
+        return sigmoid_fp32(logits32)
+    raise ValueError(f"unknown scoring {scoring!r}")
+
+
 def topk_plain(p: np.ndarray, k: int) -> np.ndarray:
     """Indices of the k largest p per row, by descending p, ties to the lower id.
 
@@ -107,25 +131,39 @@ def topk_grouped(p: np.ndarray, k: int, n_group: int, topk_group: int) -> np.nda
 
 
 def route(x, router_w, router_b=None, *, top_k, renormalize,
-          n_group=0, topk_group=0):
-    """(topk_ids [T,K] int32 global ids, topk_w [T,K] fp32, p [T,E] fp32).
+          n_group=0, topk_group=0, scoring="softmax", bias_mode="logit"):
+    """(topk_ids [T,K] int32 global ids, topk_w [T,K] fp32, sel [T,E] fp32).
 
     MixtralMoE.forward: softmax in fp32, topk, then ``routing_weights /=
     routing_weights.sum(dim=-1, keepdim=True)`` when renormalising
     (``renormalize = norm_topk_prob`` in ``MoEMixin.recursive_replace``).
-    The weights are the unmasked softmax values of the chosen experts.
-    Routing is global: every rank selects among all experts
-    (ep_fused_moe_patch.py, ``_ep_forward`` step 1).
+    The weights are the unmasked scores of the chosen experts. Routing is
+    global: every rank selects among all experts (ep_fused_moe_patch.py,
+    ``_ep_forward`` step 1).
+
+    ``router_b`` has one of two roles (``bias_mode``). "logit": this library's
+    skew input, added to the logits before scoring. "select": the per-expert
+    score correction that the pages name as ``e_score_correction_bias``
+    without defining it. Reading taken: it is added to the scores for choosing
+    the groups and the top-k only, and the weights stay the uncorrected
+    scores. ``sel`` are the scores the choice was taken on (= p without a
+    selection bias).
     """
-    p = softmax_fp32(router_logits(x, router_w, router_b))
+    if bias_mode not in ("logit", "select"):
+        raise ValueError(f"unknown bias_mode {bias_mode!r}")
+    logit_b = router_b if bias_mode == "logit" else None
+    p = scores_fp32(router_logits(x, router_w, logit_b), scoring)
+    sel = p
+    if bias_mode == "select" and router_b is not None:
+        sel = (p + np.asarray(router_b, np.float32)[None, :]).astype(np.float32)
     if n_group > 0:
-        ids = topk_grouped(p, top_k, n_group, topk_group)
+        ids = topk_grouped(sel, top_k, n_group, topk_group)
     else:
-        ids = topk_plain(p, top_k)
+        ids = topk_plain(sel, top_k)
     w = np.take_along_axis(p, ids, axis=1).astype(np.float32)
     if renormalize:
         w = (w / w.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
-    return ids, w, p
+    return ids, w, sel
 
 
 def routing_min_gap(p: np.ndarray, top_k: int, n_group: int = 0,
@@ -191,7 +229,8 @@ def expert_mlp(x_rows, w13_e, w2_e) -> np.ndarray:
 # ---------------------------------------------------------------------------
 def moe_forward(x, router_w, w13, w2, *, top_k, renormalize=True, n_group=0,
                 topk_group=0, rsf=1.0, router_b=None, shared_w13=None,
-                shared_w2=None, emap=None, tokens=None, routing=None):
+                shared_w2=None, emap=None, tokens=None, routing=None,
+                scoring="softmax", bias_mode="logit"):
     """Output rows of the MoE layer for ``tokens`` (default: all), fp64.
 
     out[t] = rsf * sum_{k : emap[id_tk] >= 0} w_tk * f_{emap[id_tk]}(x_t)
@@ -210,7 +249,7 @@ def moe_forward(x, router_w, w13, w2, *, top_k, renormalize=True, n_group=0,
     if routing is None:
         ids, w, _ = route(x[tok], router_w, router_b, top_k=top_k,
                           renormalize=renormalize, n_group=n_group,
-                          topk_group=topk_group)
+                          topk_group=topk_group, scoring=scoring, bias_mode=bias_mode)
     else:
         ids, w = routing[0][tok], routing[1][tok]
     E_l = w13.shape[0]

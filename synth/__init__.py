@@ -154,7 +154,10 @@ class Workload:
     ep_rank: int = 0
     act: str = "bf16"           # "bf16" or "f32": x, expert weights, output
     router: str = "bf16"        # "bf16" or "f32": router weight storage
-    router_bias: bool = False   # per-expert logit bias b ~ N(0, 1)
+    router_bias: bool = False   # per-expert bias b ~ N(0, 1) (role: bias_mode)
+    bias_mode: str = "logit"    # "logit": b skews the logits; "select": b corrects
+                                # the scores for the top-k choice only
+    scoring: str = "softmax"    # "softmax" or "sigmoid" routing scores
     x_std: float = 1.0
 
     @property

@@ -28,7 +28,7 @@ W_RTOL, W_ATOL = 1e-4, 1e-7
 def cfg_of(wl) -> B.MoeConfig:
     return B.make_config(wl.E, wl.K, wl.H, wl.I, wl.renormalize, wl.n_group, wl.topk_group,
                          wl.rsf, wl.n_shared, wl.I_shared, wl.ep_size, wl.ep_rank, wl.act,
-                         wl.router)
+                         wl.router, wl.scoring, wl.bias_mode)
 
 
 def _dev(a: np.ndarray, bf16: bool) -> torch.Tensor:
@@ -77,7 +77,8 @@ class DeviceCase:
         self.d["router_w"] = _dev(rw, wl.router == "bf16")
         self.d["router_b"] = None if rb is None else torch.from_numpy(rb).cuda()
         ids, w, p = O.route(x, rw, rb, top_k=wl.K, renormalize=wl.renormalize,
-                            n_group=wl.n_group, topk_group=wl.topk_group)
+                            n_group=wl.n_group, topk_group=wl.topk_group,
+                            scoring=wl.scoring, bias_mode=wl.bias_mode)
         self.ids, self.w, self.p = ids, w, p
         self.cfg = cfg_of(wl)
 
@@ -88,7 +89,8 @@ class DeviceCase:
                              renormalize=wl.renormalize, n_group=wl.n_group,
                              topk_group=wl.topk_group, rsf=wl.rsf, router_b=h["router_b"],
                              shared_w13=h["shared_w13"], shared_w2=h["shared_w2"],
-                             emap=h["emap"], tokens=tokens, routing=(self.ids, self.w))
+                             emap=h["emap"], tokens=tokens, routing=(self.ids, self.w),
+                             scoring=wl.scoring, bias_mode=wl.bias_mode)
 
     def oracle_align(self, block):
         return O.align_permute(self.ids, self.h["emap"], self.wl.E_local, block)

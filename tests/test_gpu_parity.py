@@ -48,7 +48,23 @@ SMALL = {
     "ep_decode": synth.EP_SHARD.with_(name="ep_decode", T=32, H=256, I=256),
     "wide_router": W("wide_router", T=12, H=128, I=128, E=320, K=4, ep_size=2, ep_rank=1,
                      router_bias=True),
+    # sigmoid scores with the selection-only score correction (e_score_correction_bias
+    # reading), grouped, on each top-k path: the fused route kernel (T <= 128),
+    # CTA per token (T < 256) and warp per token
+    "sigmoid_select": W("sigmoid_select", T=40, H=256, I=256, E=64, K=6, n_group=8,
+                        topk_group=4, rsf=2.5, n_shared=1, I_shared=256, router_bias=True,
+                        bias_mode="select", scoring="sigmoid"),
+    "sigmoid_select_mid": W("sigmoid_select_mid", T=200, H=256, I=256, E=64, K=6, n_group=8,
+                            topk_group=4, rsf=2.5, router_bias=True, bias_mode="select",
+                            scoring="sigmoid"),
+    "sigmoid_select_wide": W("sigmoid_select_wide", T=300, H=256, I=256, E=32, K=4,
+                             router_bias=True, bias_mode="select", scoring="sigmoid",
+                             renormalize=False),
+    # sigmoid with a logit bias, fp32 layer
+    "sigmoid_f32": W("sigmoid_f32", T=50, H=128, I=128, E=8, K=2, act="f32", router="f32",
+                     router_bias=True, scoring="sigmoid", x_std=0.3),
 }
+SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
                "grouped_decode", "ep_decode", "wide_router")
@@ -111,7 +127,7 @@ def test_forward_full_size_sampled(name):
 
 # ------------------------------------------------------------------ components
 @pytest.mark.parametrize("name", ["ragged_prefill", "grouped_shared", "ragged_decode",
-                                  "tiny_f32", "ep_rank1"])
+                                  "tiny_f32", "ep_rank1", *SCORING])
 def test_route_entry_point(name):
     c = case(name)
     wl = c.wl

@@ -145,6 +145,86 @@ def test_route_weights_renormalised_and_raw():
     assert (np.diff(w2, axis=1) <= 0).all()
 
 
+def _router_for_logits(logits):
+    """x = identity rows, router = the logits as its first column: the oracle's
+    logits are then exactly the given values."""
+    l = np.asarray(logits, np.float64)
+    T, E = l.shape
+    return np.eye(T, T + 1), np.concatenate([l.T, np.zeros((E, 1))], axis=1)
+
+
+def test_sigmoid_scores_closed_form():
+    l = np.array([[0.0, math.log(3.0), -math.log(3.0), math.log(1 / 9)]], np.float32)
+    np.testing.assert_allclose(O.sigmoid_fp32(l), [[0.5, 0.75, 0.25, 0.1]], rtol=1e-6)
+    np.testing.assert_allclose(O.sigmoid_fp32(l), scipy.special.expit(l.astype(np.float64)),
+                               rtol=1e-6)
+
+
+def test_route_sigmoid_hand_example():
+    # sigmoid scores 0.5, 0.75, 0.25, 0.1: top-2 = experts 1, 0
+    x, rw = _router_for_logits([[0.0, math.log(3.0), -math.log(3.0), math.log(1 / 9)]])
+    ids, w, sel = O.route(x, rw, top_k=2, renormalize=False, scoring="sigmoid")
+    assert list(ids[0]) == [1, 0]
+    np.testing.assert_allclose(w[0], [0.75, 0.5], rtol=1e-6)
+    _, wr, _ = O.route(x, rw, top_k=2, renormalize=True, scoring="sigmoid")
+    np.testing.assert_allclose(wr[0], [0.6, 0.4], rtol=1e-6)
+
+
+def test_selection_bias_changes_choice_not_weights():
+    # scores 0.5, 0.75, 0.25, 0.1; correction +0.6 on expert 2 -> selection
+    # scores 0.5, 0.75, 0.85, 0.1: experts 2, 1 are chosen, with their
+    # uncorrected scores 0.25, 0.75 as weights
+    x, rw = _router_for_logits([[0.0, math.log(3.0), -math.log(3.0), math.log(1 / 9)]])
+    b = np.array([0.0, 0.0, 0.6, 0.0])
+    ids, w, sel = O.route(x, rw, b, top_k=2, renormalize=False, scoring="sigmoid",
+                          bias_mode="select")
+    assert list(ids[0]) == [2, 1]
+    np.testing.assert_allclose(w[0], [0.25, 0.75], rtol=1e-6)
+    np.testing.assert_allclose(sel[0], [0.5, 0.75, 0.85, 0.1], rtol=1e-6)
+    _, wr, _ = O.route(x, rw, b, top_k=2, renormalize=True, scoring="sigmoid",
+                       bias_mode="select")
+    np.testing.assert_allclose(wr[0], [0.25, 0.75], rtol=1e-6)  # already sums to 1
+    # the same bias as a logit bias moves the weights as well
+    _, wl, _ = O.route(x, rw, b, top_k=2, renormalize=False, scoring="sigmoid",
+                       bias_mode="logit")
+    assert not np.allclose(wl[0], w[0])
+
+
+@pytest.mark.parametrize("scoring", ["softmax", "sigmoid"])
+def test_zero_selection_bias_is_plain_routing(scoring):
+    d = _layer(T=30, E=16, seed=5)
+    for kw in (dict(), dict(n_group=4, topk_group=2)):
+        ref = O.route(d["x"], d["router_w"], top_k=3, renormalize=True, scoring=scoring, **kw)
+        got = O.route(d["x"], d["router_w"], np.zeros(16), top_k=3, renormalize=True,
+                      scoring=scoring, bias_mode="select", **kw)
+        for a, b in zip(ref, got):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_sigmoid_choice_follows_logit_order():
+    d = _layer(T=60, E=24, seed=6)
+    lg = O.router_logits(d["x"], d["router_w"])
+    ids, w, _ = O.route(d["x"], d["router_w"], top_k=5, renormalize=False, scoring="sigmoid")
+    for t in range(60):
+        assert list(ids[t]) == _brute_topk(list(lg[t]), 5, range(24))
+    np.testing.assert_allclose(w, scipy.special.expit(np.take_along_axis(lg, ids, 1)
+                                                      .astype(np.float64)), rtol=1e-6)
+
+
+def test_grouped_selection_bias_brute_force():
+    r = np.random.default_rng(11)
+    for _ in range(40):
+        l = r.standard_normal((1, 16)).astype(np.float32)
+        b = (r.integers(-3, 4, size=16) / 8.0)
+        x, rw = _router_for_logits(l)
+        ids, w, sel = O.route(x, rw, b, top_k=3, renormalize=False, scoring="sigmoid",
+                              bias_mode="select", n_group=4, topk_group=2)
+        p = scipy.special.expit(l[0].astype(np.float64))
+        s32 = (p.astype(np.float32) + b.astype(np.float32)).astype(np.float32)
+        assert list(ids[0]) == _subset_grouped(list(s32), 3, 4, 2)
+        np.testing.assert_allclose(w[0], p[ids[0]], rtol=1e-6)
+
+
 def test_min_gap_detects_near_ties():
     p = np.array([[0.5, 0.3, 0.2 + 5e-6, 0.2 - 5e-6],
                   [0.4, 0.3, 0.2, 0.1]], dtype=np.float64)
@@ -458,8 +538,21 @@ def _mutants():
     def topk_ascending(p, k):
         return orig_topk(p, k)[:, ::-1].copy()
 
-    return {"expert_mlp": [mlp_swapped, mlp_sigmoid], "route": [route_no_renorm],
-            "topk_plain": [topk_ties_high, topk_ascending]}
+    orig_sig = O.sigmoid_fp32
+
+    def sigmoid_as_tanh(l):
+        return np.tanh(np.asarray(l, np.float32)).astype(np.float32)
+
+    def route_weights_corrected(*a, **kw):
+        ids, w, sel = orig_route(*a, **kw)
+        ws = np.take_along_axis(sel, ids, axis=1).astype(np.float32)
+        if kw.get("renormalize"):
+            ws = (ws / ws.sum(axis=1, keepdims=True)).astype(np.float32)
+        return ids, ws, sel
+
+    return {"expert_mlp": [mlp_swapped, mlp_sigmoid],
+            "route": [route_no_renorm, route_weights_corrected],
+            "topk_plain": [topk_ties_high, topk_ascending], "sigmoid_fp32": [sigmoid_as_tanh]}
 
 
 def _brute_checks_pass():
@@ -469,13 +562,17 @@ def _brute_checks_pass():
         test_topk_plain_brute_force_with_ties()
         test_gate_up_roles_and_down_layout()
         test_route_weights_renormalised_and_raw()
+        test_sigmoid_scores_closed_form()
+        test_route_sigmoid_hand_example()
+        test_selection_bias_changes_choice_not_weights()
     except AssertionError:
         return False
     return True
 
 
 @pytest.mark.parametrize("name,idx", [("expert_mlp", 0), ("expert_mlp", 1), ("route", 0),
-                                      ("topk_plain", 0), ("topk_plain", 1)])
+                                      ("route", 1), ("topk_plain", 0), ("topk_plain", 1),
+                                      ("sigmoid_fp32", 0)])
 def test_planted_mistakes_are_caught(monkeypatch, name, idx):
     assert _brute_checks_pass()
     mutant = _mutants()[name][idx]
