@@ -90,14 +90,17 @@ template <int MODE, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_pair(const __grid_constant__ CUtensorMap mapA,
                   const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
-                  const int* __restrict__ group_start, int n_groups, int m_tiles, int k_blocks,
-                  int a_rows_per_expert, int a_up_offset, int b_from_out,
+                  const int* __restrict__ group_start, int n_groups, int dense_T, int m_tiles,
+                  int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
                   __nv_bfloat16* __restrict__ out, long out_ld, unsigned* status) {
   using S = PairShape<MODE, NMAX>;
   const uint32_t rank = ptx::cluster_rank();
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
-  const int total = group_start[n_groups] * m_tiles;
+  // Dense problems (shared experts: every token of dense_T for each of
+  // n_groups weight slabs) pass no tile table; their tiles are implicit.
+  const int dense_per = (dense_T + NMAX - 1) / NMAX;
+  const int total = (tiles ? group_start[n_groups] : n_groups * dense_per) * m_tiles;
   if (pair >= total) return;  // both CTAs of the pair leave together
 
   extern __shared__ uint8_t smem_raw[];
@@ -117,7 +120,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kNBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
-  for (int i = threadIdx.x; i <= n_groups; i += kThreads) gstart[i] = group_start[i];
+  for (int i = threadIdx.x; i <= n_groups; i += kThreads)
+    gstart[i] = tiles ? group_start[i] : i * dense_per;
+  auto tile_at = [&](int ti) -> Tile {
+    if (tiles) return tiles[ti];
+    const int sl = ti / dense_per, t0 = (ti - sl * dense_per) * NMAX;
+    return make_int4(sl, t0, sl * dense_T + t0, min(NMAX, dense_T - t0));
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = pair; u < total && pre < S::kStages; u += n_pairs) {
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-        const Tile tl = tiles[ti];
+        const Tile tl = tile_at(ti);
         const int a_row =
             MODE == kGemmSiluUp
                 ? tl.x * a_rows_per_expert + static_cast<int>(rank) * a_up_offset + m * 128
@@ -178,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = pair; u < total && ok; u += n_pairs) {
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-        const Tile tl = tiles[ti];
+        const Tile tl = tile_at(ti);
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
         const int a_row =
@@ -218,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-        const Tile tl = tiles[ti];
+        const Tile tl = tile_at(ti);
         const int n_mma = (tl.w + 31) & ~31;
         const uint32_t idesc = ptx::idesc_make(1u, 256, n_mma);
         const int b = ai % S::kNAcc;
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
       int ti, m;
       decode_unit(u, gstart, n_groups, m_tiles, ti, m);
-      const Tile tl = tiles[ti];
+      const Tile tl = tile_at(ti);
       const int b = ai % S::kNAcc;
       const uint32_t aph = (ai / S::kNAcc) & 1;
       if (!ptx::mbar_wait_cluster(tfull0 + 8 * b, aph, abort_flag, status)) break;
@@ -373,7 +382,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return counted(cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
-                            a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
+                            a.dense_T, a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
                             a.b_from_out, static_cast<__nv_bfloat16*>(a.out), a.out_ld,
                             a.status));
 }
@@ -382,7 +391,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
 
 cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num_sms,
                              cudaStream_t st) {
-  if (a.tiles == nullptr || a.k_split != 1) return cudaErrorInvalidValue;
+  if ((a.tiles == nullptr && a.dense_T <= 0) || a.k_split != 1) return cudaErrorInvalidValue;
   if (nmax == 256 && mode == kGemmPlain)
     return launch_pair_variant<kGemmPlain, 256>(a, num_sms, st);
   if (nmax == 256 && mode == kGemmSiluUp)

@@ -158,6 +158,12 @@ bool gemms_on_pairs(const moe_config* c, int T) {
   return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
 }
 
+// Shared experts over at least two 256-token tiles per slab run on CTA pairs
+// like the long routed segments.
+bool shared_on_pairs(const moe_config* c, int T) {
+  return c->act_dtype == MOE_BF16 && T >= 512 && c->hidden_size % 256 == 0;
+}
+
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -717,15 +723,16 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   if (with_shared) {
     S = cfg->num_shared_experts;
     const int Is = cfg->shared_intermediate_size;
-    const int nm = dense_nmax(T);
+    const bool sp = shared_on_pairs(cfg, T);
+    const int nm = sp ? 256 : dense_nmax(T);
     void* h_sh = at<void>(ws, L.h_sh);
     void* y_sh = at<void>(ws, L.y_sh);
     MOE_TRY(run_gemm(kGemmSiluUp, cfg->act_dtype, nm, shared_w13, static_cast<long>(S) * 2 * Is,
                      x, T, H, nullptr, nullptr, S, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
-                     st, 1, 0, T));
+                     st, 1, 0, T, sp));
     MOE_TRY(run_gemm(kGemmPlain, cfg->act_dtype, nm, shared_w2, static_cast<long>(S) * H, h_sh,
-                     static_cast<long>(S) * T, Is, nullptr, nullptr, S, H / 128, H, 0, 1, y_sh,
-                     H, H, status, st, 1, 0, T));
+                     static_cast<long>(S) * T, Is, nullptr, nullptr, S, H / (sp ? 256 : 128), H,
+                     0, 1, y_sh, H, H, status, st, 1, 0, T, sp));
     shared_y = y_sh;
   }
   MOE_TRY(mark(6));

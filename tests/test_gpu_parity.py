@@ -60,6 +60,9 @@ SMALL = {
     "sigmoid_select_wide": W("sigmoid_select_wide", T=300, H=256, I=256, E=32, K=4,
                              router_bias=True, bias_mode="select", scoring="sigmoid",
                              renormalize=False),
+    # two shared experts over T >= 512 tokens: dense tiles on CTA pairs, ragged last tile
+    "shared_pairs": W("shared_pairs", T=600, H=256, I=256, E=16, K=2, n_shared=2,
+                      I_shared=384),
     # sigmoid with a logit bias, fp32 layer
     "sigmoid_f32": W("sigmoid_f32", T=50, H=128, I=128, E=8, K=2, act="f32", router="f32",
                      router_bias=True, scoring="sigmoid", x_std=0.3),
