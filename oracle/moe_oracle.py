@@ -22,7 +22,10 @@ Pins (checked by ``tests/test_oracle_pins.py``):
   * expert MLP: pinned by the SiLU closed form and the gate/up role test;
   * forward: pinned by the page's dense per-expert masked loop, the EP
     shard-sum identity, shared-expert merging and rsf linearity;
-  * align/permute: pinned by a brute-force stable sort and counting.
+  * align/permute: pinned by a brute-force stable sort and counting;
+  * EP dispatch, expert compute, exchange and combine: pinned by the
+    all-ranks pipeline equalling the unsharded forward, and by a brute-force
+    stable partition by destination rank.
   The output values themselves have no numeric worked example on the pages,
   so they are pinned only by these identities.
 """
@@ -395,3 +398,84 @@ def weight_bytes_per_card(n_experts, intermediate, hidden, n_layers, elem_bytes)
     """
     per_expert = 2 * intermediate * hidden + hidden * intermediate
     return n_experts * per_expert * elem_bytes * n_layers
+
+
+# ---------------------------------------------------------------------------
+# expert-parallel dispatch and combine (the rank-local halves of the exchange)
+# ---------------------------------------------------------------------------
+def ep_dispatch(x, topk_ids, topk_w, num_experts, ep_size):
+    """Send buffers of one rank, ordered by destination rank.
+
+    ep_fused_moe_patch.py ``_ep_forward`` step 2: every (token, slot) work
+    item goes to the rank owning its expert (dest = id // (E / ep_size)). Items
+    are sorted by destination and (hidden row, weight, global id, token index)
+    are packed, with per-destination counts for the all-to-all. The page sorts
+    with ``argsort``, which leaves the order inside a destination open. Reading
+    taken: a stable sort, so items keep ascending t*K + k order.
+
+    Returns (counts [ep] int64, send_pos [T*K] int32 = each item's row in the
+    send buffer, send_x [T*K, H], send_ids [T*K] int32, send_w [T*K] fp32,
+    send_tok [T*K] int32).
+    """
+    ids = np.asarray(topk_ids).reshape(-1)
+    w = np.asarray(topk_w, np.float32).reshape(-1)
+    T, K = np.asarray(topk_ids).shape
+    n_local = num_experts // ep_size
+    dest = ids // n_local
+    order = np.argsort(dest, kind="stable")
+    counts = np.bincount(dest, minlength=ep_size).astype(np.int64)
+    send_pos = np.empty(T * K, dtype=np.int32)
+    send_pos[order] = np.arange(T * K, dtype=np.int32)
+    tok = order // K
+    return (counts, send_pos, np.asarray(x)[tok], ids[order].astype(np.int32),
+            w[order], tok.astype(np.int32))
+
+
+def ep_expert_compute(recv_x, recv_ids, recv_w, w13_local, w2_local, start_expert):
+    """Rows a rank sends back for the items it received, fp64.
+
+    ``_ep_forward`` step 3: local id = global id - start_expert, and the local
+    experts run with top_k = 1 per received item. The page passes the item's
+    weight to ``fused_experts``, so each returned row is already weighted:
+    y[r] = w[r] * f_{id[r] - start}(x[r]).
+    """
+    rx = np.asarray(recv_x, np.float64)
+    lid = np.asarray(recv_ids) - start_expert
+    y = np.zeros_like(rx)
+    for e in np.unique(lid):
+        rows = np.nonzero(lid == e)[0]
+        y[rows] = expert_mlp(rx[rows], w13_local[e], w2_local[e])
+    return y * np.asarray(recv_w, np.float64)[:, None]
+
+
+def ep_combine(ret_rows, send_pos, top_k, rsf=1.0, shared_out=None):
+    """out[t] = rsf * sum_k ret[send_pos[t*K + k]] + shared_out[t].
+
+    ``_ep_forward`` step 4: the returned rows come back in send order. They
+    are un-sorted and scatter-added by token index, unweighted because the
+    weights were applied by the expert-holding rank. rsf and the shared
+    experts then apply as in the single-rank forward.
+    """
+    ret = np.asarray(ret_rows, np.float64)
+    pos = np.asarray(send_pos).reshape(-1, top_k)
+    out = np.zeros((pos.shape[0], ret.shape[1]), dtype=np.float64)
+    for k in range(top_k):
+        out += ret[pos[:, k]]
+    out *= np.float64(rsf)
+    if shared_out is not None:
+        out += np.asarray(shared_out, np.float64)
+    return out
+
+
+def ep_exchange(send_bufs, send_counts):
+    """All-to-all of per-rank send buffers (host simulation of the exchange).
+
+    send_bufs[r] is rank r's buffer ordered by destination and
+    send_counts[r][d] the number of its rows for rank d. Rank d receives the
+    rows for it from every rank, concatenated in source-rank order, as
+    ``all_to_all_single`` with split sizes does.
+    """
+    ep = len(send_bufs)
+    offs = [np.concatenate([[0], np.cumsum(c)]) for c in send_counts]
+    return [np.concatenate([send_bufs[s][offs[s][d]:offs[s][d + 1]] for s in range(ep)])
+            for d in range(ep)]

@@ -501,6 +501,82 @@ def test_grouped_mlp_and_combine_recompose_forward():
 # ---------------------------------------------------------------------------
 # the pages' printed figures
 # ---------------------------------------------------------------------------
+def _ep_pipeline(rank_x, d, ep, top_k, rsf=1.0, routing_kw=None, combine=None):
+    """Every rank routes its own tokens globally, dispatches, exchanges, runs
+    its expert shard, returns and combines (host-simulated all-to-alls)."""
+    E = d["router_w"].shape[0]
+    El = E // ep
+    kw = dict(top_k=top_k, renormalize=True, **(routing_kw or {}))
+    sends = []
+    for x in rank_x:
+        ids, w, _ = O.route(x, d["router_w"], d["router_b"], **kw)
+        sends.append(O.ep_dispatch(x, ids, w, E, ep))
+    counts = [s[0] for s in sends]
+    recv_x = O.ep_exchange([s[2] for s in sends], counts)
+    recv_ids = O.ep_exchange([s[3] for s in sends], counts)
+    recv_w = O.ep_exchange([s[4] for s in sends], counts)
+    outs = [O.ep_expert_compute(recv_x[r], recv_ids[r], recv_w[r],
+                                d["w13"][r * El:(r + 1) * El], d["w2"][r * El:(r + 1) * El],
+                                r * El) for r in range(ep)]
+    back_counts = [[counts[s][r] for s in range(ep)] for r in range(ep)]
+    ret = O.ep_exchange(outs, back_counts)
+    comb = combine or O.ep_combine
+    res = []
+    for r, x in enumerate(rank_x):
+        sh = None
+        if d["shared_w13"] is not None:
+            sh = sum(O.expert_mlp(x, d["shared_w13"][s], d["shared_w2"][s])
+                     for s in range(d["shared_w13"].shape[0]))
+        res.append(comb(ret[r], sends[r][1], top_k, rsf, sh))
+    return res
+
+
+@pytest.mark.parametrize("ep", [2, 4])
+def test_ep_dispatch_pipeline_equals_unsharded(ep):
+    d = _layer(T=1, H=12, I=10, E=8, S=1, seed=21, bias=True)
+    r = np.random.default_rng(22)
+    rank_x = [r.standard_normal((n, 12)) for n in (7, 0, 5, 9)[:ep]]
+    for kw in (dict(), dict(n_group=4, topk_group=2)):
+        got = _ep_pipeline(rank_x, d, ep, 3, rsf=1.5, routing_kw=kw)
+        for x, g in zip(rank_x, got):
+            ref = _fwd(dict(d, x=x), top_k=3, rsf=1.5, **kw)
+            np.testing.assert_allclose(g, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_ep_dispatch_brute_force():
+    r = np.random.default_rng(23)
+    T, K, E, ep = 13, 3, 12, 4
+    ids = np.stack([r.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    w = r.random((T, K)).astype(np.float32)
+    x = r.standard_normal((T, 5))
+    counts, pos, sx, sid, sw, stok = O.ep_dispatch(x, ids, w, E, ep)
+    # brute force: walk items in order, append each to its destination's list
+    lists = [[] for _ in range(ep)]
+    for t in range(T):
+        for k in range(K):
+            lists[ids[t, k] // (E // ep)].append((t, k))
+    order = [it for l in lists for it in l]
+    assert list(counts) == [len(l) for l in lists]
+    for row, (t, k) in enumerate(order):
+        assert pos[t * K + k] == row and sid[row] == ids[t, k] and stok[row] == t
+        assert sw[row] == w[t, k]
+        np.testing.assert_array_equal(sx[row], x[t])
+
+
+def test_planted_ep_mistakes_are_caught():
+    d = _layer(T=1, H=12, I=10, E=8, S=0, seed=24)
+    r = np.random.default_rng(25)
+    rank_x = [r.standard_normal((6, 12)) for _ in range(2)]
+    ref = [_fwd(dict(d, x=x), top_k=2) for x in rank_x]
+
+    def combine_reweighted(ret, pos, k, rsf=1.0, sh=None):
+        return 2.0 * O.ep_combine(ret, pos, k, rsf, sh)  # weights applied twice (w ~ 1/2)
+    bad = _ep_pipeline(rank_x, d, 2, 2, combine=combine_reweighted)
+    assert not all(np.allclose(b, f) for b, f in zip(bad, ref))
+    good = _ep_pipeline(rank_x, d, 2, 2)
+    assert all(np.allclose(g, f) for g, f in zip(good, ref))
+
+
 def test_weight_sizing_formula_matches_page():
     g = json.load(open(os.path.join(HERE, "golden", "ep_weight_sizing.json")))
     for c in g["cases"]:
