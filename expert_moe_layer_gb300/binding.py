@@ -97,6 +97,11 @@ _SIGS = {
                                ctypes.POINTER(ctypes.c_int)]),
     "moe_get_status": (_I, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32)]),
     "moe_forward_plan": (_I, [_CFG, _I, ctypes.POINTER(Plan)]),
+    "moe_ep_dispatch_workspace_size": (_SZ, [_CFG, _I]),
+    "moe_ep_dispatch": (_I, [_CFG, _I] + [_VP] * 11 + [_SZ, _VP]),
+    "moe_ep_expert_compute_workspace_size": (_SZ, [_CFG, _I]),
+    "moe_ep_expert_compute": (_I, [_CFG, _I] + [_VP] * 7 + [_SZ, _VP]),
+    "moe_ep_combine": (_I, [_CFG, _I] + [_VP] * 5 + [_SZ, _VP]),
 }
 
 
@@ -191,6 +196,34 @@ def forward_plan(cfg, T) -> Plan:
     out = Plan()
     _check("moe_forward_plan", lib().moe_forward_plan(ctypes.byref(cfg), T, ctypes.byref(out)))
     return out
+
+
+def ep_dispatch_workspace_size(cfg, T) -> int:
+    return lib().moe_ep_dispatch_workspace_size(ctypes.byref(cfg), T)
+
+
+def moe_ep_dispatch(cfg, T, x, topk_ids, topk_w, send_counts, send_offsets, send_pos, send_x,
+                    send_ids, send_w, send_tok, ws, stream=None):
+    _check("moe_ep_dispatch", lib().moe_ep_dispatch(
+        ctypes.byref(cfg), T, _p(x), _p(topk_ids), _p(topk_w), _p(send_counts),
+        _p(send_offsets), _p(send_pos), _p(send_x), _p(send_ids), _p(send_w), _p(send_tok),
+        _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def ep_expert_compute_workspace_size(cfg, R) -> int:
+    return lib().moe_ep_expert_compute_workspace_size(ctypes.byref(cfg), R)
+
+
+def moe_ep_expert_compute(cfg, R, recv_x, recv_ids, recv_w, w13, w2, y, ws, stream=None):
+    _check("moe_ep_expert_compute", lib().moe_ep_expert_compute(
+        ctypes.byref(cfg), R, _p(recv_x), _p(recv_ids), _p(recv_w), _p(w13), _p(w2), _p(y),
+        _p(ws), _nbytes(ws), _stream(stream)))
+
+
+def moe_ep_combine(cfg, T, ret, send_pos, shared_out, out, ws=None, stream=None):
+    _check("moe_ep_combine", lib().moe_ep_combine(
+        ctypes.byref(cfg), T, _p(ret), _p(send_pos), _p(shared_out), _p(out), _p(ws),
+        _nbytes(ws), _stream(stream)))
 
 
 def moe_route(cfg, T, x, router_w, router_bias, topk_ids, topk_w, ws, stream=None):

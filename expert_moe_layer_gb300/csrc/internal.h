@@ -170,7 +170,18 @@ struct MlpFusedArgs {
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st);
 size_t mlp_fused_smem_bytes();
 
-// out[t] = rsf * sum_k w[t,k] y_perm[inv_pos[t,k]] + sum_s shared[s][t].
+// Expert-parallel dispatch: dest[i] = ids[i] / n_local (-1 outside [0, E)),
+// then, after an align over the destination ranks, the send buffers in
+// destination order (row r = item sorted_ids[r], rows_dev[0] valid rows).
+cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32_t* dest,
+                           cudaStream_t st);
+cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const float* w,
+                           const int32_t* sorted_ids, const int32_t* rows_dev, long n_items,
+                           int K, int H, void* send_x, int32_t* send_ids, float* send_w,
+                           int32_t* send_tok, cudaStream_t st);
+
+// out[t] = rsf * sum_k w[t,k] y_perm[inv_pos[t,k]] + sum_s shared[s][t]
+// (topk_w may be null: unit weights).
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
                            const float* topk_w, int K, const void* shared, int n_shared,
                            long shared_stride, float rsf, void* out, int T, int H,

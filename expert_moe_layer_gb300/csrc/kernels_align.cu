@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256, KB > 4 ? 3 : 4) combine_kernel(
     float w = 0.f;
     if (t < T && lane < K) {
       p = inv_pos[t * K + lane];
-      w = topk_w[t * K + lane];
+      w = topk_w ? topk_w[t * K + lane] : 1.f;
       if (p >= cap) {
         if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
         p = -1;
@@ -473,6 +473,46 @@ __global__ void __launch_bounds__(256, KB > 4 ? 3 : 4) combine_kernel(
       }
       st8(out + t * H + c, acc[u]);
     }
+  }
+}
+
+// Expert-parallel dispatch (ep_fused_moe_patch.py _ep_forward step 2):
+// destination rank of each work item, -1 for an id outside [0, E).
+__global__ void __launch_bounds__(256) ep_dest_kernel(const int32_t* __restrict__ ids,
+                                                      long n, int E, int n_local,
+                                                      int32_t* __restrict__ dest) {
+  pdl_enter();
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x) {
+    const int id = ids[i];
+    dest[i] = (id >= 0 && id < E) ? id / n_local : -1;
+  }
+}
+
+// Send buffers in destination order: row r holds item sorted_ids[r] (one
+// warp per row, 16-byte vectors for the hidden row).
+template <typename TE>
+__global__ void __launch_bounds__(256) ep_pack_kernel(
+    const TE* __restrict__ x, const int32_t* __restrict__ ids, const float* __restrict__ w,
+    const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ rows_dev, long n_items,
+    int K, int H, TE* __restrict__ send_x, int32_t* __restrict__ send_ids,
+    float* __restrict__ send_w, int32_t* __restrict__ send_tok) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  long rows = *rows_dev;
+  if (rows > n_items) rows = n_items;
+  constexpr int kVec = 16 / sizeof(TE);
+  for (long r = blockIdx.x * 8L + warp; r < rows; r += 8L * gridDim.x) {
+    const int item = sorted_ids[r];
+    if (item < 0 || item >= n_items) continue;
+    const long t = item / K;
+    if (lane == 0) {
+      send_ids[r] = ids[item];
+      send_w[r] = w[item];
+      send_tok[r] = static_cast<int32_t>(t);
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    uint4* dst = reinterpret_cast<uint4*>(send_x + r * H);
+    for (int c = lane; c < H / kVec; c += 32) dst[c] = src[c];
   }
 }
 
@@ -548,6 +588,27 @@ cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long 
                       n_part, part_stride, rows_dev, cap, I, static_cast<__nv_bfloat16*>(h));
   return launch_pdl(silu_finalize_kernel<float>, dim3(grid), dim3(256), 0, st, part, n_part,
                     part_stride, rows_dev, cap, I, static_cast<float*>(h));
+}
+
+cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32_t* dest,
+                           cudaStream_t st) {
+  return launch_pdl(ep_dest_kernel, dim3(grid_for(n, 256, 8 * 152)), dim3(256), 0, st, ids, n,
+                    E, n_local, dest);
+}
+
+cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const float* w,
+                           const int32_t* sorted_ids, const int32_t* rows_dev, long n_items,
+                           int K, int H, void* send_x, int32_t* send_ids, float* send_w,
+                           int32_t* send_tok, cudaStream_t st) {
+  const int grid = grid_for(n_items, 8, 8 * 152);
+  if (bf16)
+    return launch_pdl(ep_pack_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16*>(x), ids, w, sorted_ids, rows_dev,
+                      n_items, K, H, static_cast<__nv_bfloat16*>(send_x), send_ids, send_w,
+                      send_tok);
+  return launch_pdl(ep_pack_kernel<float>, dim3(grid), dim3(256), 0, st,
+                    static_cast<const float*>(x), ids, w, sorted_ids, rows_dev, n_items, K, H,
+                    static_cast<float*>(send_x), send_ids, send_w, send_tok);
 }
 
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,

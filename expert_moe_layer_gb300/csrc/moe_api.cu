@@ -343,6 +343,40 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   return L;
 }
 
+// Workspace of moe_ep_dispatch.
+struct EpLayout {
+  size_t status, dest, hist, sorted, total;
+};
+EpLayout ep_layout(const moe_config* c, int T) {
+  Carver cv;
+  EpLayout L;
+  const size_t n = static_cast<size_t>(T) * c->top_k;
+  L.status = cv.take(4);
+  L.dest = cv.take(4 * n);
+  L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(static_cast<long>(n))) *
+                   c->ep_size);
+  L.sorted = cv.take(4 * n);
+  L.total = cv.off;
+  return L;
+}
+
+// The config of the expert compute on received items: one slot per item,
+// no routing, no shared experts, no scaling.
+moe_config ep_item_config(const moe_config* c) {
+  moe_config c1 = *c;
+  c1.top_k = 1;
+  c1.use_grouped_topk = 0;
+  c1.num_expert_group = 0;
+  c1.topk_group = 0;
+  c1.num_shared_experts = 0;
+  c1.shared_intermediate_size = 0;
+  c1.routed_scaling_factor = 1.0f;
+  c1.scoring_func = MOE_SCORE_SOFTMAX;
+  c1.bias_mode = MOE_BIAS_LOGIT;
+  return c1;
+}
+
+
 template <typename P>
 P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
@@ -581,6 +615,103 @@ int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const
   if (status) MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, y_perm, cap, inv_pos, topk_w,
                                 cfg->top_k, shared_out, shared_out ? 1 : 0, 0,
+                                cfg->routed_scaling_factor, out, T, cfg->hidden_size, status,
+                                st));
+}
+
+// ------------------------------------------------------ expert parallel
+size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(T) != MOE_OK) return 0;
+  return ep_layout(cfg, T).total;
+}
+
+int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
+                    const float* topk_w, int32_t* send_counts, int32_t* send_offsets,
+                    int32_t* send_pos, void* send_x, int32_t* send_ids, float* send_w,
+                    int32_t* send_tok, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (!send_counts || !send_offsets) return MOE_ERR_INVALID_ARG;
+  const int ep = cfg->ep_size;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    MOE_TRY(cuda_ok(cudaMemsetAsync(send_counts, 0, 4 * static_cast<size_t>(ep), st)));
+    return cuda_ok(cudaMemsetAsync(send_offsets, 0, 4 * static_cast<size_t>(ep + 1), st));
+  }
+  if (!x || !topk_ids || !topk_w || !send_pos || !send_x || !send_ids || !send_w || !send_tok)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(send_x)) return MOE_ERR_INVALID_ARG;
+  const EpLayout L = ep_layout(cfg, T);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  unsigned* status = at<unsigned>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  const long n = static_cast<long>(T) * cfg->top_k;
+  int32_t* dest = at<int32_t>(ws, L.dest);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+  MOE_TRY(cuda_ok(launch_ep_dest(topk_ids, n, cfg->num_experts, n_local(cfg), dest, st)));
+  // a stable counting sort of the items over the destination ranks
+  MOE_TRY(cuda_ok(launch_align(dest, n, nullptr, ep, ep, 0, 1, at<int>(ws, L.hist), send_counts,
+                               send_offsets, sorted, send_pos, static_cast<int>(n), status, st)));
+  return cuda_ok(launch_ep_pack(cfg->act_dtype == MOE_BF16, x, topk_ids, topk_w, sorted,
+                                send_offsets + ep, n, cfg->top_k, cfg->hidden_size, send_x,
+                                send_ids, send_w, send_tok, st));
+}
+
+size_t moe_ep_expert_compute_workspace_size(const moe_config* cfg, int R) {
+  if (validate_cfg(cfg) != MOE_OK || validate_T(R) != MOE_OK) return 0;
+  const moe_config c1 = ep_item_config(cfg);
+  return fwd_layout(&c1, R).total;
+}
+
+int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
+                          const int32_t* recv_ids, const float* recv_w, const void* w13,
+                          const void* w2, void* y, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(R));
+  if (R == 0) return MOE_OK;
+  if (!recv_x || !recv_ids || !recv_w || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv_x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c1 = ep_item_config(cfg);
+  const FwdLayout L = fwd_layout(&c1, R);
+  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = at<unsigned>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.sync.bytes, st)));
+  const int El = n_local(&c1);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* sorted_ids = at<int32_t>(ws, L.sorted_ids);
+  int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
+  MOE_TRY(cuda_ok(launch_align(recv_ids, R, nullptr, c1.num_experts, El, c1.ep_rank * El,
+                               kForwardBlock, at<int>(ws, L.hist), counts, offsets, sorted_ids,
+                               inv_pos, L.cap, status, st, at<Tile>(ws, L.tiles),
+                               at<int>(ws, L.groups), routed_nmax(&c1, R),
+                               static_cast<int>(max_routed_tiles(&c1, R)))));
+  MOE_TRY(do_mlp(&c1, R, recv_x, sorted_ids, counts, offsets, L.cap, w13, w2,
+                 at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups), L.sync,
+                 at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
+                 st, nullptr, true));
+  return cuda_ok(launch_combine(c1.act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
+                                inv_pos, recv_w, 1, nullptr, 0, 0, 1.0f, y, R,
+                                c1.hidden_size, status, st));
+}
+
+int moe_ep_combine(const moe_config* cfg, int T, const void* ret, const int32_t* send_pos,
+                   const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                   void* stream) {
+  MOE_TRY(validate_cfg(cfg));
+  MOE_TRY(validate_T(T));
+  if (T == 0) return MOE_OK;
+  if (!ret || !send_pos || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ret) || !aligned16(out) || (shared_out && !aligned16(shared_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (ws && ws_bytes < 4) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* status = ws ? static_cast<unsigned*>(ws) : nullptr;
+  if (status) MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
+  return cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, ret, T * cfg->top_k, send_pos,
+                                nullptr, cfg->top_k, shared_out, shared_out ? 1 : 0, 0,
                                 cfg->routed_scaling_factor, out, T, cfg->hidden_size, status,
                                 st));
 }

@@ -311,6 +311,59 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
                       void* ws, size_t ws_bytes, void* stream,
                       void* const* events, int* kernels_launched);
 
+/* ------------------------------------------------------------------------ */
+/* Expert-parallel dispatch and combine: the rank-local halves of
+ * ep_fused_moe_patch.py _ep_forward steps 2-4. The exchange between ranks
+ * (all_to_all_single of the send buffers with the counts as split sizes, and
+ * back) is the caller's: this library runs no collective.
+ *
+ * moe_ep_dispatch (step 2). Work item i = t*K + k goes to rank
+ * topk_ids[i] / (E / ep_size). The items are sorted by destination rank and
+ * packed. The page's argsort leaves the order inside a destination open; here
+ * it is stable (ascending i).
+ *   x        [T, H] act_dtype
+ *   topk_ids [T, K] int32 global ids, topk_w [T, K] fp32 (from moe_route)
+ *   send_counts  [ep_size] int32 out: rows for each destination rank
+ *   send_offsets [ep_size + 1] int32 out: exclusive prefix of send_counts
+ *   send_pos [T*K] int32 out: row of item i in the send buffers (-1 for an id
+ *            outside [0, E), which also sets MOE_DEV_BAD_EXPERT_ID)
+ *   send_x   [T*K, H] act_dtype out, send_ids [T*K] int32 out (global ids),
+ *   send_w   [T*K] fp32 out, send_tok [T*K] int32 out (token index); rows
+ *            past send_offsets[ep_size] are left untouched.
+ * ws: moe_ep_dispatch_workspace_size(cfg, T) bytes. */
+size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T);
+int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
+                    const float* topk_w, int32_t* send_counts, int32_t* send_offsets,
+                    int32_t* send_pos, void* send_x, int32_t* send_ids, float* send_w,
+                    int32_t* send_tok, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_ep_expert_compute (step 3): the R items this rank received, each run
+ * through its expert with top_k = 1 and weighted, as the page's call to
+ * fused_experts does:
+ *   y[r] = recv_w[r] * f_{recv_ids[r] - ep_rank*E_local}(recv_x[r]).
+ * Rows whose id is not one of this rank's experts come back as zeros.
+ *   recv_x [R, H] act_dtype, recv_ids [R] int32 global ids, recv_w [R] fp32
+ *   w13, w2: this rank's experts, as for moe_forward
+ *   y      [R, H] act_dtype out
+ * cfg's top_k, shared experts, routed_scaling_factor and routing fields are
+ * not used. ws: moe_ep_expert_compute_workspace_size(cfg, R) bytes. */
+size_t moe_ep_expert_compute_workspace_size(const moe_config* cfg, int R);
+int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
+                          const int32_t* recv_ids, const float* recv_w, const void* w13,
+                          const void* w2, void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_ep_combine (step 4): the rows returned to this rank (in its send
+ * order) are added back by token, unweighted (the expert-holding rank applied
+ * the weights), then scaled by rsf; the shared output is added:
+ *   out[t] = rsf * sum_{k : send_pos[t*K+k] >= 0} ret[send_pos[t*K+k]]
+ *            + shared_out[t]
+ *   ret [T*K, H] act_dtype, send_pos [T*K] int32 (from moe_ep_dispatch),
+ *   shared_out [T, H] nullable, out [T, H] act_dtype out.
+ * ws: NULL, or >= 4 bytes for the status word. */
+int moe_ep_combine(const moe_config* cfg, int T, const void* ret, const int32_t* send_pos,
+                   const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                   void* stream);
+
 /* The kernel plan moe_forward follows for (cfg, T): which variant runs each
  * stage. No page counterpart; it describes this library's own kernels, for
  * instrumentation and tests. Host-only (no device work); returns the

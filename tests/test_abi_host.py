@@ -138,3 +138,21 @@ def test_forward_plan_per_workload():
     assert _plan(synth.TINY, 0).kernels == 0
     with pytest.raises(B.MoeError):
         B.forward_plan(_cfg(top_k=0), 16)
+
+
+def test_ep_entry_points_reject_bad_args_without_cuda():
+    cfg = _cfg(num_experts=16, top_k=4, hidden_size=256, intermediate_size=256, ep_size=4)
+    L = B.lib()
+    bp = ctypes.byref
+    assert B.ep_dispatch_workspace_size(cfg, 64) > 0
+    assert B.ep_expert_compute_workspace_size(cfg, 64) > 0
+    assert B.ep_dispatch_workspace_size(_cfg(top_k=0), 64) == 0
+    # dispatch: missing outputs, then a workspace that is too small
+    assert L.moe_ep_dispatch(bp(cfg), 8, *([None] * 11), 0, None) == 1
+    fake = 1 << 20
+    args = [fake] * 10
+    assert L.moe_ep_dispatch(bp(cfg), 8, *args, fake, 8, None) == 3
+    # expert compute and combine: missing pointers
+    assert L.moe_ep_expert_compute(bp(cfg), 8, *([None] * 7), 0, None) == 1
+    assert L.moe_ep_combine(bp(cfg), 8, None, None, None, None, None, 0, None) == 1
+    assert L.moe_ep_combine(bp(_cfg(top_k=0)), 8, None, None, None, None, None, 0, None) == 1

@@ -63,6 +63,48 @@ def _ep_worker(rank, world, port, q):
     dist.destroy_process_group()
 
 
+def _a2a(buf, send_counts, recv_counts):
+    """all_to_all_single of the rows of a numpy buffer with split sizes."""
+    t = torch.from_numpy(np.ascontiguousarray(buf))
+    out = torch.empty((int(sum(recv_counts)),) + tuple(t.shape[1:]), dtype=t.dtype)
+    dist.all_to_all_single(out, t, output_split_sizes=[int(c) for c in recv_counts],
+                           input_split_sizes=[int(c) for c in send_counts])
+    return out.numpy()
+
+
+def _ep_dispatch_worker(rank, world, port, q):
+    """The page's _ep_forward on real ranks: every rank routes its own tokens
+    over all experts, all-gathers the send counts, exchanges (rows, ids,
+    weights) with all_to_all_single, runs its expert shard on what it
+    received, sends the rows back and combines. The exchange logic around
+    the library's dispatch/compute/combine calls is checked here, with the
+    oracle standing in for them."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import moe_oracle as O
+    _init(rank, world, port)
+    d = _layer()
+    E = d["w13"].shape[0]
+    El = E // world
+    x = np.random.default_rng(40 + rank).standard_normal(((9, 4)[rank], d["x"].shape[1]))
+    ids, w, _ = O.route(x, d["router_w"], top_k=3, renormalize=True)
+    counts, pos, sx, sids, sw, _ = O.ep_dispatch(x, ids, w, E, world)
+    parts = [torch.zeros(world, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(parts, torch.from_numpy(counts))
+    recv_counts = [int(p[rank]) for p in parts]
+    rx = _a2a(sx, counts, recv_counts)
+    rids = _a2a(sids, counts, recv_counts)
+    rw = _a2a(sw, counts, recv_counts)
+    y = O.ep_expert_compute(rx, rids, rw, d["w13"][rank * El:(rank + 1) * El],
+                            d["w2"][rank * El:(rank + 1) * El], rank * El)
+    ret = _a2a(y, recv_counts, counts)
+    out = O.ep_combine(ret, pos, 3, rsf=2.0)
+    full = O.moe_forward(x, d["router_w"], d["w13"], d["w2"], top_k=3, renormalize=True,
+                         rsf=2.0)
+    q.put(float(np.abs(out - full).max()))
+    dist.destroy_process_group()
+
+
 def _bench_worker(rank, world, port, q):
     import sys
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -95,6 +137,11 @@ def _run(fn, world=2):
 def test_ep_partial_outputs_all_reduce_to_unsharded_layer():
     out = _run(_ep_worker)
     assert len(out) == 1 and out[0] < 1e-12
+
+
+def test_ep_dispatch_all_to_all_equals_unsharded_layer():
+    out = _run(_ep_dispatch_worker)
+    assert len(out) == 2 and max(out) < 1e-12
 
 
 def test_bench_aggregates_slowest_rank_and_all_tokens():
