@@ -116,7 +116,7 @@ def cfg_of(wl):
     from expert_moe_layer_gb300 import binding as B
     return B.make_config(wl.E, wl.K, wl.H, wl.I, wl.renormalize, wl.n_group, wl.topk_group,
                          wl.rsf, wl.n_shared, wl.I_shared, wl.ep_size, wl.ep_rank, wl.act,
-                         wl.router)
+                         wl.router, wl.scoring, wl.bias_mode)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -498,6 +498,118 @@ def run_reference(args, wl):
                     "d2h_bytes_per_step": 0}}
 
 
+# --------------------------------------------------------------------------- EP dispatch
+def run_ep_dispatch(args, device):
+    """One expert-parallel rank's step at the EP-shard shape (T=8192 own tokens,
+    E=256, K=8, ep 4, rank 1): route, dispatch, the exchange, expert compute on
+    what the rank receives, the return, combine. No collective runs here; the
+    exchange stand-in is device copies. This rank receives its own segment for
+    rank 1 from each of the 4 ranks (the sources are assumed alike), so it
+    computes about T*K items as a real rank does. The rows returned for its
+    items sent elsewhere are zero, a stand-in for the other ranks' results,
+    and do not change the work. Timed per call with CUDA events, eager, L2
+    flushed before each step."""
+    from expert_moe_layer_gb300 import binding as B
+    wl = synth.EP_SHARD
+    T, H, K, E, ep, r = wl.T, wl.H, wl.K, wl.E, wl.ep_size, wl.ep_rank
+    cfg = cfg_of(wl)
+    d = device_layer(wl, device)
+    peaks = load_peaks()
+    n = T * K
+    stream = torch.cuda.current_stream(device)
+    ids = torch.empty(T, K, dtype=torch.int32, device=device)
+    w = torch.empty(T, K, dtype=torch.float32, device=device)
+    rws = torch.empty(B.route_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+    counts = torch.empty(ep, dtype=torch.int32, device=device)
+    offsets = torch.empty(ep + 1, dtype=torch.int32, device=device)
+    pos = torch.empty(n, dtype=torch.int32, device=device)
+    sx = torch.empty(n, H, dtype=torch.bfloat16, device=device)
+    sids = torch.empty(n, dtype=torch.int32, device=device)
+    sw = torch.empty(n, dtype=torch.float32, device=device)
+    stok = torch.empty(n, dtype=torch.int32, device=device)
+    dws = torch.empty(B.ep_dispatch_workspace_size(cfg, T), dtype=torch.uint8, device=device)
+    # the receive side is sized from one routing of this batch
+    B.moe_route(cfg, T, d["x"], d["router_w"], d["router_b"], ids, w, rws)
+    B.moe_ep_dispatch(cfg, T, d["x"], ids, w, counts, offsets, pos, sx, sids, sw, stok, dws)
+    off = offsets.cpu().numpy()
+    c_r = int(off[r + 1] - off[r])
+    R = ep * c_r
+    rx = torch.empty(R, H, dtype=torch.bfloat16, device=device)
+    rids = torch.empty(R, dtype=torch.int32, device=device)
+    rw = torch.empty(R, dtype=torch.float32, device=device)
+    y = torch.empty(R, H, dtype=torch.bfloat16, device=device)
+    ret = torch.zeros(n, H, dtype=torch.bfloat16, device=device)
+    cws = torch.empty(B.ep_expert_compute_workspace_size(cfg, R), dtype=torch.uint8,
+                      device=device)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+    sws = torch.zeros(256, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
+    names = ["route", "dispatch", "exchange", "expert_compute", "return", "combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        B.moe_route(cfg, T, d["x"], d["router_w"], d["router_b"], ids, w, rws, stream)
+        mark(1)
+        B.moe_ep_dispatch(cfg, T, d["x"], ids, w, counts, offsets, pos, sx, sids, sw, stok,
+                          dws, stream)
+        mark(2)
+        seg = slice(int(off[r]), int(off[r + 1]))
+        for s in range(ep):
+            rx[s * c_r:(s + 1) * c_r].copy_(sx[seg])
+            rids[s * c_r:(s + 1) * c_r].copy_(sids[seg])
+            rw[s * c_r:(s + 1) * c_r].copy_(sw[seg])
+        mark(3)
+        B.moe_ep_expert_compute(cfg, R, rx, rids, rw, d["w13"], d["w2"], y, cws, stream)
+        mark(4)
+        ret[seg].copy_(y[:c_r])
+        mark(5)
+        B.moe_ep_combine(cfg, T, ret, pos, None, out, sws, stream)
+        mark(6)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    for i in range(args.steps):
+        flush()
+        step(evs[i])
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    for ws in (rws, dws, cws, sws):
+        rc, flags = B.moe_get_status(ws, stream)
+        if rc != 0:
+            raise RuntimeError(f"device status {rc} flags {flags:#x}")
+    per = {nm: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+           for j, nm in enumerate(names)}
+    ms = statistics.mean(e[0].elapsed_time(e[6]) for e in evs)
+    eb = 2
+    # algorithmic bytes: dispatch reads x once and writes the send buffers;
+    # combine reads the returned rows and writes out
+    disp_bytes = T * H * eb + n * H * eb + n * 16
+    comb_bytes = n * H * eb + T * H * eb + n * 4
+    hbm = peaks["hbm_gbs"]
+    return {"metric": "EP rank step tokens/s (route, dispatch, expert compute, combine; "
+                      "exchange stand-in: device copies)",
+            "value": round(T / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "bf16", "data": DATA,
+            "config": {"workload": "ep_dispatch", "T": T, "H": H, "I": wl.I, "E": E, "K": K,
+                       "ep": [ep, r], "items_sent": n, "items_received": R,
+                       "l2": "flushed before every step, outside the timed events"},
+            "calls_ms": {k: round(v, 4) for k, v in per.items()},
+            "dispatch": {"bytes": disp_bytes, "gbs": round(disp_bytes / per["dispatch"] / 1e6, 1),
+                         "frac_of_hbm": round(disp_bytes / per["dispatch"] / 1e6 / hbm, 4)},
+            "combine": {"bytes": comb_bytes, "gbs": round(comb_bytes / per["combine"] / 1e6, 1),
+                        "frac_of_hbm": round(comb_bytes / per["combine"] / 1e6 / hbm, 4)},
+            "peak_basis": f"{peaks['source']} HBM copy {hbm} GB/s",
+            "clocks": clocks}
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
@@ -506,11 +618,15 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mixtral_prefill")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["ep_dispatch"],
+                    default="mixtral_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload == "ep_dispatch":
+        print(json.dumps(run_ep_dispatch(args, torch.device("cuda", 0))), flush=True)
+        return
     wl = WORKLOADS[args.workload]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

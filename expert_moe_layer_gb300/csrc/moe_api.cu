@@ -360,10 +360,16 @@ EpLayout ep_layout(const moe_config* c, int T) {
   return L;
 }
 
-// The config of the expert compute on received items: one slot per item,
-// no routing, no shared experts, no scaling.
+// The configuration an expert-parallel rank computes its received items with:
+// top_k 1 over its own shard, seen as a layer of E_l experts on one rank, so
+// that the tile-size and split heuristics count every item as local: one
+// slot per item, no routing, no shared experts, no scaling. The align step
+// still maps the global ids with the caller's E and rank.
 moe_config ep_item_config(const moe_config* c) {
   moe_config c1 = *c;
+  c1.num_experts = c->num_experts / c->ep_size;
+  c1.ep_size = 1;
+  c1.ep_rank = 0;
   c1.top_k = 1;
   c1.use_grouped_topk = 0;
   c1.num_expert_group = 0;
@@ -683,7 +689,7 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* sorted_ids = at<int32_t>(ws, L.sorted_ids);
   int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
-  MOE_TRY(cuda_ok(launch_align(recv_ids, R, nullptr, c1.num_experts, El, c1.ep_rank * El,
+  MOE_TRY(cuda_ok(launch_align(recv_ids, R, nullptr, cfg->num_experts, El, cfg->ep_rank * El,
                                kForwardBlock, at<int>(ws, L.hist), counts, offsets, sorted_ids,
                                inv_pos, L.cap, status, st, at<Tile>(ws, L.tiles),
                                at<int>(ws, L.groups), routed_nmax(&c1, R),

@@ -185,3 +185,45 @@ def test_ep_dispatch_flags_bad_ids_and_handles_empty():
     torch.cuda.synchronize()
     assert counts.cpu().numpy().tolist() == [0, 0]
     assert offsets.cpu().numpy().tolist() == [0, 0, 0]
+
+
+def test_ep_expert_compute_full_shard_sampled():
+    """One rank's expert compute at the EP-shard shape (H=2048, I=512, E=256,
+    ep 4, rank 1): 66,049 received items over the 64 local experts, skewed,
+    two experts without items, so segments run to thousands of rows (256-row
+    tiles on CTA pairs) with ragged ends. Each returned row depends on its
+    own item only, so sampled rows are checked against the oracle."""
+    wl = synth.EP_SHARD
+    El, e0, H, I = wl.E_local, wl.ep_rank * wl.E_local, wl.H, wl.I
+    R = 66049
+    rng = np.random.default_rng(7)
+    pop = rng.dirichlet(np.full(El, 0.7))
+    pop[[5, 40]] = 0.0
+    lid = rng.choice(El, size=R, p=pop / pop.sum()).astype(np.int32)
+    ids = lid + e0
+    w = rng.uniform(0.05, 1.0, size=R).astype(np.float32)
+    x = synth.draw(3, synth.X, 0, R, H, wl.std(synth.X), True)
+    w13b = synth.draw_bf16_bits(0, synth.W13, e0 * 2 * I, El * 2 * I, H,
+                                wl.std(synth.W13)).reshape(El, 2 * I, H)
+    w2b = synth.draw_bf16_bits(0, synth.W2, e0 * H, El * H, I,
+                               wl.std(synth.W2)).reshape(El, H, I)
+    cfg = cfg_of(wl)
+    y = torch.zeros(R, H, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(B.ep_expert_compute_workspace_size(cfg, R), dtype=torch.uint8,
+                     device="cuda")
+    B.moe_ep_expert_compute(cfg, R, _dev(x), torch.from_numpy(ids).cuda(),
+                            torch.from_numpy(w).cuda(),
+                            torch.from_numpy(w13b.view(np.int16)).view(torch.bfloat16).cuda(),
+                            torch.from_numpy(w2b.view(np.int16)).view(torch.bfloat16).cuda(),
+                            y, ws)
+    assert B.moe_get_status(ws) == (0, 0)
+    # every local expert's first and last item, plus an even spread
+    rows = set(np.linspace(0, R - 1, 256).astype(np.int64).tolist())
+    for e in range(El):
+        hit = np.nonzero(lid == e)[0]
+        if hit.size:
+            rows.update((int(hit[0]), int(hit[-1])))
+    rows = np.array(sorted(rows))
+    w13h, w2h = synth.BF16Experts(w13b), synth.BF16Experts(w2b)
+    ref = O.ep_expert_compute(x[rows], ids[rows], w[rows], w13h, w2h, e0)
+    assert_close(y.float().cpu().numpy()[rows], ref, "EP-shard expert rows")
