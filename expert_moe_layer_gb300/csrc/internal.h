@@ -34,6 +34,9 @@ struct GemmArgs {
   int b_from_out;              // 1: B row = tile.z instead of tile.y
   void* out;                   // output rows
   long out_ld;                 // output row stride (elements)
+  const int32_t* out_rows = nullptr;  // CTA-pair plain mode: token column p (a segment
+  const float* out_scale = nullptr;   //   position) goes to out row out_rows[p], times
+                                      //   out_scale[p]
   int m_valid;                 // weight rows with an output (router: E)
   unsigned* status;
 };
@@ -139,9 +142,12 @@ cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long 
                                  cudaStream_t st);
 
 // x_perm[r] = x[sorted_ids[r] / K] for rows holding an item.
+// x_perm rows in segment order; with w_perm also the items' weights in that
+// order (w_perm[r] = w_items[sorted_ids[r]]).
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
                           const int32_t* offsets_end, int cap, long n_items, int K, int H,
-                          void* x_perm, cudaStream_t st);
+                          void* x_perm, cudaStream_t st, const float* w_items = nullptr,
+                          float* w_perm = nullptr);
 
 // Both routed GEMMs of a decode-sized batch (32-token tiles, bf16) in one
 // persistent kernel: h = silu(x W_gate^T) * (x W_up^T) per tile, then
@@ -175,6 +181,9 @@ size_t mlp_fused_smem_bytes();
 // destination order (row r = item sorted_ids[r], rows_dev[0] valid rows).
 cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32_t* dest,
                            cudaStream_t st);
+// Zero y rows [i] with inv_pos[i] < 0 (row_bytes a multiple of 16).
+cudaError_t launch_zero_dropped_rows(const int32_t* inv_pos, long n, long row_bytes, void* y,
+                                     cudaStream_t st);
 cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const float* w,
                            const int32_t* sorted_ids, const int32_t* rows_dev, long n_items,
                            int K, int H, void* send_x, int32_t* send_ids, float* send_w,

@@ -259,13 +259,16 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
   }
 }
 
-// x_perm[r] = x[sorted_ids[r] / K], one warp per row, 16-byte vectors.
+// x_perm[r] = x[sorted_ids[r] / K], one warp per row, 16-byte vectors; with
+// w_perm also w_perm[r] = w_items[sorted_ids[r]].
 template <typename TE>
 __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
                                                      const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets_end,
                                                      int cap, long n_items, int K, int H,
-                                                     TE* __restrict__ x_perm) {
+                                                     TE* __restrict__ x_perm,
+                                                     const float* __restrict__ w_items,
+                                                     float* __restrict__ w_perm) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rows = *offsets_end;
@@ -274,6 +277,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
   for (long r = blockIdx.x * 8L + warp; r < rows; r += 8L * gridDim.x) {
     const int id = sorted_ids[r];
     if (id < 0 || id >= n_items) continue;
+    if (w_perm && lane == 0) w_perm[r] = w_items[id];
     const uint4* src = reinterpret_cast<const uint4*>(x + (id / K) * static_cast<long>(H));
     uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
     for (int c = lane; c < H / kVec; c += 32) dst[c] = src[c];
@@ -488,6 +492,19 @@ __global__ void __launch_bounds__(256) ep_dest_kernel(const int32_t* __restrict_
   }
 }
 
+// Rows of items that the align step dropped (inv_pos < 0) are zeroed; the
+// others were written by the scattering GEMM2. Row bytes are a multiple of 16.
+__global__ void __launch_bounds__(256) zero_dropped_rows_kernel(const int32_t* __restrict__ inv_pos,
+                                                                long n, long row_bytes,
+                                                                uint8_t* __restrict__ y) {
+  pdl_enter();
+  for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x) {
+    if (inv_pos[i] >= 0) continue;
+    int4* row = reinterpret_cast<int4*>(y + i * row_bytes);
+    for (long c = 0; c < row_bytes / 16; ++c) row[c] = make_int4(0, 0, 0, 0);
+  }
+}
+
 // Send buffers in destination order: row r holds item sorted_ids[r] (one
 // warp per row, 16-byte vectors for the hidden row).
 template <typename TE>
@@ -568,15 +585,16 @@ cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, in
 
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,
                           const int32_t* offsets_end, int cap, long n_items, int K, int H,
-                          void* x_perm, cudaStream_t st) {
+                          void* x_perm, cudaStream_t st, const float* w_items,
+                          float* w_perm) {
   const int grid = grid_for(cap, 8, 8 * 152);
   if (bf16)
     return launch_pdl(gather_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, st,
                       static_cast<const __nv_bfloat16*>(x), sorted_ids, offsets_end, cap, n_items,
-                      K, H, static_cast<__nv_bfloat16*>(x_perm));
+                      K, H, static_cast<__nv_bfloat16*>(x_perm), w_items, w_perm);
   return launch_pdl(gather_kernel<float>, dim3(grid), dim3(256), 0, st,
                     static_cast<const float*>(x), sorted_ids, offsets_end, cap, n_items, K, H,
-                    static_cast<float*>(x_perm));
+                    static_cast<float*>(x_perm), w_items, w_perm);
 }
 
 cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long part_stride,
@@ -594,6 +612,12 @@ cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32
                            cudaStream_t st) {
   return launch_pdl(ep_dest_kernel, dim3(grid_for(n, 256, 8 * 152)), dim3(256), 0, st, ids, n,
                     E, n_local, dest);
+}
+
+cudaError_t launch_zero_dropped_rows(const int32_t* inv_pos, long n, long row_bytes, void* y,
+                                     cudaStream_t st) {
+  return launch_pdl(zero_dropped_rows_kernel, dim3(grid_for(n, 256, 8 * 152)), dim3(256), 0, st,
+                    inv_pos, n, row_bytes, static_cast<uint8_t*>(y));
 }
 
 cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const float* w,

@@ -5,14 +5,17 @@
 // per byte with 256-token tiles, with the accumulator double-buffered.
 //
 //   plain mode (GEMM2): the pair's 256 rows are 256 consecutive output rows.
-//   SiLU mode (GEMM1):  rank 0 holds 128 gate rows and rank 1 the matching
-//                       128 up rows, so the pair computes gate and up for the
-//                       same 128 intermediate indices. Rank 1's epilogue sends
-//                       its up values to rank 0 over distributed shared memory
-//                       in 16-column chunks. Two slots alternate: st.async
-//                       completes bytes on rank 0's full barrier, and rank 0
-//                       frees a slot with a relaxed arrive. Rank 0 then applies
-//                       SiLU(gate)*up and stores.
+//                       Optionally the epilogue writes token column p to out
+//                       row out_rows[p], times out_scale[p] (the weighted
+//                       un-permute of an EP expert rank).
+//   SiLU mode (GEMM1):  a pair tile covers 128 intermediate indices. Each CTA
+//                       stages 64 gate rows and the 64 up rows of the same
+//                       indices (two 64-row boxes), so its accumulator holds
+//                       gate in lanes 0..63 and up in lanes 64..127. The warps
+//                       on the up lanes pass their values through shared
+//                       memory to the warps on the gate lanes, in 32-column
+//                       chunks over two slots; those apply SiLU(gate)*up and
+//                       store. Both CTAs store half of the pair's outputs.
 //
 // Roles per CTA (persistent, 320 threads), as in moe_gemm_tc:
 //   warp 0      TMA producer of this CTA's rows. The bytes of both CTAs are
@@ -21,9 +24,9 @@
 //               MMA issuer. Its commits arrive on the stage-free and
 //               accumulator-full barriers of both CTAs.
 //   warps 2..9  epilogue on this CTA's 128 accumulator lanes (two warps per
-//               lane quarter: 8 columns each of a 16-column SiLU chunk, or
-//               alternate 16-column blocks in plain mode). Each warp
-//               then arrives once on rank 0's accumulator-free barrier.
+//               lane quarter, each on one 16-column half of a 32-column
+//               chunk). Each warp then arrives once on rank 0's
+//               accumulator-free barrier.
 // Work units (one 256-row pair tile x one token tile) are ordered as in
 // moe_gemm_tc: expert by expert.
 #include <cuda_bf16.h>
@@ -38,9 +41,9 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int kABytes = 128 * 128;
-constexpr int kChunk = 16;                       // columns per SiLU exchange chunk
+constexpr int kChunk = 32;                       // columns per SiLU exchange chunk
 constexpr int kHalfCols = kChunk / 2;            // columns of a chunk per epilogue warp
-constexpr int kXSlotBytes = 128 * kChunk * 4;    // one chunk of up values, fp32
+constexpr int kXSlotBytes = 64 * kChunk * 4;     // one chunk of up values, fp32
 
 template <int MODE, int NMAX>
 struct PairShape {
@@ -48,15 +51,22 @@ struct PairShape {
   static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kXBytes = (MODE == kGemmSiluUp) ? 2 * kXSlotBytes : 0;
-  static constexpr int kStages0 = (216 * 1024 - kXBytes) / kStageBytes;
+  // output staging: per column half, two buffers of 16 token rows of this
+  // CTA's output columns (64 of h in SiLU mode, 128 of y in plain mode)
+  static constexpr int kOutRowBytes = (MODE == kGemmSiluUp) ? 64 * 2 : 128 * 2;
+  static constexpr int kOutBufBytes = 16 * kOutRowBytes;
+  static constexpr int kOutBytes = 2 * 2 * kOutBufBytes;
+  static constexpr int kStages0 = (216 * 1024 - kXBytes - kOutBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kAccCols = NMAX;
   static constexpr int kNAcc = 2;
   static constexpr int kTmemCols = kAccCols * kNAcc <= 256 ? 256 : 512;
   static constexpr int kMaxGroups = 1024;
-  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4;  // + xfull[2], xempty[2]
+  // + xfull[2], xempty[2], ofull[2 halves][2 buffers]
+  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4 + 4;
   static constexpr int kBarBytes = 8 * kNBars + 16 + 4 * (kMaxGroups + 1);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kXBytes + kBarBytes;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + kXBytes + kOutBytes + kBarBytes;
   static_assert(kAccCols * kNAcc <= 512, "TMEM overflow");
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(NMAX % 32 == 0 && NMAX <= 256, "bad NMAX");
@@ -92,7 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
                   const int* __restrict__ group_start, int n_groups, int dense_T, int m_tiles,
                   int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
-                  __nv_bfloat16* __restrict__ out, long out_ld, unsigned* status) {
+                  __nv_bfloat16* __restrict__ out, long out_ld,
+                  const int32_t* __restrict__ out_rows, const float* __restrict__ out_scale,
+                  unsigned* status) {
   using S = PairShape<MODE, NMAX>;
   const uint32_t rank = ptx::cluster_rank();
   const int pair = blockIdx.x >> 1;
@@ -109,14 +121,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = ptx::smem_u32(smem);
   const uint32_t xbase = sbase + S::kStages * S::kStageBytes;  // SiLU exchange slots
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes + S::kXBytes);
+      reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes + S::kXBytes + S::kOutBytes);
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S::kStages;
   const uint32_t tfull0 = empty0 + 8 * S::kStages;
   const uint32_t tempty0 = tfull0 + 8 * S::kNAcc;
   const uint32_t drain = tempty0 + 8 * S::kNAcc;
-  const uint32_t xfull0 = drain + 8;     // on rank 0: rank 1 wrote a chunk
-  const uint32_t xempty0 = xfull0 + 16;  // on rank 1: rank 0 consumed a chunk
+  const uint32_t xfull0 = drain + 8;     // the up warps wrote a chunk
+  const uint32_t xempty0 = xfull0 + 16;  // the gate warps consumed a chunk
+  const uint32_t ofull0 = xempty0 + 16;  // [half][buffer]: a chunk's outputs are staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kNBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
@@ -142,9 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(drain, 1);
     for (int x = 0; x < 2; ++x) {
-      ptx::mbar_init(xfull0 + 8 * x, 1);          // rank 0 arms it with the chunk's bytes
-      ptx::mbar_init(xempty0 + 8 * x, kEpiWarps);
+      ptx::mbar_init(xfull0 + 8 * x, kEpiWarps / 2);   // the four up warps
+      ptx::mbar_init(xempty0 + 8 * x, kEpiWarps / 2);  // the four gate warps
     }
+    // the epilogue warps that stage a half's chunk: two gate warps (SiLU
+    // mode) or the four lane-quarter warps (plain mode)
+    for (int x = 0; x < 4; ++x)
+      ptx::mbar_init(ofull0 + 8 * x, MODE == kGemmSiluUp ? 2 : 4);
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async();
@@ -164,6 +181,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint32_t full_r0 = ptx::map_to_rank(full0, 0);  // rank 0's full barriers
+      // this CTA's weight rows of unit (tile, m) for K block kb: SiLU mode
+      // loads 64 gate and the matching 64 up rows, plain mode 128 rows
+      auto load_a = [&](uint32_t dst, uint32_t fb, int kb, const Tile& tl, int m) {
+        if constexpr (MODE == kGemmSiluUp) {
+          const int g_row = tl.x * a_rows_per_expert + m * 128 + static_cast<int>(rank) * 64;
+          ptx::tma_load_2d_pair(dst, &mapA, fb, kb * 64, g_row);
+          ptx::tma_load_2d_pair(dst + kABytes / 2, &mapA, fb, kb * 64, g_row + a_up_offset);
+        } else {
+          ptx::tma_load_2d_pair(dst, &mapA, fb, kb * 64,
+                                tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128);
+        }
+      };
       // Operand A (weights) of the first kStages stages before the
       // dependency wait; operand B (token rows) only after it.
       int pre = 0;
@@ -171,14 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
         const Tile tl = tile_at(ti);
-        const int a_row =
-            MODE == kGemmSiluUp
-                ? tl.x * a_rows_per_expert + static_cast<int>(rank) * a_up_offset + m * 128
-                : tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < k_blocks && pre < S::kStages; ++kb, ++pre) {
           if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * pre, 2 * S::kStageBytes);
-          ptx::tma_load_2d_pair(sbase + pre * S::kStageBytes, &mapA, full_r0 + 8 * pre,
-                                kb * 64, a_row);
+          load_a(sbase + pre * S::kStageBytes, full_r0 + 8 * pre, kb, tl, m);
         }
       }
       pdl_enter();
@@ -190,10 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(ti);
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
-        const int a_row =
-            MODE == kGemmSiluUp
-                ? tl.x * a_rows_per_expert + static_cast<int>(rank) * a_up_offset + m * 128
-                : tl.x * a_rows_per_expert + m * 256 + static_cast<int>(rank) * 128;
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
@@ -209,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage s again only after rank 0's MMAs freed it, so its bytes
             // never land in an older phase.
             if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * S::kStageBytes);
-            ptx::tma_load_2d_pair(st, &mapA, fb, kb * 64, a_row);
+            load_a(st, fb, kb, tl, m);
           }
           ptx::tma_load_2d_pair(st + kABytes, &mapB, fb, kb * 64, b_row);
         }
@@ -264,13 +284,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Each 16-column piece of the accumulator goes through a staging buffer
+    // in shared memory, so that the global stores are whole 16-byte vectors
+    // along output rows instead of 2-byte values down a column.
     pdl_enter();
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
     const uint32_t tempty_r0 = ptx::map_to_rank(tempty0, 0);
-    const uint32_t xfull_r0 = ptx::map_to_rank(xfull0, 0);
-    const uint32_t xempty_r1 = ptx::map_to_rank(xempty0, 1);
     const int row_l = q * 32 + lane;  // accumulator lane of this thread
+    uint8_t* const stg =
+        smem + S::kStages * S::kStageBytes + S::kXBytes + half * 2 * S::kOutBufBytes;
+    const uint32_t ofull = ofull0 + 16 * half;
     int ai = 0, cc = 0;
     bool ok = true;
     for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
@@ -283,63 +307,119 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + b * S::kAccCols + (static_cast<uint32_t>(q * 32) << 16);
       if constexpr (MODE == kGemmSiluUp) {
-        const int i = m * 128 + row_l;
-        __nv_bfloat16* orow = out + static_cast<long>(tl.z) * out_ld + i;
+        // lanes 0..63: gate, 64..127: up, of the CTA's 64 intermediate indices
+        const bool up_warp = q >= 2;
+        const int r64 = (q & 1) * 32 + lane;
+        const long h_col0 = static_cast<long>(m) * 128 + static_cast<int>(rank) * 64;
         for (int c0 = 0; c0 < tl.w; c0 += kChunk, ++cc) {
           const int slot = cc & 1;
           const uint32_t xph = (cc >> 1) & 1;
           const int col = c0 + kHalfCols * half;
-          // slot layout [column group of 4][row][4]: eight lanes' 16-byte
-          // accesses cover 128 contiguous bytes, free of bank conflicts
-          const uint32_t xg = xbase + slot * kXSlotBytes + (2 * half * 128 + row_l) * 16;
+          // slot layout [column group of 4][row of 64][4 floats]: a warp's
+          // 16-byte accesses cover 512 contiguous bytes, free of bank conflicts
+          float4* xs = reinterpret_cast<float4*>(smem + (xbase - sbase) + slot * kXSlotBytes) +
+                       (kHalfCols / 4) * half * 64 + r64;
           float v[kHalfCols];
-          ptx::tmem_ld8(tb + col, v);
-          if (rank == 1) {
-            // up values -> rank 0's slot, once rank 0 has drained it; the
-            // asynchronous stores complete bytes on rank 0's xfull barrier
-            if (!ptx::mbar_wait_cluster(xempty0 + 8 * slot, xph ^ 1, abort_flag, status)) {
+          ptx::tmem_ld16(tb + col, v);
+          if (up_warp) {
+            if (!ptx::mbar_wait(xempty0 + 8 * slot, xph ^ 1, abort_flag, status)) {
               ok = false;
               break;
             }
-            const uint32_t dst = ptx::map_to_rank(xg, 0);
 #pragma unroll
             for (int j = 0; j < kHalfCols; j += 4)
-              ptx::st_async_v4(dst + (j / 4) * 128 * 16, v[j], v[j + 1], v[j + 2], v[j + 3],
-                               xfull_r0 + 8 * slot);
-          } else {
-            if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(xfull0 + 8 * slot, kXSlotBytes);
-            if (!ptx::mbar_wait_cluster(xfull0 + 8 * slot, xph, abort_flag, status)) {
-              ok = false;
-              break;
-            }
-            const float4* up = reinterpret_cast<const float4*>(smem + (xg - sbase));
-#pragma unroll
-            for (int j = 0; j < kHalfCols; j += 4) {
-              const float4 u4 = up[(j / 4) * 128];
-              const float uj[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-              for (int t = 0; t < 4; ++t) {
-                if (col + j + t < tl.w)
-                  orow[static_cast<long>(col + j + t) * out_ld] =
-                      __float2bfloat16_rn(silu_f(v[j + t]) * uj[t]);
-              }
-            }
+              xs[(j / 4) * 64] = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(xempty_r1 + 8 * slot);
+            if (lane == 0) ptx::mbar_arrive(xfull0 + 8 * slot);
+            continue;
+          }
+          if (!ptx::mbar_wait(xfull0 + 8 * slot, xph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          // staging [16 columns][64 indices] bf16: h of this lane's index
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg + (cc & 1) * S::kOutBufBytes);
+#pragma unroll
+          for (int j = 0; j < kHalfCols; j += 4) {
+            const float4 u4 = xs[(j / 4) * 64];
+            const float uj[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              sb[(j + t) * 64 + r64] = __float2bfloat16_rn(silu_f(v[j + t]) * uj[t]);
+          }
+          __syncwarp();
+          if (lane == 0) {
+            ptx::mbar_arrive(xempty0 + 8 * slot);
+            ptx::mbar_arrive(ofull + 8 * (cc & 1));
+          }
+          if (!ptx::mbar_wait(ofull + 8 * (cc & 1), (cc >> 1) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          // 16 rows of 128 bytes: the two gate warps of this half store 16
+          // bytes per lane, 4 rows per warp per pass
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int t = k * 8 + (r64 >> 3);
+            if (col + t < tl.w) {
+              const uint4 val = *reinterpret_cast<const uint4*>(sb + t * 64 + (r64 & 7) * 8);
+              *reinterpret_cast<uint4*>(out + static_cast<long>(tl.z + col + t) * out_ld +
+                                        h_col0 + (r64 & 7) * 8) = val;
+            }
           }
         }
         if (!ok) break;
       } else {
-        const int row = m * 256 + static_cast<int>(rank) * 128 + row_l;
-        __nv_bfloat16* orow = out + static_cast<long>(tl.z) * out_ld + row;
-        for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
+        // columns c0 = 16*half + 32*it of the tile; per piece, staging
+        // [16 columns][128 rows] bf16, written out as 16 rows of 256 bytes
+        const long y_col0 = static_cast<long>(m) * 256 + static_cast<int>(rank) * 128;
+        const int t_out = row_l >> 4;     // this lane's first output row in a piece
+        const int c8 = (row_l & 15) * 8;  // and its 8 columns of that row
+        // with out_rows: each lane's destination rows and, lane j < 16, the
+        // scales of column j of every piece, fetched once per unit
+        int dst[8][2];
+        float scl[8];
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int c0 = 16 * half + 32 * it;
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int t = c0 + k * 8 + t_out;
+            dst[it][k] = t < tl.w ? (out_rows ? out_rows[tl.z + t] : tl.z + t) : -1;
+          }
+          scl[it] = (out_scale && (lane & 15) + c0 < tl.w) ? out_scale[tl.z + c0 + (lane & 15)]
+                                                           : 1.f;
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int c0 = 16 * half + 32 * it;
+          if (c0 >= tl.w) break;
           float v[16];
           ptx::tmem_ld16(tb + c0, v);
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg + (cc & 1) * S::kOutBufBytes);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * out_ld] = __float2bfloat16_rn(v[j]);
+            const float f = __shfl_sync(0xffffffffu, scl[it], j);
+            sb[j * 128 + row_l] = __float2bfloat16_rn(v[j] * f);
           }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ofull + 8 * (cc & 1));
+          if (!ptx::mbar_wait(ofull + 8 * (cc & 1), (cc >> 1) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (dst[it][k] >= 0) {
+              const uint4 val =
+                  *reinterpret_cast<const uint4*>(sb + (k * 8 + t_out) * 128 + c8);
+              *reinterpret_cast<uint4*>(out + static_cast<long>(dst[it][k]) * out_ld + y_col0 +
+                                        c8) = val;
+            }
+          }
+          ++cc;
         }
+        if (!ok) break;
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -384,7 +464,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
   return counted(cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
                             a.dense_T, a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
                             a.b_from_out, static_cast<__nv_bfloat16*>(a.out), a.out_ld,
-                            a.status));
+                            a.out_rows, a.out_scale, a.status));
 }
 
 }  // namespace
@@ -392,6 +472,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
 cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num_sms,
                              cudaStream_t st) {
   if ((a.tiles == nullptr && a.dense_T <= 0) || a.k_split != 1) return cudaErrorInvalidValue;
+  if (a.out_rows && mode != kGemmPlain) return cudaErrorInvalidValue;
   if (nmax == 256 && mode == kGemmPlain)
     return launch_pair_variant<kGemmPlain, 256>(a, num_sms, st);
   if (nmax == 256 && mode == kGemmSiluUp)

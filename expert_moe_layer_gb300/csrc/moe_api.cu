@@ -217,9 +217,12 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              int m_tiles, int rows_per_slab, int up_off, int b_from_out, void* out, long out_ld,
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
              long split_stride = 0, int dense_T = 0, bool pair = false,
-             float* part = nullptr) {
+             float* part = nullptr, const int32_t* out_rows = nullptr,
+             const float* out_scale = nullptr) {
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, dt, a_rows, Kdim, 128)) return MOE_ERR_CUDA;
+  // CTA pairs in SiLU mode stage 64 gate and 64 up rows per CTA: 64-row boxes
+  const int a_box = (pair && mode == kGemmSiluUp) ? 64 : 128;
+  if (!make_map(&ma, A, dt, a_rows, Kdim, a_box)) return MOE_ERR_CUDA;
   if (!make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax)) return MOE_ERR_CUDA;
   GemmArgs g;
   g.mapA = &ma;
@@ -238,6 +241,8 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.b_from_out = b_from_out;
   g.out = out;
   g.out_ld = out_ld;
+  g.out_rows = out_rows;
+  g.out_scale = out_scale;
   g.m_valid = m_valid;
   g.status = status;
   const int sms = sm_count();
@@ -436,7 +441,9 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
            const int32_t* counts, const int32_t* offsets, int cap, const void* w13,
            const void* w2, void* y_perm, Tile* tiles, int* groups, const SyncRegion& sync,
            void* x_perm, void* h_perm, float* part1, unsigned* status, cudaStream_t st,
-           void* const* ev = nullptr, bool tiles_ready = false) {
+           void* const* ev = nullptr, bool tiles_ready = false,
+           const int32_t* y_rows = nullptr, const float* w_items = nullptr,
+           float* w_perm = nullptr) {
   const int El = n_local(c), H = c->hidden_size, I = c->intermediate_size, K = c->top_k;
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
@@ -447,7 +454,8 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
                                        status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
-                                n_items, K, H, x_perm, st)));
+                                n_items, K, H, x_perm, st, y_rows ? w_items : nullptr,
+                                y_rows ? w_perm : nullptr)));
   if (ev) MOE_TRY(record_event(ev[0], st));
   if (fused) {
     const int ks = gemm1_ksplit(c, T);
@@ -496,9 +504,12 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
                      1, 0, 0, pairs));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
+  // with y_rows (CTA pairs only) GEMM2 writes segment position p to row
+  // y_rows[p] of y_perm, times the item weight w_perm[p] (from the gather)
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
                    tiles, groups, El, H / (pairs ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
-                   1, 0, 0, pairs));
+                   1, 0, 0, pairs, nullptr, pairs ? y_rows : nullptr,
+                   pairs && y_rows ? w_perm : nullptr));
   return MOE_OK;
 }
 
@@ -666,7 +677,8 @@ int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* 
 size_t moe_ep_expert_compute_workspace_size(const moe_config* cfg, int R) {
   if (validate_cfg(cfg) != MOE_OK || validate_T(R) != MOE_OK) return 0;
   const moe_config c1 = ep_item_config(cfg);
-  return fwd_layout(&c1, R).total;
+  // the forward's layout, then the items' weights in segment order
+  return fwd_layout(&c1, R).total + rup(4 * static_cast<size_t>(R));
 }
 
 int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
@@ -680,7 +692,8 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
     return MOE_ERR_INVALID_ARG;
   const moe_config c1 = ep_item_config(cfg);
   const FwdLayout L = fwd_layout(&c1, R);
-  if (!ws || ws_bytes < L.total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < moe_ep_expert_compute_workspace_size(cfg, R) || !aligned16(ws))
+    return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned* status = at<unsigned>(ws, L.status);
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.sync.bytes, st)));
@@ -694,6 +707,17 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
                                inv_pos, L.cap, status, st, at<Tile>(ws, L.tiles),
                                at<int>(ws, L.groups), routed_nmax(&c1, R),
                                static_cast<int>(max_routed_tiles(&c1, R)))));
+  if (gemms_on_pairs(&c1, R)) {
+    // GEMM2 writes each item's row straight to y, weighted; dropped items
+    // (ids outside the shard) get zero rows
+    MOE_TRY(do_mlp(&c1, R, recv_x, sorted_ids, counts, offsets, L.cap, w13, w2, y,
+                   at<Tile>(ws, L.tiles), at<int>(ws, L.groups), L.sync, at<void>(ws, L.x_perm),
+                   at<void>(ws, L.h_perm), at<float>(ws, L.part1), status, st, nullptr, true,
+                   sorted_ids, recv_w, at<float>(ws, L.total)));
+    return cuda_ok(launch_zero_dropped_rows(inv_pos, R,
+                                            static_cast<long>(c1.hidden_size) * ebytes(c1.act_dtype),
+                                            y, st));
+  }
   MOE_TRY(do_mlp(&c1, R, recv_x, sorted_ids, counts, offsets, L.cap, w13, w2,
                  at<void>(ws, L.y_perm), at<Tile>(ws, L.tiles), at<int>(ws, L.groups), L.sync,
                  at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,

@@ -191,8 +191,9 @@ def test_ep_expert_compute_full_shard_sampled():
     """One rank's expert compute at the EP-shard shape (H=2048, I=512, E=256,
     ep 4, rank 1): 66,049 received items over the 64 local experts, skewed,
     two experts without items, so segments run to thousands of rows (256-row
-    tiles on CTA pairs) with ragged ends. Each returned row depends on its
-    own item only, so sampled rows are checked against the oracle."""
+    tiles on CTA pairs) with ragged ends, and 40 items whose expert belongs to
+    another rank (their rows must come back zero). Each returned row depends
+    on its own item only, so sampled rows are checked against the oracle."""
     wl = synth.EP_SHARD
     El, e0, H, I = wl.E_local, wl.ep_rank * wl.E_local, wl.H, wl.I
     R = 66049
@@ -201,6 +202,9 @@ def test_ep_expert_compute_full_shard_sampled():
     pop[[5, 40]] = 0.0
     lid = rng.choice(El, size=R, p=pop / pop.sum()).astype(np.int32)
     ids = lid + e0
+    foreign = rng.choice(R, size=40, replace=False)
+    ids[foreign] = rng.choice(np.r_[0:e0, e0 + El:wl.E], size=40)
+    lid[foreign] = -1
     w = rng.uniform(0.05, 1.0, size=R).astype(np.float32)
     x = synth.draw(3, synth.X, 0, R, H, wl.std(synth.X), True)
     w13b = synth.draw_bf16_bits(0, synth.W13, e0 * 2 * I, El * 2 * I, H,
@@ -208,7 +212,7 @@ def test_ep_expert_compute_full_shard_sampled():
     w2b = synth.draw_bf16_bits(0, synth.W2, e0 * H, El * H, I,
                                wl.std(synth.W2)).reshape(El, H, I)
     cfg = cfg_of(wl)
-    y = torch.zeros(R, H, dtype=torch.bfloat16, device="cuda")
+    y = torch.full((R, H), 7.0, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(B.ep_expert_compute_workspace_size(cfg, R), dtype=torch.uint8,
                      device="cuda")
     B.moe_ep_expert_compute(cfg, R, _dev(x), torch.from_numpy(ids).cuda(),
@@ -223,7 +227,9 @@ def test_ep_expert_compute_full_shard_sampled():
         hit = np.nonzero(lid == e)[0]
         if hit.size:
             rows.update((int(hit[0]), int(hit[-1])))
-    rows = np.array(sorted(rows))
+    rows = np.array(sorted(rows.difference(foreign.tolist())))
     w13h, w2h = synth.BF16Experts(w13b), synth.BF16Experts(w2b)
     ref = O.ep_expert_compute(x[rows], ids[rows], w[rows], w13h, w2h, e0)
-    assert_close(y.float().cpu().numpy()[rows], ref, "EP-shard expert rows")
+    yh = y.float().cpu().numpy()
+    assert_close(yh[rows], ref, "EP-shard expert rows")
+    assert not yh[foreign].any(), "rows of other ranks' items must be zero"
