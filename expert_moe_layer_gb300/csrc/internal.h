@@ -56,9 +56,6 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a,
 cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num_sms,
                              cudaStream_t st);
 
-// Shared-memory bytes a GEMM variant needs (for validation/tests).
-size_t gemm_smem_bytes(GemmMode mode, int nmax);
-
 // Router logits on CUDA cores: logits[t,e] = x[t].Wg[e] (fp32 accumulation).
 // For E <= 32 the sum over H is split into slices of kRouterSplitCols
 // columns, each written to its own partial slab (T*E floats apart); larger E

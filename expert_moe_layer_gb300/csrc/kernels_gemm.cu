@@ -15,7 +15,9 @@
 //               the "up" rows shares the same B stage
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator (two warps per 32-lane
 //               TMEM quarter, alternating 16-column chunks), SiLU(gate)*up or
-//               plain, store to global
+//               plain, store to global. bf16 outputs go through a staging
+//               buffer in shared memory per 16-column chunk, so the stores
+//               are 16-byte vectors along output rows.
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
 // overlaps the main loop of the next.
 //
@@ -38,12 +40,17 @@ constexpr int kThreads = 320;       // 10 warps
 constexpr int kEpiThreads = 256;    // warps 2..9
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, bool STG>
 struct GemmShape {
   static constexpr int kNA = (MODE == kGemmSiluUp) ? 2 : 1;  // weight boxes per stage
   static constexpr int kBBytes = NMAX * 128;
   static constexpr int kStageBytes = kNA * kABytes + kBBytes;
-  static constexpr int kStages0 = (200 * 1024) / kStageBytes;
+  // output staging (bf16 outputs): per column half, two buffers of 16 token
+  // rows x 128 output columns
+  static constexpr int kOutBufBytes = 16 * 128 * 2;
+  static constexpr int kOutBytes = STG ? 2 * 2 * kOutBufBytes : 0;
+  static constexpr int kStages0 =
+      STG ? (216 * 1024 - kOutBytes) / kStageBytes : (200 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kAccCols = kNA * NMAX;            // fp32 columns per buffer
   static constexpr int kNAcc = kAccCols <= 256 ? 2 : 1;  // TMEM accumulator buffers
@@ -54,8 +61,9 @@ struct GemmShape {
                                    : kTmemNeed <= 256 ? 256
                                                       : 512;
   static constexpr int kMaxGroups = 1024;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kNAcc + 1) + 16 + 4 * (kMaxGroups + 1);
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
+  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4;  // + ofull[2 halves][2 bufs]
+  static constexpr int kBarBytes = 8 * kNBars + 16 + 4 * (kMaxGroups + 1);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes;
   static_assert(kTmemNeed <= 512, "TMEM overflow");
   static_assert(kStages >= 2, "need at least two stages");
   static_assert(NMAX % 16 == 0 && NMAX <= 256, "bad NMAX");
@@ -97,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
                 float* __restrict__ part, int m_valid, unsigned* status) {
-  using S = GemmShape<MODE, NMAX>;
+  constexpr bool kStaged = sizeof(TOut) == 2;
+  using S = GemmShape<MODE, NMAX, kStaged>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
 
@@ -116,13 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes + S::kOutBytes);
   const uint32_t full0 = ptx::smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * S::kStages;
   const uint32_t tfull0 = empty0 + 8 * S::kStages;
   const uint32_t tempty0 = tfull0 + 8 * S::kNAcc;
   const uint32_t drain = tempty0 + 8 * S::kNAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S::kStages + 2 * S::kNAcc + 1);
+  const uint32_t ofull0 = drain + 8;  // [half][buffer]: a chunk's outputs are staged
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kNBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
   for (int i = threadIdx.x; i <= n_groups; i += kThreads)
@@ -146,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty0 + 8 * b, kEpiThreads);
     }
     ptx::mbar_init(drain, 1);
+    for (int x = 0; x < 4; ++x) ptx::mbar_init(ofull0 + 8 * x, 4);  // the half's 4 warps
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async();
@@ -282,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_enter();
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // two warps per quarter split the columns
-    int ai = 0;
+    int ai = 0, cc = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
       int ti, m;
       const int ks = u % k_split;
@@ -324,6 +335,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(tempty0 + 8 * b);
         continue;
       }
+      if constexpr (kStaged) {
+        // staging [16 columns][128 rows] bf16 per chunk, written out as 16
+        // rows of 256 bytes, 16 bytes per lane
+        uint8_t* const stg = smem + S::kStages * S::kStageBytes + half * 2 * S::kOutBufBytes;
+        const uint32_t ofull = ofull0 + 16 * half;
+        const int row_l = q * 32 + lane;
+        const int t_out = row_l >> 4, c8 = (row_l & 15) * 8;
+        const bool cols_ok = m * 128 + c8 < m_valid;
+        bool ok = true;
+        for (int c0 = 16 * half; c0 < tl.w; c0 += 32, ++cc) {
+          float v[16];
+          if constexpr (MODE == kGemmSiluUp) {
+            float w[16];
+            ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = silu_f(v[j]) * w[j];
+          } else {
+            ptx::tmem_ld16(tb + c0, v);
+          }
+          __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stg + (cc & 1) * S::kOutBufBytes);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sb[j * 128 + row_l] = __float2bfloat16_rn(v[j]);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ofull + 8 * (cc & 1));
+          if (!ptx::mbar_wait(ofull + 8 * (cc & 1), (cc >> 1) & 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int t = k * 8 + t_out;
+            if (c0 + t < tl.w && cols_ok) {
+              const uint4 val = *reinterpret_cast<const uint4*>(sb + t * 128 + c8);
+              *reinterpret_cast<uint4*>(out + static_cast<long>(tl.z + c0 + t) * out_ld +
+                                        m * 128 + c8) = val;
+            }
+          }
+        }
+        if (!ok) break;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(tempty0 + 8 * b);
+        continue;
+      }
       TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
       for (int c0 = 16 * half; c0 < tl.w; c0 += 32) {
         float v[16];
@@ -357,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE, bool TF32, typename TOut, int NMAX>
 cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
-  using S = GemmShape<MODE, NMAX>;
+  using S = GemmShape<MODE, NMAX, sizeof(TOut) == 2>;
   auto kern = moe_gemm_tc<MODE, TF32, TOut, NMAX>;
   static bool configured = false;  // per process; attribute is per function
   if (!configured) {
@@ -373,16 +427,6 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
 }
 
 }  // namespace
-
-size_t gemm_smem_bytes(GemmMode mode, int nmax) {
-  if (mode == kGemmSiluUp)
-    return nmax == 256   ? GemmShape<0, 256>::kSmemBytes
-           : nmax == 128 ? GemmShape<0, 128>::kSmemBytes
-                         : GemmShape<0, 32>::kSmemBytes;
-  return nmax == 256   ? GemmShape<1, 256>::kSmemBytes
-         : nmax == 128 ? GemmShape<1, 128>::kSmemBytes
-                       : GemmShape<1, 32>::kSmemBytes;
-}
 
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
