@@ -89,12 +89,91 @@ __device__ __forceinline__ void write_tile_table(int e, int E_l, int c, int off,
 constexpr int kSmallItems = 32 * 256;
 constexpr int kSmallExperts = 256;
 
+// Up to kTinyItems items: one CTA of 1024 threads, G = 1024 / E_l threads per
+// local expert. The local ids sit in shared memory; thread (g, e) counts expert e
+// in the g-th range of items, the counts become padded offsets (one scan),
+// and the same thread writes its range's items of expert e in item order
+// (a stable counting sort without per-warp histograms). Each thread walks
+// n/G items twice, so this only pays below a few dozen items (decode
+// batches of a token or a few), where it skips the per-warp passes.
+constexpr int kTinyItems = 64;
+
+__device__ __forceinline__ void align_tiny_block(
+    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
+    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+    int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
+    int* __restrict__ group_start, int nmax, int max_tiles, int* smem, int* warp_sums) {
+  int* le_s = smem;            // [kTinyItems] local expert of each item
+  int* part = smem + 1024;     // [G][E_l] counts, then bases
+  int* off_s = smem + 2048;    // [E_l] first row of each expert
+  const int tid = threadIdx.x;
+  for (int r = tid; r < cap; r += 1024) sorted_ids[r] = n_items;
+  if (tid < n_items) le_s[tid] = local_expert(ids[tid], emap, E, E_l, ep_start, status);
+  __syncthreads();
+  const int G = 1024 / E_l;  // E_l <= 256: at least 4
+  const int g = tid / E_l, e = tid - g * E_l;
+  const bool active = g < G;
+  const int R = (n_items + G - 1) / G;
+  const int i0 = min(n_items, g * R), i1 = min(n_items, i0 + R);
+  if (active) {
+    int c = 0;
+    for (int i = i0; i < i1; ++i) c += le_s[i] == e;
+    part[tid] = c;
+  }
+  __syncthreads();
+  int c = 0;
+  if (tid < E_l) {
+    for (int gg = 0; gg < G; ++gg) {
+      const int v = part[gg * E_l + tid];
+      part[gg * E_l + tid] = c;
+      c += v;
+    }
+  }
+  const int padded = tid < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(padded, warp_sums, total);
+  if (tid < E_l) {
+    counts[tid] = c;
+    offsets[tid] = start;
+    off_s[tid] = start;
+  }
+  if (tid == 0) {
+    offsets[E_l] = total;
+    if (total > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+  }
+  if (tiles)
+    write_tile_table(tid, E_l, tid < E_l ? c : 0, start, nmax, tiles, group_start, max_tiles,
+                     warp_sums, status);
+  __syncthreads();
+  if (active) {
+    int pos = off_s[e] + part[tid];
+    for (int i = i0; i < i1; ++i) {
+      if (le_s[i] != e) continue;
+      if (pos < cap) {
+        sorted_ids[pos] = i;
+        inv_pos[i] = pos;
+      } else {
+        if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+        inv_pos[i] = -1;
+      }
+      ++pos;
+    }
+  }
+  if (tid < n_items && le_s[tid] < 0) inv_pos[tid] = -1;
+}
+
 __device__ __forceinline__ void align_small_block(
     const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
     int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles, int* hist, int* warp_sums) {
+  if (n_items <= kTinyItems) {
+    align_tiny_block(ids, n_items, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
+                     inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ipw = ((n_items + 31) / 32 + 31) / 32 * 32;  // items per warp, multiple of 32
   for (int r = threadIdx.x; r < cap; r += 1024) sorted_ids[r] = n_items;

@@ -438,15 +438,18 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(
                    ids + static_cast<long>(t) * K, wout + static_cast<long>(t) * K);
   }
 
-  // last token block: alignment of all T*K items
+  // last token block: alignment of all T*K items (a single token block is
+  // its own last one)
   __syncthreads();
-  int* block_ticket = tickets + gridDim.y;
-  if (threadIdx.x == 0) {
-    is_last = ticket_acq_rel(block_ticket) == static_cast<int>(gridDim.y) - 1;
-    if (is_last) *block_ticket = 0;
+  if (gridDim.y > 1) {
+    int* block_ticket = tickets + gridDim.y;
+    if (threadIdx.x == 0) {
+      is_last = ticket_acq_rel(block_ticket) == static_cast<int>(gridDim.y) - 1;
+      if (is_last) *block_ticket = 0;
+    }
+    __syncthreads();
+    if (!is_last) return;
   }
-  __syncthreads();
-  if (!is_last) return;
   align_small_block(ids, T * K, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
                     inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
 }

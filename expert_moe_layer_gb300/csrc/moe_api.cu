@@ -105,7 +105,9 @@ int router_ksplit(const moe_config* c, int T) {
 }
 
 // Decode batches leave few GEMM1 units (token tiles x I/128): split K = H
-// so that ~2 units per SM exist. Estimate tiles as one per touched expert.
+// into as many ranges as still fit the units into one wave on the SMs (a
+// second wave adds a full DRAM round trip and partial-sum chain). Estimate
+// tiles as one per touched expert.
 int gemm1_ksplit(const moe_config* c, int T) {
   const long local_items = static_cast<long>(T) * c->top_k / c->ep_size;
   long tiles = local_items < n_local(c) ? local_items : n_local(c);
@@ -113,7 +115,8 @@ int gemm1_ksplit(const moe_config* c, int T) {
   const long units = tiles * (c->intermediate_size / 128);
   if (units >= 152) return 1;
   const int k_blocks = c->hidden_size * (c->act_dtype == MOE_BF16 ? 2 : 4) / 128;
-  long ks = (304 + units - 1) / units;
+  long ks = 152 / units;
+  if (ks < 1) ks = 1;
   if (ks > 8) ks = 8;
   if (ks > k_blocks) ks = k_blocks;
   const long kb_per = (k_blocks + ks - 1) / ks;

@@ -162,8 +162,11 @@ def _align(c, ids_np, block, emap=None, cap=None):
 
 
 @pytest.mark.parametrize("block", [1, 7, 16, 64, 128])
-@pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1"])
+@pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1", "single_token", "wide_router"])
 def test_align_entry_point(name, block):
+    """Per-warp counting sort (ragged_prefill, ep_rank1) and the small-batch
+    path of up to 64 items (single_token: 4 items; wide_router: 48 items of an
+    EP shard with 160 local experts)."""
     c = case(name)
     counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, block)
     assert st == (0, 0)
