@@ -37,6 +37,8 @@ struct GemmArgs {
   const int32_t* out_rows = nullptr;  // CTA-pair plain mode: token column p (a segment
   const float* out_scale = nullptr;   //   position) goes to out row out_rows[p], times
                                       //   out_scale[p]
+  int b_cap = 0;                      // CTA-pair: rows of the position space (tile entries
+                                      //   past it are skipped and flagged); 0: unchecked
   int m_valid;                 // weight rows with an output (router: E)
   unsigned* status;
 };

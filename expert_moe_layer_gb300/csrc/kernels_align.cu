@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256) align_count_kernel(
     int E_l, int ep_start, int* __restrict__ hist, int n_warps, int32_t* __restrict__ sorted_ids,
     int cap, unsigned* status) {
   pdl_enter();
+  ids = fresh(ids);
   extern __shared__ int cnt[];  // [kWarpsPerBlock][E_l]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (long r = blockIdx.x * 256L + threadIdx.x; r < cap; r += 256L * gridDim.x)
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
                                                           int* __restrict__ group_start,
                                                           int nmax, int max_tiles) {
   pdl_enter();
+  hist = fresh(hist);
   __shared__ int warp_sums[32];
   __shared__ int part[1024];   // per-(group, expert) sums, then their exclusive prefixes
   __shared__ int sbase[1024];  // each expert's first row
@@ -147,6 +149,8 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
     unsigned* status) {
   pdl_enter();
+  ids = fresh(ids);
+  hist = fresh(hist);
   extern __shared__ int run[];  // [kWarpsPerBlock][E_l]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kWarpsPerBlock + warp;
@@ -197,6 +201,7 @@ __global__ void __launch_bounds__(1024) align_small_kernel(
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles) {
   pdl_enter();
+  ids = fresh(ids);
   __shared__ int hist[32 * kSmallExperts];
   __shared__ int warp_sums[32];
   align_small_block(ids, n_items, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
@@ -210,6 +215,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
                                                            int* __restrict__ group_start,
                                                            int max_tiles, unsigned* status) {
   pdl_enter();
+  counts = fresh(counts);
+  offsets = fresh(offsets);
   __shared__ int warp_sums[32];
   const int e = threadIdx.x;
   int n = 0, c = 0, off = 0;
@@ -270,6 +277,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
                                                      const float* __restrict__ w_items,
                                                      float* __restrict__ w_perm) {
   pdl_enter();
+  sorted_ids = fresh(sorted_ids);
+  offsets_end = fresh(offsets_end);
+  w_items = fresh(w_items);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rows = *offsets_end;
   if (rows > cap) rows = cap;
@@ -321,6 +331,8 @@ __global__ void __launch_bounds__(256) silu_finalize_kernel(const float* __restr
                                                             const int32_t* __restrict__ rows_dev,
                                                             int cap, int I, TE* __restrict__ h) {
   pdl_enter();
+  part = fresh(part);
+  rows_dev = fresh(rows_dev);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rows = *rows_dev;
   if (rows > cap) rows = cap;
@@ -399,6 +411,10 @@ __global__ void __launch_bounds__(256, KB > 4 ? 3 : 4) combine_kernel(
     unsigned* status) {
   constexpr int U = KB >= 4 ? 1 : 4 / KB;  // chunks per warp step
   pdl_enter();
+  y_perm = fresh(y_perm);
+  inv_pos = fresh(inv_pos);
+  topk_w = fresh(topk_w);
+  shared = fresh(shared);
   __shared__ int s_pos[kCombTok][32];
   __shared__ float s_w[kCombTok][32];
   __shared__ int s_n[kCombTok];
@@ -486,6 +502,7 @@ __global__ void __launch_bounds__(256) ep_dest_kernel(const int32_t* __restrict_
                                                       long n, int E, int n_local,
                                                       int32_t* __restrict__ dest) {
   pdl_enter();
+  ids = fresh(ids);
   for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x) {
     const int id = ids[i];
     dest[i] = (id >= 0 && id < E) ? id / n_local : -1;
@@ -498,6 +515,7 @@ __global__ void __launch_bounds__(256) zero_dropped_rows_kernel(const int32_t* _
                                                                 long n, long row_bytes,
                                                                 uint8_t* __restrict__ y) {
   pdl_enter();
+  inv_pos = fresh(inv_pos);
   for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x) {
     if (inv_pos[i] >= 0) continue;
     int4* row = reinterpret_cast<int4*>(y + i * row_bytes);
@@ -514,6 +532,11 @@ __global__ void __launch_bounds__(256) ep_pack_kernel(
     int K, int H, TE* __restrict__ send_x, int32_t* __restrict__ send_ids,
     float* __restrict__ send_w, int32_t* __restrict__ send_tok) {
   pdl_enter();
+  x = fresh(x);
+  ids = fresh(ids);
+  w = fresh(w);
+  sorted_ids = fresh(sorted_ids);
+  rows_dev = fresh(rows_dev);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long rows = *rows_dev;
   if (rows > n_items) rows = n_items;

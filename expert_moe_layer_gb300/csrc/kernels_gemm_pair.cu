@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
                   __nv_bfloat16* __restrict__ out, long out_ld,
                   const int32_t* __restrict__ out_rows, const float* __restrict__ out_scale,
-                  unsigned* status) {
+                  int b_cap, unsigned* status) {
   using S = PairShape<MODE, NMAX>;
   const uint32_t rank = ptx::cluster_rank();
   const int pair = blockIdx.x >> 1;
@@ -139,6 +139,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tiles) return tiles[ti];
     const int sl = ti / dense_per, t0 = (ti - sl * dense_per) * NMAX;
     return make_int4(sl, t0, sl * dense_T + t0, min(NMAX, dense_T - t0));
+  };
+  // A tile table entry every role can act on: a valid width and, when the
+  // row count b_cap of the position space is given, rows inside it. Every
+  // role skips the same entries (and flags them), so their pipelines stay
+  // in step.
+  auto tile_ok = [&](const Tile& tl) {
+    return tl.w >= 1 && tl.w <= NMAX && tl.x >= 0 && tl.y >= 0 && tl.z >= 0 &&
+           (b_cap <= 0 || (tl.y <= b_cap - tl.w && tl.z <= b_cap - tl.w));
   };
 
   const int warp = threadIdx.x >> 5;
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
         const Tile tl = tile_at(ti);
+        if (!tile_ok(tl)) continue;
         for (int kb = 0; kb < k_blocks && pre < S::kStages; ++kb, ++pre) {
           if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * pre, 2 * S::kStageBytes);
           load_a(sbase + pre * S::kStageBytes, full_r0 + 8 * pre, kb, tl, m);
@@ -212,6 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
         const Tile tl = tile_at(ti);
+        if (!tile_ok(tl)) {
+          if (rank == 0) atomicOr(status, MOE_DEV_BAD_SEGMENT);
+          continue;
+        }
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
         for (int kb = 0; kb < k_blocks; ++kb, ++it) {
@@ -244,10 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && rank == 0) {
       int it = 0, ai = 0;
       bool ok = true;
-      for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
+      for (int u = pair; u < total && ok; u += n_pairs) {
         int ti, m;
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
         const Tile tl = tile_at(ti);
+        if (!tile_ok(tl)) continue;
         const int n_mma = (tl.w + 31) & ~31;
         const uint32_t idesc = ptx::idesc_make(1u, 256, n_mma);
         const int b = ai % S::kNAcc;
@@ -276,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ptx::tc_commit_pair(tfull0 + 8 * b);
+        ++ai;
       }
       if (!ok) {
         ptx::tc_commit_pair(drain);
@@ -297,10 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ofull = ofull0 + 16 * half;
     int ai = 0, cc = 0;
     bool ok = true;
-    for (int u = pair; u < total && ok; u += n_pairs, ++ai) {
+    for (int u = pair; u < total && ok; u += n_pairs) {
       int ti, m;
       decode_unit(u, gstart, n_groups, m_tiles, ti, m);
       const Tile tl = tile_at(ti);
+      if (!tile_ok(tl)) continue;
       const int b = ai % S::kNAcc;
       const uint32_t aph = (ai / S::kNAcc) & 1;
       if (!ptx::mbar_wait_cluster(tfull0 + 8 * b, aph, abort_flag, status)) break;
@@ -424,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive_cluster(tempty_r0 + 8 * b);
+      ++ai;
     }
   }
 
@@ -464,7 +481,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
   return counted(cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
                             a.dense_T, a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
                             a.b_from_out, static_cast<__nv_bfloat16*>(a.out), a.out_ld,
-                            a.out_rows, a.out_scale, a.status));
+                            a.out_rows, a.out_scale, a.b_cap, a.status));
 }
 
 }  // namespace

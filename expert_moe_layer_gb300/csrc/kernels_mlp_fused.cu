@@ -433,8 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) old = add_acq_rel(split_cnt + (ui.ti * m1 + ui.m) * kEpiWarps + blk, 1);
       old = __shfl_sync(0xffffffffu, old, 0);
       if (old != ks1 - 1) continue;
-      // every slab's value is loaded before the sum, which runs in slab order
-      const float* qrow = part + static_cast<long>(tl.z) * 2 * I + row;
+      // every slab's value is loaded before the sum, which runs in slab order;
+      // the other slabs were written by other CTAs before their counter add
+      const float* qrow = fresh(part) + static_cast<long>(tl.z) * 2 * I + row;
       for (int j = 0; j < 16 && c0 + j < tl.w; ++j) {
         const float* pc = qrow + static_cast<long>(c0 + j) * 2 * I;
         float gs[kMaxSplit], us[kMaxSplit];

@@ -79,12 +79,14 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
   }
 }
 
-// Split-H variant for small E (<= 32). A CTA covers 64 tokens (8 per warp),
-// one kRouterSplitCols-wide slice of H and up to 8 experts (blockIdx.z picks
-// the expert octet). Each lane keeps its 8 columns of those experts' router
-// rows in registers, so the router weights are read once per warp and every
-// token row once per octet. The slice sums go to partial slab blockIdx.y; the
-// top-k kernel adds the slabs in slab order.
+// Split-H variant for small E (<= 32). A CTA covers one kRouterSplitCols-wide
+// slice of H (blockIdx.x), 64 tokens (blockIdx.y; 8 per warp) and up to 8
+// experts (blockIdx.z picks the expert octet). Each lane keeps its 8 columns
+// of those experts' router rows in registers, so the router weights are read
+// once per warp and every token row once per octet. The slice index varies
+// fastest, so CTAs launched together read whole token rows. The slice sums
+// go to partial slab blockIdx.x; the top-k kernel adds the slabs in slab
+// order.
 constexpr int kSplitTokWarp = 8;
 
 // Sum acc[0..7] over the 32 lanes; lane l ends up with the total of entry
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __re
                                                                   int T, int E, int H) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kRouterSplitCols + lane * 8;
+  const int h = blockIdx.x * kRouterSplitCols + lane * 8;
   const bool hv = h < H;  // H is a multiple of 128
   const int e0 = blockIdx.z * 8;
   float w[8][8];
@@ -133,8 +135,8 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __re
       for (int i = 0; i < 8; ++i) w[j][i] = 0.f;
     }
   }
-  float* slab = logits + static_cast<long>(blockIdx.y) * T * E;
-  const long tw = (static_cast<long>(blockIdx.x) * 8 + warp) * kSplitTokWarp;
+  float* slab = logits + static_cast<long>(blockIdx.x) * T * E;
+  const long tw = (static_cast<long>(blockIdx.y) * 8 + warp) * kSplitTokWarp;
   const int ex = (lane >> 2) & 7;
 #pragma unroll
   for (int a = 0; a < kSplitTokWarp; a += 4) {
@@ -176,6 +178,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
                                                    int32_t* __restrict__ ids,
                                                    float* __restrict__ wout) {
   pdl_enter();
+  logits = fresh(logits);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -211,6 +214,7 @@ __global__ void __launch_bounds__(256) topk_cta_kernel(const float* __restrict__
                                                        int32_t* __restrict__ ids,
                                                        float* __restrict__ wout) {
   pdl_enter();
+  logits = fresh(logits);
   __shared__ float sl[32 * VPL];
   const long t = blockIdx.x;
   const float* row = logits + t * E;
@@ -423,6 +427,7 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(
   }
   __syncthreads();
   if (!is_last) return;
+  logits = fresh(logits);  // written by the other CTAs of this token block
   if (warp < nt) {
     const int t = tb0 + warp;
     float p[VPL], sb[VPL];
@@ -463,8 +468,8 @@ cudaError_t logits_launch(const void* x, const void* wg, float* logits, int T, i
   const TW* wp = static_cast<const TW*>(wg);
   if (E <= 32)
     return launch_pdl(router_logits_split_kernel<TX, TW>,
-                      dim3((T + 8 * kSplitTokWarp - 1) / (8 * kSplitTokWarp),
-                           router_split_slabs(H), (E + 7) / 8),
+                      dim3(router_split_slabs(H), (T + 8 * kSplitTokWarp - 1) / (8 * kSplitTokWarp),
+                           (E + 7) / 8),
                       dim3(256), 0, st, xp, wp, logits, T, E, H);
   return launch_pdl(router_logits_kernel<TX, TW>, dim3((E + 7) / 8, (T + kTok - 1) / kTok),
                     dim3(256), 0, st, xp, wp, logits, T, E, H);

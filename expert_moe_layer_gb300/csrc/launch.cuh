@@ -29,6 +29,18 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_launch_dependents();
 }
 
+// The same pointer, with a value the compiler cannot know before this point.
+// Kernel pointer parameters are restrict-qualified, so the compiler may assume
+// that an asm statement (the dependency wait, an acquire atomic) does not
+// write through them and move their loads above it. A kernel reads data that
+// the preceding kernel, or another CTA, has just written through pointers
+// passed through this after the wait.
+template <typename T>
+__device__ __forceinline__ T* fresh(T* p) {
+  asm volatile("" : "+l"(p));
+  return p;
+}
+
 // Kernels this host thread has launched (successfully) through the library;
 // moe_forward_timed reports the difference across one call.
 inline thread_local long g_kernel_launches = 0;

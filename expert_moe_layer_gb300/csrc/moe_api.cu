@@ -221,7 +221,7 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
              long split_stride = 0, int dense_T = 0, bool pair = false,
              float* part = nullptr, const int32_t* out_rows = nullptr,
-             const float* out_scale = nullptr) {
+             const float* out_scale = nullptr, int b_cap = 0) {
   CUtensorMap ma, mb;
   // CTA pairs in SiLU mode stage 64 gate and 64 up rows per CTA: 64-row boxes
   const int a_box = (pair && mode == kGemmSiluUp) ? 64 : 128;
@@ -246,6 +246,7 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.out_ld = out_ld;
   g.out_rows = out_rows;
   g.out_scale = out_scale;
+  g.b_cap = b_cap;
   g.m_valid = m_valid;
   g.status = status;
   const int sms = sm_count();
@@ -492,7 +493,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
     return MOE_OK;
   }
-  const int ks1 = gemm1_ksplit(c, T);
+  const int ks1 = pairs ? 1 : gemm1_ksplit(c, T);  // pairs: long segments, never split
   if (ks1 > 1) {
     // split over K: raw gate/up partials, then the SiLU*up epilogue
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
@@ -504,7 +505,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   } else {
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st,
-                     1, 0, 0, pairs));
+                     1, 0, 0, pairs, nullptr, nullptr, nullptr, pairs ? cap : 0));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
   // with y_rows (CTA pairs only) GEMM2 writes segment position p to row
@@ -512,7 +513,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
                    tiles, groups, El, H / (pairs ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
                    1, 0, 0, pairs, nullptr, pairs ? y_rows : nullptr,
-                   pairs && y_rows ? w_perm : nullptr));
+                   pairs && y_rows ? w_perm : nullptr, pairs ? cap : 0));
   return MOE_OK;
 }
 
