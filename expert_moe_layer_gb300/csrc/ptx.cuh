@@ -208,20 +208,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Load 8 consecutive fp32 columns of this warp's 32 TMEM lanes and wait.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-  uint32_t r[8];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-        "=r"(r[6]), "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Two 16-column loads (e.g. the gate and up accumulators) and one wait.
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&a)[16],
                                             float (&b)[16]) {
@@ -276,13 +262,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cbar, uint32_t bytes) {
-  asm volatile(
-      "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar),
-      "r"(bytes)
-      : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -311,31 +290,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
       }
     }
   }
-}
-
-// Store four floats to shared memory of any CTA in the cluster.
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-
-// Asynchronous store of four floats into another CTA's shared memory; the
-// 16 bytes complete a transaction on that CTA's mbarrier (no fence needed).
-__device__ __forceinline__ void st_async_v4(uint32_t caddr, float a, float b, float c, float d,
-                                            uint32_t cbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-      "[%5];" ::"r"(caddr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cbar)
-      : "memory");
-}
-
-// Arrive on a cluster mbarrier without release ordering (the caller's reads
-// have already been consumed by dependent instructions).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cbar) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar)
-               : "memory");
 }
 
 // TMA load whose completion is counted on an mbarrier that may live in the
