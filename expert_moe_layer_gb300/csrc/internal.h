@@ -124,9 +124,11 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                          int* group_start = nullptr, int nmax = 0, int max_tiles = 0);
 
 // Routed tile table: group_start gets E_l+1 ints, one group per local expert.
-// (Dense problems need no table: the GEMM derives their tiles from T.)
+// (Dense problems need no table: the GEMM derives their tiles from T.) A
+// segment outside [0, cap) or past the next one's start is dropped and flagged
+// (MOE_DEV_BAD_SEGMENT).
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l,
-                               int nmax, Tile* tiles, int* group_start, int max_tiles,
+                               int nmax, Tile* tiles, int* group_start, int max_tiles, int cap,
                                unsigned* status, cudaStream_t st);
 inline int dense_tile_count(int T, int S, int nmax) { return S * ((T + nmax - 1) / nmax); }
 inline long routed_tile_bound(long n_items, int E_l, int nmax) {

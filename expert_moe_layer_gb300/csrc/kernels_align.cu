@@ -213,7 +213,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ offsets,
                                                            int E_l, int nmax, Tile* __restrict__ tiles,
                                                            int* __restrict__ group_start,
-                                                           int max_tiles, unsigned* status) {
+                                                           int max_tiles, int cap,
+                                                           unsigned* status) {
   pdl_enter();
   counts = fresh(counts);
   offsets = fresh(offsets);
@@ -223,7 +224,8 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
   if (e < E_l) {
     c = counts[e];
     off = offsets[e];
-    if (c < 0 || (e + 1 <= E_l && off + c > offsets[e + 1])) {
+    // a segment must lie inside [0, cap) and end before the next one starts
+    if (c < 0 || off < 0 || off > cap - c || off + c > offsets[e + 1]) {
       if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
       c = 0;
     }
@@ -600,10 +602,10 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
 }
 
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l, int nmax,
-                               Tile* tiles, int* group_start, int max_tiles, unsigned* status,
-                               cudaStream_t st) {
+                               Tile* tiles, int* group_start, int max_tiles, int cap,
+                               unsigned* status, cudaStream_t st) {
   return launch_pdl(build_tiles_kernel, dim3(1), dim3(1024), 0, st, counts, offsets, E_l, nmax,
-                    tiles, group_start, max_tiles, status);
+                    tiles, group_start, max_tiles, cap, status);
 }
 
 cudaError_t launch_gather(bool bf16, const void* x, const int32_t* sorted_ids,

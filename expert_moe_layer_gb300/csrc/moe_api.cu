@@ -456,7 +456,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   const int max_tiles = static_cast<int>(max_routed_tiles(c, T));
   if (!tiles_ready)
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
-                                       status, st)));
+                                       cap, status, st)));
   MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
                                 n_items, K, H, x_perm, st, y_rows ? w_items : nullptr,
                                 y_rows ? w_perm : nullptr)));

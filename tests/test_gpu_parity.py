@@ -239,6 +239,43 @@ def test_grouped_mlp_and_combine_entry_points(name):
     assert_close(out.float().cpu().numpy(), want, f"{name} combine", atol=1e-2, rtol=1e-2)
 
 
+@pytest.mark.parametrize("name", ["ragged_prefill", "ragged_decode"])
+def test_grouped_mlp_drops_segments_outside_cap(name):
+    """Caller-provided segments that start below 0 or run past cap are dropped
+    and flagged (MOE_DEV_BAD_SEGMENT); the other experts' rows are still
+    computed. ragged_prefill runs the 128-row grouped GEMM, ragged_decode the
+    fused decode kernel."""
+    c = case(name)
+    wl = c.wl
+    counts, offsets, sorted_ids, inv_pos = c.oracle_align(16)
+    cap = len(sorted_ids)
+    counts, offsets = counts.copy(), offsets.copy()
+    El = wl.E_local
+    bad = {0, 1, El - 1}                  # expert 0 now ends past expert 1's start
+    offsets[1] = -5                       # starts before row 0
+    counts[El - 1] = max(int(counts[El - 1]), 1) + 9
+    offsets[El] = offsets[El - 1] + counts[El - 1]
+    if offsets[El] <= cap:                # make the last segment run past cap
+        offsets[El - 1] = cap - 2
+        offsets[El] = cap - 2 + counts[El - 1]
+    dt = c.d["x"].dtype
+    y = torch.full((cap, wl.H), float("nan"), dtype=dt, device="cuda")
+    ws = torch.empty(B.grouped_mlp_workspace_size(c.cfg, wl.T, cap), dtype=torch.uint8,
+                     device="cuda")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    B.moe_grouped_mlp(c.cfg, wl.T, c.d["x"], dev(sorted_ids), dev(counts), dev(offsets), cap,
+                      c.d["w13"], c.d["w2"], y, ws)
+    rc, flags = B.moe_get_status(ws)
+    assert rc == 5 and flags & B.DEV_BAD_SEGMENT
+    _, good_off, good_ids, _ = c.oracle_align(16)
+    rows = [r for e in range(El) if e not in bad
+            for r in range(int(good_off[e]), int(good_off[e]) + int(counts[e]))]
+    rows = np.array([r for r in rows if good_ids[r] < wl.T * wl.K])
+    ref = O.grouped_mlp(c.h["x"], good_ids, good_off, c.h["w13"], c.h["w2"], wl.K, rows)
+    assert_close(y.float().cpu().numpy()[rows], np.stack([ref[int(r)] for r in rows]),
+                 f"{name} y_perm of the valid segments")
+
+
 # ------------------------------------------------------------------ edge cases
 def test_no_local_items_gives_shared_only():
     c = case("grouped_shared")
