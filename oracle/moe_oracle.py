@@ -25,7 +25,10 @@ Pins (checked by ``tests/test_oracle_pins.py``):
   * align/permute: pinned by a brute-force stable sort and counting;
   * EP dispatch, expert compute, exchange and combine: pinned by the
     all-ranks pipeline equalling the unsharded forward, and by a brute-force
-    stable partition by destination rank.
+    stable partition by destination rank;
+  * redundant experts (replica maps): pinned by the all-ranks sum equalling
+    the unsharded forward, by the one-replica map equalling the plain map,
+    and by every item landing on exactly one replica.
   The output values themselves have no numeric worked example on the pages,
   so they are pinned only by these identities.
 """
@@ -228,6 +231,61 @@ def expert_mlp(x_rows, w13_e, w2_e) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# redundant experts: a logical expert with several physical replicas
+# ---------------------------------------------------------------------------
+REPLICA_ON_OTHER_RANK = -1
+NO_REPLICA = -2
+
+
+def local_slots(ids, emap):
+    """Local physical slot of each (token, slot) item, -1 = not on this rank.
+
+    ``emap`` is either the plain map [E] (global id -> local slot or -1,
+    ep_fused_moe_patch.py ``_ep_init``) or a replica map [E, R] for redundant
+    experts: row e lists the physical replicas of logical expert e in a fixed
+    global order, each entry the local slot of a replica on this rank or -1
+    for one on another rank, padded with -2. Reading taken, since the pages
+    name redundant experts (``num_redundant_experts``) but give no placement
+    policy: item (t, k) goes to replica t mod n_e of its expert, with n_e the
+    number of replicas, so a hot expert's tokens are spread round robin and
+    every item lands on exactly one replica across the ranks. An expert
+    without replicas is an error.
+    """
+    ids = np.asarray(ids)
+    emap = np.asarray(emap)
+    if emap.ndim == 1:
+        return emap[ids]
+    T = ids.shape[0]
+    loc = np.empty_like(ids, dtype=np.int32)
+    for t in range(T):
+        for k in range(ids.shape[1]):
+            row = emap[ids[t, k]]
+            n = int(np.sum(row != NO_REPLICA))
+            if n == 0 or np.any(row[:n] == NO_REPLICA):
+                raise ValueError("a replica list must be a non-empty prefix of its row")
+            loc[t, k] = row[t % n]
+    return loc
+
+
+def replica_maps(placement, ep_size: int, max_replicas: int):
+    """Per-rank replica maps [E, R] from a global placement.
+
+    ``placement[e]`` lists (rank, local slot) of each replica of logical
+    expert e, in the global replica order. Rank r's map holds the local slot
+    for its own replicas and -1 for the others, padded with -2.
+    """
+    E = len(placement)
+    maps = np.full((ep_size, E, max_replicas), NO_REPLICA, dtype=np.int32)
+    for e, reps in enumerate(placement):
+        if not 1 <= len(reps) <= max_replicas:
+            raise ValueError("each expert needs 1..max_replicas replicas")
+        for j, (rank, slot) in enumerate(reps):
+            maps[:, e, j] = REPLICA_ON_OTHER_RANK
+            maps[rank, e, j] = slot
+    return maps
+
+
+# ---------------------------------------------------------------------------
 # forward
 # ---------------------------------------------------------------------------
 def moe_forward(x, router_w, w13, w2, *, top_k, renormalize=True, n_group=0,
@@ -258,7 +316,12 @@ def moe_forward(x, router_w, w13, w2, *, top_k, renormalize=True, n_group=0,
     E_l = w13.shape[0]
     if emap is None:
         emap = np.arange(E_l, dtype=np.int32)
-    loc = emap[ids]                                   # [n, K], -1 = not local
+    if np.asarray(emap).ndim == 1:
+        loc = np.asarray(emap)[ids]                   # [n, K], -1 = not local
+    else:  # replica map: the token index picks the replica
+        full = np.zeros((T, ids.shape[1]), dtype=ids.dtype)
+        full[tok] = ids
+        loc = local_slots(full, emap)[tok]
     f = np.zeros(ids.shape + (x.shape[1],), dtype=np.float64)
     for e in range(E_l):
         rows, slots = np.nonzero(loc == e)
@@ -330,8 +393,7 @@ def align_permute(topk_ids, emap, n_local: int, block: int, cap=None):
     n_items = T * K
     if cap is None:
         cap = align_cap(T, K, n_local, block)
-    flat = ids.reshape(-1)
-    loc = np.asarray(emap)[flat]
+    loc = local_slots(ids, emap).reshape(-1)
     counts = np.zeros(n_local, dtype=np.int32)
     offsets = np.zeros(n_local + 1, dtype=np.int32)
     sorted_ids = np.full(cap, n_items, dtype=np.int32)

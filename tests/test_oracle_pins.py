@@ -323,6 +323,64 @@ def test_ep_shard_sum_equals_unsharded(ep):
     np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-12)
 
 
+# A global placement with redundant experts over 2 ranks: logical experts 0-7,
+# experts 2 and 5 replicated (expert 2 three times). Each rank holds physical
+# slots; a slot carries its logical expert's weights.
+_PLACEMENT = [[(0, 0)], [(0, 1)], [(0, 2), (1, 4), (0, 5)], [(0, 3)],
+              [(1, 0)], [(1, 1), (0, 4)], [(1, 2)], [(1, 3)]]
+_SLOTS = [[0, 1, 2, 3, 5, 2], [4, 5, 6, 7, 2]]   # logical expert of each slot, per rank
+
+
+def test_replica_maps_partition_items_and_sum_to_unsharded():
+    """Redundant experts: every (token, slot) item lands on exactly one replica
+    across the ranks, a hot expert's items spread round robin over its
+    replicas, and the ranks' partial outputs add up to the unsharded layer
+    (the replicas hold the same weights)."""
+    d = _layer(T=13, E=8, S=1, bias=True)
+    kw = dict(top_k=3, renormalize=True, rsf=1.5)
+    full = _fwd(d, **kw)
+    kw["router_b"] = d["router_b"]
+    maps = O.replica_maps(_PLACEMENT, 2, 3)
+    ids, _, _ = O.route(d["x"], d["router_w"], d["router_b"], top_k=3, renormalize=True)
+    hits = np.zeros(ids.shape, dtype=np.int64)
+    acc = np.zeros_like(full)
+    for r in range(2):
+        loc = O.local_slots(ids, maps[r])
+        hits += loc >= 0
+        for t, k in zip(*np.nonzero(loc >= 0)):
+            assert _SLOTS[r][loc[t, k]] == ids[t, k]       # the slot holds that expert
+        w13 = np.stack([d["w13"][e] for e in _SLOTS[r]])
+        w2 = np.stack([d["w2"][e] for e in _SLOTS[r]])
+        acc += O.moe_forward(d["x"], d["router_w"], w13, w2, emap=maps[r],
+                             shared_w13=d["shared_w13"] if r == 0 else None,
+                             shared_w2=d["shared_w2"] if r == 0 else None, **kw)
+    np.testing.assert_array_equal(hits, 1)
+    np.testing.assert_allclose(acc, full, rtol=1e-12, atol=1e-12)
+    # expert 2's items: token t uses replica t mod 3
+    for t, k in zip(*np.nonzero(ids == 2)):
+        rank, slot = _PLACEMENT[2][t % 3]
+        assert O.local_slots(ids, maps[rank])[t, k] == slot
+
+
+def test_one_replica_map_equals_plain_map_and_bad_rows_are_refused():
+    d = _layer(T=9, E=8)
+    em = O.expert_map(8, 2, 1)
+    rmap = np.full((8, 2), O.NO_REPLICA, dtype=np.int32)
+    rmap[:, 0] = em
+    ids, _, _ = O.route(d["x"], d["router_w"], None, top_k=2, renormalize=True)
+    np.testing.assert_array_equal(O.local_slots(ids, rmap), em[ids])
+    a = O.align_permute(ids, em, 4, 16)
+    b = O.align_permute(ids, rmap, 4, 16)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
+    bad = rmap.copy()
+    bad[int(ids[0, 0])] = O.NO_REPLICA            # an expert without replicas
+    with pytest.raises(ValueError):
+        O.local_slots(ids, bad)
+    with pytest.raises(ValueError):
+        O.replica_maps([[(0, 0)] * 4], 1, 3)      # more replicas than max_replicas
+
+
 def test_expert_map_matches_array_split_and_page_example():
     for E, ep in [(8, 2), (256, 4), (160, 8), (64, 8)]:
         for r in range(ep):
