@@ -38,7 +38,8 @@ class MoeConfig(ctypes.Structure):
                 ("shared_intermediate_size", ctypes.c_int),
                 ("ep_size", ctypes.c_int), ("ep_rank", ctypes.c_int),
                 ("act_dtype", ctypes.c_int), ("router_dtype", ctypes.c_int),
-                ("scoring_func", ctypes.c_int), ("bias_mode", ctypes.c_int)]
+                ("scoring_func", ctypes.c_int), ("bias_mode", ctypes.c_int),
+                ("max_replicas", ctypes.c_int), ("num_redundant_experts", ctypes.c_int)]
 
 
 class WorkspaceOffsets(ctypes.Structure):
@@ -61,7 +62,7 @@ def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=
                 num_expert_group=0, topk_group=0, routed_scaling_factor=1.0,
                 num_shared_experts=0, shared_intermediate_size=0, ep_size=1, ep_rank=0,
                 act_dtype="bf16", router_dtype="bf16", scoring="softmax",
-                bias_mode="logit") -> MoeConfig:
+                bias_mode="logit", max_replicas=0, num_redundant_experts=0) -> MoeConfig:
     dt = {"bf16": MOE_BF16, "f32": MOE_F32}
     sc = {"softmax": 0, "sigmoid": 1}
     bm = {"logit": 0, "select": 1}
@@ -69,7 +70,8 @@ def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=
                      int(num_expert_group > 0), num_expert_group, topk_group,
                      float(routed_scaling_factor), num_shared_experts,
                      shared_intermediate_size, ep_size, ep_rank, dt[act_dtype],
-                     dt[router_dtype], sc[scoring], bm[bias_mode])
+                     dt[router_dtype], sc[scoring], bm[bias_mode], max_replicas,
+                     num_redundant_experts)
 
 
 _lib = None

@@ -9,14 +9,29 @@
 
 namespace moe {
 
-__device__ __forceinline__ int local_expert(int id, const int32_t* __restrict__ emap, int E,
-                                            int E_l, int ep_start, unsigned* status) {
+// Local slot of a work item of global expert id and token t, or -1 (not on
+// this rank, or flagged as bad). emap: NULL (contiguous shard from
+// ep_start), the plain map [E], or with R > 0 a replica map [E, R]: the item
+// goes to replica t mod n of the n replicas listed in row id (entries -1 for
+// another rank, padded with -2).
+__device__ __forceinline__ int local_expert(int id, int t, const int32_t* __restrict__ emap,
+                                            int R, int E, int E_l, int ep_start,
+                                            unsigned* status) {
   if (id < 0 || id >= E) {
     if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
     return -1;
   }
   int le;
-  if (emap) {
+  if (emap && R > 0) {
+    const int32_t* row = emap + static_cast<long>(id) * R;
+    int n = 0;
+    while (n < R && row[n] != -2) ++n;
+    le = n > 0 ? row[t % n] : -3;
+    if (le < -1 || le >= E_l) {
+      if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
+      return -1;
+    }
+  } else if (emap) {
     le = emap[id];
     if (le < -1 || le >= E_l) {
       if (status) atomicOr(status, MOE_DEV_BAD_EXPERT_ID);
@@ -99,8 +114,8 @@ constexpr int kSmallExperts = 256;
 constexpr int kTinyItems = 64;
 
 __device__ __forceinline__ void align_tiny_block(
-    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
-    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, int n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles, int* smem, int* warp_sums) {
@@ -109,13 +124,14 @@ __device__ __forceinline__ void align_tiny_block(
   int* off_s = smem + 2048;    // [E_l] first row of each expert
   const int tid = threadIdx.x;
   for (int r = tid; r < cap; r += 1024) sorted_ids[r] = n_items;
-  if (tid < n_items) le_s[tid] = local_expert(ids[tid], emap, E, E_l, ep_start, status);
+  if (tid < n_items)
+    le_s[tid] = local_expert(ids[tid], tid / K, emap, R, E, E_l, ep_start, status);
   __syncthreads();
   const int G = 1024 / E_l;  // E_l <= 256: at least 4
   const int g = tid / E_l, e = tid - g * E_l;
   const bool active = g < G;
-  const int R = (n_items + G - 1) / G;
-  const int i0 = min(n_items, g * R), i1 = min(n_items, i0 + R);
+  const int per = (n_items + G - 1) / G;  // items of each range
+  const int i0 = min(n_items, g * per), i1 = min(n_items, i0 + per);
   if (active) {
     int c = 0;
     for (int i = i0; i < i1; ++i) c += le_s[i] == e;
@@ -164,14 +180,15 @@ __device__ __forceinline__ void align_tiny_block(
 }
 
 __device__ __forceinline__ void align_small_block(
-    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
-    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, int n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles, int* hist, int* warp_sums) {
   if (n_items <= kTinyItems) {
-    align_tiny_block(ids, n_items, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
-                     inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
+    align_tiny_block(ids, n_items, K, emap, R, E, E_l, ep_start, block_m, counts, offsets,
+                     sorted_ids, inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist,
+                     warp_sums);
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,7 +211,8 @@ __device__ __forceinline__ void align_small_block(
   for (int i = 0; i < kRuns; ++i) {
     if (32 * i >= ipw) break;
     const int item = base + 32 * i + lane;
-    lev[i] = item < n_items ? local_expert(lev[i], emap, E, E_l, ep_start, status) : -1;
+    lev[i] = item < n_items ? local_expert(lev[i], item / K, emap, R, E, E_l, ep_start, status)
+                            : -1;
     const int le = lev[i];
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);

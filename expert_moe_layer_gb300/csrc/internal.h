@@ -95,6 +95,7 @@ struct RouteAlignArgs {
   int32_t* ids;
   float* w;
   const int32_t* emap;
+  int R;                      // replica map width (0: plain map or contiguous shard)
   int E_l, ep_start, block_m;
   int32_t* counts;
   int32_t* offsets;
@@ -121,7 +122,8 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                          int E_l, int ep_start, int block_m, int* hist, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
                          unsigned* status, cudaStream_t st, Tile* tiles = nullptr,
-                         int* group_start = nullptr, int nmax = 0, int max_tiles = 0);
+                         int* group_start = nullptr, int nmax = 0, int max_tiles = 0,
+                         int K = 1, int R = 0);
 
 // Routed tile table: group_start gets E_l+1 ints, one group per local expert.
 // (Dense problems need no table: the GEMM derives their tiles from T.) A

@@ -23,9 +23,9 @@ constexpr int kWarpsPerBlock = 8;
 
 // Pass 1: per-warp expert counts; also fills sorted_ids with the sentinel.
 __global__ void __launch_bounds__(256) align_count_kernel(
-    const int32_t* __restrict__ ids, long n_items, const int32_t* __restrict__ emap, int E,
-    int E_l, int ep_start, int* __restrict__ hist, int n_warps, int32_t* __restrict__ sorted_ids,
-    int cap, unsigned* status) {
+    const int32_t* __restrict__ ids, long n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, int* __restrict__ hist, int n_warps,
+    int32_t* __restrict__ sorted_ids, int cap, unsigned* status) {
   pdl_enter();
   ids = fresh(ids);
   extern __shared__ int cnt[];  // [kWarpsPerBlock][E_l]
@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(256) align_count_kernel(
   for (int i = 0; i < kItemsPerWarp / 32; ++i) {
     const long item = base + 32 * i + lane;
     int le = -1;
-    if (item < n_items) le = local_expert(idv[i], emap, E, E_l, ep_start, status);
+    if (item < n_items)
+      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, status);
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
     __syncwarp();
@@ -144,8 +145,8 @@ __global__ void __launch_bounds__(1024) align_scan_kernel(int* __restrict__ hist
 
 // Pass 3: stable scatter of item ids into their segments.
 __global__ void __launch_bounds__(256) align_scatter_kernel(
-    const int32_t* __restrict__ ids, long n_items, const int32_t* __restrict__ emap, int E,
-    int E_l, int ep_start, const int* __restrict__ hist, int n_warps,
+    const int32_t* __restrict__ ids, long n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, const int* __restrict__ hist, int n_warps,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
     unsigned* status) {
   pdl_enter();
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
     const long item = base + 32 * i + lane;
     int le = -1;
     // status already recorded by pass 1 for bad ids
-    if (item < n_items) le = local_expert(idv[i], emap, E, E_l, ep_start, nullptr);
+    if (item < n_items)
+      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, nullptr);
     const unsigned peers = __match_any_sync(0xffffffffu, le);
     if (item < n_items) {
       int pos = -1;
@@ -195,8 +197,8 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
 // Small inputs (n_items <= kSmallItems, E_l <= kSmallExperts): the three
 // passes above in one CTA of 32 warps (align_small_block).
 __global__ void __launch_bounds__(1024) align_small_kernel(
-    const int32_t* __restrict__ ids, int n_items, const int32_t* __restrict__ emap, int E,
-    int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, int n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles) {
@@ -204,8 +206,9 @@ __global__ void __launch_bounds__(1024) align_small_kernel(
   ids = fresh(ids);
   __shared__ int hist[32 * kSmallExperts];
   __shared__ int warp_sums[32];
-  align_small_block(ids, n_items, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
-                    inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
+  align_small_block(ids, n_items, K, emap, R, E, E_l, ep_start, block_m, counts, offsets,
+                    sorted_ids, inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist,
+                    warp_sums);
 }
 
 // Tile table of the routed experts: each segment's rows in chunks of nmax.
@@ -580,10 +583,10 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                          int ep_start, int block_m, int* hist, int32_t* counts,
                          int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos, int cap,
                          unsigned* status, cudaStream_t st, Tile* tiles, int* group_start,
-                         int nmax, int max_tiles) {
+                         int nmax, int max_tiles, int K, int R) {
   if (n_items <= kSmallItems && E_l <= kSmallExperts) {
     return launch_pdl(align_small_kernel, dim3(1), dim3(1024), 0, st, ids,
-                      static_cast<int>(n_items), emap, E, E_l, ep_start, block_m, counts,
+                      static_cast<int>(n_items), K, emap, R, E, E_l, ep_start, block_m, counts,
                       offsets, sorted_ids, inv_pos, cap, status, tiles, group_start, nmax,
                       max_tiles);
   }
@@ -591,14 +594,15 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
   const int blocks = (n_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const size_t smem = sizeof(int) * kWarpsPerBlock * E_l;
   cudaError_t e = launch_pdl(align_count_kernel, dim3(blocks), dim3(256), smem, st, ids, n_items,
-                             emap, E, E_l, ep_start, hist, n_warps, sorted_ids, cap, status);
+                             K, emap, R, E, E_l, ep_start, hist, n_warps, sorted_ids, cap,
+                             status);
   if (e != cudaSuccess) return e;
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, st, hist, n_warps, E_l, block_m,
                  counts, offsets, cap, status, tiles, group_start, nmax, max_tiles);
   if (e != cudaSuccess) return e;
-  return launch_pdl(align_scatter_kernel, dim3(blocks), dim3(256), smem, st, ids, n_items, emap,
-                    E, E_l, ep_start, static_cast<const int*>(hist), n_warps, sorted_ids, inv_pos,
-                    cap, status);
+  return launch_pdl(align_scatter_kernel, dim3(blocks), dim3(256), smem, st, ids, n_items, K,
+                    emap, R, E, E_l, ep_start, static_cast<const int*>(hist), n_warps, sorted_ids,
+                    inv_pos, cap, status);
 }
 
 cudaError_t launch_build_tiles(const int32_t* counts, const int32_t* offsets, int E_l, int nmax,

@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(
     int E, int H, int K, int renorm, int flags, int n_group, int topk_group,
     float* __restrict__ logits,
     int* __restrict__ tickets, int32_t* __restrict__ ids, float* __restrict__ wout,
-    const int32_t* __restrict__ emap, int E_l, int ep_start, int block_m,
+    const int32_t* __restrict__ emap, int R, int E_l, int ep_start, int block_m,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap,
     unsigned* status, Tile* __restrict__ tiles, int* __restrict__ group_start, int nmax,
@@ -455,8 +455,9 @@ __global__ void __launch_bounds__(1024) route_align_small_kernel(
     __syncthreads();
     if (!is_last) return;
   }
-  align_small_block(ids, T * K, emap, E, E_l, ep_start, block_m, counts, offsets, sorted_ids,
-                    inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist, warp_sums);
+  align_small_block(ids, T * K, K, emap, R, E, E_l, ep_start, block_m, counts, offsets,
+                    sorted_ids, inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist,
+                    warp_sums);
 }
 
 }  // namespace
@@ -512,7 +513,7 @@ cudaError_t route_align_launch(const RouteAlignArgs& a, cudaStream_t st) {
                     static_cast<const TW*>(a.wg), a.bias, a.T,
                     a.E, a.H, a.K, a.renorm, a.flags, a.n_group, a.topk_group, a.logits,
                     a.tickets, a.ids,
-                    a.w, a.emap, a.E_l, a.ep_start, a.block_m, a.counts, a.offsets,
+                    a.w, a.emap, a.R, a.E_l, a.ep_start, a.block_m, a.counts, a.offsets,
                     a.sorted_ids, a.inv_pos, a.cap, a.status, a.tiles, a.group_start, a.nmax,
                     a.max_tiles);
 }

@@ -33,7 +33,10 @@ int validate_cfg(const moe_config* c) {
   const int E = c->num_experts, K = c->top_k, H = c->hidden_size, I = c->intermediate_size;
   if (E < 1 || K < 1 || K > E) return MOE_ERR_INVALID_ARG;
   if (H < 128 || H % 128 != 0 || I < 128 || I % 128 != 0) return MOE_ERR_INVALID_ARG;
-  if (c->ep_size < 1 || E % c->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  if (c->num_redundant_experts < 0 || (c->num_redundant_experts > 0 && c->max_replicas < 1))
+    return MOE_ERR_INVALID_ARG;
+  if (c->ep_size < 1 || (E + c->num_redundant_experts) % c->ep_size != 0)
+    return MOE_ERR_INVALID_ARG;
   if (c->ep_rank < 0 || c->ep_rank >= c->ep_size) return MOE_ERR_INVALID_ARG;
   if (c->use_grouped_topk) {
     const int g = c->num_expert_group, tg = c->topk_group;
@@ -50,10 +53,11 @@ int validate_cfg(const moe_config* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->bias_mode != MOE_BIAS_LOGIT && c->bias_mode != MOE_BIAS_SELECT)
     return MOE_ERR_INVALID_ARG;
+  if (c->max_replicas < 0 || c->max_replicas > 16) return MOE_ERR_INVALID_ARG;
   // kernel coverage
   if (E > 512 || K > 32) return MOE_ERR_UNSUPPORTED;
   if (c->use_grouped_topk && c->num_expert_group > 32) return MOE_ERR_UNSUPPORTED;
-  if (E / c->ep_size > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((E + c->num_redundant_experts) / c->ep_size > 1024) return MOE_ERR_UNSUPPORTED;
   if (c->num_shared_experts > 1024) return MOE_ERR_UNSUPPORTED;
   if (c->act_dtype == MOE_F32 && c->router_dtype == MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -61,7 +65,11 @@ int validate_cfg(const moe_config* c) {
 
 int validate_T(int T) { return (T < 0 || T > kMaxT) ? MOE_ERR_INVALID_ARG : MOE_OK; }
 
-int n_local(const moe_config* c) { return c->num_experts / c->ep_size; }
+// Local weight slots: the rank's share of the logical experts plus the
+// redundant replicas.
+int n_local(const moe_config* c) {
+  return (c->num_experts + c->num_redundant_experts) / c->ep_size;
+}
 
 // Token tile (MMA N) of the routed GEMMs, from the average segment length:
 // 256 (bf16) from 192 rows when that still leaves >= 512 GEMM1 work units
@@ -376,7 +384,8 @@ EpLayout ep_layout(const moe_config* c, int T) {
 // still maps the global ids with the caller's E and rank.
 moe_config ep_item_config(const moe_config* c) {
   moe_config c1 = *c;
-  c1.num_experts = c->num_experts / c->ep_size;
+  c1.num_experts = n_local(c);
+  c1.num_redundant_experts = 0;
   c1.ep_size = 1;
   c1.ep_rank = 0;
   c1.top_k = 1;
@@ -581,6 +590,7 @@ int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
   if (block_m < 1 || block_m > 4096) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!topk_ids || !counts || !offsets || !sorted_ids || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (cfg->max_replicas > 0 && !expert_map) return MOE_ERR_INVALID_ARG;
   if (cap < 0 || static_cast<size_t>(cap) < moe_align_cap(cfg, T, block_m))
     return MOE_ERR_WORKSPACE;
   const AlignLayout L = align_layout(cfg, T);
@@ -592,7 +602,8 @@ int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
   return cuda_ok(launch_align(topk_ids, static_cast<long>(T) * cfg->top_k, expert_map,
                               cfg->num_experts, El, cfg->ep_rank * El, block_m,
                               at<int>(ws, L.hist), counts, offsets, sorted_ids, inv_pos, cap,
-                              status, st));
+                              status, st, nullptr, nullptr, 0, 0, cfg->top_k,
+                              cfg->max_replicas));
 }
 
 size_t moe_grouped_mlp_workspace_size(const moe_config* cfg, int T, int cap) {
@@ -651,6 +662,8 @@ int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* 
                     int32_t* send_pos, void* send_x, int32_t* send_ids, float* send_w,
                     int32_t* send_tok, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(validate_cfg(cfg));
+  // the dispatch has no replica placement (redundant experts): plain maps only
+  if (cfg->max_replicas > 0) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_T(T));
   if (!send_counts || !send_offsets) return MOE_ERR_INVALID_ARG;
   const int ep = cfg->ep_size;
@@ -689,6 +702,8 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
                           const int32_t* recv_ids, const float* recv_w, const void* w13,
                           const void* w2, void* y, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(validate_cfg(cfg));
+  // the dispatch has no replica placement (redundant experts): plain maps only
+  if (cfg->max_replicas > 0) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_T(R));
   if (R == 0) return MOE_OK;
   if (!recv_x || !recv_ids || !recv_w || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
@@ -809,6 +824,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   if (kernels) *kernels = 0;
   if (T == 0) return MOE_OK;
   if (!x || !router_w || !w13 || !w2 || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->max_replicas > 0 && !expert_map) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(w13) || !aligned16(w2) ||
       !aligned16(out))
     return MOE_ERR_INVALID_ARG;
@@ -850,6 +866,7 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     a.ids = ids;
     a.w = w;
     a.emap = expert_map;
+    a.R = cfg->max_replicas;
     a.E_l = El;
     a.ep_start = cfg->ep_rank * El;
     a.block_m = kForwardBlock;
@@ -875,7 +892,8 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
                                  counts, offsets, sorted_ids, inv_pos, L.cap, status, st,
                                  at<Tile>(ws, L.tiles), at<int>(ws, L.groups),
                                  routed_nmax(cfg, T),
-                                 static_cast<int>(max_routed_tiles(cfg, T)))));
+                                 static_cast<int>(max_routed_tiles(cfg, T)), K,
+                                 cfg->max_replicas)));
   }
   MOE_TRY(mark(2));
   MOE_TRY(do_mlp(cfg, T, x, sorted_ids, counts, offsets, L.cap, w13, w2,
@@ -979,6 +997,7 @@ extern "C" int moe_align_permute_noalloc(const moe_config* cfg, int T, const int
   if (block_m < 1 || block_m > 4096) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!topk_ids || !counts || !offsets || !sorted_ids || !inv_pos) return MOE_ERR_INVALID_ARG;
+  if (cfg->max_replicas > 0 && !expert_map) return MOE_ERR_INVALID_ARG;
   if (cap < 0 || static_cast<size_t>(cap) < moe_align_cap(cfg, T, block_m))
     return MOE_ERR_WORKSPACE;
   const AlignLayout L = align_layout(cfg, T);
@@ -993,5 +1012,6 @@ extern "C" int moe_align_permute_noalloc(const moe_config* cfg, int T, const int
   return cuda_ok(launch_align(topk_ids, static_cast<long>(T) * cfg->top_k, expert_map,
                               cfg->num_experts, El, cfg->ep_rank * El, block_m,
                               at<int>(scratch, L.hist), counts, offsets, sorted_ids, inv_pos,
-                              cap, status, st));
+                              cap, status, st, nullptr, nullptr, 0, 0, cfg->top_k,
+                              cfg->max_replicas));
 }

@@ -92,16 +92,34 @@ typedef struct {
   float routed_scaling_factor; /* rsf: multiplies the routed sum; 1 = off    */
   int num_shared_experts;    /* S >= 0 shared experts, added unweighted      */
   int shared_intermediate_size; /* I_s of each shared expert (x128)          */
-  int ep_size;               /* expert-parallel size; E % ep_size == 0       */
+  int ep_size;               /* expert-parallel size; (E + redundant) % ep_size
+                                == 0                                         */
   int ep_rank;               /* this shard, 0 <= ep_rank < ep_size           */
   moe_dtype act_dtype;       /* x, expert weights, y_perm, out               */
   moe_dtype router_dtype;    /* router weight storage (logits are fp32)      */
   int scoring_func;          /* MOE_SCORE_SOFTMAX (0) or MOE_SCORE_SIGMOID (1) */
   int bias_mode;             /* role of router_bias: MOE_BIAS_LOGIT (0) or
                                 MOE_BIAS_SELECT (1), reading below          */
+  int max_replicas;          /* 0: expert_map is the plain map [E]; R in 1..16:
+                                expert_map is a replica map [E, R] (redundant
+                                experts, reading below)                      */
+  int num_redundant_experts; /* extra physical replicas over all ranks (needs
+                                max_replicas > 0); each rank holds
+                                E_local = (E + this) / ep_size weight slots  */
 } moe_config;
 
-/* Routing scores p: fp32 softmax over the E logits (MixtralMoE.forward), or,
+/* Redundant experts (max_replicas = R > 0). The pages name redundant experts
+ * (num_redundant_experts, physical and logical experts) without a placement
+ * policy. Row e of the replica map lists the physical replicas of logical
+ * expert e in one global order: the local slot in [0, E_l) of a replica on
+ * this rank, -1 for a replica on another rank, then -2 padding. The reading
+ * taken: work item (t, k) of expert e goes to replica t mod n_e (n_e = the
+ * replicas listed), so a hot expert's tokens are spread round robin and each
+ * item lands on exactly one replica across the ranks; the slot's weights are
+ * w13[slot], w2[slot]. A row without replicas, or with a value outside
+ * [-2, E_l), drops the item and sets MOE_DEV_BAD_EXPERT_ID.
+ *
+ * Routing scores p: fp32 softmax over the E logits (MixtralMoE.forward), or,
  * with MOE_SCORE_SIGMOID, 1 / (1 + exp(-logit)) per expert. The pages name a
  * non-softmax scoring_func among the FusedMoE routing arguments without
  * defining it; the elementwise logistic is the reading taken.
@@ -167,7 +185,9 @@ int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
  * keeps only local ids).
  *   topk_ids    [T, K] int32 global ids
  *   expert_map  [E] int32 (values in [-1, E_local)), or NULL for the
- *               contiguous shard of cfg->ep_rank: id - ep_rank*E/ep_size.
+ *               contiguous shard of cfg->ep_rank: id - ep_rank*E/ep_size;
+ *               with cfg->max_replicas = R > 0 a replica map [E, R]
+ *               (required; see the redundant-experts reading above).
  *   block_m     segment padding (>= 1). The grouped MLP accepts any value.
  *   counts      [E_local]   out: items per local expert (unpadded)
  *   offsets     [E_local+1] out: exclusive prefix of counts, each rounded
@@ -315,7 +335,8 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
 /* Expert-parallel dispatch and combine: the rank-local halves of
  * ep_fused_moe_patch.py _ep_forward steps 2-4. The exchange between ranks
  * (all_to_all_single of the send buffers with the counts as split sizes, and
- * back) is the caller's: this library runs no collective.
+ * back) is the caller's: this library runs no collective. These calls take
+ * no replica map: with cfg->max_replicas > 0 they return MOE_ERR_UNSUPPORTED.
  *
  * moe_ep_dispatch (step 2). Work item i = t*K + k goes to rank
  * topk_ids[i] / (E / ep_size). The items are sorted by destination rank and

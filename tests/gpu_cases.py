@@ -109,7 +109,7 @@ class DeviceCase:
 def ws_views(cfg, T, ws: torch.Tensor):
     """The routing / permutation arrays moe_forward leaves in its workspace."""
     lay = B.workspace_layout(cfg, T)
-    K, El = cfg.top_k, cfg.num_experts // cfg.ep_size
+    K, El = cfg.top_k, (cfg.num_experts + cfg.num_redundant_experts) // cfg.ep_size
 
     def i32(off, n):
         return ws[off:off + 4 * n].view(torch.int32).cpu().numpy()

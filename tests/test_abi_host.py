@@ -140,6 +140,31 @@ def test_forward_plan_per_workload():
         B.forward_plan(_cfg(top_k=0), 16)
 
 
+def test_replica_configs_are_validated_without_cuda():
+    """Redundant experts: the replica map width, the redundant count and the
+    divisibility of the physical experts are checked on the host; a replica
+    config needs a map; the expert-parallel calls refuse replica maps."""
+    L = B.lib()
+    bp = ctypes.byref
+    ok = _cfg(num_experts=16, top_k=4, hidden_size=256, intermediate_size=256, ep_size=2,
+              max_replicas=2, num_redundant_experts=2)
+    assert L.moe_validate_config(bp(ok)) == 0
+    assert B.align_cap(ok, 4, 1) == 4 * 4        # 9 local slots, block 1: T*K rows
+    for bad in (_cfg(max_replicas=17), _cfg(max_replicas=-1),
+                _cfg(num_redundant_experts=2),  # redundant experts need a replica map
+                _cfg(num_experts=16, ep_size=2, max_replicas=2, num_redundant_experts=1)):
+        assert L.moe_validate_config(bp(bad)) == 1
+    fake = 1 << 20
+    # a replica config without a map
+    assert L.moe_forward(bp(ok), 4, fake, fake, None, fake, fake, None, None, None, fake,
+                         fake, 1 << 30, None) == 1
+    assert L.moe_align_permute(bp(ok), 4, fake, None, 1, fake, fake, fake, fake, 1000, fake,
+                               1 << 30, None) == 1
+    # expert-parallel dispatch and expert compute: no replica maps
+    assert L.moe_ep_dispatch(bp(ok), 8, *([fake] * 10), fake, 1 << 30, None) == 2
+    assert L.moe_ep_expert_compute(bp(ok), 8, *([fake] * 7), 1 << 30, None) == 2
+
+
 def test_ep_entry_points_reject_bad_args_without_cuda():
     cfg = _cfg(num_experts=16, top_k=4, hidden_size=256, intermediate_size=256, ep_size=4)
     L = B.lib()
