@@ -42,7 +42,10 @@
  *     MOE_ERR_CUDA. Data-dependent faults found on the device (an expert id
  *     out of range, a full segment buffer, a pipeline wait that timed out)
  *     never trap. They set a MOE_DEV_* flag and skip the offending access.
- *   - T == 0 is a valid no-op that returns MOE_OK.
+ *   - T == 0 is a valid no-op that returns MOE_OK. T (and the received row
+ *     count R of moe_ep_expert_compute) may be at most 262144 (2^18);
+ *     larger or negative values return MOE_ERR_INVALID_ARG, and the
+ *     workspace queries return 0 for them.
  *   - Calls that share a `ws` buffer must be ordered, as on one stream.
  */
 #ifndef MOE_H

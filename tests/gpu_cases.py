@@ -140,3 +140,23 @@ def sample_tokens(T, n=64):
     if T <= n:
         return np.arange(T)
     return np.unique(np.linspace(0, T - 1, n).astype(np.int64))
+
+
+def check_forward(c: DeviceCase, tokens=None):
+    wl = c.wl
+    out, ws = c.forward()
+    rc, flags = B.moe_get_status(ws)
+    assert rc == 0 and flags == 0, (rc, flags)
+    v = ws_views(c.cfg, wl.T, ws)
+    np.testing.assert_array_equal(v["topk_ids"], c.ids)
+    np.testing.assert_allclose(v["topk_w"], c.w, rtol=W_RTOL, atol=W_ATOL)
+    counts, offsets, sorted_ids, inv_pos = c.oracle_align(v["block_m"])
+    np.testing.assert_array_equal(v["counts"], counts)
+    np.testing.assert_array_equal(v["offsets"], offsets)
+    np.testing.assert_array_equal(v["sorted_ids"], sorted_ids)
+    np.testing.assert_array_equal(v["inv_pos"], inv_pos)
+    tok = np.arange(wl.T) if tokens is None else tokens
+    ref = c.oracle_out(tokens=tok)
+    got = out[torch.from_numpy(tok).cuda()].float().cpu().numpy()
+    assert_close(got, ref, f"{wl.name} out")
+    return out, ws

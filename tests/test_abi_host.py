@@ -48,6 +48,11 @@ def _cfg(**kw):
     (dict(routed_scaling_factor=float("inf")), 1),
     (dict(num_experts=1024, top_k=2), 2),  # beyond kernel coverage
     (dict(num_experts=64, top_k=33), 2),
+    (dict(num_experts=512, top_k=32), 0),  # at the kernel limits
+    (dict(num_experts=512, top_k=32, num_expert_group=32, topk_group=8), 0),
+    (dict(num_experts=512, top_k=2, num_expert_group=64, topk_group=8), 2),
+    (dict(num_experts=512, top_k=2, max_replicas=16, num_redundant_experts=512), 0),
+    (dict(num_experts=512, top_k=2, max_replicas=2, num_redundant_experts=513), 2),
     (dict(act_dtype="f32", router_dtype="bf16"), 2),
 ])
 def test_validate_config(kw, expect):
@@ -80,6 +85,13 @@ def test_entry_points_reject_bad_args_without_cuda():
     # T == 0 is a no-op
     assert L.moe_forward(ctypes.byref(cfg), 0, null, null, null, null, null, null, null,
                          null, null, null, 0, null) == 0
+    # at most 2^18 tokens
+    assert B.workspace_size(cfg, 1 << 18) > 0
+    assert B.workspace_size(cfg, (1 << 18) + 1) == 0
+    assert L.moe_forward(ctypes.byref(cfg), (1 << 18) + 1, 16, 16, null, 16, 16, null, null,
+                         null, 16, 16, 1 << 40, null) == 1
+    assert L.moe_route(ctypes.byref(cfg), (1 << 18) + 1, 16, 16, null, 16, 16, 16, 1 << 30,
+                       null) == 1
 
 
 def test_workspace_sizes_and_layout():

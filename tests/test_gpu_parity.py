@@ -15,8 +15,8 @@ import synth
 from expert_moe_layer_gb300 import binding as B
 from oracle import moe_oracle as O
 
-from gpu_cases import (ATOL, RTOL, W_ATOL, W_RTOL, DeviceCase, assert_close, sample_tokens,
-                       ws_views)
+from gpu_cases import (ATOL, RTOL, W_ATOL, W_RTOL, DeviceCase, assert_close, check_forward,
+                       sample_tokens, ws_views)
 
 pytestmark = pytest.mark.gpu
 
@@ -90,26 +90,6 @@ def case(name):
             wl = synth.QWEN_DECODE.with_(name=name, T=T)
         _cache[name] = DeviceCase(wl)
     return _cache[name]
-
-
-def check_forward(c: DeviceCase, tokens=None):
-    wl = c.wl
-    out, ws = c.forward()
-    rc, flags = B.moe_get_status(ws)
-    assert rc == 0 and flags == 0, (rc, flags)
-    v = ws_views(c.cfg, wl.T, ws)
-    np.testing.assert_array_equal(v["topk_ids"], c.ids)
-    np.testing.assert_allclose(v["topk_w"], c.w, rtol=W_RTOL, atol=W_ATOL)
-    counts, offsets, sorted_ids, inv_pos = c.oracle_align(v["block_m"])
-    np.testing.assert_array_equal(v["counts"], counts)
-    np.testing.assert_array_equal(v["offsets"], offsets)
-    np.testing.assert_array_equal(v["sorted_ids"], sorted_ids)
-    np.testing.assert_array_equal(v["inv_pos"], inv_pos)
-    tok = np.arange(wl.T) if tokens is None else tokens
-    ref = c.oracle_out(tokens=tok)
-    got = out.float().cpu().numpy()[tok]
-    assert_close(got, ref, f"{wl.name} out")
-    return out, ws
 
 
 @pytest.mark.parametrize("name", list(SMALL))
