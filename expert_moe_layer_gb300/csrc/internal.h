@@ -193,10 +193,12 @@ cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const f
                            int32_t* send_tok, cudaStream_t st);
 
 // out[t] = rsf * sum_k w[t,k] y_perm[inv_pos[t,k]] + sum_s shared[s][t]
-// (topk_w may be null: unit weights).
+// (topk_w may be null: unit weights). k_local: the expected number of local
+// rows per token (K, or about K/ep on an EP shard); it only picks the kernel
+// variant.
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
-                           const float* topk_w, int K, const void* shared, int n_shared,
-                           long shared_stride, float rsf, void* out, int T, int H,
+                           const float* topk_w, int K, int k_local, const void* shared,
+                           int n_shared, long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st);
 
 }  // namespace moe

@@ -665,12 +665,17 @@ cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const f
 }
 
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
-                           const float* topk_w, int K, const void* shared, int n_shared,
-                           long shared_stride, float rsf, void* out, int T, int H,
+                           const float* topk_w, int K, int k_local, const void* shared,
+                           int n_shared, long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st) {
-  // up to kCombTok tokens per CTA, about four warp steps per warp, and at
-  // least two CTAs per SM where the batch allows
-  const int kb = bf16 ? (K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : 8) : (K <= 2 ? 2 : 8);
+  // Rows loaded together (KB) follow the expected number of local rows per
+  // token, not K: on an EP shard most slots are elsewhere, and a narrower
+  // batch over more column chunks keeps more bytes in flight per warp. A
+  // token with more local rows takes several batches, in slot order.
+  // Up to kCombTok tokens per CTA, about four warp steps per warp, and at
+  // least two CTAs per SM where the batch allows.
+  const int kl = k_local < 1 ? 1 : k_local > K ? K : k_local;
+  const int kb = bf16 ? (kl <= 1 ? 1 : kl <= 2 ? 2 : kl <= 4 ? 4 : 8) : (kl <= 2 ? 2 : 8);
   const int chunks = (H + 255) / 256;
   const int u = kb >= 4 ? 1 : 4 / kb;
   const int steps = (chunks + u - 1) / u;
@@ -684,12 +689,12 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
                     static_cast<const TE*>(shared), n_shared, shared_stride, rsf,          \
                     static_cast<TE*>(out), T, H, tpc, status)
   if (bf16) {
-    if (K <= 1) MOE_COMBINE(__nv_bfloat16, 1);
-    else if (K <= 2) MOE_COMBINE(__nv_bfloat16, 2);
-    else if (K <= 4) MOE_COMBINE(__nv_bfloat16, 4);
+    if (kb == 1) MOE_COMBINE(__nv_bfloat16, 1);
+    else if (kb == 2) MOE_COMBINE(__nv_bfloat16, 2);
+    else if (kb == 4) MOE_COMBINE(__nv_bfloat16, 4);
     else MOE_COMBINE(__nv_bfloat16, 8);
   } else {
-    if (K <= 2) MOE_COMBINE(float, 2);
+    if (kb == 2) MOE_COMBINE(float, 2);
     else MOE_COMBINE(float, 8);
   }
 #undef MOE_COMBINE

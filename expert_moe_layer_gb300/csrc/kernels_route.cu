@@ -80,14 +80,52 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
 }
 
 // Split-H variant for small E (<= 32). A CTA covers one kRouterSplitCols-wide
-// slice of H (blockIdx.x), 64 tokens (blockIdx.y; 8 per warp) and up to 8
-// experts (blockIdx.z picks the expert octet). Each lane keeps its 8 columns
-// of those experts' router rows in registers, so the router weights are read
-// once per warp and every token row once per octet. The slice index varies
-// fastest, so CTAs launched together read whole token rows. The slice sums
-// go to partial slab blockIdx.x; the top-k kernel adds the slabs in slab
-// order.
-constexpr int kSplitTokWarp = 8;
+// slice of H (blockIdx.x) and up to 8 experts (blockIdx.z picks the expert
+// octet). Each lane keeps its 8 columns of those experts' router rows in
+// registers, loaded once per CTA. The CTA's warps then stream token batches
+// (blockIdx.y*8 + warp, then every gridDim.y*8-th batch): each lane copies its
+// own 16-byte pieces of x with cp.async, kSplitDepth batches ahead, into a
+// per-warp ring in shared memory and reads them back once its own copy group
+// has landed, so a few KB per warp stay in flight with few registers. The
+// grid is sized for two CTAs per SM. The slice sums go to partial slab
+// blockIdx.x; the top-k kernel adds the slabs in slab order.
+constexpr int kSplitDepth = 4;                     // token batches in flight per warp
+template <typename TX>  // tokens per batch
+__host__ __device__ constexpr int split_batch() { return sizeof(TX) == 2 ? 4 : 2; }
+template <typename TX>
+constexpr int split_smem_bytes() {                 // 8 warps x depth x batch x 32 lanes
+  return 8 * kSplitDepth * split_batch<TX>() * 32 * 8 * static_cast<int>(sizeof(TX));
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(ptx::smem_u32(smem)),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4* s, __nv_bfloat16, float (&v)[8]) {
+  const uint4 r = s[0];
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void unpack8(const uint4* s, float, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(s)[0];
+  const float4 b = reinterpret_cast<const float4*>(s)[32];  // second piece, 32 lanes on
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
 // Sum acc[0..7] over the 32 lanes; lane l ends up with the total of entry
 // (l >> 2) & 7. Each halving step keeps half of the entries and hands the
@@ -116,10 +154,13 @@ __device__ __forceinline__ float warp_sum8(const float (&acc)[8], int lane) {
 }
 
 template <typename TX, typename TW>
-__global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __restrict__ x,
-                                                                  const TW* __restrict__ wg,
-                                                                  float* __restrict__ logits,
-                                                                  int T, int E, int H) {
+__global__ void __launch_bounds__(256, 2) router_logits_split_kernel(const TX* __restrict__ x,
+                                                                     const TW* __restrict__ wg,
+                                                                     float* __restrict__ logits,
+                                                                     int T, int E, int H) {
+  constexpr int kTB = split_batch<TX>();
+  constexpr int kPieces = static_cast<int>(sizeof(TX)) / 2;  // 16-byte pieces per lane and token
+  extern __shared__ uint4 xs[];  // [warp][depth][kTB][kPieces][32 lanes]
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x * kRouterSplitCols + lane * 8;
@@ -136,35 +177,58 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(const TX* __re
     }
   }
   float* slab = logits + static_cast<long>(blockIdx.x) * T * E;
-  const long tw = (static_cast<long>(blockIdx.y) * 8 + warp) * kSplitTokWarp;
   const int ex = (lane >> 2) & 7;
+  uint4* ring = xs + warp * (kSplitDepth * kTB * kPieces * 32) + lane;
+  const long nb = (T + kTB - 1) / kTB;
+  const long stride = static_cast<long>(gridDim.y) * 8;
+  const long b0 = static_cast<long>(blockIdx.y) * 8 + warp;
+  // every call commits one group (possibly empty), so group i is batch i
+  auto issue = [&](long b, int slot) {
+    if (hv && b < nb) {
 #pragma unroll
-  for (int a = 0; a < kSplitTokWarp; a += 4) {
-    float xv[4][8];
+      for (int i = 0; i < kTB; ++i) {
+        const long t = b * kTB + i;
+        if (t < T) {
+          const uint4* src = reinterpret_cast<const uint4*>(x + t * H + h);
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      if (hv && tw + a + b < T) {
-        load8(x + (tw + a + b) * H + h, xv[b]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xv[b][i] = 0.f;
+          for (int q = 0; q < kPieces; ++q)
+            cp_async16(ring + ((slot * kTB + i) * kPieces + q) * 32, src + q);
+        }
       }
     }
+    cp_async_commit();
+  };
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+  for (int d = 0; d < kSplitDepth - 1; ++d) issue(b0 + d * stride, d);
+  int slot = 0;
+  for (long b = b0; b < nb; b += stride) {
+    issue(b + (kSplitDepth - 1) * stride, (slot + kSplitDepth - 1) % kSplitDepth);
+    cp_async_wait<kSplitDepth - 1>();  // this lane's copies of batch b have landed
+#pragma unroll
+    for (int i = 0; i < kTB; ++i) {
+      const long t = b * kTB + i;
+      if (t >= T) break;  // uniform over the warp
+      float xv[8];
+      if (hv) {
+        unpack8(ring + (slot * kTB + i) * kPieces * 32, TX(), xv);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xv[k] = 0.f;
+      }
       float acc[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float d = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d = fmaf(xv[b][i], w[j][i], d);
+        for (int k = 0; k < 8; ++k) d = fmaf(xv[k], w[j][k], d);
         acc[j] = d;
       }
       const float v = warp_sum8(acc, lane);
-      const long t = tw + a + b;
-      if ((lane & 3) == 0 && t < T && e0 + ex < E) slab[t * E + e0 + ex] = v;
+      if ((lane & 3) == 0 && e0 + ex < E) slab[t * E + e0 + ex] = v;
     }
+    slot = (slot + 1) % kSplitDepth;
   }
+  cp_async_wait<0>();
 }
 
 // --------------------------------------------------------------- top-k
@@ -467,11 +531,26 @@ cudaError_t logits_launch(const void* x, const void* wg, float* logits, int T, i
                           cudaStream_t st) {
   const TX* xp = static_cast<const TX*>(x);
   const TW* wp = static_cast<const TW*>(wg);
-  if (E <= 32)
-    return launch_pdl(router_logits_split_kernel<TX, TW>,
-                      dim3(router_split_slabs(H), (T + 8 * kSplitTokWarp - 1) / (8 * kSplitTokWarp),
-                           (E + 7) / 8),
-                      dim3(256), 0, st, xp, wp, logits, T, E, H);
+  if (E <= 32) {
+    auto kern = router_logits_split_kernel<TX, TW>;
+    constexpr int kSmem = split_smem_bytes<TX>();
+    static bool configured = false;
+    if (!configured) {
+      cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      configured = true;
+    }
+    // two CTAs per SM over (slices x token groups x expert octets)
+    const long slices = router_split_slabs(H), octets = (E + 7) / 8;
+    const long batches = (T + split_batch<TX>() - 1) / split_batch<TX>();
+    long groups = (2L * 152) / (slices * octets);
+    if (groups > (batches + 7) / 8) groups = (batches + 7) / 8;
+    if (groups < 1) groups = 1;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(slices), static_cast<unsigned>(groups),
+                                 static_cast<unsigned>(octets)),
+                      dim3(256), kSmem, st, xp, wp, logits, T, E, H);
+  }
   return launch_pdl(router_logits_kernel<TX, TW>, dim3((E + 7) / 8, (T + kTok - 1) / kTok),
                     dim3(256), 0, st, xp, wp, logits, T, E, H);
 }

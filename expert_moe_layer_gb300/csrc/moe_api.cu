@@ -71,6 +71,10 @@ int n_local(const moe_config* c) {
   return (c->num_experts + c->num_redundant_experts) / c->ep_size;
 }
 
+// Expected local rows per token: each of the K slots lands on this rank with
+// probability about 1/ep_size.
+int local_rows(const moe_config* c) { return (c->top_k + c->ep_size - 1) / c->ep_size; }
+
 // Token tile (MMA N) of the routed GEMMs, from the average segment length:
 // 256 (bf16) from 192 rows when that still leaves >= 512 GEMM1 work units
 // (several per SM), 128 from 48 rows, else 32. A larger N means more FLOPs
@@ -646,9 +650,9 @@ int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap, const
   unsigned* status = ws ? static_cast<unsigned*>(ws) : nullptr;
   if (status) MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, y_perm, cap, inv_pos, topk_w,
-                                cfg->top_k, shared_out, shared_out ? 1 : 0, 0,
-                                cfg->routed_scaling_factor, out, T, cfg->hidden_size, status,
-                                st));
+                                cfg->top_k, local_rows(cfg), shared_out, shared_out ? 1 : 0,
+                                0, cfg->routed_scaling_factor, out, T, cfg->hidden_size,
+                                status, st));
 }
 
 // ------------------------------------------------------ expert parallel
@@ -742,7 +746,7 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
                  at<void>(ws, L.x_perm), at<void>(ws, L.h_perm), at<float>(ws, L.part1), status,
                  st, nullptr, true));
   return cuda_ok(launch_combine(c1.act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
-                                inv_pos, recv_w, 1, nullptr, 0, 0, 1.0f, y, R,
+                                inv_pos, recv_w, 1, 1, nullptr, 0, 0, 1.0f, y, R,
                                 c1.hidden_size, status, st));
 }
 
@@ -760,9 +764,9 @@ int moe_ep_combine(const moe_config* cfg, int T, const void* ret, const int32_t*
   unsigned* status = ws ? static_cast<unsigned*>(ws) : nullptr;
   if (status) MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   return cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, ret, T * cfg->top_k, send_pos,
-                                nullptr, cfg->top_k, shared_out, shared_out ? 1 : 0, 0,
-                                cfg->routed_scaling_factor, out, T, cfg->hidden_size, status,
-                                st));
+                                nullptr, cfg->top_k, cfg->top_k, shared_out,
+                                shared_out ? 1 : 0, 0, cfg->routed_scaling_factor, out, T,
+                                cfg->hidden_size, status, st));
 }
 
 size_t moe_workspace_size(const moe_config* cfg, int T) {
@@ -920,7 +924,8 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   }
   MOE_TRY(mark(6));
   MOE_TRY(cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
-                                 inv_pos, w, K, shared_y, S, static_cast<long>(T) * H,
+                                 inv_pos, w, K, local_rows(cfg), shared_y, S,
+                                 static_cast<long>(T) * H,
                                  cfg->routed_scaling_factor, out, T, H, status, st)));
   MOE_TRY(mark(7));
   if (kernels) *kernels = static_cast<int>(g_kernel_launches - launches0);

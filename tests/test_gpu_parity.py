@@ -66,6 +66,14 @@ SMALL = {
     # sigmoid with a logit bias, fp32 layer
     "sigmoid_f32": W("sigmoid_f32", T=50, H=128, I=128, E=8, K=2, act="f32", router="f32",
                      router_bias=True, scoring="sigmoid", x_std=0.3),
+    # fp32 routers above 128 tokens run on CUDA cores: split over H for E <= 32
+    # (bf16 x with a ragged last token batch; an fp32 layer whose last H slice
+    # is half full, over two expert octets), one warp per expert beyond 32
+    "f32_router_prefill": W("f32_router_prefill", T=701, H=512, I=256, E=8, K=2, router="f32"),
+    "f32_layer_prefill": W("f32_layer_prefill", T=301, H=384, I=256, E=12, K=3, act="f32",
+                           router="f32", x_std=0.3),
+    "f32_router_wide": W("f32_router_wide", T=300, H=256, I=128, E=64, K=6, router="f32",
+                         router_bias=True),
 }
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
