@@ -166,9 +166,10 @@ SyncRegion sync_region(const moe_config* c, int T) {
 }
 
 // With 256-token tiles both GEMMs run on CTA pairs: one M = 256 MMA over two
-// SMs, each SM staging half of the token rows. GEMM1 puts the 128 gate rows on
-// rank 0 and the matching 128 up rows on rank 1 (one double-buffered
-// accumulator per CTA); GEMM2 puts 256 consecutive output rows on the pair.
+// SMs, each SM staging half of the token rows. In GEMM1 each CTA holds 64 gate
+// rows and the matching 64 up rows of a 128-index slice of I (two
+// accumulators of the double buffer fit in TMEM); GEMM2 puts 256 consecutive
+// output rows on the pair.
 bool gemms_on_pairs(const moe_config* c, int T) {
   return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
 }
