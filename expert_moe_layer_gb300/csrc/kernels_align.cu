@@ -408,8 +408,15 @@ template <> struct Raw8<float> {
   __device__ __forceinline__ void add_to(float (&acc)[8], float w) const { raw8_add(acc, v, w); }
 };
 
+// CTAs per SM from the registers a variant holds: fp32 rows take twice the
+// registers of bf16 ones; KB = 1 keeps four column chunks in flight.
 template <typename TE, int KB>
-__global__ void __launch_bounds__(256, KB > 4 ? 3 : 4) combine_kernel(
+constexpr int combine_ctas_per_sm() {
+  return sizeof(TE) == 4 ? 2 : (KB > 4 || KB == 1) ? 3 : 4;
+}
+
+template <typename TE, int KB>
+__global__ void __launch_bounds__(256, (combine_ctas_per_sm<TE, KB>())) combine_kernel(
     const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
     const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
     long shared_stride, float rsf, TE* __restrict__ out, int T, int H, int tpc,

@@ -34,11 +34,15 @@ __device__ __forceinline__ void pdl_enter() {
 // that an asm statement (the dependency wait, an acquire atomic) does not
 // write through them and move their loads above it. A kernel reads data that
 // the preceding kernel, or another CTA, has just written through pointers
-// passed through this after the wait.
+// passed through this after the wait. The unknown value is a zero offset
+// rather than the pointer itself: passing the pointer through the asm made
+// the compiler keep small per-thread arrays of the same kernel in local
+// memory.
 template <typename T>
 __device__ __forceinline__ T* fresh(T* p) {
-  asm volatile("" : "+l"(p));
-  return p;
+  long off = 0;
+  asm volatile("" : "+l"(off));
+  return p + off;
 }
 
 // Kernels this host thread has launched (successfully) through the library;

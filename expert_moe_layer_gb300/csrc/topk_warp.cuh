@@ -7,8 +7,12 @@
 // Order: larger selection score first, equal scores -> lower expert id.
 // Every argmax is two single-instruction warp reductions (redux.sync) on an
 // order-preserving 32-bit key of the float: the largest key, then the lowest
-// expert id among the lanes that hold it. Each lane sorts its own candidates
-// once, so a selection round only pops the winner's head.
+// expert id among the lanes that hold it. A lane's candidates stay in expert
+// order (expert lane + 32*j in slot j); each round the lane offers its best
+// remaining one (ties to the lower slot, which is the lower id) and the
+// owner of the winner marks that slot taken. Nothing per lane is sorted, so
+// no id array is kept: the routing kernel runs this in CTAs of 1024 threads,
+// whose 64-register budget would otherwise push an array into local memory.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -80,12 +84,8 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
   // score = the largest corrected score in the group; topk_group groups by
   // score, ties to lower group)
   uint32_t ck[VPL];
-  int ci[VPL];
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    ck[j] = fkey(lane + 32 * j < E ? p[j] + sb[j] : -CUDART_INF_F);
-    ci[j] = lane + 32 * j;
-  }
+  for (int j = 0; j < VPL; ++j) ck[j] = fkey(lane + 32 * j < E ? p[j] + sb[j] : -CUDART_INF_F);
   if (n_group > 0) {
     const int gs = E / n_group;
     uint32_t my_score = 0;  // lane g holds the key of group g's score
@@ -115,56 +115,37 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
     }
   }
 
-  // this lane's candidates in decision order (odd-even transposition sort)
-#pragma unroll
-  for (int r = 0; r < VPL; ++r) {
-#pragma unroll
-    for (int j = r & 1; j + 1 < VPL; j += 2) {
-      const bool swap = ck[j + 1] > ck[j] || (ck[j + 1] == ck[j] && ci[j + 1] < ci[j]);
-      if (swap) {
-        const uint32_t tk = ck[j];
-        ck[j] = ck[j + 1];
-        ck[j + 1] = tk;
-        const int ti = ci[j];
-        ci[j] = ci[j + 1];
-        ci[j + 1] = ti;
-      }
-    }
-  }
-  // lanes beyond E hold -inf entries with ids >= E; they never win while a
-  // real expert remains
-  int head = 0;
-  uint32_t hk = ck[0];
-  int hi = ci[0];
   float my_w = 0.f;
   int my_id = 0;
   float wsum = 0.f;
+  uint32_t taken = 0u;  // bit j: slot j already chosen
   for (int k = 0; k < K; ++k) {
-    uint32_t key = hk;
-    int id = hi;
-    warp_argmax_key(key, id);
-    // the winner's score: the key itself, or with a selection correction the
-    // uncorrected score from the lane that holds it
-    float pw = fkey_inv(key);
-    if (flags & kRouteBiasSelect) {
-      float mine = 0.f;
+    // this lane's best remaining candidate, or id 0x7fffffff when none is left
+    // (slots beyond E hold -inf keys with ids >= E; they never win while a
+    // real expert remains; a NaN score has key 0 and is offered last)
+    uint32_t key = 0u;
+    int id = 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if ((hi >> 5) == j) mine = p[j];
-      pw = __shfl_sync(0xffffffffu, mine, id & 31);
-    }
-    if (hi == id) {  // the owner pops its head
-      ++head;
-      hk = 0u;
-      hi = 0x7fffffff;
-#pragma unroll
-      for (int j = 1; j < VPL; ++j) {
-        if (j == head) {
-          hk = ck[j];
-          hi = ci[j];
-        }
+    for (int j = 0; j < VPL; ++j) {
+      if (!((taken >> j) & 1u) && (id == 0x7fffffff || ck[j] > key)) {
+        key = ck[j];
+        id = lane + 32 * j;
       }
     }
+    warp_argmax_key(key, id);
+    // the winner's score: the key itself, or with a selection correction the
+    // uncorrected score from the lane that holds it (picked by a bit mask,
+    // not a select, so that p stays in registers and is not indexed in local
+    // memory)
+    const int ws = id >> 5;
+    float pw = fkey_inv(key);
+    if (flags & kRouteBiasSelect) {
+      uint32_t mine = 0u;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) mine |= __float_as_uint(p[j]) & (0u - (ws == j));
+      pw = __shfl_sync(0xffffffffu, __uint_as_float(mine), id & 31);
+    }
+    if (lane == (id & 31) && ws < VPL) taken |= 1u << ws;  // the owner retires the slot
     wsum += pw;
     if (lane == k) {
       my_w = pw;
