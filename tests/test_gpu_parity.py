@@ -46,6 +46,8 @@ SMALL = {
     "grouped_decode": synth.DEEPSEEK.with_(name="grouped_decode", T=24, H=256, I=256,
                                            I_shared=256),
     "ep_decode": synth.EP_SHARD.with_(name="ep_decode", T=32, H=256, I=256),
+    # at most 32 items: the single-warp align (here 24 items over 64 local experts)
+    "ep_tiny": synth.EP_SHARD.with_(name="ep_tiny", T=3, H=256, I=256),
     "wide_router": W("wide_router", T=12, H=128, I=128, E=320, K=4, ep_size=2, ep_rank=1,
                      router_bias=True),
     # sigmoid scores with the selection-only score correction (e_score_correction_bias
@@ -78,7 +80,7 @@ SMALL = {
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
-               "grouped_decode", "ep_decode", "wide_router")
+               "grouped_decode", "ep_decode", "ep_tiny", "wide_router")
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
     "deepseek_v2_prefill": synth.DEEPSEEK,
@@ -150,11 +152,13 @@ def _align(c, ids_np, block, emap=None, cap=None):
 
 
 @pytest.mark.parametrize("block", [1, 7, 16, 64, 128])
-@pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1", "single_token", "wide_router"])
+@pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1", "single_token", "ep_tiny",
+                                  "wide_router"])
 def test_align_entry_point(name, block):
-    """Per-warp counting sort (ragged_prefill, ep_rank1) and the small-batch
-    path of up to 64 items (single_token: 4 items; wide_router: 48 items of an
-    EP shard with 160 local experts)."""
+    """Per-warp counting sort (ragged_prefill, ep_rank1), the single-warp align
+    of up to 32 items (single_token: 4 items; ep_tiny: 24 items over 64 local
+    experts) and the small-batch path of up to 64 items (wide_router: 48 items
+    of an EP shard with 160 local experts)."""
     c = case(name)
     counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, block)
     assert st == (0, 0)
@@ -165,8 +169,12 @@ def test_align_entry_point(name, block):
     np.testing.assert_array_equal(inv_pos, ri)
 
 
-def test_align_general_expert_map_and_bad_ids():
-    c = case("ep_rank1")
+@pytest.mark.parametrize("name", ["ep_rank1", "ep_tiny"])
+def test_align_general_expert_map_and_bad_ids(name):
+    """A permuted partial expert map, then flagged bad ids and map values, on
+    the three-pass align (ep_rank1: 4000 items) and the single-warp one
+    (ep_tiny: 24 items)."""
+    c = case(name)
     wl = c.wl
     rng = np.random.default_rng(7)
     emap = np.full(wl.E, -1, dtype=np.int32)
