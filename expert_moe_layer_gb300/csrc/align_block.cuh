@@ -179,117 +179,12 @@ __device__ __forceinline__ void align_tiny_block(
   if (tid < n_items && le_s[tid] < 0) inv_pos[tid] = -1;
 }
 
-// Up to kWarpItems items (decode batches of a few tokens) on warp 0 alone:
-// no block barriers. Lane i holds item i; __match_any_sync gives each item
-// its expert's count and its stable rank among that expert's items. Lane l
-// owns local experts 8l..8l+7 (E_l <= 256): it reads their counts from
-// shared memory (cnt, E_l ints), and one warp scan of its padded-row and
-// tile sums gives the offsets and the tile starts. Outputs equal those of
-// align_tiny_block.
-constexpr int kWarpItems = 32;
-
-__device__ __forceinline__ void align_warp_block(
-    const int32_t* __restrict__ ids, int n_items, int K, const int32_t* __restrict__ emap, int R,
-    int E, int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
-    int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
-    int* __restrict__ group_start, int nmax, int max_tiles, int* cnt) {
-  const int lane = threadIdx.x & 31;
-  for (int r = lane; r < cap; r += 32) sorted_ids[r] = n_items;
-  for (int e = lane; e < E_l; e += 32) cnt[e] = 0;
-  const int le =
-      lane < n_items ? local_expert(ids[lane], lane / K, emap, R, E, E_l, ep_start, status) : -1;
-  const unsigned peers = __match_any_sync(0xffffffffu, le);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  __syncwarp();
-  if (le >= 0 && rank == 0) cnt[le] = __popc(peers);
-  __syncwarp();
-  // this lane's experts: counts, padded rows and tiles, then their prefixes
-  int c[8], pr[8], tl[8];
-  int sum_r = 0, sum_t = 0;
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int e = 8 * lane + m;
-    c[m] = e < E_l ? cnt[e] : 0;
-    const int rows = ((c[m] + block_m - 1) / block_m) * block_m;
-    const int nt = tiles ? (c[m] + nmax - 1) / nmax : 0;
-    pr[m] = sum_r;
-    tl[m] = sum_t;
-    sum_r += rows;
-    sum_t += nt;
-  }
-  int base_r = sum_r, base_t = sum_t;  // inclusive scan over lanes, then exclusive
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int vr = __shfl_up_sync(0xffffffffu, base_r, o);
-    const int vt = __shfl_up_sync(0xffffffffu, base_t, o);
-    if (lane >= o) {
-      base_r += vr;
-      base_t += vt;
-    }
-  }
-  const int total_r = __shfl_sync(0xffffffffu, base_r, 31);
-  const int total_t = __shfl_sync(0xffffffffu, base_t, 31);
-  base_r -= sum_r;
-  base_t -= sum_t;
-  __syncwarp();  // every lane has read cnt before it becomes the row offsets
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int e = 8 * lane + m;
-    if (e >= E_l) break;
-    const int off = base_r + pr[m];
-    counts[e] = c[m];
-    offsets[e] = off;
-    cnt[e] = off;
-    if (tiles) {
-      const int start = base_t + tl[m];
-      for (int j = 0; j * nmax < c[m]; ++j) {
-        const int idx = start + j;
-        if (idx < max_tiles) {
-          const int r0 = off + j * nmax;
-          tiles[idx] = make_int4(e, r0, r0, min(nmax, c[m] - j * nmax));
-        }
-      }
-      group_start[e] = min(start, max_tiles);
-    }
-  }
-  if (lane == 0) {
-    offsets[E_l] = total_r;
-    if (total_r > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
-    if (tiles) {
-      group_start[E_l] = min(total_t, max_tiles);
-      if (total_t > max_tiles && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
-    }
-  }
-  __syncwarp();  // the row offsets are in cnt; the sentinel fill is done
-  if (lane < n_items) {
-    int pos = -1;
-    if (le >= 0) {
-      pos = cnt[le] + rank;
-      if (pos < cap) {
-        sorted_ids[pos] = lane;
-      } else {
-        if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
-        pos = -1;
-      }
-    }
-    inv_pos[lane] = pos;
-  }
-}
-
 __device__ __forceinline__ void align_small_block(
     const int32_t* __restrict__ ids, int n_items, int K, const int32_t* __restrict__ emap, int R,
     int E, int E_l, int ep_start, int block_m, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
     int32_t* __restrict__ inv_pos, int cap, unsigned* status, Tile* __restrict__ tiles,
     int* __restrict__ group_start, int nmax, int max_tiles, int* hist, int* warp_sums) {
-  if (n_items <= kWarpItems) {
-    if (threadIdx.x < 32)
-      align_warp_block(ids, n_items, K, emap, R, E, E_l, ep_start, block_m, counts, offsets,
-                       sorted_ids, inv_pos, cap, status, tiles, group_start, nmax, max_tiles,
-                       hist);
-    return;
-  }
   if (n_items <= kTinyItems) {
     align_tiny_block(ids, n_items, K, emap, R, E, E_l, ep_start, block_m, counts, offsets,
                      sorted_ids, inv_pos, cap, status, tiles, group_start, nmax, max_tiles, hist,

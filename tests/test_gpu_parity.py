@@ -46,7 +46,7 @@ SMALL = {
     "grouped_decode": synth.DEEPSEEK.with_(name="grouped_decode", T=24, H=256, I=256,
                                            I_shared=256),
     "ep_decode": synth.EP_SHARD.with_(name="ep_decode", T=32, H=256, I=256),
-    # at most 32 items: the single-warp align (here 24 items over 64 local experts)
+    # a few items over many local experts (24 items over 64)
     "ep_tiny": synth.EP_SHARD.with_(name="ep_tiny", T=3, H=256, I=256),
     "wide_router": W("wide_router", T=12, H=128, I=128, E=320, K=4, ep_size=2, ep_rank=1,
                      router_bias=True),
@@ -155,10 +155,10 @@ def _align(c, ids_np, block, emap=None, cap=None):
 @pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1", "single_token", "ep_tiny",
                                   "wide_router"])
 def test_align_entry_point(name, block):
-    """Per-warp counting sort (ragged_prefill, ep_rank1), the single-warp align
-    of up to 32 items (single_token: 4 items; ep_tiny: 24 items over 64 local
-    experts) and the small-batch path of up to 64 items (wide_router: 48 items
-    of an EP shard with 160 local experts)."""
+    """Per-warp counting sort (ragged_prefill, ep_rank1) and the small-batch
+    path of up to 64 items (single_token: 4 items; ep_tiny: 24 items over 64
+    local experts; wide_router: 48 items of an EP shard with 160 local
+    experts)."""
     c = case(name)
     counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, block)
     assert st == (0, 0)
@@ -172,7 +172,7 @@ def test_align_entry_point(name, block):
 @pytest.mark.parametrize("name", ["ep_rank1", "ep_tiny"])
 def test_align_general_expert_map_and_bad_ids(name):
     """A permuted partial expert map, then flagged bad ids and map values, on
-    the three-pass align (ep_rank1: 4000 items) and the single-warp one
+    the three-pass align (ep_rank1: 4000 items) and the small-batch one
     (ep_tiny: 24 items)."""
     c = case(name)
     wl = c.wl
