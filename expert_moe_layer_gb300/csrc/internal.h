@@ -195,10 +195,12 @@ cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const f
 // out[t] = rsf * sum_k w[t,k] y_perm[inv_pos[t,k]] + sum_s shared[s][t]
 // (topk_w may be null: unit weights). k_local: the expected number of local
 // rows per token (K, or about K/ep on an EP shard); it only picks the kernel
-// variant.
+// variant. slots_early: inv_pos and topk_w were written by a kernel at least
+// two launches back on this stream (true only inside moe_forward), so the
+// kernel may read them before its dependency wait.
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
                            const float* topk_w, int K, int k_local, const void* shared,
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,
-                           unsigned* status, cudaStream_t st);
+                           unsigned* status, cudaStream_t st, bool slots_early = false);
 
 }  // namespace moe

@@ -420,13 +420,16 @@ __global__ void __launch_bounds__(256, (combine_ctas_per_sm<TE, KB>())) combine_
     const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
     const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
     long shared_stride, float rsf, TE* __restrict__ out, int T, int H, int tpc,
-    unsigned* status) {
+    int slots_early, unsigned* status) {
   constexpr int U = KB >= 4 ? 1 : 4 / KB;  // chunks per warp step
-  pdl_enter();
-  y_perm = fresh(y_perm);
-  inv_pos = fresh(inv_pos);
-  topk_w = fresh(topk_w);
-  shared = fresh(shared);
+  // slots_early: inv_pos and topk_w were written at least two kernels back,
+  // so they are staged before the dependency wait, while the kernel before
+  // finishes; the rows of y_perm and shared are read only after it.
+  if (!slots_early) {
+    pdl_enter();
+    inv_pos = fresh(inv_pos);
+    topk_w = fresh(topk_w);
+  }
   __shared__ int s_pos[kCombTok][32];
   __shared__ float s_w[kCombTok][32];
   __shared__ int s_n[kCombTok];
@@ -452,6 +455,9 @@ __global__ void __launch_bounds__(256, (combine_ctas_per_sm<TE, KB>())) combine_
     }
     if (lane == 0) s_n[tt] = __popc(local);
   }
+  if (slots_early) pdl_enter();
+  y_perm = fresh(y_perm);
+  shared = fresh(shared);
   __syncthreads();
   const int chunks = (H + 255) / 256;
   const int steps = (chunks + U - 1) / U;  // warp steps per token
@@ -674,7 +680,7 @@ cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const f
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
                            const float* topk_w, int K, int k_local, const void* shared,
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,
-                           unsigned* status, cudaStream_t st) {
+                           unsigned* status, cudaStream_t st, bool slots_early) {
   // Rows loaded together (KB) follow the expected number of local rows per
   // token, not K: on an EP shard most slots are elsewhere, and a narrower
   // batch over more column chunks keeps more bytes in flight per warp. A
@@ -694,7 +700,7 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
   return launch_pdl(combine_kernel<TE, KB>, dim3(grid), dim3(256), 0, st,                  \
                     static_cast<const TE*>(y_perm), cap, inv_pos, topk_w, K,               \
                     static_cast<const TE*>(shared), n_shared, shared_stride, rsf,          \
-                    static_cast<TE*>(out), T, H, tpc, status)
+                    static_cast<TE*>(out), T, H, tpc, slots_early ? 1 : 0, status)
   if (bf16) {
     if (kb == 1) MOE_COMBINE(__nv_bfloat16, 1);
     else if (kb == 2) MOE_COMBINE(__nv_bfloat16, 2);

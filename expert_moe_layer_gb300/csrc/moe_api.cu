@@ -927,7 +927,8 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
   MOE_TRY(cuda_ok(launch_combine(cfg->act_dtype == MOE_BF16, at<void>(ws, L.y_perm), L.cap,
                                  inv_pos, w, K, local_rows(cfg), shared_y, S,
                                  static_cast<long>(T) * H,
-                                 cfg->routed_scaling_factor, out, T, H, status, st)));
+                                 cfg->routed_scaling_factor, out, T, H, status, st,
+                                 /*slots_early=*/true)));  // ids, weights, inv_pos: >= 3 back
   MOE_TRY(mark(7));
   if (kernels) *kernels = static_cast<int>(g_kernel_launches - launches0);
   return MOE_OK;
