@@ -147,25 +147,33 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
-            for line in fh:
-                f = [c.strip() for c in line.split(",")]
-                if len(f) < 9:
-                    continue
-                try:
-                    sm.append(float(f[1]))
-                    mx.append(float(f[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, f[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            return summarize_clocks(fh)
+
+
+def summarize_clocks(lines):
+    """Median SM clock, the largest max clock and the throttle reasons that
+    were active in any sample, from nvidia-smi CSV rows in ClockSampler.FIELDS
+    order (no header, no units). Rows that do not parse are skipped; None when
+    no row does."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        f = [c.strip() for c in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # --------------------------------------------------------------------------- ranks
@@ -460,12 +468,12 @@ def run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world, step_bytes)
             "ms_per_step": round(ms, 4), "steps": n, "mode": mode}
 
 
-def traffic_from_profile(workload, kernel_source):
+def traffic_from_profile(workload, kernel_source, root=ROOT):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, or None when there is none for this workload or the kernel's
     source changed since the capture."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
+    p = os.path.join(root, "profiles", "dominant_kernel_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
@@ -473,7 +481,7 @@ def traffic_from_profile(workload, kernel_source):
     v = d["workloads"].get(workload)
     if v is None or os.path.basename(v["kernel_source"]) != kernel_source:
         return None
-    with open(os.path.join(ROOT, v["kernel_source"]), "rb") as fh:
+    with open(os.path.join(root, v["kernel_source"]), "rb") as fh:
         if hashlib.sha256(fh.read()).hexdigest() != v["kernel_sha256"]:
             return None
     return v.get("dram_bytes_per_launch")

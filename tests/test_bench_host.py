@@ -1,0 +1,63 @@
+"""Host-side pieces of bench.py that need no GPU: the clock record summary,
+the DRAM-traffic lookup from the committed ncu summaries, and the rules
+those summaries follow (every ncu command leaves the clocks alone)."""
+import hashlib
+import json
+import os
+import re
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _row(sm, mx, power_cap="Not Active", hw="Not Active"):
+    # index, clocks.sm, clocks.max.sm, power.draw, reasons.active, hw_slowdown,
+    # hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    return f"0, {sm}, {mx}, 1210.50, 0x0000000000000004, {hw}, Not Active, Not Active, {power_cap}"
+
+
+def test_clock_summary_takes_median_max_and_every_active_reason():
+    lines = [_row(1785, 2070), _row(1800, 2070, power_cap="Active"), _row(1900, 2070),
+             "0, [N/A], [N/A], [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",
+             "garbage", ""]
+    s = bench.summarize_clocks(lines)
+    assert s == {"sm_mhz": 1800.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 3}
+    s = bench.summarize_clocks([_row(2070, 2070, hw="Active"), _row(2070, 2070)])
+    assert s["reasons"] == ["hw_slowdown"] and s["sm_mhz"] == 2070.0
+    assert bench.summarize_clocks(["garbage"]) is None
+
+
+def test_traffic_lookup_follows_the_kernel_source_hash(tmp_path):
+    src = tmp_path / "k.cu"
+    src.write_text("// kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    entry = {"kernel": "k", "kernel_source": "k.cu",
+             "kernel_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+             "dram_bytes_per_launch": 12345}
+    (tmp_path / "profiles" / "dominant_kernel_traffic.json").write_text(
+        json.dumps({"workloads": {"w": entry}}))
+    assert bench.traffic_from_profile("w", "k.cu", root=str(tmp_path)) == 12345
+    assert bench.traffic_from_profile("other", "k.cu", root=str(tmp_path)) is None
+    assert bench.traffic_from_profile("w", "j.cu", root=str(tmp_path)) is None
+    src.write_text("// kernel v2\n")  # the kernel changed since the capture
+    assert bench.traffic_from_profile("w", "k.cu", root=str(tmp_path)) is None
+
+
+def test_committed_profiles_name_existing_sources_and_leave_clocks_alone():
+    with open(os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")) as fh:
+        d = json.load(fh)
+    assert d["workloads"]
+    for name, v in d["workloads"].items():
+        assert os.path.exists(os.path.join(ROOT, v["kernel_source"])), name
+        assert re.fullmatch(r"[0-9a-f]{64}", v["kernel_sha256"]), name
+        assert v["dram_bytes_per_launch"] > 0, name
+        assert v["command"].startswith("ncu ") and "--clock-control none" in v["command"]
+        assert "bench.py" in v["command"] and "_work" not in v["command"]
+    for fn in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+        if not fn.endswith(".md"):
+            continue
+        text = open(os.path.join(ROOT, "profiles", fn)).read()
+        for cmd in re.findall(r"^ncu [^\n]*(?:\\\n[^\n]*)*", text, flags=re.M):
+            assert "--clock-control none" in cmd, (fn, cmd)
