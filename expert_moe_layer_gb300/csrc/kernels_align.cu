@@ -299,17 +299,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
   }
 }
 
-// out[t] = rsf * sum_k w[t,k] * y_perm[inv_pos[t,k]] + sum_s shared[s][t]
-__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 r = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(h[i]);
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
-}
+// 8 consecutive fp32 values (two 16-byte loads) and 8 outputs in one store.
 __device__ __forceinline__ void ld8(const float* p, float (&v)[8]) {
   const float4 a = *reinterpret_cast<const float4*>(p);
   const float4 b = *reinterpret_cast<const float4*>(p + 4);
