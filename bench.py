@@ -126,10 +126,12 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index, interval_ms=50):
+        import tempfile
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples go to a temporary file; only their summary is kept
+        fd, self.path = tempfile.mkstemp(prefix=f"moe_clocks_gpu{gpu_index}_", suffix=".csv")
+        os.close(fd)
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
@@ -140,6 +142,9 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
+            if getattr(self, "fh", None) is not None:
+                self.fh.close()
+            os.remove(self.path)
             return None
         self.proc.terminate()
         try:
@@ -148,7 +153,9 @@ class ClockSampler:
             self.proc.kill()
         self.fh.close()
         with open(self.path) as fh:
-            return summarize_clocks(fh)
+            summary = summarize_clocks(fh)
+        os.remove(self.path)
+        return summary
 
 
 def summarize_clocks(lines):

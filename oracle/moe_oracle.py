@@ -89,8 +89,8 @@ def sigmoid_fp32(logits32: np.ndarray) -> np.ndarray:
     """Per-expert sigmoid scores in fp32: 1 / (1 + exp(-l)).
 
     ``scoring_func`` is named among the FusedMoE routing arguments the pages
-    list but not defined there (SURVEY reading: the non-softmax scoring is an
-    elementwise logistic of each logit, in the same fp32 as the softmax).
+    list but not defined there. The reading taken: the non-softmax scoring is
+    an elementwise logistic of each logit, in the same fp32 as the softmax.
     """
     l = np.asarray(logits32, np.float32)
     with np.errstate(over="ignore"):
