@@ -142,6 +142,8 @@ def _p(t):
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError("libmoe takes device tensors; got one on " + str(t.device))
     if not t.is_contiguous():
         raise ValueError("tensors passed to libmoe must be contiguous")
     return t.data_ptr()
