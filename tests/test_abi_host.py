@@ -193,3 +193,13 @@ def test_ep_entry_points_reject_bad_args_without_cuda():
     assert L.moe_ep_expert_compute(bp(cfg), 8, *([None] * 7), 0, None) == 1
     assert L.moe_ep_combine(bp(cfg), 8, None, None, None, None, None, 0, None) == 1
     assert L.moe_ep_combine(bp(_cfg(top_k=0)), 8, None, None, None, None, None, 0, None) == 1
+
+
+def test_binding_refuses_host_tensors_for_device_arguments():
+    import torch
+    assert B._p(None) is None and B._p(1 << 20) == 1 << 20
+    with pytest.raises(ValueError, match="device tensors"):
+        B._p(torch.zeros(4))
+    with pytest.raises(ValueError, match="device tensors"):
+        B.moe_combine(_cfg(), 4, torch.zeros(8, 4096), 8, torch.zeros(8, dtype=torch.int32),
+                      torch.zeros(8), None, torch.zeros(4, 4096))
