@@ -4,7 +4,10 @@
 One step = one moe_forward of a whole layer (routing, align/permute, grouped
 SiLU-gated MLP of the local and shared experts, combine) over one batch of
 synthetic tokens. The default workload is the Mixtral-8x7B-shape prefill layer
-(T=4096, H=4096, I=14336, E=8, top_k=2). Prints one JSON line.
+(T=4096, H=4096, I=14336, E=8, top_k=2). Prints one JSON line. On one GPU
+the line also carries the other workloads (Qwen3-MoE-shape decode at T = 1, 8
+and 64, the DeepSeek-V2-shape prefill, the EP shard), each timed the same way,
+under "workloads" (--no-extra skips them).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -54,6 +57,10 @@ class L2Flush:
 WORKLOADS = {w.name: w for w in (synth.TINY, synth.MIXTRAL, synth.DEEPSEEK, synth.EP_SHARD)}
 for _t in synth.DECODE_TOKENS:
     WORKLOADS[f"qwen3_decode_T{_t}"] = synth.QWEN_DECODE.with_(name=f"qwen3_decode_T{_t}", T=_t)
+# timed beside the headline workload in the same run; the decode sizes last,
+# largest T last (their weights are drawn once, with that T's x)
+EXTRA_WORKLOADS = ["deepseek_v2_prefill", "ep_shard", "mixtral_prefill",
+                   *[f"qwen3_decode_T{t}" for t in sorted(synth.DECODE_TOKENS)]]
 
 
 def load_peaks():
@@ -196,12 +203,76 @@ def aggregate_over_ranks(local_ms, tokens_per_rank, steps, world, device=None):
 
 
 # --------------------------------------------------------------------------- our arm
-def run_ours(args, wl, rank, world, device):
+def dominant_kernel_roofline(wl, plan, A, touched, k_ms, peaks):
+    """Roofline of the layer's dominant kernel: GEMM1 (gate/up with the SiLU
+    epilogue), or for decode-sized batches the fused kernel that runs GEMM1
+    and GEMM2 together. Algorithmic FLOPs and bytes per launch over its
+    measured duration, against the measured peak: the bf16 burst peak for a
+    tensor-bound kernel (the timed regions here last milliseconds, not the
+    seconds of the sustained figure, which is reported beside it), the HBM
+    copy peak otherwise."""
+    eb = 2 if wl.act == "bf16" else 4
+    w13_bytes = touched * 2 * wl.I * wl.H * eb
+    w2_bytes = touched * wl.H * wl.I * eb
+    if plan.fused_mlp:
+        kname, ksrc = "moe_mlp_fused (GEMM1 + GEMM2)", "kernels_mlp_fused.cu"
+        k_flops = 6 * A * wl.H * wl.I
+        # weights once; x rows in, h out and back in, y out
+        k_bytes = w13_bytes + w2_bytes + (2 * A * wl.H + 2 * A * wl.I) * eb
+    else:
+        kname, ksrc = (("moe_gemm_pair<SiLU> (GEMM1, CTA pairs)", "kernels_gemm_pair.cu")
+                       if plan.cta_pairs else
+                       ("moe_gemm_tc<SiLU> (GEMM1)", "kernels_gemm.cu"))
+        k_flops = 4 * A * wl.H * wl.I
+        k_bytes = w13_bytes + A * wl.H * eb + A * wl.I * eb
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if k_flops / max(k_bytes, 1) >= ridge:
+        ach = k_flops / (k_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_basis": f"{peaks['source']} bf16 burst (the kernel runs inside a "
+                              "timed region of milliseconds)",
+                "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4)}
+    else:
+        ach = k_bytes / (k_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_basis": f"{peaks['source']} HBM copy",
+                "frac_of_nominal_8TBs": round(ach / 8000.0, 4)}
+    roof.update({"kernel": kname, "ms_per_launch": round(k_ms, 4),
+                 "algorithmic_flops": k_flops, "algorithmic_bytes": k_bytes,
+                 "traffic": traffic_from_profile(wl.name, ksrc)})
+    return roof
+
+
+def layer_work(wl, A, touched):
+    """Algorithmic FLOPs and bytes of one layer forward: the expert MLPs of
+    the A local assignments, the router and shared experts; the weights of
+    each touched expert, the router and shared weights, x in and out once."""
+    rb = 2 if wl.router == "bf16" else 4
+    eb = 2 if wl.act == "bf16" else 4
+    alg_bytes = (touched * 3 * wl.H * wl.I * eb + wl.E * wl.H * rb
+                 + wl.n_shared * 3 * wl.H * wl.I_shared * eb + 2 * wl.T * wl.H * eb)
+    return wl.flops(A), alg_bytes
+
+
+def layer_roofline(flops, alg_bytes, ms, peaks):
+    """The whole layer against both roofs: algorithmic bytes over the HBM copy
+    peak, FLOPs over the bf16 burst peak."""
+    gbs = alg_bytes / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    return {"gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "tflops": round(tfs, 2), "frac_of_bf16_burst": round(tfs / peaks["bf16_tflops"], 4)}
+
+
+def time_layer(args, wl, d, device, world, headline):
+    """Times moe_forward on one workload: K steps (L2 flush + layer forward)
+    captured into one CUDA graph and replayed once, step times from CUDA events
+    the library records at each step's start and end. With headline, also the
+    eager pass and the per-rank aggregation of the JSON line's main value."""
     from expert_moe_layer_gb300 import binding as B
-    B.lib()
-    torch.cuda.set_device(device)
     peaks = load_peaks()
-    d = device_layer(wl, device)
     cfg = cfg_of(wl)
     T, H = wl.T, wl.H
     ws = torch.empty(B.workspace_size(cfg, T), dtype=torch.uint8, device=device)
@@ -210,14 +281,14 @@ def run_ours(args, wl, rank, world, device):
     stream = torch.cuda.current_stream(device)
 
     def fwd(events=None):
-        st = torch.cuda.current_stream(device)
         if events is None:
             B.moe_forward(cfg, T, d["x"], d["router_w"], d["router_b"], d["w13"], d["w2"],
-                          d["shared_w13"], d["shared_w2"], None, out, ws, st)
+                          d["shared_w13"], d["shared_w2"], None, out, ws,
+                          torch.cuda.current_stream(device))
             return 0
         return B.moe_forward_timed(cfg, T, d["x"], d["router_w"], d["router_b"], d["w13"],
                                    d["w2"], d["shared_w13"], d["shared_w2"], None, out, ws,
-                                   events, st)
+                                   events, torch.cuda.current_stream(device))
 
     for _ in range(args.warmup):
         flush()
@@ -225,7 +296,7 @@ def run_ours(args, wl, rank, world, device):
     torch.cuda.synchronize(device)
     rc, flags = B.moe_get_status(ws, stream)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} after warm-up")
+        raise RuntimeError(f"{wl.name}: device status {rc} flags {flags:#x} after warm-up")
 
     # routing statistics of this batch (for the algorithmic work counts)
     lay = B.workspace_layout(cfg, T)
@@ -241,15 +312,17 @@ def run_ours(args, wl, rank, world, device):
                 ev.record(stream)
         return evs
 
-    # Eager pass (host launches every kernel): a secondary number.
-    eager_ev = new_events(args.steps)
-    torch.cuda.synchronize(device)
-    for i in range(args.steps):
-        flush()
-        fwd(eager_ev[i])
-    torch.cuda.synchronize(device)
-    eager_ms = statistics.mean(eager_ev[i][0].elapsed_time(eager_ev[i][7])
-                               for i in range(args.steps))
+    eager_ms = None
+    if headline:
+        # Eager pass (host launches every kernel): a secondary number.
+        eager_ev = new_events(args.steps)
+        torch.cuda.synchronize(device)
+        for i in range(args.steps):
+            flush()
+            fwd(eager_ev[i])
+        torch.cuda.synchronize(device)
+        eager_ms = statistics.mean(eager_ev[i][0].elapsed_time(eager_ev[i][7])
+                                   for i in range(args.steps))
 
     def capture(evs):
         g = torch.cuda.CUDAGraph()
@@ -293,7 +366,7 @@ def run_ours(args, wl, rank, world, device):
         clocks["untimed_replays"] = extra
     rc, flags = B.moe_get_status(ws, stream)
     if rc != 0:
-        raise RuntimeError(f"device status {rc} flags {flags:#x} in the timed region")
+        raise RuntimeError(f"{wl.name}: device status {rc} flags {flags:#x} in the timed region")
     del graph
 
     # Per-stage breakdown (and the dominant kernel's live duration): a second
@@ -307,89 +380,95 @@ def run_ours(args, wl, rank, world, device):
     def span(a, b):
         return [sevents[i][a].elapsed_time(sevents[i][b]) for i in range(args.steps)]
 
-    total_ms, tokens_per_s = aggregate_over_ranks(sum(step_ms), T, args.steps, world, device)
+    if headline:
+        total_ms, tokens_per_s = aggregate_over_ranks(sum(step_ms), T, args.steps, world,
+                                                      device)
+    else:
+        total_ms = sum(step_ms)
+        tokens_per_s = T * args.steps / (total_ms / 1e3)
     stage_names = ["route", "align", "tiles_gather", "gemm1_silu", "gemm2", "shared", "combine"]
     stages = {n: statistics.mean(span(i, i + 1)) for i, n in enumerate(stage_names)}
     ms_per_step = total_ms / args.steps
-
-    # algorithmic work per step
-    rb = 2 if wl.router == "bf16" else 4
-    eb = 2 if wl.act == "bf16" else 4
-    flops = wl.flops(A)
-    alg_bytes = (touched * 3 * wl.H * wl.I * eb + wl.E * wl.H * rb
-                 + wl.n_shared * 3 * wl.H * wl.I_shared * eb + 2 * T * wl.H * eb)
-
-    # dominant kernel: GEMM1 (gate/up, SiLU epilogue), or for decode-sized
-    # batches the fused kernel that runs GEMM1 and GEMM2 together
+    flops, alg_bytes = layer_work(wl, A, touched)
     plan = B.forward_plan(cfg, T)
-    w13_bytes = touched * 2 * wl.I * wl.H * eb
-    w2_bytes = touched * wl.H * wl.I * eb
-    if plan.fused_mlp:
-        kname, ksrc = "moe_mlp_fused (GEMM1 + GEMM2)", "kernels_mlp_fused.cu"
-        k_ms = stages["gemm1_silu"]
-        k_flops = 6 * A * wl.H * wl.I
-        # weights once; x rows in, h out and back in, y out
-        k_bytes = w13_bytes + w2_bytes + (2 * A * wl.H + 2 * A * wl.I) * eb
-    else:
-        kname, ksrc = (("moe_gemm_pair<SiLU> (GEMM1, CTA pairs)", "kernels_gemm_pair.cu")
-                       if plan.cta_pairs else
-                       ("moe_gemm_tc<SiLU> (GEMM1)", "kernels_gemm.cu"))
-        k_ms = stages["gemm1_silu"]
-        k_flops = 4 * A * wl.H * wl.I
-        k_bytes = w13_bytes + A * wl.H * eb + A * wl.I * eb
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    tensor_bound = k_flops / max(k_bytes, 1) >= ridge
-    if tensor_bound:
-        ach = k_flops / (k_ms / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4),
-                "peak_basis": f"{peaks['source']} bf16 sustained (kernel timed inside a long step)",
-                "frac_of_burst": round(ach / peaks["bf16_tflops"], 4)}
-    else:
-        ach = k_bytes / (k_ms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_basis": f"{peaks['source']} HBM copy",
-                "frac_of_nominal_8TBs": round(ach / 8000.0, 4)}
-    roof.update({"kernel": kname, "ms_per_launch": round(k_ms, 4),
-                 "algorithmic_flops": k_flops, "algorithmic_bytes": k_bytes,
-                 "traffic": traffic_from_profile(wl.name, ksrc)})
+    roof = dominant_kernel_roofline(wl, plan, A, touched, stages["gemm1_silu"], peaks)
     path = {f: getattr(plan, f) for f, _ in B.Plan._fields_}
-
-    # end to end through the public API with host buffers
     e2e = run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world, alg_bytes)
-
     res = {
-        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.act == "bf16" else "f32",
-        "data": DATA,
-        "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
-                   "E_local": El, "shared_experts": wl.n_shared, "ep": [wl.ep_size, wl.ep_rank],
-                   "assignments": A, "experts_touched": touched,
-                   "l2": f"flushed before every step, outside the timed events: a "
-                         f"{L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 20} "
-                         "MiB read so that no dirty flush lines are written back inside "
-                         "the step",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "value": round(tokens_per_s, 1), "unit": "tokens/s",
+        "ms_per_step": round(ms_per_step, 4),
         "tflops": round(flops / (ms_per_step / 1e3) / 1e12, 2),
         "gbs": round(alg_bytes / (ms_per_step / 1e3) / 1e9, 1),
+        "layer_roofline": layer_roofline(flops, alg_bytes, ms_per_step, peaks),
+        "roofline": roof,
+        "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "K": wl.K,
+                   "E_local": El, "shared_experts": wl.n_shared,
+                   "ep": [wl.ep_size, wl.ep_rank], "assignments": A,
+                   "experts_touched": touched},
         "alg_flops_per_step": flops, "alg_bytes_per_step": alg_bytes,
         "stages_ms": {k: round(v, 4) for k, v in stages.items()},
-        "timing": "one CUDA graph of the K steps replayed once; step times from CUDA events "
-                  "the library records at each step's start and end; stage times from a "
-                  "second graph with events at every stage boundary",
         "staged_ms_per_step": round(statistics.mean(span(0, 7)), 4),
-        "eager_ms_per_step": round(eager_ms, 4),
-        "roofline": roof,
         "path": path,
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if eager_ms is not None:
+        res["eager_ms_per_step"] = round(eager_ms, 4)
     return res
+
+
+L2_NOTE = (f"flushed before every step, outside the timed events: a {L2_FLUSH_BYTES >> 20} "
+           f"MiB write, then a {L2_FLUSH_BYTES >> 20} MiB read so that no dirty flush lines "
+           "are written back inside the step")
+TIMING_NOTE = ("one CUDA graph of the K steps replayed once; step times from CUDA events "
+               "the library records at each step's start and end; stage times from a "
+               "second graph with events at every stage boundary")
+
+
+def run_ours(args, wl, rank, world, device):
+    from expert_moe_layer_gb300 import binding as B
+    B.lib()
+    torch.cuda.set_device(device)
+    d = device_layer(wl, device)
+    r = time_layer(args, wl, d, device, world, headline=True)
+    del d
+    res = {
+        "metric": METRIC, "value": r["value"], "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.act == "bf16" else "f32",
+        "data": DATA,
+        "config": {**r["config"], "l2": L2_NOTE,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "timing": TIMING_NOTE,
+    }
+    res.update({k: v for k, v in r.items() if k not in res})
+    return res
+
+
+def extra_workloads(args, headline, device):
+    """The other workloads of the layer, each timed as the headline one (graph
+    of K steps, L2 flushed outside the events), on this GPU. The decode sizes
+    share one set of weights."""
+    out = {}
+    decode_d = None
+    for name in EXTRA_WORKLOADS:
+        if name == headline:
+            continue
+        wl = WORKLOADS[name]
+        if name.startswith("qwen3_decode_T"):
+            if decode_d is None:
+                decode_d = device_layer(WORKLOADS[EXTRA_WORKLOADS[-1]], device)
+            d = dict(decode_d)
+            d["x"] = decode_d["x"][:wl.T].contiguous()
+        else:
+            d = device_layer(wl, device)
+        r = time_layer(args, wl, d, device, 1, headline=False)
+        del d
+        torch.cuda.empty_cache()
+        out[name] = r
+    return out
 
 
 def run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world, step_bytes):
@@ -698,6 +777,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["ep_dispatch"],
                     default="mixtral_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only --workload (by default rank 0 of a 1-GPU run also times "
+                         "the other workloads and reports them under 'workloads')")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -721,6 +803,8 @@ def main():
     device = torch.device("cuda", local_rank)
     res = run_ours(args, wl, rank, world, device)
     if rank == 0:
+        if world == 1 and not args.no_extra:
+            res["workloads"] = extra_workloads(args, wl.name, device)
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(res), flush=True)

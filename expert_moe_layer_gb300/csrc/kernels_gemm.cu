@@ -413,13 +413,9 @@ template <int MODE, bool TF32, typename TOut, int NMAX>
 cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
   using S = GemmShape<MODE, NMAX, sizeof(TOut) == 2>;
   auto kern = moe_gemm_tc<MODE, TF32, TOut, NMAX>;
-  static bool configured = false;  // per process; attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), S::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(num_sms), dim3(kThreads), S::kSmemBytes, st, *a.mapA, *a.mapB,
                     a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
                     a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),

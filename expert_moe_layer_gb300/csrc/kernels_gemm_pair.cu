@@ -457,13 +457,9 @@ template <int MODE, int NMAX>
 cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
   using S = PairShape<MODE, NMAX>;
   auto kern = moe_gemm_pair<MODE, NMAX>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         S::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), S::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((num_sms / 2) * 2);
   cfg.blockDim = dim3(kThreads);

@@ -471,13 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t mlp_fused_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(moe_mlp_fused,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
+  const cudaError_t e =
+      opt_in_smem(reinterpret_cast<const void*>(moe_mlp_fused), kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups || a.ks1 < 1 ||
       a.ks1 > kMaxSplit || (a.ks1 > 1 && (!a.part || !a.split_cnt)))
     return cudaErrorInvalidValue;

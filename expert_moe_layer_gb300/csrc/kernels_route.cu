@@ -534,13 +534,9 @@ cudaError_t logits_launch(const void* x, const void* wg, float* logits, int T, i
   if (E <= 32) {
     auto kern = router_logits_split_kernel<TX, TW>;
     constexpr int kSmem = split_smem_bytes<TX>();
-    static bool configured = false;
-    if (!configured) {
-      cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      configured = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), kSmem, smem_set);
+    if (e != cudaSuccess) return e;
     // two CTAs per SM over (slices x token groups x expert octets)
     const long slices = router_split_slabs(H), octets = (E + 7) / 8;
     const long batches = (T + split_batch<TX>() - 1) / split_batch<TX>();
@@ -580,13 +576,9 @@ template <typename TX, typename TW, int VPL>
 cudaError_t route_align_launch(const RouteAlignArgs& a, cudaStream_t st) {
   using S = RouteSmem<TX, TW>;
   auto kern = route_align_small_kernel<TX, TW, VPL>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
+  const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), S::kBytes, smem_set);
+  if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((a.E + 7) / 8, (a.T + kRouteTokBlock - 1) / kRouteTokBlock),
                     dim3(1024), S::kBytes, st, static_cast<const TX*>(a.x),
                     static_cast<const TW*>(a.wg), a.bias, a.T,

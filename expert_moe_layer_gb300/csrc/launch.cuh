@@ -16,6 +16,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 namespace moe {
@@ -51,6 +52,23 @@ inline thread_local long g_kernel_launches = 0;
 
 inline cudaError_t counted(cudaError_t e) {
   if (e == cudaSuccess) ++g_kernel_launches;
+  return e;
+}
+
+// Allow a kernel more than 48 KB of dynamic shared memory on the current
+// device. Function attributes belong to each device's context, so `done` (one
+// per kernel) records the device ordinals already set, one bit each; an
+// ordinal past 63 is set on every call. Two host threads that race here both
+// set the attribute, which is harmless.
+inline cudaError_t opt_in_smem(const void* kern, int bytes,
+                               std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
 

@@ -972,24 +972,18 @@ static __device__ __align__(256) unsigned char moe_align_noalloc_scratch
 
 namespace {
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {};
-
-// Device address of the static scratch on the current device. The host-side
-// name of the array is only a stand-in, so the address is looked up once per
-// device with that device current.
+// Device address of the static scratch in the current context. The host-side
+// name of the array is only a stand-in, so the address is looked up with the
+// caller's device current, on every call: a cached address would go stale
+// once the module is loaded again (after cudaDeviceReset, or in another
+// context made current on the same device). The lookup allocates nothing;
+// the first one in a context loads the library's device code, which is why
+// that first call belongs before any stream capture.
 int noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, moe_align_noalloc_scratch) != cudaSuccess || !p)
-      return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, moe_align_noalloc_scratch) != cudaSuccess || !p)
+    return MOE_ERR_CUDA;
+  *out = p;
   return MOE_OK;
 }
 

@@ -225,9 +225,11 @@ int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
  *     that (T, top_k, E_local) need, moe_align_workspace_size(cfg, T), exceeds
  *     MOE_ALIGN_NOALLOC_SCRATCH_BYTES. At 256 local experts that is about
  *     260k (token, slot) items.
- *   - The first call on each device looks up the array's device address once
- *     (cudaGetSymbolAddress with that device current). Make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress with the caller's device current), so an address
+ *     never outlives a cudaDeviceReset or a context switch. The first lookup
+ *     in a context loads the library's device code: make the first call on
+ *     each device before any stream capture.
  *   - All calls share the one array, and it keeps the last call's contents.
  *     Each call clears the status word it uses, and every count it reads is
  *     rewritten first. Calls that can overlap on the GPU (different streams

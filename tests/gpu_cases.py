@@ -142,6 +142,23 @@ def sample_tokens(T, n=64):
     return np.unique(np.linspace(0, T - 1, n).astype(np.int64))
 
 
+def tile_edge_tokens(c: DeviceCase, tile_rows: int) -> np.ndarray:
+    """Tokens that own the first and the last item of every tile of every
+    expert segment, for tiles of tile_rows rows laid from each segment's start
+    (the routed GEMMs' tile table on moe_forward's unpadded segments). A
+    tile-table or out-of-bounds TMA mistake shows in exactly these rows: a
+    segment's ragged last tile and the first tile after a segment boundary."""
+    counts, offsets, sorted_ids, _ = c.oracle_align(1)
+    K = c.wl.K
+    toks = set()
+    for e in range(len(counts)):
+        s, n = int(offsets[e]), int(counts[e])
+        for r0 in range(s, s + n, tile_rows):
+            toks.add(int(sorted_ids[r0]) // K)
+            toks.add(int(sorted_ids[min(r0 + tile_rows, s + n) - 1]) // K)
+    return np.array(sorted(toks), dtype=np.int64)
+
+
 def check_forward(c: DeviceCase, tokens=None):
     wl = c.wl
     out, ws = c.forward()

@@ -61,3 +61,51 @@ def test_committed_profiles_name_existing_sources_and_leave_clocks_alone():
         text = open(os.path.join(ROOT, "profiles", fn)).read()
         for cmd in re.findall(r"^ncu [^\n]*(?:\\\n[^\n]*)*", text, flags=re.M):
             assert "--clock-control none" in cmd, (fn, cmd)
+
+
+def test_tensor_bound_roofline_takes_the_burst_peak():
+    """The dominant kernel runs inside a timed region of milliseconds, so a
+    tensor-bound fraction is taken against the burst bf16 peak; the sustained
+    fraction is a secondary key. An HBM-bound kernel is taken against the copy
+    peak."""
+    import synth
+
+    class Plan:
+        fused_mlp, cta_pairs = 0, 1
+
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0,
+             "source": "measured"}
+    wl = synth.MIXTRAL
+    A, touched = 8192, 8
+    flops = 4 * A * wl.H * wl.I
+    k_ms = flops / 1.5e15 * 1e3          # 1500 TFLOP/s
+    r = bench.dominant_kernel_roofline(wl, Plan, A, touched, k_ms, peaks)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0
+    assert abs(r["frac"] - 0.75) < 1e-3 and abs(r["frac_of_sustained"] - 0.9375) < 1e-3
+
+    class Fused:
+        fused_mlp, cta_pairs = 1, 0
+
+    wl = synth.QWEN_DECODE.with_(T=8)
+    A, touched = 64, 36
+    r = bench.dominant_kernel_roofline(wl, Fused, A, touched, 0.05, peaks)
+    assert r["bound"] == "hbm" and r["peak"] == 6000.0
+    want = (touched * 3 * wl.H * wl.I * 2 + (2 * A * wl.H + 2 * A * wl.I) * 2) / 0.05e-3 / 1e9
+    assert abs(r["achieved"] - want) < 0.1
+
+
+def test_layer_roofline_and_extra_workload_list():
+    import synth
+    wl = synth.QWEN_DECODE.with_(T=8)
+    flops, nbytes = bench.layer_work(wl, 64, 36)
+    assert nbytes == 36 * 3 * 2048 * 512 * 2 + 256 * 2048 * 2 + 2 * 8 * 2048 * 2
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    r = bench.layer_roofline(flops, nbytes, 0.05, peaks)
+    assert abs(r["frac_of_hbm"] - nbytes / 0.05e-3 / 6e12) < 1e-4
+    # every configured workload except the tiny parity case is timed in one run,
+    # the decode sizes last with the largest T (whose weights they share) last
+    names = set(bench.EXTRA_WORKLOADS)
+    assert names == {n for n in bench.WORKLOADS if n != "tiny"}
+    dec = [n for n in bench.EXTRA_WORKLOADS if n.startswith("qwen3_decode_T")]
+    assert bench.EXTRA_WORKLOADS[-len(dec):] == dec
+    assert dec[-1] == f"qwen3_decode_T{max(synth.DECODE_TOKENS)}"

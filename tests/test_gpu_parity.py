@@ -16,7 +16,7 @@ from expert_moe_layer_gb300 import binding as B
 from oracle import moe_oracle as O
 
 from gpu_cases import (ATOL, RTOL, W_ATOL, W_RTOL, DeviceCase, assert_close, check_forward,
-                       sample_tokens, ws_views)
+                       sample_tokens, tile_edge_tokens, ws_views)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,8 +114,25 @@ def test_forward_decode_full_shape(T):
 
 @pytest.mark.parametrize("name", list(FULL))
 def test_forward_full_size_sampled(name):
+    """Full-size layers, run as bench.py runs them: every routing and
+    permutation array in full, and the output rows of 64 evenly spaced tokens
+    plus every token that owns the first or last item of a GEMM tile (128-row
+    steps inside each expert segment: the single-CTA tile, or each CTA's half
+    of a 256-row pair tile), so that every tile of every segment has compared
+    rows, its ragged end included."""
     c = case(name)
-    check_forward(c, tokens=sample_tokens(c.wl.T))
+    plan = B.forward_plan(c.cfg, c.wl.T)
+    step = min(plan.tile_rows, 128)
+    edges = tile_edge_tokens(c, step)
+    tokens = np.union1d(sample_tokens(c.wl.T), edges)
+    counts, offsets, sorted_ids, _ = c.oracle_align(1)
+    chosen = np.isin(np.arange(c.wl.T), tokens)
+    for e in range(len(counts)):
+        s, n = int(offsets[e]), int(counts[e])
+        for r0 in range(s, s + n, step):
+            rows = sorted_ids[r0:min(r0 + step, s + n)] // c.wl.K
+            assert chosen[rows].any(), (name, e, r0)
+    check_forward(c, tokens=tokens)
 
 
 # ------------------------------------------------------------------ components
