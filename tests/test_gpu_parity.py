@@ -62,6 +62,15 @@ SMALL = {
     "sigmoid_select_wide": W("sigmoid_select_wide", T=300, H=256, I=256, E=32, K=4,
                              router_bias=True, bias_mode="select", scoring="sigmoid",
                              renormalize=False),
+    # batches of up to 16 tokens run the one-kernel decode layer: group-limited
+    # sigmoid scores with the selection-only correction, no renormalisation,
+    # rsf; the largest hidden size it takes (token rows of 128 KB in shared
+    # memory, five pipeline stages) at 16 tokens; an odd number of slices
+    "decode_grouped_select": W("decode_grouped_select", T=7, H=256, I=256, E=64, K=6,
+                               n_group=8, topk_group=4, rsf=2.5, router_bias=True,
+                               bias_mode="select", scoring="sigmoid", renormalize=False),
+    "decode_wide_hidden": W("decode_wide_hidden", T=16, H=4096, I=384, E=16, K=4,
+                            router_bias=True),
     # two shared experts over T >= 512 tokens: dense tiles on CTA pairs, ragged last tile
     "shared_pairs": W("shared_pairs", T=600, H=256, I=256, E=16, K=2, n_shared=2,
                       I_shared=384),
@@ -81,6 +90,8 @@ SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmo
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
                "grouped_decode", "ep_decode", "ep_tiny", "wide_router")
+DECODE = ("single_token", "ep_tiny", "wide_router", "decode_grouped_select",
+          "decode_wide_hidden")
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
     "deepseek_v2_prefill": synth.DEEPSEEK,
@@ -323,6 +334,15 @@ def test_zero_tokens_is_noop_and_repeat_calls_agree():
     assert torch.equal(a, b)        # deterministic: no atomics in the reductions
 
 
+def test_decode_layer_repeat_calls_agree():
+    """The one-kernel decode layer sums its fp32 partials in a fixed order, so
+    repeat calls give the same bits."""
+    c = case("decode_grouped_select")
+    a, _ = c.forward()
+    b, _ = c.forward()
+    assert torch.equal(a, b)
+
+
 def test_skewed_single_expert_segment():
     """Nearly all tokens choose expert 0 first: one long segment, many short or
     empty ones. (A much larger bias would leave the other experts' weights in
@@ -341,7 +361,8 @@ def test_skewed_single_expert_segment():
     check_forward(c)
 
 
-@pytest.mark.parametrize("name", ["ragged_decode", "grouped_shared", "fused_decode"])
+@pytest.mark.parametrize("name", ["ragged_decode", "grouped_shared", "fused_decode",
+                                  "decode_grouped_select"])
 def test_forward_captured_in_cuda_graph_matches_eager(name):
     """moe_forward enqueues only stream work (no host sync, no allocation), so
     it can be captured once and replayed; replays must equal the eager call."""
@@ -364,7 +385,8 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
     assert B.moe_get_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED])
+@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED,
+                                  *DECODE])
 def test_plan_matches_the_kernels_launched(name):
     """moe_forward_plan (host only) names the path; moe_forward_timed counts
     the kernels that path launched. The fused cases must take the fused
@@ -376,6 +398,7 @@ def test_plan_matches_the_kernels_launched(name):
         assert plan.fused_mlp == 1 and plan.tile_rows == 32
     if name in ROUTE_FUSED:
         assert plan.fused_route == 1
+    assert plan.decode_layer == (1 if name in DECODE else 0)
     if name in ("pair_prefill", "ragged_prefill"):
         assert plan.fused_route == 0 and plan.align_kernels == 1
     ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
