@@ -214,15 +214,7 @@ def dominant_kernel_roofline(wl, plan, A, touched, k_ms, peaks):
     eb = 2 if wl.act == "bf16" else 4
     w13_bytes = touched * 2 * wl.I * wl.H * eb
     w2_bytes = touched * wl.H * wl.I * eb
-    if getattr(plan, "decode_layer", 0):
-        kname, ksrc = "moe_decode_layer (routing + GEMM1 + GEMM2)", "kernels_decode.cu"
-        rb = 2 if wl.router == "bf16" else 4
-        k_flops = 6 * A * wl.H * wl.I + 2 * wl.T * wl.H * wl.E
-        # weights once, router, x in; the weighted fp32 partial of every
-        # (local item, 64-index slice) out, logits out and back in
-        k_bytes = (w13_bytes + w2_bytes + wl.E * wl.H * rb + wl.T * wl.H * eb
-                   + A * (wl.I // 64) * wl.H * 4 + 2 * wl.T * wl.E * 4)
-    elif plan.fused_mlp:
+    if plan.fused_mlp:
         kname, ksrc = "moe_mlp_fused (GEMM1 + GEMM2)", "kernels_mlp_fused.cu"
         k_flops = 6 * A * wl.H * wl.I
         # weights once; x rows in, h out and back in, y out

@@ -23,7 +23,6 @@ LIB = os.path.join(PKG, "libmoe.so")
 STAMP = LIB + ".stamp"
 
 SOURCES = ["moe_api.cu", "kernels_gemm.cu", "kernels_gemm_pair.cu", "kernels_mlp_fused.cu",
-           "kernels_decode.cu",
            "kernels_route.cu", "kernels_align.cu"]
 HEADERS = ["ptx.cuh", "internal.h", "launch.cuh", "align_block.cuh", "topk_warp.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -179,44 +179,6 @@ struct MlpFusedArgs {
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st);
 size_t mlp_fused_smem_bytes();
 
-// The routed layer of a decode-sized batch (T <= kDecodeMaxTokens) in one
-// persistent kernel: router logits, grid barrier, per-CTA top-k, then units
-// of (touched expert, 64 intermediate indices) running GEMM1 and GEMM2 back to
-// back on the token rows held in shared memory, writing weighted fp32
-// partials [T*K, I/64, H]; then a combine kernel sums them per token. Also
-// writes ids, w and the align arrays (block_m 1). grid_bar must be zero
-// before the launch. bf16 activations and router, no shared experts.
-constexpr int kDecodeMaxTokens = 16;
-constexpr int kDecodeMaxItems = 512;
-constexpr int kDecodeMaxLocal = 1024;
-constexpr int kDecodeMaxHidden = 4096;
-struct DecodeArgs {
-  const CUtensorMap* mapX;    // x [T, H], box 64 x 16 (rows past T read as zero)
-  const CUtensorMap* mapW13;  // [E_l*2I, H], box 64 x 64
-  const CUtensorMap* mapW2;   // [E_l*H, I], box 64 x 128
-  const void* wg;             // router [E, H] bf16
-  const float* bias;          // [E] or null
-  int T, E, H, I, K, renorm, flags, n_group, topk_group;
-  float rsf;
-  float* logits;              // [T, E]
-  int* grid_bar;
-  int32_t* ids;               // [T, K]
-  float* w;                   // [T, K]
-  const int32_t* emap;
-  int R, E_l, ep_start;
-  float* part;                // decode_part_floats(T, K, H, I) floats
-  int32_t* counts;
-  int32_t* offsets;
-  int32_t* sorted_ids;        // cap = T*K
-  int32_t* inv_pos;
-  void* out;                  // [T, H] bf16
-  unsigned* status;
-};
-bool decode_layer_ok(int T, int E, int H, int I, int K, int E_l);
-size_t decode_part_floats(int T, int K, int H, int I);
-cudaError_t launch_decode_layer(const DecodeArgs& a, int num_sms, cudaStream_t st);
-cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t st);
-
 // Expert-parallel dispatch: dest[i] = ids[i] / n_local (-1 outside [0, E)),
 // then, after an align over the destination ranks, the send buffers in
 // destination order (row r = item sorted_ids[r], rows_dev[0] valid rows).

@@ -139,21 +139,10 @@ long max_routed_tiles(const moe_config* c, int T) {
   return routed_tile_bound(static_cast<long>(T) * c->top_k, n_local(c), routed_nmax(c, T));
 }
 
-// Batches of at most 16 tokens (bf16, bf16 router, no shared experts) run the
-// whole routed layer, routing included, in one persistent kernel plus a
-// combine kernel.
-bool decode_path(const moe_config* c, int T) {
-  return c->act_dtype == MOE_BF16 && c->router_dtype == MOE_BF16 &&
-         c->num_shared_experts == 0 &&
-         decode_layer_ok(T, c->num_experts, c->hidden_size, c->intermediate_size, c->top_k,
-                         n_local(c));
-}
-
-// Other decode-sized bf16 batches (32-token tiles) run both routed GEMMs in
-// one persistent kernel on the gathered token rows.
+// Decode-sized bf16 batches (32-token tiles) run both routed GEMMs in one
+// persistent kernel that gathers its token rows from x itself.
 bool mlp_fused(const moe_config* c, int T) {
-  return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && n_local(c) <= 1024 &&
-         !decode_path(c, T);
+  return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && n_local(c) <= 1024;
 }
 
 // Zeroed at the start of every call (one memset): the status word, the
@@ -339,7 +328,7 @@ MlpLayout mlp_layout(const moe_config* c, int T, int cap) {
 
 struct FwdLayout {
   size_t status, topk_ids, topk_w, logits, hist, counts, offsets, sorted_ids, inv_pos;
-  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, part1, part_dec, total;
+  size_t tiles, groups, x_perm, h_perm, y_perm, h_sh, y_sh, part1, total;
   int cap;
   SyncRegion sync;
 };
@@ -372,10 +361,6 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
   L.part1 = cv.take(gemm1_ksplit(c, T) > 1 ? sizeof(float) * gemm1_ksplit(c, T) * L.cap * 2 *
                                                  static_cast<size_t>(c->intermediate_size)
                                            : 0);
-  L.part_dec = cv.take(decode_path(c, T) ? sizeof(float) *
-                                               decode_part_floats(T, c->top_k, c->hidden_size,
-                                                                  c->intermediate_size)
-                                         : 0);
   L.total = cv.off;
   return L;
 }
@@ -813,20 +798,17 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   MOE_TRY(validate_T(T));
   if (!out) return MOE_ERR_INVALID_ARG;
   moe_plan p;
-  p.decode_layer = decode_path(cfg, T) ? 1 : 0;
-  p.fused_route = (p.decode_layer || route_align_small_ok(T, cfg->top_k, n_local(cfg))) ? 1 : 0;
+  p.fused_route = route_align_small_ok(T, cfg->top_k, n_local(cfg)) ? 1 : 0;
   p.router_tensor_cores = !p.fused_route && router_on_tensor_cores(cfg, T) ? 1 : 0;
   p.router_partials = p.fused_route ? 1 : router_ksplit(cfg, T);
   p.align_kernels =
       p.fused_route ? 0 : align_kernel_count(static_cast<long>(T) * cfg->top_k, n_local(cfg));
-  p.tile_rows = p.decode_layer ? kDecodeMaxTokens : routed_nmax(cfg, T);
-  p.fused_mlp = (p.decode_layer || mlp_fused(cfg, T)) ? 1 : 0;
-  p.gemm1_k_split = p.decode_layer ? 1 : gemm1_ksplit(cfg, T);
+  p.tile_rows = routed_nmax(cfg, T);
+  p.fused_mlp = mlp_fused(cfg, T) ? 1 : 0;
+  p.gemm1_k_split = gemm1_ksplit(cfg, T);
   p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
   p.kernels = 0;
-  if (T > 0 && p.decode_layer) {
-    p.kernels = 2;  // the decode layer kernel and its combine
-  } else if (T > 0) {
+  if (T > 0) {
     // logits + top-k and align (or the fused route kernel), the routed MLP
     // (fused kernel, or gather + GEMMs), shared GEMMs, combine
     p.kernels = (p.fused_route ? 1 : 2 + p.align_kernels) +
@@ -871,55 +853,6 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
 
   MOE_TRY(mark(0));
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.sync.bytes, st)));
-  if (decode_path(cfg, T) && !with_shared) {
-    // the whole routed layer in one kernel, then the combine
-    const int I = cfg->intermediate_size;
-    CUtensorMap mx, m13, m2;
-    if (!make_map(&mx, x, cfg->act_dtype, T, H, kDecodeMaxTokens) ||
-        !make_map(&m13, w13, cfg->act_dtype, static_cast<long>(El) * 2 * I, H, 64) ||
-        !make_map(&m2, w2, cfg->act_dtype, static_cast<long>(El) * H, I, 128))
-      return MOE_ERR_CUDA;
-    DecodeArgs a;
-    a.mapX = &mx;
-    a.mapW13 = &m13;
-    a.mapW2 = &m2;
-    a.wg = router_w;
-    a.bias = router_bias;
-    a.T = T;
-    a.E = cfg->num_experts;
-    a.H = H;
-    a.I = I;
-    a.K = K;
-    a.renorm = cfg->renormalize ? 1 : 0;
-    a.flags = route_flags(cfg);
-    a.n_group = cfg->use_grouped_topk ? cfg->num_expert_group : 0;
-    a.topk_group = cfg->use_grouped_topk ? cfg->topk_group : 0;
-    a.rsf = cfg->routed_scaling_factor;
-    a.logits = at<float>(ws, L.logits);
-    a.grid_bar = reinterpret_cast<int*>(status + 1);
-    a.ids = ids;
-    a.w = w;
-    a.emap = expert_map;
-    a.R = cfg->max_replicas;
-    a.E_l = El;
-    a.ep_start = cfg->ep_rank * El;
-    a.part = at<float>(ws, L.part_dec);
-    a.counts = counts;
-    a.offsets = offsets;
-    a.sorted_ids = sorted_ids;
-    a.inv_pos = inv_pos;
-    a.out = out;
-    a.status = status;
-    const int sms = sm_count();
-    if (sms <= 0) return MOE_ERR_CUDA;
-    for (int i = 1; i <= 3; ++i) MOE_TRY(mark(i));  // routing, align, gather: in-kernel
-    MOE_TRY(cuda_ok(launch_decode_layer(a, sms, st)));
-    for (int i = 4; i <= 6; ++i) MOE_TRY(mark(i));  // GEMM2 is in the same kernel
-    MOE_TRY(cuda_ok(launch_decode_combine(a, st)));
-    MOE_TRY(mark(7));
-    if (kernels) *kernels = static_cast<int>(g_kernel_launches - launches0);
-    return MOE_OK;
-  }
   if (route_align_small_ok(T, K, El)) {
     RouteAlignArgs a;
     a.x = x;

@@ -56,11 +56,17 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
                                           int E, int K, int renorm, int flags, int n_group,
                                           int topk_group, int32_t* __restrict__ ids_row,
                                           float* __restrict__ w_row) {
+  // A division per score would serialise this warp: the IEEE quotient takes a
+  // checked path per element, which costs some hundreds of cycles each on a
+  // single warp's dependency chain. Softmax divides by one reciprocal of the
+  // sum instead, the logistic uses the fast quotient; both agree with the
+  // IEEE quotients to a few ulp, far inside the routing weights' tolerance
+  // and below the score gaps the routing decisions see.
   if (flags & kRouteSigmoid) {
     // per-expert logistic in fp32
 #pragma unroll
     for (int j = 0; j < VPL; ++j)
-      p[j] = (lane + 32 * j < E) ? 1.0f / (1.0f + expf(-p[j])) : -CUDART_INF_F;
+      p[j] = (lane + 32 * j < E) ? __fdividef(1.0f, 1.0f + expf(-p[j])) : -CUDART_INF_F;
   } else {
     // softmax in fp32: max, exp, sum, divide
     float lmx = -CUDART_INF_F;
@@ -76,8 +82,9 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = 1.0f / sum;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] / sum : -CUDART_INF_F;
+    for (int j = 0; j < VPL; ++j) p[j] = (lane + 32 * j < E) ? p[j] * inv : -CUDART_INF_F;
   }
 
   // candidate keys: p + correction, or -inf outside the kept groups (group

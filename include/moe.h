@@ -407,9 +407,6 @@ typedef struct {
   int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */
   int fused_mlp;           /* 1: token gather, GEMM1 and GEMM2 in one
                               persistent kernel                               */
-  int decode_layer;        /* 1: batches of <= 16 tokens: routing, top-k,
-                              both GEMMs in one persistent kernel, then a
-                              combine kernel (kernels == 2)                   */
 } moe_plan;
 int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 

@@ -125,28 +125,17 @@ def test_forward_plan_per_workload():
     # route 2, align 1, gather + GEMM1 + GEMM2, combine
     assert p.kernels == 2 + 1 + 3 + 1
     assert p.fused_route == 0 and p.align_kernels == 1
-    # decode, up to 16 tokens: routing, top-k and both GEMMs in one kernel over
-    # all the batch's token rows, then the combine
-    for T in (1, 8, 16):
-        p = _plan(synth.QWEN_DECODE, T)
-        assert (p.decode_layer, p.tile_rows, p.fused_mlp, p.fused_route) == (1, 16, 1, 1)
-        assert (p.align_kernels, p.gemm1_k_split, p.cta_pairs) == (0, 1, 0)
-        assert p.kernels == 2
-    # decode above 16 tokens: routing and align in one kernel; 32-token tiles;
-    # gather, GEMM1 and GEMM2 in the fused kernel
-    for T in (17, 64):
+    # decode: routing and align in one kernel; 32-token tiles; gather, GEMM1
+    # and GEMM2 in the fused kernel; T=1 leaves few GEMM1 units, so GEMM1 is
+    # also split over K (finished inside the fused kernel)
+    for T in (8, 64):
         p = _plan(synth.QWEN_DECODE, T)
         assert (p.tile_rows, p.fused_mlp, p.gemm1_k_split, p.cta_pairs) == (32, 1, 1, 0)
         assert (p.fused_route, p.align_kernels, p.router_partials) == (1, 0, 1)
-        assert p.decode_layer == 0
         assert p.kernels == 1 + 2 + 1  # route+align, gather + fused MLP, combine
-    # the one-kernel decode layer needs a bf16 router and no shared experts;
-    # an fp32 router at T=1 takes the fused route and MLP kernels, GEMM1 split
-    # over K (few units)
-    p = _plan(synth.QWEN_DECODE.with_(router="f32"), 1)
-    assert p.decode_layer == 0 and p.fused_mlp == 1 and p.gemm1_k_split > 1
+    p = _plan(synth.QWEN_DECODE, 1)
+    assert (p.fused_mlp, p.tile_rows, p.fused_route) == (1, 32, 1) and p.gemm1_k_split > 1
     assert p.kernels == 1 + 2 + 1
-    assert _plan(synth.DEEPSEEK, 8).decode_layer == 0
     # the fused route kernel stops at 128 tokens
     assert _plan(synth.QWEN_DECODE, 128).fused_route == 1
     assert _plan(synth.QWEN_DECODE, 129).fused_route == 0

@@ -37,8 +37,8 @@ LIMITS = {
     "experts512_k32_warp_topk": W("experts512_k32_warp_topk", T=300, H=128, I=128, E=512,
                                   K=32, router_bias=True),
     "groups32": W("groups32", T=300, H=128, I=128, E=512, K=32, n_group=32, topk_group=8),
-    # the one-kernel decode layer at its item limit: 16 tokens x 32 slots over
-    # 512 experts, and the most groups
+    # decode-sized batches at the limits: 16 tokens x 32 slots over 512
+    # experts in the fused route kernel, and the most groups
     "decode_experts512_k32": W("decode_experts512_k32", T=16, H=128, I=128, E=512, K=32,
                                router_bias=True),
     "decode_groups32": W("decode_groups32", T=16, H=128, I=128, E=512, K=32, n_group=32,

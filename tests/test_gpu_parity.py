@@ -62,10 +62,9 @@ SMALL = {
     "sigmoid_select_wide": W("sigmoid_select_wide", T=300, H=256, I=256, E=32, K=4,
                              router_bias=True, bias_mode="select", scoring="sigmoid",
                              renormalize=False),
-    # batches of up to 16 tokens run the one-kernel decode layer: group-limited
+    # decode-sized batches on the fused route and MLP kernels: group-limited
     # sigmoid scores with the selection-only correction, no renormalisation,
-    # rsf; the largest hidden size it takes (token rows of 128 KB in shared
-    # memory, five pipeline stages) at 16 tokens; an odd number of slices
+    # rsf; a wide hidden size at 16 tokens
     "decode_grouped_select": W("decode_grouped_select", T=7, H=256, I=256, E=64, K=6,
                                n_group=8, topk_group=4, rsf=2.5, router_bias=True,
                                bias_mode="select", scoring="sigmoid", renormalize=False),
@@ -89,9 +88,8 @@ SMALL = {
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
-               "grouped_decode", "ep_decode", "ep_tiny", "wide_router")
-DECODE = ("single_token", "ep_tiny", "wide_router", "decode_grouped_select",
-          "decode_wide_hidden")
+               "grouped_decode", "ep_decode", "ep_tiny", "wide_router", "decode_grouped_select",
+               "decode_wide_hidden")
 FULL = {
     "mixtral_prefill": synth.MIXTRAL,
     "deepseek_v2_prefill": synth.DEEPSEEK,
@@ -334,9 +332,9 @@ def test_zero_tokens_is_noop_and_repeat_calls_agree():
     assert torch.equal(a, b)        # deterministic: no atomics in the reductions
 
 
-def test_decode_layer_repeat_calls_agree():
-    """The one-kernel decode layer sums its fp32 partials in a fixed order, so
-    repeat calls give the same bits."""
+def test_decode_repeat_calls_agree():
+    """The decode-sized path (fused route and MLP kernels, split GEMM1 sums in
+    a fixed order) gives the same bits on repeat calls."""
     c = case("decode_grouped_select")
     a, _ = c.forward()
     b, _ = c.forward()
@@ -385,8 +383,7 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
     assert B.moe_get_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED,
-                                  *DECODE])
+@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED])
 def test_plan_matches_the_kernels_launched(name):
     """moe_forward_plan (host only) names the path; moe_forward_timed counts
     the kernels that path launched. The fused cases must take the fused
@@ -398,7 +395,6 @@ def test_plan_matches_the_kernels_launched(name):
         assert plan.fused_mlp == 1 and plan.tile_rows == 32
     if name in ROUTE_FUSED:
         assert plan.fused_route == 1
-    assert plan.decode_layer == (1 if name in DECODE else 0)
     if name in ("pair_prefill", "ragged_prefill"):
         assert plan.fused_route == 0 and plan.align_kernels == 1
     ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
