@@ -24,7 +24,7 @@ STAMP = LIB + ".stamp"
 
 SOURCES = ["moe_api.cu", "kernels_gemm.cu", "kernels_gemm_pair.cu", "kernels_mlp_fused.cu",
            "kernels_route.cu", "kernels_align.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "launch.cuh", "align_block.cuh", "topk_warp.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "launch.cuh", "align_block.cuh", "topk_warp.cuh", "act.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I" + INCLUDE, "-I" + CSRC]

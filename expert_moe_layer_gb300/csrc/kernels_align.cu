@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 
 #include "align_block.cuh"
+#include "act.cuh"
 #include "internal.h"
 #include "launch.cuh"
 
@@ -352,7 +353,7 @@ __global__ void __launch_bounds__(256) silu_finalize_kernel(const float* __restr
     }
     float o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+    for (int i = 0; i < 8; ++i) o[i] = silu(g[i]) * u[i];
     st8(h + r * I + c, o);
   }
 }

@@ -29,6 +29,7 @@
 // stream past them.
 #include <cuda_bf16.h>
 
+#include "act.cuh"
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -78,7 +79,6 @@ __device__ __forceinline__ __nv_bfloat16 to_out<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 // Unit u -> (tile index, weight tile m). gstart (shared memory) holds the
 // first tile of each group and the total at [n_groups]; group g owns units
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float w[16];
             ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = silu_f(v[j]) * w[j];
+            for (int j = 0; j < 16; ++j) v[j] = silu(v[j]) * w[j];
           } else {
             ptx::tmem_ld16(tb + c0, v);
           }
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float w[16];
           ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = silu_f(v[j]) * w[j];
+          for (int j = 0; j < 16; ++j) v[j] = silu(v[j]) * w[j];
         } else {
           ptx::tmem_ld16(tb + c0, v);
         }

@@ -31,6 +31,7 @@
 // moe_gemm_tc: expert by expert.
 #include <cuda_bf16.h>
 
+#include "act.cuh"
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -72,7 +73,6 @@ struct PairShape {
   static_assert(NMAX % 32 == 0 && NMAX <= 256, "bad NMAX");
 };
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 __device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_groups, int m_tiles,
                                             int& tile, int& m) {
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float uj[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              sb[(j + t) * 64 + r64] = __float2bfloat16_rn(silu_f(v[j + t]) * uj[t]);
+              sb[(j + t) * 64 + r64] = __float2bfloat16_rn(silu(v[j + t]) * uj[t]);
           }
           __syncwarp();
           if (lane == 0) {

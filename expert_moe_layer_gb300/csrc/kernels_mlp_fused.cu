@@ -38,6 +38,7 @@
 // MMA issuer, warps 2..9 epilogue (two per TMEM lane quarter).
 #include <cuda_bf16.h>
 
+#include "act.cuh"
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
@@ -63,7 +64,6 @@ constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes;
 static_assert(kAccCols * kNAcc <= kTmemCols, "TMEM overflow");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
 __device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_groups, int m_tiles,
                                             int& tile, int& m) {
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ks1 == 1) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (c0 + j < tl.w) hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(v[j]) * w[j]);
+          if (c0 + j < tl.w) hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu(v[j]) * w[j]);
         publish_h(ready + ui.ti, lane);
         continue;
       }
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             up += us[s];
           }
         }
-        hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu_f(g) * up);
+        hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu(g) * up);
       }
       publish_h(ready + ui.ti, lane);
     }
