@@ -98,6 +98,7 @@ _SIGS = {
                                _SZ, _VP, ctypes.POINTER(ctypes.c_void_p),
                                ctypes.POINTER(ctypes.c_int)]),
     "moe_get_status": (_I, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "moe_forward_plan": (_I, [_CFG, _I, ctypes.POINTER(Plan)]),
     "moe_ep_dispatch_workspace_size": (_SZ, [_CFG, _I]),
     "moe_ep_dispatch": (_I, [_CFG, _I] + [_VP] * 11 + [_SZ, _VP]),
@@ -293,3 +294,9 @@ def moe_get_status(ws, stream=None) -> tuple[int, int]:
     flags = ctypes.c_uint32(0)
     rc = lib().moe_get_status(_p(ws), _stream(stream), ctypes.byref(flags))
     return rc, flags.value
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Time limit of the kernels' pipeline waits on the current device, in ns
+    (0 restores the default of 1 s)."""
+    _check("moe_set_wait_limit_ns", lib().moe_set_wait_limit_ns(int(ns)))

@@ -203,4 +203,11 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st, bool slots_early = false);
 
+// The pipeline-wait limit of each translation unit with bounded waits (ns of
+// %globaltimer), set on the current device.
+cudaError_t set_wait_limit_gemm(unsigned long long ns);
+cudaError_t set_wait_limit_gemm_pair(unsigned long long ns);
+cudaError_t set_wait_limit_mlp_fused(unsigned long long ns);
+cudaError_t set_wait_limit_route(unsigned long long ns);
+
 }  // namespace moe

@@ -458,4 +458,6 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
   return cudaErrorInvalidValue;
 }
 
+MOE_WAIT_LIMIT_SETTER(set_wait_limit_gemm)
+
 }  // namespace moe

@@ -493,4 +493,6 @@ cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num
   return cudaErrorInvalidValue;
 }
 
+MOE_WAIT_LIMIT_SETTER(set_wait_limit_gemm_pair)
+
 }  // namespace moe

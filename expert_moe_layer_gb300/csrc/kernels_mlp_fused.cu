@@ -130,11 +130,12 @@ __device__ __forceinline__ bool wait_count(const int* p, int target, volatile in
                                            unsigned* status) {
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = ptx::globaltimer();
+  const uint64_t limit = ptx::g_wait_limit_ns;
   for (uint32_t n = 1;; ++n) {
     if (ld_acquire(p) >= target) return true;
     if ((n & 15u) == 0) {
       if (*abort) return false;
-      if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) {
+      if (ptx::globaltimer() - t0 > limit) {
         *abort = 1;
         if (status) atomicOr(status, MOE_DEV_TIMEOUT);
         return false;
@@ -483,5 +484,7 @@ cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st
                     a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
                     static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y), a.status);
 }
+
+MOE_WAIT_LIMIT_SETTER(set_wait_limit_mlp_fused)
 
 }  // namespace moe

@@ -631,4 +631,6 @@ cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
   return cudaErrorInvalidValue;
 }
 
+MOE_WAIT_LIMIT_SETTER(set_wait_limit_route)
+
 }  // namespace moe

@@ -951,6 +951,16 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x, const void* r
                       expert_map, out, ws, ws_bytes, stream, events, kernels_launched);
 }
 
+int moe_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns ? ns : 1000000000ull;  // 0: the default, 1 s
+  cudaError_t (*const setters[])(unsigned long long) = {
+      set_wait_limit_gemm, set_wait_limit_gemm_pair, set_wait_limit_mlp_fused,
+      set_wait_limit_route};
+  for (auto set : setters)
+    if (set(v) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 int moe_get_status(const void* ws, void* stream, uint32_t* flags) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -15,8 +15,19 @@ namespace moe {
 namespace ptx {
 
 // Per-wait limit in ns of %globaltimer. A healthy wait in these kernels
-// lasts microseconds.
+// lasts microseconds. The pipeline waits read it from g_wait_limit_ns, which
+// moe_set_wait_limit_ns can shorten (to make a wait run out in a test); the
+// waits that let copies and MMAs land while a kernel unwinds keep this value.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// One copy per translation unit (internal linkage); every unit with pipeline
+// waits defines a setter with MOE_WAIT_LIMIT_SETTER, and moe_set_wait_limit_ns
+// calls them all.
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+#define MOE_WAIT_LIMIT_SETTER(fn)                                            \
+  cudaError_t fn(unsigned long long ns) {                                    \
+    return cudaMemcpyToSymbol(::moe::ptx::g_wait_limit_ns, &ns, sizeof(ns)); \
+  }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,17 +76,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `parity` to complete. Returns false (without waiting
-// further) once *abort is set, or after kWaitLimitNs, in which case it sets
+// further) once *abort is set, or after g_wait_limit_ns, in which case it sets
 // *abort and the timeout flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort, unsigned* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = g_wait_limit_ns;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit) {
         *abort = 1;
         if (status) atomicOr(status, MOE_DEV_TIMEOUT);
         return false;
@@ -279,11 +291,12 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, unsigned* status) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = g_wait_limit_ns;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit) {
         *abort = 1;
         if (status) atomicOr(status, MOE_DEV_TIMEOUT);
         return false;

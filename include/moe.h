@@ -410,6 +410,19 @@ typedef struct {
 } moe_plan;
 int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 
+/* Sets the time limit of the library's pipeline waits on the current device,
+ * in ns of the GPU's global timer; 0 restores the default of 1 s. No page
+ * counterpart: it exists so that a test can make a bounded device wait run
+ * out. Every wait on a barrier or a cross-CTA counter inside the kernels gives
+ * up after this limit; the kernel then sets MOE_DEV_TIMEOUT, lets its own
+ * copies and MMAs land (those waits keep 1 s), frees its tensor memory and
+ * exits, and moe_get_status returns MOE_ERR_TIMEOUT. Outputs of such a call
+ * are unusable. The setting applies to every kernel launched after this call
+ * returns (it synchronises with the device) until it is set again; a process
+ * with several host threads must not change it while others launch. Returns
+ * MOE_ERR_CUDA if a copy to the device fails. */
+int moe_set_wait_limit_ns(uint64_t ns);
+
 /* ------------------------------------------------------------------------ */
 /* Synchronises `stream` and reads the device status word at the start of
  * `ws`. Writes the raw MOE_DEV_* bits to *flags (nullable). Returns MOE_OK if
