@@ -285,6 +285,45 @@ def replica_maps(placement, ep_size: int, max_replicas: int):
     return maps
 
 
+def physical_map(placement, ep_size: int, n_local: int, max_replicas: int):
+    """Global replica map [E, R] of physical expert ids from a placement.
+
+    ``placement[e]`` lists (rank, local slot) of each replica of logical
+    expert e in the global replica order, as for ``replica_maps``. A rank that
+    sends tokens to the expert-holding ranks (the EP patch's ``_ep_forward``)
+    must know where every replica lives, so this map names each replica by its
+    physical id rank * n_local + slot (n_local weight slots per rank), padded
+    with -2. It is the placement the per-rank replica maps are cut from.
+    """
+    E = len(placement)
+    pmap = np.full((E, max_replicas), NO_REPLICA, dtype=np.int32)
+    for e, reps in enumerate(placement):
+        if not 1 <= len(reps) <= max_replicas:
+            raise ValueError("each expert needs 1..max_replicas replicas")
+        for j, (rank, slot) in enumerate(reps):
+            if not (0 <= rank < ep_size and 0 <= slot < n_local):
+                raise ValueError("replica outside the physical slots")
+            pmap[e, j] = rank * n_local + slot
+    return pmap
+
+
+def physical_ids(ids, pmap):
+    """Physical expert id of each (token, slot) item under a global replica
+    map: item (t, k) of logical expert e goes to replica t mod n_e of e's n_e
+    replicas, the reading ``local_slots`` takes for redundant experts."""
+    ids = np.asarray(ids)
+    pmap = np.asarray(pmap)
+    phys = np.empty_like(ids, dtype=np.int32)
+    for t in range(ids.shape[0]):
+        for k in range(ids.shape[1]):
+            row = pmap[ids[t, k]]
+            n = int(np.sum(row != NO_REPLICA))
+            if n == 0 or np.any(row[:n] == NO_REPLICA):
+                raise ValueError("a replica list must be a non-empty prefix of its row")
+            phys[t, k] = row[t % n]
+    return phys
+
+
 # ---------------------------------------------------------------------------
 # forward
 # ---------------------------------------------------------------------------
@@ -465,7 +504,7 @@ def weight_bytes_per_card(n_experts, intermediate, hidden, n_layers, elem_bytes)
 # ---------------------------------------------------------------------------
 # expert-parallel dispatch and combine (the rank-local halves of the exchange)
 # ---------------------------------------------------------------------------
-def ep_dispatch(x, topk_ids, topk_w, num_experts, ep_size):
+def ep_dispatch(x, topk_ids, topk_w, num_experts, ep_size, pmap=None, n_local=None):
     """Send buffers of one rank, ordered by destination rank.
 
     ep_fused_moe_patch.py ``_ep_forward`` step 2: every (token, slot) work
@@ -475,14 +514,23 @@ def ep_dispatch(x, topk_ids, topk_w, num_experts, ep_size):
     with ``argsort``, which leaves the order inside a destination open. Reading
     taken: a stable sort, so items keep ascending t*K + k order.
 
+    With redundant experts (MoEMixin ``num_redundant_experts``: physical vs
+    logical experts), ``pmap`` is the global replica map of ``physical_map``
+    and ``n_local`` the weight slots per rank: an item goes to the replica
+    ``physical_ids`` picks, dest = physical id // n_local, and the id sent is
+    the physical one, so the receiver's local slot is id - rank * n_local.
+
     Returns (counts [ep] int64, send_pos [T*K] int32 = each item's row in the
     send buffer, send_x [T*K, H], send_ids [T*K] int32, send_w [T*K] fp32,
     send_tok [T*K] int32).
     """
-    ids = np.asarray(topk_ids).reshape(-1)
-    w = np.asarray(topk_w, np.float32).reshape(-1)
     T, K = np.asarray(topk_ids).shape
-    n_local = num_experts // ep_size
+    if pmap is None:
+        ids = np.asarray(topk_ids).reshape(-1)
+        n_local = num_experts // ep_size
+    else:
+        ids = physical_ids(topk_ids, pmap).reshape(-1)
+    w = np.asarray(topk_w, np.float32).reshape(-1)
     dest = ids // n_local
     order = np.argsort(dest, kind="stable")
     counts = np.bincount(dest, minlength=ep_size).astype(np.int64)

@@ -621,6 +621,79 @@ def test_ep_dispatch_brute_force():
         np.testing.assert_array_equal(sx[row], x[t])
 
 
+def test_ep_dispatch_with_replicas_brute_force():
+    """Redundant experts in the token-dispatch form: each item goes to the rank
+    of replica t mod n_e of its expert (the local_slots reading), its physical
+    id travels in send_ids, and the items a rank receives are exactly those its
+    own replica map keeps, at the same slots."""
+    r = np.random.default_rng(31)
+    T, K, E, ep, n_local = 17, 3, 8, 2, 6
+    ids = np.stack([r.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    for t in range(0, T, 2):                  # expert 2 (three replicas) is hot
+        if 2 not in ids[t]:
+            ids[t, 0] = 2
+    w = r.random((T, K)).astype(np.float32)
+    x = r.standard_normal((T, 5))
+    pmap = O.physical_map(_PLACEMENT, ep, n_local, 3)
+    counts, pos, sx, sid, sw, stok = O.ep_dispatch(x, ids, w, E, ep, pmap, n_local)
+    lists = [[] for _ in range(ep)]
+    for t in range(T):
+        for k in range(K):
+            reps = _PLACEMENT[ids[t, k]]
+            rank, slot = reps[t % len(reps)]
+            lists[rank].append((t, k, rank * n_local + slot))
+    order = [it for l in lists for it in l]
+    assert list(counts) == [len(l) for l in lists]
+    for row, (t, k, phys) in enumerate(order):
+        assert pos[t * K + k] == row and sid[row] == phys and stok[row] == t
+        assert sw[row] == w[t, k]
+        np.testing.assert_array_equal(sx[row], x[t])
+    maps = O.replica_maps(_PLACEMENT, ep, 3)
+    offs = np.concatenate([[0], np.cumsum(counts)])
+    item_of_row = np.empty(T * K, dtype=np.int64)
+    item_of_row[pos] = np.arange(T * K)
+    for rank in range(ep):
+        loc = O.local_slots(ids, maps[rank])
+        mine = sorted((int(t), int(k)) for t, k in zip(*np.nonzero(loc >= 0)))
+        got = [divmod(int(item_of_row[q]), K) for q in range(offs[rank], offs[rank + 1])]
+        assert sorted(got) == mine
+        for q, (t, k) in zip(range(offs[rank], offs[rank + 1]), got):
+            assert sid[q] - rank * n_local == loc[t, k]
+    with pytest.raises(ValueError):
+        O.physical_map([[(0, 9)]], 1, 4, 1)     # a slot past the rank's slots
+
+
+def test_ep_dispatch_pipeline_with_replicas_equals_unsharded():
+    """All ranks route, dispatch to the replicas, exchange, run their physical
+    slots (each holding its logical expert's weights), return and combine: the
+    result equals the unsharded layer."""
+    d = _layer(T=1, H=12, I=10, E=8, S=1, seed=32, bias=True)
+    r = np.random.default_rng(33)
+    ep, n_local, K = 2, 6, 3
+    pmap = O.physical_map(_PLACEMENT, ep, n_local, 3)
+    slot_expert = [[0, 1, 2, 3, 5, 2], [4, 5, 6, 7, 2, 0]]   # rank 1 slot 5 unused
+    rank_x = [r.standard_normal((n, 12)) for n in (9, 6)]
+    sends = []
+    for x in rank_x:
+        ids, w, _ = O.route(x, d["router_w"], d["router_b"], top_k=K, renormalize=True)
+        sends.append(O.ep_dispatch(x, ids, w, 8, ep, pmap, n_local))
+    counts = [s[0] for s in sends]
+    recv = [O.ep_exchange([s[i] for s in sends], counts) for i in (2, 3, 4)]
+    outs = []
+    for rank in range(ep):
+        w13 = np.stack([d["w13"][e] for e in slot_expert[rank]])
+        w2 = np.stack([d["w2"][e] for e in slot_expert[rank]])
+        outs.append(O.ep_expert_compute(recv[0][rank], recv[1][rank], recv[2][rank], w13, w2,
+                                        rank * n_local))
+    back = [[counts[s][rank] for s in range(ep)] for rank in range(ep)]
+    ret = O.ep_exchange(outs, back)
+    for rank, x in enumerate(rank_x):
+        sh = O.expert_mlp(x, d["shared_w13"][0], d["shared_w2"][0])
+        got = O.ep_combine(ret[rank], sends[rank][1], K, 1.5, sh)
+        ref = _fwd(dict(d, x=x), top_k=K, rsf=1.5)
+        np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 def test_planted_ep_mistakes_are_caught():
     d = _layer(T=1, H=12, I=10, E=8, S=0, seed=24)
     r = np.random.default_rng(25)
