@@ -101,7 +101,7 @@ _SIGS = {
     "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "moe_forward_plan": (_I, [_CFG, _I, ctypes.POINTER(Plan)]),
     "moe_ep_dispatch_workspace_size": (_SZ, [_CFG, _I]),
-    "moe_ep_dispatch": (_I, [_CFG, _I] + [_VP] * 11 + [_SZ, _VP]),
+    "moe_ep_dispatch": (_I, [_CFG, _I] + [_VP] * 12 + [_SZ, _VP]),
     "moe_ep_expert_compute_workspace_size": (_SZ, [_CFG, _I]),
     "moe_ep_expert_compute": (_I, [_CFG, _I] + [_VP] * 7 + [_SZ, _VP]),
     "moe_ep_combine": (_I, [_CFG, _I] + [_VP] * 5 + [_SZ, _VP]),
@@ -208,9 +208,9 @@ def ep_dispatch_workspace_size(cfg, T) -> int:
 
 
 def moe_ep_dispatch(cfg, T, x, topk_ids, topk_w, send_counts, send_offsets, send_pos, send_x,
-                    send_ids, send_w, send_tok, ws, stream=None):
+                    send_ids, send_w, send_tok, ws, stream=None, phys_map=None):
     _check("moe_ep_dispatch", lib().moe_ep_dispatch(
-        ctypes.byref(cfg), T, _p(x), _p(topk_ids), _p(topk_w), _p(send_counts),
+        ctypes.byref(cfg), T, _p(x), _p(topk_ids), _p(topk_w), _p(phys_map), _p(send_counts),
         _p(send_offsets), _p(send_pos), _p(send_x), _p(send_ids), _p(send_w), _p(send_tok),
         _p(ws), _nbytes(ws), _stream(stream)))
 

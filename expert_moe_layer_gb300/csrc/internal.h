@@ -179,10 +179,14 @@ struct MlpFusedArgs {
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st);
 size_t mlp_fused_smem_bytes();
 
-// Expert-parallel dispatch: dest[i] = ids[i] / n_local (-1 outside [0, E)),
-// then, after an align over the destination ranks, the send buffers in
-// destination order (row r = item sorted_ids[r], rows_dev[0] valid rows).
+// Expert-parallel dispatch: the physical id of each item (the global id, or
+// with a global replica map [E, R] replica (i / K) mod n of the id's row,
+// -1 when invalid or outside [0, E_phys)) and dest[i] = phys[i] / n_local
+// (-1 when invalid); then, after an align over the destination ranks, the
+// send buffers in destination order (row r = item sorted_ids[r], rows_dev[0]
+// valid rows).
 cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32_t* dest,
+                           int32_t* phys, const int32_t* phys_map, int R, int K, int E_phys,
                            cudaStream_t st);
 // Zero y rows [i] with inv_pos[i] < 0 (row_bytes a multiple of 16).
 cudaError_t launch_zero_dropped_rows(const int32_t* inv_pos, long n, long row_bytes, void* y,

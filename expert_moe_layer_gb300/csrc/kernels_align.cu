@@ -509,12 +509,31 @@ __global__ void __launch_bounds__(256, (combine_ctas_per_sm<TE, KB>())) combine_
 // destination rank of each work item, -1 for an id outside [0, E).
 __global__ void __launch_bounds__(256) ep_dest_kernel(const int32_t* __restrict__ ids,
                                                       long n, int E, int n_local,
-                                                      int32_t* __restrict__ dest) {
+                                                      int32_t* __restrict__ dest,
+                                                      int32_t* __restrict__ phys,
+                                                      const int32_t* __restrict__ phys_map,
+                                                      int R, int K, int E_phys) {
   pdl_enter();
   ids = fresh(ids);
   for (long i = blockIdx.x * 256L + threadIdx.x; i < n; i += 256L * gridDim.x) {
     const int id = ids[i];
-    dest[i] = (id >= 0 && id < E) ? id / n_local : -1;
+    int p = -1;
+    if (id >= 0 && id < E) {
+      if (phys_map) {
+        // replica t mod n_e of the id's replicas (a prefix of its row)
+        const int32_t* row = phys_map + static_cast<long>(id) * R;
+        int nrep = 0;
+        while (nrep < R && row[nrep] != -2) ++nrep;
+        if (nrep > 0) {
+          const int q = row[(i / K) % nrep];
+          if (q >= 0 && q < E_phys) p = q;
+        }
+      } else {
+        p = id;
+      }
+    }
+    phys[i] = p;
+    dest[i] = p >= 0 ? p / n_local : -1;
   }
 }
 
@@ -642,9 +661,11 @@ cudaError_t launch_silu_finalize(bool bf16, const float* part, int n_part, long 
 }
 
 cudaError_t launch_ep_dest(const int32_t* ids, long n, int E, int n_local, int32_t* dest,
+                           int32_t* phys, const int32_t* phys_map, int R, int K, int E_phys,
                            cudaStream_t st) {
+  if (phys_map && (R < 1 || K < 1)) return cudaErrorInvalidValue;
   return launch_pdl(ep_dest_kernel, dim3(grid_for(n, 256, 8 * 152)), dim3(256), 0, st, ids, n,
-                    E, n_local, dest);
+                    E, n_local, dest, phys, phys_map, R, K, E_phys);
 }
 
 cudaError_t launch_zero_dropped_rows(const int32_t* inv_pos, long n, long row_bytes, void* y,

@@ -367,7 +367,7 @@ FwdLayout fwd_layout(const moe_config* c, int T) {
 
 // Workspace of moe_ep_dispatch.
 struct EpLayout {
-  size_t status, dest, hist, sorted, total;
+  size_t status, dest, phys, hist, sorted, total;
 };
 EpLayout ep_layout(const moe_config* c, int T) {
   Carver cv;
@@ -375,6 +375,7 @@ EpLayout ep_layout(const moe_config* c, int T) {
   const size_t n = static_cast<size_t>(T) * c->top_k;
   L.status = cv.take(4);
   L.dest = cv.take(4 * n);
+  L.phys = cv.take(4 * n);
   L.hist = cv.take(sizeof(int) * static_cast<size_t>(align_warps(static_cast<long>(n))) *
                    c->ep_size);
   L.sorted = cv.take(4 * n);
@@ -663,12 +664,12 @@ size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T) {
 }
 
 int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
-                    const float* topk_w, int32_t* send_counts, int32_t* send_offsets,
-                    int32_t* send_pos, void* send_x, int32_t* send_ids, float* send_w,
-                    int32_t* send_tok, void* ws, size_t ws_bytes, void* stream) {
+                    const float* topk_w, const int32_t* phys_map, int32_t* send_counts,
+                    int32_t* send_offsets, int32_t* send_pos, void* send_x, int32_t* send_ids,
+                    float* send_w, int32_t* send_tok, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(validate_cfg(cfg));
-  // the dispatch has no replica placement (redundant experts): plain maps only
-  if (cfg->max_replicas > 0) return MOE_ERR_UNSUPPORTED;
+  // the global placement goes with replicas, and only with them
+  if ((cfg->max_replicas > 0) != (phys_map != nullptr)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(validate_T(T));
   if (!send_counts || !send_offsets) return MOE_ERR_INVALID_ARG;
   const int ep = cfg->ep_size;
@@ -686,12 +687,15 @@ int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* 
   MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, 4, st)));
   const long n = static_cast<long>(T) * cfg->top_k;
   int32_t* dest = at<int32_t>(ws, L.dest);
+  int32_t* phys = at<int32_t>(ws, L.phys);
   int32_t* sorted = at<int32_t>(ws, L.sorted);
-  MOE_TRY(cuda_ok(launch_ep_dest(topk_ids, n, cfg->num_experts, n_local(cfg), dest, st)));
+  MOE_TRY(cuda_ok(launch_ep_dest(topk_ids, n, cfg->num_experts, n_local(cfg), dest, phys,
+                                 phys_map, cfg->max_replicas, cfg->top_k,
+                                 cfg->num_experts + cfg->num_redundant_experts, st)));
   // a stable counting sort of the items over the destination ranks
   MOE_TRY(cuda_ok(launch_align(dest, n, nullptr, ep, ep, 0, 1, at<int>(ws, L.hist), send_counts,
                                send_offsets, sorted, send_pos, static_cast<int>(n), status, st)));
-  return cuda_ok(launch_ep_pack(cfg->act_dtype == MOE_BF16, x, topk_ids, topk_w, sorted,
+  return cuda_ok(launch_ep_pack(cfg->act_dtype == MOE_BF16, x, phys, topk_w, sorted,
                                 send_offsets + ep, n, cfg->top_k, cfg->hidden_size, send_x,
                                 send_ids, send_w, send_tok, st));
 }
@@ -707,8 +711,6 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
                           const int32_t* recv_ids, const float* recv_w, const void* w13,
                           const void* w2, void* y, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(validate_cfg(cfg));
-  // the dispatch has no replica placement (redundant experts): plain maps only
-  if (cfg->max_replicas > 0) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(validate_T(R));
   if (R == 0) return MOE_OK;
   if (!recv_x || !recv_ids || !recv_w || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
@@ -726,7 +728,10 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* sorted_ids = at<int32_t>(ws, L.sorted_ids);
   int32_t* inv_pos = at<int32_t>(ws, L.inv_pos);
-  MOE_TRY(cuda_ok(launch_align(recv_ids, R, nullptr, cfg->num_experts, El, cfg->ep_rank * El,
+  // ids are global, or physical with replicas: slot = id - ep_rank * E_local
+  MOE_TRY(cuda_ok(launch_align(recv_ids, R, nullptr,
+                               cfg->num_experts + cfg->num_redundant_experts, El,
+                               cfg->ep_rank * El,
                                kForwardBlock, at<int>(ws, L.hist), counts, offsets, sorted_ids,
                                inv_pos, L.cap, status, st, at<Tile>(ws, L.tiles),
                                at<int>(ws, L.groups), routed_nmax(&c1, R),

@@ -340,34 +340,51 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
 /* Expert-parallel dispatch and combine: the rank-local halves of
  * ep_fused_moe_patch.py _ep_forward steps 2-4. The exchange between ranks
  * (all_to_all_single of the send buffers with the counts as split sizes, and
- * back) is the caller's: this library runs no collective. These calls take
- * no replica map: with cfg->max_replicas > 0 they return MOE_ERR_UNSUPPORTED.
+ * back) is the caller's: this library runs no collective.
+ *
+ * Redundant experts (cfg->max_replicas > 0; MoEMixin num_redundant_experts,
+ * physical vs logical experts): each rank holds E_local =
+ * (E + num_redundant_experts) / ep_size weight slots, and the physical expert
+ * id of slot s on rank r is r * E_local + s. The sender picks the replica, so
+ * moe_ep_dispatch takes the global placement: phys_map [E, max_replicas]
+ * int32, row e listing the physical ids of logical expert e's replicas in
+ * their global order, padded with -2 (the same order the per-rank replica
+ * maps of moe_forward use). Item (t, k) goes to replica t mod n_e of its n_e
+ * replicas, and the physical id is what it carries.
  *
  * moe_ep_dispatch (step 2). Work item i = t*K + k goes to rank
- * topk_ids[i] / (E / ep_size). The items are sorted by destination rank and
- * packed. The page's argsort leaves the order inside a destination open; here
- * it is stable (ascending i).
+ * topk_ids[i] / (E / ep_size), or with replicas to rank phys / E_local of the
+ * replica chosen above. The items are sorted by destination rank and packed.
+ * The page's argsort leaves the order inside a destination open; here it is
+ * stable (ascending i).
  *   x        [T, H] act_dtype
- *   topk_ids [T, K] int32 global ids, topk_w [T, K] fp32 (from moe_route)
+ *   topk_ids [T, K] int32 global (logical) ids, topk_w [T, K] fp32 (from
+ *            moe_route)
+ *   phys_map NULL without replicas; [E, max_replicas] as above with them
+ *            (MOE_ERR_INVALID_ARG if given without, or missing with)
  *   send_counts  [ep_size] int32 out: rows for each destination rank
  *   send_offsets [ep_size + 1] int32 out: exclusive prefix of send_counts
  *   send_pos [T*K] int32 out: row of item i in the send buffers (-1 for an id
- *            outside [0, E), which also sets MOE_DEV_BAD_EXPERT_ID)
- *   send_x   [T*K, H] act_dtype out, send_ids [T*K] int32 out (global ids),
- *   send_w   [T*K] fp32 out, send_tok [T*K] int32 out (token index); rows
- *            past send_offsets[ep_size] are left untouched.
+ *            outside [0, E), or a replica row with no entry or an entry
+ *            outside the physical ids, which also sets MOE_DEV_BAD_EXPERT_ID)
+ *   send_x   [T*K, H] act_dtype out, send_ids [T*K] int32 out (global ids, or
+ *            physical ids with replicas), send_w [T*K] fp32 out, send_tok
+ *            [T*K] int32 out (token index); rows past send_offsets[ep_size]
+ *            are left untouched.
  * ws: moe_ep_dispatch_workspace_size(cfg, T) bytes. */
 size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T);
 int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
-                    const float* topk_w, int32_t* send_counts, int32_t* send_offsets,
-                    int32_t* send_pos, void* send_x, int32_t* send_ids, float* send_w,
-                    int32_t* send_tok, void* ws, size_t ws_bytes, void* stream);
+                    const float* topk_w, const int32_t* phys_map, int32_t* send_counts,
+                    int32_t* send_offsets, int32_t* send_pos, void* send_x, int32_t* send_ids,
+                    float* send_w, int32_t* send_tok, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_ep_expert_compute (step 3): the R items this rank received, each run
  * through its expert with top_k = 1 and weighted, as the page's call to
  * fused_experts does:
  *   y[r] = recv_w[r] * f_{recv_ids[r] - ep_rank*E_local}(recv_x[r]).
- * Rows whose id is not one of this rank's experts come back as zeros.
+ * Rows whose id is not one of this rank's experts come back as zeros. With
+ * replicas the ids are physical (as moe_ep_dispatch sends them) and the slot
+ * is recv_ids[r] - ep_rank*E_local in the same way.
  *   recv_x [R, H] act_dtype, recv_ids [R] int32 global ids, recv_w [R] fp32
  *   w13, w2: this rank's experts, as for moe_forward
  *   y      [R, H] act_dtype out

@@ -172,9 +172,13 @@ def test_replica_configs_are_validated_without_cuda():
                          fake, 1 << 30, None) == 1
     assert L.moe_align_permute(bp(ok), 4, fake, None, 1, fake, fake, fake, fake, 1000, fake,
                                1 << 30, None) == 1
-    # expert-parallel dispatch and expert compute: no replica maps
-    assert L.moe_ep_dispatch(bp(ok), 8, *([fake] * 10), fake, 1 << 30, None) == 2
-    assert L.moe_ep_expert_compute(bp(ok), 8, *([fake] * 7), 1 << 30, None) == 2
+    # expert-parallel dispatch: the global placement map goes with replicas,
+    # and only with them
+    assert L.moe_ep_dispatch(bp(ok), 8, fake, fake, fake, None, *([fake] * 7), fake, 1 << 30,
+                             None) == 1
+    plain = _cfg(num_experts=16, top_k=4, hidden_size=256, intermediate_size=256, ep_size=2)
+    assert L.moe_ep_dispatch(bp(plain), 8, fake, fake, fake, fake, *([fake] * 7), fake,
+                             1 << 30, None) == 1
 
 
 def test_ep_entry_points_reject_bad_args_without_cuda():
@@ -185,9 +189,9 @@ def test_ep_entry_points_reject_bad_args_without_cuda():
     assert B.ep_expert_compute_workspace_size(cfg, 64) > 0
     assert B.ep_dispatch_workspace_size(_cfg(top_k=0), 64) == 0
     # dispatch: missing outputs, then a workspace that is too small
-    assert L.moe_ep_dispatch(bp(cfg), 8, *([None] * 11), 0, None) == 1
+    assert L.moe_ep_dispatch(bp(cfg), 8, *([None] * 12), 0, None) == 1
     fake = 1 << 20
-    args = [fake] * 10
+    args = [fake] * 3 + [None] + [fake] * 7      # no placement map: no replicas
     assert L.moe_ep_dispatch(bp(cfg), 8, *args, fake, 8, None) == 3
     # expert compute and combine: missing pointers
     assert L.moe_ep_expert_compute(bp(cfg), 8, *([None] * 7), 0, None) == 1

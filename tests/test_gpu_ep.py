@@ -157,6 +157,95 @@ def test_ep_dispatch_exchange_compute_combine(name):
         assert_close(out.float().cpu().numpy(), ref, f"{name} rank {r} output")
 
 
+# Redundant experts over 2 ranks (as in test_gpu_replicas): logical experts
+# 0-15, experts 3 and 11 with a second replica; 9 weight slots per rank.
+REP_E, REP_K, REP_H, REP_I, REP_EP, REP_SLOTS = 16, 4, 256, 256, 2, 9
+REP_PLACEMENT = [[(e // 8, e % 8)] for e in range(REP_E)]
+REP_PLACEMENT[3] = [(0, 3), (1, 8)]
+REP_PLACEMENT[11] = [(1, 3), (0, 8)]
+REP_SLOT_EXPERT = [list(range(8)) + [11], list(range(8, 16)) + [3]]
+
+
+def test_ep_dispatch_to_replicas_exchange_compute_combine():
+    """The token-dispatch form with redundant experts: each item goes to the
+    rank of replica t mod n_e of its expert and carries the physical id; the
+    send buffers equal the oracle's bit for bit, each rank computes its
+    physical slots (a slot holds its logical expert's weights), and the
+    combined outputs equal the unsharded layer."""
+    base = W("ep_replicas", T=1, H=REP_H, I=REP_I, E=REP_E, K=REP_K, router_bias=True)
+    rw = synth.draw_tensor(base, synth.ROUTER_W, 0)
+    rb = synth.draw_tensor(base, synth.ROUTER_B, 0)
+    rb[[3, 11]] += 2.0                                  # two hot experts
+    w13 = synth.draw_tensor(base, synth.W13, 0, local=False)
+    w2 = synth.draw_tensor(base, synth.W2, 0, local=False)
+    pmap = O.physical_map(REP_PLACEMENT, REP_EP, REP_SLOTS, 2)
+    d_pmap = torch.from_numpy(pmap).cuda()
+    tokens = (70, 41)
+    cfg = [B.make_config(REP_E, REP_K, REP_H, REP_I, True, ep_size=REP_EP, ep_rank=r,
+                         max_replicas=2, num_redundant_experts=2) for r in range(REP_EP)]
+    xs, sends, host_sends = [], [], []
+    for r, T in enumerate(tokens):
+        x = cases.gap_checked_x(base.with_(T=T), 30 + r, rw, rb)[0]
+        xs.append(x)
+        ids, w, _ = O.route(x, rw, rb, top_k=REP_K, renormalize=True)
+        assert (ids == 3).any() and (ids == 11).any()
+        host = O.ep_dispatch(x, ids, w, REP_E, REP_EP, pmap, REP_SLOTS)
+        host_sends.append(host)
+        n = T * REP_K
+        out = dict(counts=torch.full((REP_EP,), -1, dtype=torch.int32, device="cuda"),
+                   offsets=torch.full((REP_EP + 1,), -1, dtype=torch.int32, device="cuda"),
+                   pos=torch.full((n,), -7, dtype=torch.int32, device="cuda"),
+                   x=torch.zeros(n, REP_H, dtype=torch.bfloat16, device="cuda"),
+                   ids=torch.full((n,), -7, dtype=torch.int32, device="cuda"),
+                   w=torch.full((n,), -7.0, dtype=torch.float32, device="cuda"),
+                   tok=torch.full((n,), -7, dtype=torch.int32, device="cuda"))
+        ws = torch.empty(B.ep_dispatch_workspace_size(cfg[r], T), dtype=torch.uint8,
+                         device="cuda")
+        B.moe_ep_dispatch(cfg[r], T, _dev(x), torch.from_numpy(ids).cuda(),
+                          torch.from_numpy(w).cuda(), out["counts"], out["offsets"], out["pos"],
+                          out["x"], out["ids"], out["w"], out["tok"], ws, phys_map=d_pmap)
+        assert B.moe_get_status(ws) == (0, 0)
+        counts, pos, sx, sids, sw, stok = host
+        np.testing.assert_array_equal(out["counts"].cpu().numpy(), counts)
+        np.testing.assert_array_equal(out["pos"].cpu().numpy(), pos)
+        np.testing.assert_array_equal(out["ids"].cpu().numpy(), sids)
+        np.testing.assert_array_equal(out["tok"].cpu().numpy(), stok)
+        np.testing.assert_array_equal(out["w"].cpu().numpy(), sw)
+        np.testing.assert_array_equal(out["x"].float().cpu().numpy(), sx.astype(np.float32))
+        sends.append(out)
+
+    counts = [h[0] for h in host_sends]
+    recv = {k: _exchange([s[k] for s in sends], counts) for k in ("x", "ids", "w")}
+    host_recv = {k: O.ep_exchange([h[i] for h in host_sends], counts)
+                 for k, i in (("x", 2), ("ids", 3), ("w", 4))}
+    ys = []
+    for r in range(REP_EP):
+        R = recv["x"][r].shape[0]
+        w13_r = np.stack([w13[e] for e in REP_SLOT_EXPERT[r]])
+        w2_r = np.stack([w2[e] for e in REP_SLOT_EXPERT[r]])
+        y = torch.zeros(R, REP_H, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(B.ep_expert_compute_workspace_size(cfg[r], R), dtype=torch.uint8,
+                         device="cuda")
+        B.moe_ep_expert_compute(cfg[r], R, recv["x"][r].contiguous(),
+                                recv["ids"][r].contiguous(), recv["w"][r].contiguous(),
+                                _dev(w13_r), _dev(w2_r), y, ws)
+        assert B.moe_get_status(ws) == (0, 0)
+        ref = O.ep_expert_compute(host_recv["x"][r], host_recv["ids"][r], host_recv["w"][r],
+                                  w13_r, w2_r, r * REP_SLOTS)
+        assert_close(y.float().cpu().numpy(), ref, f"replicas rank {r} expert rows")
+        ys.append(y)
+
+    back = [[counts[s][r] for s in range(REP_EP)] for r in range(REP_EP)]
+    rets = _exchange(ys, back)
+    for r, T in enumerate(tokens):
+        out = torch.empty(T, REP_H, dtype=torch.bfloat16, device="cuda")
+        cws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        B.moe_ep_combine(cfg[r], T, rets[r].contiguous(), sends[r]["pos"], None, out, cws)
+        assert B.moe_get_status(cws) == (0, 0)
+        ref = O.moe_forward(xs[r], rw, w13, w2, top_k=REP_K, renormalize=True, router_b=rb)
+        assert_close(out.float().cpu().numpy(), ref, f"replicas rank {r} output")
+
+
 def test_ep_dispatch_flags_bad_ids_and_handles_empty():
     wl = W("ep_bad", T=6, H=128, I=128, E=8, K=2, ep_size=2)
     cfg = cfg_of(wl)
