@@ -46,11 +46,16 @@ constexpr int kChunk = 32;                       // columns per SiLU exchange ch
 constexpr int kHalfCols = kChunk / 2;            // columns of a chunk per epilogue warp
 constexpr int kXSlotBytes = 64 * kChunk * 4;     // one chunk of up values, fp32
 
-template <int MODE, int NMAX>
+// A pipeline stage holds KPS consecutive K blocks (128 bytes of K each): one
+// SM's TMA engine completes stages at a roughly fixed rate whatever their size
+// (measured: ~2 per us), so its throughput grows with the bytes per stage,
+// not with the number of stages in flight.
+template <int MODE, int NMAX, int KPS>
 struct PairShape {
   static constexpr int kBRows = NMAX / 2;  // token rows staged per CTA
   static constexpr int kBBytes = kBRows * 128;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSubBytes = kABytes + kBBytes;  // one K block: A, then B
+  static constexpr int kStageBytes = KPS * kSubBytes;
   static constexpr int kXBytes = (MODE == kGemmSiluUp) ? 2 * kXSlotBytes : 0;
   // output staging: per column half, two buffers of 16 token rows of this
   // CTA's output columns (64 of h in SiLU mode, 128 of y in plain mode)
@@ -96,7 +101,7 @@ __device__ __forceinline__ void settle(uint64_t ns) {
   }
 }
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, int KPS>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_pair(const __grid_constant__ CUtensorMap mapA,
                   const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
@@ -105,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __nv_bfloat16* __restrict__ out, long out_ld,
                   const int32_t* __restrict__ out_rows, const float* __restrict__ out_scale,
                   int b_cap, unsigned* status) {
-  using S = PairShape<MODE, NMAX>;
+  using S = PairShape<MODE, NMAX, KPS>;
+  const int n_st = k_blocks / KPS;  // stages per unit (k_blocks is a multiple of KPS)
   const uint32_t rank = ptx::cluster_rank();
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
@@ -209,9 +215,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         decode_unit(u, gstart, n_groups, m_tiles, ti, m);
         const Tile tl = tile_at(ti);
         if (!tile_ok(tl)) continue;
-        for (int kb = 0; kb < k_blocks && pre < S::kStages; ++kb, ++pre) {
+        for (int j = 0; j < n_st && pre < S::kStages; ++j, ++pre) {
           if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * pre, 2 * S::kStageBytes);
-          load_a(sbase + pre * S::kStageBytes, full_r0 + 8 * pre, kb, tl, m);
+#pragma unroll
+          for (int p = 0; p < KPS; ++p)
+            load_a(sbase + pre * S::kStageBytes + p * S::kSubBytes, full_r0 + 8 * pre,
+                   j * KPS + p, tl, m);
         }
       }
       pdl_enter();
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+        for (int j = 0; j < n_st; ++j, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           const uint32_t st = sbase + s * S::kStageBytes;
@@ -242,9 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // stage s again only after rank 0's MMAs freed it, so its bytes
             // never land in an older phase.
             if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * S::kStageBytes);
-            load_a(st, fb, kb, tl, m);
+#pragma unroll
+            for (int p = 0; p < KPS; ++p) load_a(st + p * S::kSubBytes, fb, j * KPS + p, tl, m);
           }
-          ptx::tma_load_2d_pair(st + kABytes, &mapB, fb, kb * 64, b_row);
+#pragma unroll
+          for (int p = 0; p < KPS; ++p)
+            ptx::tma_load_2d_pair(st + p * S::kSubBytes + kABytes, &mapB, fb,
+                                  (j * KPS + p) * 64, b_row);
         }
       }
       if (!ok) settle(200000);
@@ -272,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + b * S::kAccCols;
-        for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+        for (int j = 0; j < n_st; ++j, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           if (!ptx::mbar_wait_cluster(full0 + 8 * s, ph, abort_flag, status)) {
@@ -280,12 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = sbase + s * S::kStageBytes;
-          const uint64_t da = ptx::sdesc_sw128(st);
-          const uint64_t db = ptx::sdesc_sw128(st + kABytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            ptx::tc_mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+          for (int p = 0; p < KPS; ++p) {
+            const uint32_t st = sbase + s * S::kStageBytes + p * S::kSubBytes;
+            const uint64_t da = ptx::sdesc_sw128(st);
+            const uint64_t db = ptx::sdesc_sw128(st + kABytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::tc_mma_pair(d, da + 2 * kk, db + 2 * kk, idesc, (j | p | kk) ? 1u : 0u);
+          }
           ptx::tc_commit_pair(empty0 + 8 * s);
         }
         if (!ok) break;
@@ -453,10 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int NMAX>
+template <int MODE, int NMAX, int KPS>
 cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
-  using S = PairShape<MODE, NMAX>;
-  auto kern = moe_gemm_pair<MODE, NMAX>;
+  using S = PairShape<MODE, NMAX, KPS>;
+  auto kern = moe_gemm_pair<MODE, NMAX, KPS>;
   static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), S::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -486,10 +502,13 @@ cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num
                              cudaStream_t st) {
   if ((a.tiles == nullptr && a.dense_T <= 0) || a.k_split != 1) return cudaErrorInvalidValue;
   if (a.out_rows && mode != kGemmPlain) return cudaErrorInvalidValue;
+  const bool two = a.k_blocks % 2 == 0;  // two K blocks per stage when they pair up
   if (nmax == 256 && mode == kGemmPlain)
-    return launch_pair_variant<kGemmPlain, 256>(a, num_sms, st);
+    return two ? launch_pair_variant<kGemmPlain, 256, 2>(a, num_sms, st)
+               : launch_pair_variant<kGemmPlain, 256, 1>(a, num_sms, st);
   if (nmax == 256 && mode == kGemmSiluUp)
-    return launch_pair_variant<kGemmSiluUp, 256>(a, num_sms, st);
+    return two ? launch_pair_variant<kGemmSiluUp, 256, 2>(a, num_sms, st)
+               : launch_pair_variant<kGemmSiluUp, 256, 1>(a, num_sms, st);
   return cudaErrorInvalidValue;
 }
 
