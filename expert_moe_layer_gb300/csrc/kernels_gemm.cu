@@ -41,11 +41,16 @@ constexpr int kThreads = 320;       // 10 warps
 constexpr int kEpiThreads = 256;    // warps 2..9
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
 
-template <int MODE, int NMAX, bool STG>
+// A pipeline stage holds KPS consecutive K blocks (128 bytes of K each), each
+// with its weight box(es), then its token-row box. One SM's TMA engine
+// completes stages at a roughly fixed rate whatever their size, so its
+// throughput follows the bytes per stage rather than the number of stages.
+template <int MODE, int NMAX, bool STG, int KPS = 1>
 struct GemmShape {
-  static constexpr int kNA = (MODE == kGemmSiluUp) ? 2 : 1;  // weight boxes per stage
+  static constexpr int kNA = (MODE == kGemmSiluUp) ? 2 : 1;  // weight boxes per K block
   static constexpr int kBBytes = NMAX * 128;
-  static constexpr int kStageBytes = kNA * kABytes + kBBytes;
+  static constexpr int kSubBytes = kNA * kABytes + kBBytes;  // one K block
+  static constexpr int kStageBytes = KPS * kSubBytes;
   // output staging (bf16 outputs): per column half, two buffers of 16 token
   // rows x 128 output columns
   static constexpr int kOutBufBytes = 16 * 128 * 2;
@@ -97,7 +102,7 @@ __device__ __forceinline__ void decode_unit(int u, const int* gstart, int n_grou
   tile = gstart[lo] + (r - m * n);
 }
 
-template <int MODE, bool TF32, typename TOut, int NMAX>
+template <int MODE, bool TF32, typename TOut, int NMAX, int KPS>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_tc(const __grid_constant__ CUtensorMap mapA,
                 const __grid_constant__ CUtensorMap mapB, const Tile* __restrict__ tiles,
@@ -106,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
                 float* __restrict__ part, int m_valid, unsigned* status) {
   constexpr bool kStaged = sizeof(TOut) == 2;
-  using S = GemmShape<MODE, NMAX, kStaged>;
+  using S = GemmShape<MODE, NMAX, kStaged, KPS>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
 
@@ -185,13 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(ti);
         const int a_row = tl.x * a_rows_per_expert + m * 128;
         const int kb1 = min(k_blocks, (ks + 1) * kb_per);
-        for (int kb = ks * kb_per; kb < kb1 && pre < S::kStages; ++kb, ++pre) {
-          const uint32_t st = sbase + pre * S::kStageBytes;
+        for (int kb = ks * kb_per; kb < kb1 && pre < S::kStages; kb += KPS, ++pre) {
           ptx::mbar_arrive_expect_tx(full0 + 8 * pre, S::kStageBytes);
-          ptx::tma_load_2d(st, &mapA, full0 + 8 * pre, kb * kKe, a_row);
-          if (MODE == kGemmSiluUp)
-            ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * pre, kb * kKe,
-                             a_row + a_up_offset);
+#pragma unroll
+          for (int p = 0; p < KPS; ++p) {
+            const uint32_t st = sbase + pre * S::kStageBytes + p * S::kSubBytes;
+            ptx::tma_load_2d(st, &mapA, full0 + 8 * pre, (kb + p) * kKe, a_row);
+            if (MODE == kGemmSiluUp)
+              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * pre, (kb + p) * kKe,
+                               a_row + a_up_offset);
+          }
         }
       }
       pdl_enter();
@@ -204,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(ti);
         const int b_row = b_from_out ? tl.z : tl.y;
         const int kb1 = min(k_blocks, (ks + 1) * kb_per);
-        for (int kb = ks * kb_per; kb < kb1; ++kb, ++it) {
+        for (int kb = ks * kb_per; kb < kb1; kb += KPS, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
-          const uint32_t st = sbase + s * S::kStageBytes;
+          const uint32_t st0 = sbase + s * S::kStageBytes;
           if (it >= pre) {  // stages of the early loads are fresh: no empty wait
             if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
               ok = false;
@@ -215,12 +223,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::mbar_arrive_expect_tx(full0 + 8 * s, S::kStageBytes);
             const int a_row = tl.x * a_rows_per_expert + m * 128;
-            ptx::tma_load_2d(st, &mapA, full0 + 8 * s, kb * kKe, a_row);
-            if (MODE == kGemmSiluUp)
-              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, kb * kKe,
-                               a_row + a_up_offset);
+#pragma unroll
+            for (int p = 0; p < KPS; ++p) {
+              const uint32_t st = st0 + p * S::kSubBytes;
+              ptx::tma_load_2d(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row);
+              if (MODE == kGemmSiluUp)
+                ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
+                                 a_row + a_up_offset);
+            }
           }
-          ptx::tma_load_2d(st + S::kNA * kABytes, &mapB, full0 + 8 * s, kb * kKe, b_row);
+#pragma unroll
+          for (int p = 0; p < KPS; ++p)
+            ptx::tma_load_2d(st0 + p * S::kSubBytes + S::kNA * kABytes, &mapB, full0 + 8 * s,
+                             (kb + p) * kKe, b_row);
         }
       }
       if (!ok) {
@@ -257,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + b * S::kAccCols;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; kb += KPS, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           if (!ptx::mbar_wait(full0 + 8 * s, ph, abort_flag, status)) {
@@ -265,16 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t st = sbase + s * S::kStageBytes;
-          const uint64_t da = ptx::sdesc_sw128(st);
-          const uint64_t db = ptx::sdesc_sw128(st + S::kNA * kABytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            ptx::tc_mma<TF32>(d, da + 2 * kk, db + 2 * kk, idesc, acc);
-            if (MODE == kGemmSiluUp) {
-              const uint64_t du = ptx::sdesc_sw128(st + kABytes);
-              ptx::tc_mma<TF32>(d + NMAX, du + 2 * kk, db + 2 * kk, idesc, acc);
+          for (int p = 0; p < KPS; ++p) {
+            const uint32_t st = sbase + s * S::kStageBytes + p * S::kSubBytes;
+            const uint64_t da = ptx::sdesc_sw128(st);
+            const uint64_t db = ptx::sdesc_sw128(st + S::kNA * kABytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (kb + p > kb0 || kk > 0) ? 1u : 0u;
+              ptx::tc_mma<TF32>(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+              if (MODE == kGemmSiluUp) {
+                const uint64_t du = ptx::sdesc_sw128(st + kABytes);
+                ptx::tc_mma<TF32>(d + NMAX, du + 2 * kk, db + 2 * kk, idesc, acc);
+              }
             }
           }
           ptx::tc_commit(empty0 + 8 * s);
@@ -409,10 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, bool TF32, typename TOut, int NMAX>
+template <int MODE, bool TF32, typename TOut, int NMAX, int KPS = 1>
 cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
-  using S = GemmShape<MODE, NMAX, sizeof(TOut) == 2>;
-  auto kern = moe_gemm_tc<MODE, TF32, TOut, NMAX>;
+  using S = GemmShape<MODE, NMAX, sizeof(TOut) == 2, KPS>;
+  auto kern = moe_gemm_tc<MODE, TF32, TOut, NMAX, KPS>;
   static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
   const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(kern), S::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -437,6 +455,14 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
     return cudaErrorInvalidValue;
   }
   const bool big = nmax == 128;
+  // bf16 plain GEMMs with whole K ranges and an even K block count take two K
+  // blocks per stage (three or more stages still fit). The SiLU mode's
+  // stages carry two weight boxes: doubled, only two fit, and that measured
+  // slower (EP-shard GEMM1 99.5 against 93.8 us).
+  const bool two = a.k_split == 1 && a.k_blocks % 2 == 0;
+  static_assert(GemmShape<kGemmPlain, 128, true, 2>::kStages >= 3 &&
+                    GemmShape<kGemmPlain, 32, true, 2>::kStages >= 3,
+                "two K blocks per stage keep at least three stages");
   switch (mode) {
     case kGemmSiluUp:
       if (tf32)
@@ -448,6 +474,9 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
       if (tf32)
         return big ? launch_variant<kGemmPlain, true, float, 128>(a, num_sms, st)
                    : launch_variant<kGemmPlain, true, float, 32>(a, num_sms, st);
+      if (two)
+        return big ? launch_variant<kGemmPlain, false, __nv_bfloat16, 128, 2>(a, num_sms, st)
+                   : launch_variant<kGemmPlain, false, __nv_bfloat16, 32, 2>(a, num_sms, st);
       return big ? launch_variant<kGemmPlain, false, __nv_bfloat16, 128>(a, num_sms, st)
                  : launch_variant<kGemmPlain, false, __nv_bfloat16, 32>(a, num_sms, st);
     case kGemmLogits:
