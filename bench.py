@@ -353,6 +353,19 @@ def time_layer(args, wl, d, device, world, headline):
     if world > 1:
         torch.distributed.barrier()
     step_ms = [events[i][0].elapsed_time(events[i][7]) for i in range(args.steps)]
+    rc, flags = B.moe_get_status(ws, stream)
+    if rc != 0:
+        raise RuntimeError(f"{wl.name}: device status {rc} flags {flags:#x} in the timed region")
+
+    # Per-stage breakdown (and the dominant kernel's live duration): a second
+    # graph of the same K steps with events at every stage boundary, replayed
+    # right after the timed one, under the same clocks.
+    sevents = new_events(args.steps)
+    sgraph, _ = capture(sevents)
+    sgraph.replay()
+    torch.cuda.synchronize(device)
+    del sgraph
+
     # nvidia-smi samples every 50 ms and takes a moment to start: a timed
     # region shorter than that is followed by untimed replays of the same
     # graph, so that the clock record covers this workload
@@ -364,18 +377,7 @@ def time_layer(args, wl, d, device, world, headline):
     clocks = sampler.stop()
     if clocks is not None:
         clocks["untimed_replays"] = extra
-    rc, flags = B.moe_get_status(ws, stream)
-    if rc != 0:
-        raise RuntimeError(f"{wl.name}: device status {rc} flags {flags:#x} in the timed region")
     del graph
-
-    # Per-stage breakdown (and the dominant kernel's live duration): a second
-    # graph of the same K steps with events at every stage boundary.
-    sevents = new_events(args.steps)
-    sgraph, _ = capture(sevents)
-    sgraph.replay()
-    torch.cuda.synchronize(device)
-    del sgraph
 
     def span(a, b):
         return [sevents[i][a].elapsed_time(sevents[i][b]) for i in range(args.steps)]

@@ -461,7 +461,8 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
   // slower (EP-shard GEMM1 99.5 against 93.8 us).
   const bool two = a.k_split == 1 && a.k_blocks % 2 == 0;
   static_assert(GemmShape<kGemmPlain, 128, true, 2>::kStages >= 3 &&
-                    GemmShape<kGemmPlain, 32, true, 2>::kStages >= 3,
+                    GemmShape<kGemmPlain, 32, true, 2>::kStages >= 3 &&
+                    GemmShape<kGemmPlain, 128, false, 2>::kStages >= 3,
                 "two K blocks per stage keep at least three stages");
   switch (mode) {
     case kGemmSiluUp:
@@ -481,6 +482,7 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
                  : launch_variant<kGemmPlain, false, __nv_bfloat16, 32>(a, num_sms, st);
     case kGemmLogits:
       if (tf32) return cudaErrorInvalidValue;
+      if (two && big) return launch_variant<kGemmPlain, false, float, 128, 2>(a, num_sms, st);
       return big ? launch_variant<kGemmPlain, false, float, 128>(a, num_sms, st)
                  : launch_variant<kGemmPlain, false, float, 32>(a, num_sms, st);
   }
