@@ -1,4 +1,4 @@
-"""In-tree build of libmoe.so (CUDA, sm_103a) with nvcc.
+"""In-tree build of libmoe.so and libmoe_debug.so (CUDA, sm_103a) with nvcc.
 
 Each translation unit compiles in parallel into ``_build/``, then nvcc links
 the shared library next to this file. A stamp records the source hash, the
@@ -18,16 +18,27 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(ROOT, "_build", "libmoe")
 LIB = os.path.join(PKG, "libmoe.so")
-STAMP = LIB + ".stamp"
+# the same library with the device-side bounds checks of csrc/dbg.cuh
+LIB_DEBUG = os.path.join(PKG, "libmoe_debug.so")
 
 SOURCES = ["moe_api.cu", "kernels_gemm.cu", "kernels_gemm_pair.cu", "kernels_mlp_fused.cu",
            "kernels_route.cu", "kernels_align.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "launch.cuh", "align_block.cuh", "topk_warp.cuh", "act.cuh"]
+HEADERS = ["ptx.cuh", "internal.h", "launch.cuh", "align_block.cuh", "topk_warp.cuh", "act.cuh",
+           "dbg.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# hidden visibility: only the MOE_API entry points of include/moe.h are
+# exported, so two builds in one process share no internal symbol
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
-                "-I" + INCLUDE, "-I" + CSRC]
+                "-Xcompiler", "-fvisibility=hidden", "-I" + INCLUDE, "-I" + CSRC]
+
+
+def lib_path(debug: bool = False) -> str:
+    return LIB_DEBUG if debug else LIB
+
+
+def _flags(debug: bool) -> list[str]:
+    return FLAGS + (["-DMOE_DEBUG"] if debug else [])
 
 
 def nvcc() -> str:
@@ -37,35 +48,39 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _digest() -> str:
+def _digest(debug: bool = False) -> str:
     h = hashlib.sha256()
     for f in SOURCES + HEADERS:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(fh.read())
     with open(os.path.join(INCLUDE, "moe.h"), "rb") as fh:
         h.update(fh.read())
-    h.update(" ".join(FLAGS).encode())
+    h.update(" ".join(_flags(debug)).encode())
     h.update(platform.machine().encode())
     return h.hexdigest()
 
 
-def up_to_date() -> bool:
-    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
+def up_to_date(debug: bool = False) -> bool:
+    lib = lib_path(debug)
+    if not (os.path.exists(lib) and os.path.exists(lib + ".stamp")):
         return False
-    with open(STAMP) as fh:
-        return fh.read().strip() == _digest()
+    with open(lib + ".stamp") as fh:
+        return fh.read().strip() == _digest(debug)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile libmoe.so if missing or stale; returns its path."""
-    if not force and not extra_flags and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile libmoe.so (libmoe_debug.so with debug=True) if missing or
+    stale; returns its path."""
+    lib = lib_path(debug)
+    if not force and not extra_flags and up_to_date(debug):
+        return lib
+    out_dir = os.path.join(ROOT, "_build", "libmoe_debug" if debug else "libmoe")
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    flags = FLAGS + list(extra_flags)
+    flags = _flags(debug) + list(extra_flags)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -76,16 +91,24 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(STAMP, "w") as fh:
-        fh.write(_digest())
-    return LIB
+    os.replace(tmp, lib)
+    with open(lib + ".stamp", "w") as fh:
+        fh.write(_digest(debug))
+    return lib
+
+
+def build_all(force: bool = False) -> tuple[str, str]:
+    """Both libraries, compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        rel = ex.submit(build, force)
+        dbg = ex.submit(build, force, False, (), True)
+        return rel.result(), dbg.result()
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose=True))
+    print(build_all(force=True))

@@ -5,9 +5,14 @@ kernels. Tensors are torch CUDA tensors (used as plain device memory). The
 functions take the same names and arguments as the C entry points and raise
 ``MoeError`` on a non-zero status. There is no fallback: if the library cannot
 be loaded, every call fails loudly.
+
+Inside ``with debug_library():`` the same functions call libmoe_debug.so,
+the build whose kernels also check their own derived indices (see
+``debug_take``).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -25,7 +30,9 @@ DEV_BAD_EXPERT_ID, DEV_CAP_OVERFLOW, DEV_TIMEOUT, DEV_BAD_SEGMENT = 0x1, 0x2, 0x
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({strerror(status)})")
+        self.cuda_error = lib().moe_last_cuda_error() if status == 4 else 0
+        why = f", CUDA error {self.cuda_error}" if self.cuda_error else ""
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({strerror(status)}{why})")
 
 
 class MoeConfig(ctypes.Structure):
@@ -48,6 +55,15 @@ class WorkspaceOffsets(ctypes.Structure):
                 ("offsets", ctypes.c_size_t), ("sorted_ids", ctypes.c_size_t),
                 ("inv_pos", ctypes.c_size_t), ("total", ctypes.c_size_t),
                 ("cap", ctypes.c_int), ("block_m", ctypes.c_int)]
+
+
+class DebugRecord(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_uint32), ("site", ctypes.c_uint32),
+                ("index", ctypes.c_int64), ("bound", ctypes.c_int64)]
+
+
+DEBUG_FILES = {1: "moe_api.cu", 2: "kernels_gemm.cu", 3: "kernels_gemm_pair.cu",
+               4: "kernels_mlp_fused.cu", 5: "kernels_route.cu", 6: "kernels_align.cu"}
 
 
 class Plan(ctypes.Structure):
@@ -74,7 +90,8 @@ def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=
                      num_redundant_experts)
 
 
-_lib = None
+_libs: dict[bool, ctypes.CDLL] = {}  # debug build? -> loaded library
+_use_debug = False
 _lock = threading.Lock()
 _VP, _SZ, _I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
 _CFG = ctypes.POINTER(MoeConfig)
@@ -98,6 +115,7 @@ _SIGS = {
                                _SZ, _VP, ctypes.POINTER(ctypes.c_void_p),
                                ctypes.POINTER(ctypes.c_int)]),
     "moe_get_status": (_I, [_VP, _VP, ctypes.POINTER(ctypes.c_uint32)]),
+    "moe_last_cuda_error": (_I, []),
     "moe_set_wait_limit_ns": (_I, [ctypes.c_uint64]),
     "moe_forward_plan": (_I, [_CFG, _I, ctypes.POINTER(Plan)]),
     "moe_ep_dispatch_workspace_size": (_SZ, [_CFG, _I]),
@@ -105,6 +123,9 @@ _SIGS = {
     "moe_ep_expert_compute_workspace_size": (_SZ, [_CFG, _I]),
     "moe_ep_expert_compute": (_I, [_CFG, _I] + [_VP] * 7 + [_SZ, _VP]),
     "moe_ep_combine": (_I, [_CFG, _I] + [_VP] * 5 + [_SZ, _VP]),
+    "moe_debug_build": (_I, []),
+    "moe_debug_take": (_I, [ctypes.POINTER(DebugRecord)]),
+    "moe_debug_selftest": (_I, [_VP]),
 }
 
 
@@ -116,21 +137,38 @@ def header_functions() -> list[str]:
     return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
 
 
-def lib(build: bool = True) -> ctypes.CDLL:
-    """Load libmoe.so (building it in place first if missing or stale)."""
-    global _lib
+def lib(build: bool = True, debug: bool | None = None) -> ctypes.CDLL:
+    """Load libmoe.so, or libmoe_debug.so inside ``debug_library()`` (or with
+    debug=True), building it in place first if missing or stale."""
+    dbg = _use_debug if debug is None else debug
     with _lock:
-        if _lib is None:
+        L = _libs.get(dbg)
+        if L is None:
+            path = _build.lib_path(dbg)
             if build:
-                _build.build()
-            if not os.path.exists(_build.LIB):
-                raise RuntimeError("libmoe.so is not built; call __graft_entry__.build()")
-            L = ctypes.CDLL(_build.LIB)
+                _build.build(debug=dbg)
+            if not os.path.exists(path):
+                raise RuntimeError(f"{os.path.basename(path)} is not built; "
+                                   "call __graft_entry__.build()")
+            L = ctypes.CDLL(path)
             for name, (res, args) in _SIGS.items():
                 f = getattr(L, name)
                 f.restype, f.argtypes = res, args
-            _lib = L
-    return _lib
+            _libs[dbg] = L
+    return L
+
+
+@contextlib.contextmanager
+def debug_library():
+    """Route every call of this module to libmoe_debug.so for the duration
+    (one thread at a time; not reentrant across threads)."""
+    global _use_debug
+    old = _use_debug
+    _use_debug = True
+    try:
+        yield lib()
+    finally:
+        _use_debug = old
 
 
 def strerror(status: int) -> str:
@@ -294,6 +332,29 @@ def moe_get_status(ws, stream=None) -> tuple[int, int]:
     flags = ctypes.c_uint32(0)
     rc = lib().moe_get_status(_p(ws), _stream(stream), ctypes.byref(flags))
     return rc, flags.value
+
+
+def debug_build() -> bool:
+    """True when the active library is libmoe_debug.so."""
+    return bool(lib().moe_debug_build())
+
+
+def debug_take() -> DebugRecord:
+    """Synchronise the device, then read and clear the debug build's record
+    of failed bounds checks (count, and site / index / bound of the first)."""
+    rec = DebugRecord()
+    _check("moe_debug_take", lib().moe_debug_take(ctypes.byref(rec)))
+    return rec
+
+
+def debug_site(site: int) -> str:
+    """'file:line' of a record's site."""
+    return f"{DEBUG_FILES.get(site >> 16, site >> 16)}:{site & 0xffff}"
+
+
+def debug_selftest(stream=None) -> None:
+    """Enqueue the debug build's one failing check (index 5, bound 4)."""
+    _check("moe_debug_selftest", lib().moe_debug_selftest(_stream(stream)))
 
 
 def set_wait_limit_ns(ns: int) -> None:

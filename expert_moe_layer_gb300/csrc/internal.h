@@ -7,6 +7,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "dbg.cuh"
 #include "moe.h"
 
 namespace moe {
@@ -15,6 +16,18 @@ namespace moe {
 //   x = expert (weight slab index), y = first B row, z = first output row,
 //   w = rows (1..nmax).
 using Tile = int4;
+
+// Extents of the buffers a GEMM kernel touches. Only the debug build reads
+// them (its checks of the kernels' derived indices); launches there refuse
+// zero extents, so every call site fills them in.
+struct GemmBounds {
+  long a_rows = 0;    // rows behind the weight tensor map
+  long b_rows = 0;    // rows behind the token-row tensor map
+  long out_rows = 0;  // rows of out (and of each split-K slab of part)
+  long out_map = 0;   // CTA-pair plain mode with out_rows: entries of out_rows /
+                      //   out_scale (0 without them)
+  int max_tiles = 0;  // entries of the tile table (0 for dense problems)
+};
 
 struct GemmArgs {
   const CUtensorMap* mapA;     // weights, 2-D [slabs*rows_per_slab, K]
@@ -41,6 +54,7 @@ struct GemmArgs {
                                       //   past it are skipped and flagged); 0: unchecked
   int m_valid;                 // weight rows with an output (router: E)
   unsigned* status;
+  GemmBounds bnd;
 };
 
 enum GemmMode { kGemmSiluUp = 0, kGemmPlain = 1, kGemmLogits = 2 };
@@ -175,6 +189,7 @@ struct MlpFusedArgs {
   void* h;                    // h_perm
   void* y;                    // y_perm
   unsigned* status;
+  GemmBounds bnd;             // a_rows: w13 rows; b_rows = out_rows = cap; max_tiles
 };
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st);
 size_t mlp_fused_smem_bytes();
@@ -213,5 +228,14 @@ cudaError_t set_wait_limit_gemm(unsigned long long ns);
 cudaError_t set_wait_limit_gemm_pair(unsigned long long ns);
 cudaError_t set_wait_limit_mlp_fused(unsigned long long ns);
 cudaError_t set_wait_limit_route(unsigned long long ns);
+
+// Debug build: each translation unit's record of failed bounds checks, read
+// and cleared (all zero in the release build).
+cudaError_t take_dbg_api(DbgRecord* out);
+cudaError_t take_dbg_gemm(DbgRecord* out);
+cudaError_t take_dbg_gemm_pair(DbgRecord* out);
+cudaError_t take_dbg_mlp_fused(DbgRecord* out);
+cudaError_t take_dbg_route(DbgRecord* out);
+cudaError_t take_dbg_align(DbgRecord* out);
 
 }  // namespace moe

@@ -17,6 +17,7 @@
 #include "launch.cuh"
 
 namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgAlign;
 namespace {
 
 constexpr int kItemsPerWarp = 256;
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const TE* __restrict__ x,
   for (long r = blockIdx.x * 8L + warp; r < rows; r += 8L * gridDim.x) {
     const int id = sorted_ids[r];
     if (id < 0 || id >= n_items) continue;
+    if (!MOE_DCHECK(r, cap) || !MOE_DCHECK(id / K, n_items / K)) continue;
     if (w_perm && lane == 0) w_perm[r] = w_items[id];
     const uint4* src = reinterpret_cast<const uint4*>(x + (id / K) * static_cast<long>(H));
     uint4* dst = reinterpret_cast<uint4*>(x_perm + r * H);
@@ -472,7 +474,8 @@ __global__ void __launch_bounds__(256, (combine_ctas_per_sm<TE, KB>())) combine_
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
         if (j0 + j < n) {
-          const TE* row = y_perm + static_cast<long>(s_pos[tt][j0 + j]) * H;
+          const int pos = s_pos[tt][j0 + j];
+          const TE* row = y_perm + static_cast<long>(MOE_DCHECK(pos, cap) ? pos : 0) * H;
 #pragma unroll
           for (int u = 0; u < U; ++u)
             if (cb + u * 256 < H) y[j][u].load(row + cb + u * 256);
@@ -725,5 +728,7 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
 #undef MOE_COMBINE
   return cudaGetLastError();
 }
+
+MOE_DEBUG_TAKER(take_dbg_align)
 
 }  // namespace moe

@@ -35,6 +35,7 @@
 #include "ptx.cuh"
 
 namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgGemm;
 namespace {
 
 constexpr int kThreads = 320;       // 10 warps
@@ -109,7 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int* __restrict__ group_start, int n_groups, int dense_T, int m_tiles,
                 int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
-                float* __restrict__ part, int m_valid, unsigned* status) {
+                float* __restrict__ part, int m_valid, unsigned* status,
+                const GemmBounds bnd) {
   constexpr bool kStaged = sizeof(TOut) == 2;
   using S = GemmShape<MODE, NMAX, kStaged, KPS>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
@@ -142,10 +144,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
   for (int i = threadIdx.x; i <= n_groups; i += kThreads)
     gstart[i] = tiles ? group_start[i] : i * dense_per;
+  // The debug build checks every entry and clamps a bad one into range, so
+  // that all roles still walk the same pipeline.
   auto tile_at = [&](int ti) -> Tile {
-    if (tiles) return tiles[ti];
-    const int s = ti / dense_per, t0 = (ti - s * dense_per) * NMAX;
-    return make_int4(s, t0, s * dense_T + t0, min(NMAX, dense_T - t0));
+    Tile tl;
+    if (tiles) {
+      tl = tiles[MOE_DCHECK(ti, bnd.max_tiles) ? ti : 0];
+    } else {
+      const int s = ti / dense_per, t0 = (ti - s * dense_per) * NMAX;
+      tl = make_int4(s, t0, s * dense_T + t0, min(NMAX, dense_T - t0));
+    }
+#if MOE_DEBUG_BUILD
+    if (!MOE_DCHECK(tl.x, n_groups)) tl.x = 0;
+    if (!MOE_DCHECK(tl.w - 1, NMAX)) tl.w = 1;
+    if (!b_from_out && !MOE_DCHECK(tl.y, bnd.b_rows - tl.w + 1)) tl.y = 0;
+    if (!MOE_DCHECK(tl.z, (b_from_out ? min(bnd.b_rows, bnd.out_rows) : bnd.out_rows) - tl.w + 1))
+      tl.z = 0;
+#endif
+    return tl;
   };
 
   const int warp = threadIdx.x >> 5;
@@ -212,6 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = tile_at(ti);
         const int b_row = b_from_out ? tl.z : tl.y;
         const int kb1 = min(k_blocks, (ks + 1) * kb_per);
+        (void)MOE_DCHECK(tl.x * static_cast<long>(a_rows_per_expert) + m * 128 +
+                             (MODE == kGemmSiluUp ? a_up_offset : 0),
+                         bnd.a_rows);
         for (int kb = ks * kb_per; kb < kb1; kb += KPS, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
@@ -331,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MODE == kGemmSiluUp) {
             float w[16];
             ptx::tmem_ld16x2(tb + c0, tb + NMAX + c0, v, w);
-            if (row_ok) {
+            if (row_ok && MOE_DCHECK(row + a_up_offset, out_ld)) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 if (c0 + j < tl.w) {
@@ -342,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             ptx::tmem_ld16(tb + c0, v);
-            if (row_ok) {
+            if (row_ok && MOE_DCHECK(row, out_ld)) {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 if (c0 + j < tl.w) prow[static_cast<long>(c0 + j) * out_ld] = v[j];
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int t = k * 8 + t_out;
-            if (c0 + t < tl.w && cols_ok) {
+            if (c0 + t < tl.w && cols_ok && MOE_DCHECK(m * 128 + c8 + 7, out_ld)) {
               const uint4 val = *reinterpret_cast<const uint4*>(sb + t * 128 + c8);
               *reinterpret_cast<uint4*>(out + static_cast<long>(tl.z + c0 + t) * out_ld +
                                         m * 128 + c8) = val;
@@ -407,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           ptx::tmem_ld16(tb + c0, v);
         }
-        if (row_ok) {
+        if (row_ok && MOE_DCHECK(row, out_ld)) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c0 + j < tl.w) orow[static_cast<long>(c0 + j) * out_ld] = to_out<TOut>(v[j]);
@@ -437,7 +456,7 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
   return launch_pdl(kern, dim3(num_sms), dim3(kThreads), S::kSmemBytes, st, *a.mapA, *a.mapB,
                     a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
                     a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),
-                    a.out_ld, a.split_stride, a.part, a.m_valid, a.status);
+                    a.out_ld, a.split_stride, a.part, a.m_valid, a.status, a.bnd);
 }
 
 }  // namespace
@@ -445,6 +464,9 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
   if (a.k_split < 1 || (a.k_split > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
+  if (MOE_DEBUG_BUILD && (a.bnd.a_rows <= 0 || a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 ||
+                          (a.tiles && a.bnd.max_tiles <= 0)))
+    return cudaErrorInvalidValue;
   if (nmax != 32 && nmax != 128 && nmax != 256) return cudaErrorInvalidValue;
   if (nmax == 256) {  // prefill-sized segments, bf16 only
     if (tf32) return cudaErrorInvalidValue;
@@ -490,5 +512,6 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
 }
 
 MOE_WAIT_LIMIT_SETTER(set_wait_limit_gemm)
+MOE_DEBUG_TAKER(take_dbg_gemm)
 
 }  // namespace moe

@@ -37,6 +37,7 @@
 #include "ptx.cuh"
 
 namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgGemmPair;
 namespace {
 
 constexpr int kThreads = 320;
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   int k_blocks, int a_rows_per_expert, int a_up_offset, int b_from_out,
                   __nv_bfloat16* __restrict__ out, long out_ld,
                   const int32_t* __restrict__ out_rows, const float* __restrict__ out_scale,
-                  int b_cap, unsigned* status) {
+                  int b_cap, unsigned* status, const GemmBounds bnd) {
   using S = PairShape<MODE, NMAX, KPS>;
   const int n_st = k_blocks / KPS;  // stages per unit (k_blocks is a multiple of KPS)
   const uint32_t rank = ptx::cluster_rank();
@@ -142,17 +143,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i <= n_groups; i += kThreads)
     gstart[i] = tiles ? group_start[i] : i * dense_per;
   auto tile_at = [&](int ti) -> Tile {
-    if (tiles) return tiles[ti];
+    if (tiles) return tiles[MOE_DCHECK(ti, bnd.max_tiles) ? ti : 0];
     const int sl = ti / dense_per, t0 = (ti - sl * dense_per) * NMAX;
     return make_int4(sl, t0, sl * dense_T + t0, min(NMAX, dense_T - t0));
   };
   // A tile table entry every role can act on: a valid width and, when the
   // row count b_cap of the position space is given, rows inside it. Every
   // role skips the same entries (and flags them), so their pipelines stay
-  // in step.
+  // in step. The debug build also checks the entry against the buffers'
+  // extents.
   auto tile_ok = [&](const Tile& tl) {
     return tl.w >= 1 && tl.w <= NMAX && tl.x >= 0 && tl.y >= 0 && tl.z >= 0 &&
-           (b_cap <= 0 || (tl.y <= b_cap - tl.w && tl.z <= b_cap - tl.w));
+           (b_cap <= 0 || (tl.y <= b_cap - tl.w && tl.z <= b_cap - tl.w)) &&
+           MOE_DCHECK(tl.x, n_groups) &&
+           MOE_DCHECK(b_from_out ? tl.z : tl.y, bnd.b_rows - tl.w + 1) &&
+           MOE_DCHECK(tl.z, (out_rows ? bnd.out_map : bnd.out_rows) - tl.w + 1);
   };
 
   const int warp = threadIdx.x >> 5;
@@ -236,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int n_mma = (tl.w + 31) & ~31;
         const int b_row = (b_from_out ? tl.z : tl.y) + static_cast<int>(rank) * (n_mma >> 1);
+        (void)MOE_DCHECK(tl.x * static_cast<long>(a_rows_per_expert) +
+                             m * (MODE == kGemmSiluUp ? 128 : 256) +
+                             (MODE == kGemmSiluUp ? a_up_offset : 0),
+                         bnd.a_rows);
         for (int j = 0; j < n_st; ++j, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
@@ -393,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const int t = k * 8 + (r64 >> 3);
-            if (col + t < tl.w) {
+            if (col + t < tl.w && MOE_DCHECK(h_col0 + (r64 & 7) * 8 + 7, out_ld)) {
               const uint4 val = *reinterpret_cast<const uint4*>(sb + t * 64 + (r64 & 7) * 8);
               *reinterpret_cast<uint4*>(out + static_cast<long>(tl.z + col + t) * out_ld +
                                         h_col0 + (r64 & 7) * 8) = val;
@@ -418,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 2; ++k) {
             const int t = c0 + k * 8 + t_out;
             dst[it][k] = t < tl.w ? (out_rows ? out_rows[tl.z + t] : tl.z + t) : -1;
+            if (dst[it][k] >= 0 && !MOE_DCHECK(dst[it][k], bnd.out_rows)) dst[it][k] = -1;
           }
           scl[it] = (out_scale && (lane & 15) + c0 < tl.w) ? out_scale[tl.z + c0 + (lane & 15)]
                                                            : 1.f;
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
-            if (dst[it][k] >= 0) {
+            if (dst[it][k] >= 0 && MOE_DCHECK(y_col0 + c8 + 7, out_ld)) {
               const uint4 val =
                   *reinterpret_cast<const uint4*>(sb + (k * 8 + t_out) * 128 + c8);
               *reinterpret_cast<uint4*>(out + static_cast<long>(dst[it][k]) * out_ld + y_col0 +
@@ -493,7 +503,7 @@ cudaError_t launch_pair_variant(const GemmArgs& a, int num_sms, cudaStream_t st)
   return counted(cudaLaunchKernelEx(&cfg, kern, *a.mapA, *a.mapB, a.tiles, a.group_start, a.n_groups,
                             a.dense_T, a.m_tiles, a.k_blocks, a.a_rows_per_expert, a.a_up_offset,
                             a.b_from_out, static_cast<__nv_bfloat16*>(a.out), a.out_ld,
-                            a.out_rows, a.out_scale, a.b_cap, a.status));
+                            a.out_rows, a.out_scale, a.b_cap, a.status, a.bnd));
 }
 
 }  // namespace
@@ -502,6 +512,9 @@ cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num
                              cudaStream_t st) {
   if ((a.tiles == nullptr && a.dense_T <= 0) || a.k_split != 1) return cudaErrorInvalidValue;
   if (a.out_rows && mode != kGemmPlain) return cudaErrorInvalidValue;
+  if (MOE_DEBUG_BUILD && (a.bnd.a_rows <= 0 || a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 ||
+                          (a.tiles && a.bnd.max_tiles <= 0) || (a.out_rows && a.bnd.out_map <= 0)))
+    return cudaErrorInvalidValue;
   const bool two = a.k_blocks % 2 == 0;  // two K blocks per stage when they pair up
   if (nmax == 256 && mode == kGemmPlain)
     return two ? launch_pair_variant<kGemmPlain, 256, 2>(a, num_sms, st)
@@ -513,5 +526,6 @@ cudaError_t launch_gemm_pair(GemmMode mode, int nmax, const GemmArgs& a, int num
 }
 
 MOE_WAIT_LIMIT_SETTER(set_wait_limit_gemm_pair)
+MOE_DEBUG_TAKER(take_dbg_gemm_pair)
 
 }  // namespace moe

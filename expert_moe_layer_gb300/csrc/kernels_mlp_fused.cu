@@ -27,7 +27,11 @@
 // 8 blocks x I/128, then loads the h rows. All GEMM1 units precede all GEMM2
 // units in every CTA's sequence, so GEMM1 work never waits and no wait can
 // deadlock once every CTA is resident (one CTA per SM; a wait that runs out
-// sets MOE_DEV_TIMEOUT). The counters are zeroed before the kernel.
+// sets MOE_DEV_TIMEOUT). The launch is cooperative, so the runtime starts the
+// grid only when all its CTAs can be resident together (after kernels of
+// other streams free their SMs) and refuses a grid that never can be (fewer
+// SMs for this context, as under an MPS limit); the caller then runs the two
+// GEMM kernels instead. The counters are zeroed before the kernel.
 //
 // Stage layout (40 KB): two 128-row weight boxes and two token-row boxes of
 // 32 rows, each box 128 bytes of K with the 128-byte swizzle.
@@ -44,6 +48,7 @@
 #include "ptx.cuh"
 
 namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgMlpFused;
 namespace {
 
 constexpr int kThreads = 320;
@@ -162,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   int ks1, float* __restrict__ part, long part_stride,
                   int* __restrict__ split_cnt, int* __restrict__ ready,
                   __nv_bfloat16* __restrict__ h_out, __nv_bfloat16* __restrict__ y_out,
-                  unsigned* status) {
+                  unsigned* status, const GemmBounds bnd) {
   const int m1 = I / 128, m2 = H / 128;
   const int kb1 = H / 64, kb2 = I / 64;
   const int kb_per = (kb1 + ks1 - 1) / ks1;
@@ -215,14 +220,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = gstart[n_groups];
   const int U1 = n_tiles * m1 * ks1;
   const int total = U1 + n_tiles * m2;
+  // A unit's tile. The debug build checks the tile index and the entry (the
+  // rows of x_perm, h and y are b_rows = out_rows) and clamps a bad one, so
+  // that every role still walks the same pipeline.
+  auto unit_tile = [&](UnitInfo& ui) -> Tile {
+    if (!MOE_DCHECK(ui.ti, bnd.max_tiles)) ui.ti = 0;
+    Tile tl = tiles[ui.ti];
+#if MOE_DEBUG_BUILD
+    if (!MOE_DCHECK(tl.x, n_groups)) tl.x = 0;
+    if (!MOE_DCHECK(tl.w - 1, kNmax)) tl.w = 1;
+    if (!MOE_DCHECK(tl.y, bnd.b_rows - tl.w + 1)) tl.y = 0;
+    if (!MOE_DCHECK(tl.z, bnd.out_rows - tl.w + 1)) tl.z = 0;
+#endif
+    return tl;
+  };
 
   // weight boxes of the first stages before the wait
   int pre = 0;
   {
     if (warp == 0 && lane == 0) {
       for (int u = blockIdx.x; u < U1 && pre < kStages; u += gridDim.x) {
-        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
-        const Tile tl = tiles[ui.ti];
+        UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+        const Tile tl = unit_tile(ui);
         const int arow = tl.x * 2 * I + ui.m * 128;
         for (int j = 0; j < ui.n_st && pre < kStages; ++j, ++pre) {
           const uint32_t st = sbase + pre * kStageBytes, fb = full0 + 8 * pre;
@@ -243,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
-      const Tile tl = tiles[ui.ti];
+      UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+      const Tile tl = unit_tile(ui);
       if (!ui.g2) {
         // token rows from x_perm (segment rows tl.y ..) with TMA
         if (lane == 0) {
@@ -327,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, ai = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
-        const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
-        const Tile tl = tiles[ui.ti];
+        UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+        const Tile tl = unit_tile(ui);
         const int n_mma = (tl.w + 15) & ~15;
         const uint32_t idesc = ptx::idesc_make(1u, 128, n_mma);
         const int b = ai % kNAcc;
@@ -387,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int blk = warp - 2;                     // this warp's 32 x 16 block of a unit
     int ai = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
-      const UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
-      const Tile tl = tiles[ui.ti];
+      UnitInfo ui = unit_info(u, U1, gstart, n_groups, m1, m2, kb1, kb2, ks1, kb_per);
+      const Tile tl = unit_tile(ui);
       const int b = ai % kNAcc;
       const uint32_t aph = (ai / kNAcc) & 1;
       if (!ptx::mbar_wait(tfull0 + 8 * b, aph, abort_flag, status)) break;
@@ -479,12 +498,16 @@ cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st
   if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups || a.ks1 < 1 ||
       a.ks1 > kMaxSplit || (a.ks1 > 1 && (!a.part || !a.split_cnt)))
     return cudaErrorInvalidValue;
-  return launch_pdl(moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st, *a.mapW13,
-                    *a.mapW2, *a.mapH, *a.mapX, a.tiles, a.group_start, a.n_groups, a.H, a.I,
-                    a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
-                    static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y), a.status);
+  if (MOE_DEBUG_BUILD && (a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 || a.bnd.max_tiles <= 0))
+    return cudaErrorInvalidValue;
+  return launch_pdl_ex(true, moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st,
+                       *a.mapW13, *a.mapW2, *a.mapH, *a.mapX, a.tiles, a.group_start,
+                       a.n_groups, a.H, a.I, a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
+                       static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y),
+                       a.status, a.bnd);
 }
 
 MOE_WAIT_LIMIT_SETTER(set_wait_limit_mlp_fused)
+MOE_DEBUG_TAKER(take_dbg_mlp_fused)
 
 }  // namespace moe

@@ -7,6 +7,11 @@
 #include "internal.h"
 #include "launch.cuh"
 #include "ptx.cuh"
+
+namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgRoute;  // before topk_warp.cuh, which checks ids
+}  // namespace moe
+
 #include "topk_warp.cuh"
 
 namespace moe {
@@ -632,5 +637,6 @@ cudaError_t launch_topk(const float* logits, int n_part, long partial_stride,
 }
 
 MOE_WAIT_LIMIT_SETTER(set_wait_limit_route)
+MOE_DEBUG_TAKER(take_dbg_route)
 
 }  // namespace moe

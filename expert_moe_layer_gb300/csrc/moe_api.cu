@@ -11,6 +11,11 @@
 
 #include "internal.h"
 #include "launch.cuh"
+
+namespace moe {
+constexpr DbgFile kDbgFileCode = kDbgApi;  // before topk_warp.cuh
+}  // namespace moe
+
 #include "topk_warp.cuh"
 #include "moe.h"
 
@@ -21,6 +26,24 @@ constexpr int kMaxT = 1 << 18;
 constexpr int kForwardBlock = 1;    // moe_forward leaves segments unpadded (the GEMMs
                                     // read past a segment's end but never store there)
 constexpr size_t kAlignBytes = 256;
+
+// The failure behind the calling thread's latest MOE_ERR_CUDA, reported by
+// moe_last_cuda_error: a cudaError_t, or kEncodeErrorBase + the CUresult of a
+// tensor-map encoding that failed.
+constexpr int kEncodeErrorBase = 10000;
+thread_local int g_last_cuda_error = 0;
+
+int fail_cuda(int code) {
+  g_last_cuda_error = code;
+  return MOE_ERR_CUDA;
+}
+int cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : fail_cuda(static_cast<int>(e)); }
+
+#define MOE_TRY(x)              \
+  do {                          \
+    const int _rc = (x);        \
+    if (_rc != MOE_OK) return _rc; \
+  } while (0)
 
 size_t rup(size_t v) { return (v + kAlignBytes - 1) / kAlignBytes * kAlignBytes; }
 int ebytes(moe_dtype d) { return d == MOE_BF16 ? 2 : 4; }
@@ -183,11 +206,12 @@ bool shared_on_pairs(const moe_config* c, int T) {
 int sm_count() {
   static int cache[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev < 0 || dev >= 64) return 0;
+  if (cuda_ok(cudaGetDevice(&dev)) != MOE_OK) return 0;
+  if (dev < 0 || dev >= 64) return fail_cuda(static_cast<int>(cudaErrorInvalidDevice)), 0;
   if (!cache[dev]) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (cuda_ok(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != MOE_OK)
+      return 0;
     cache[dev] = n;
   }
   return cache[dev];
@@ -209,11 +233,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D row-major [rows, cols] map; box = 128 bytes of a row x box_rows rows,
-// 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long cols,
-              int box_rows) {
+// 128-byte swizzle, zero fill out of bounds. MOE_OK or MOE_ERR_CUDA.
+int make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long cols,
+             int box_rows) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) return fail_cuda(static_cast<int>(cudaErrorSymbolNotFound));
   const int eb = ebytes(dt);
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * eb};
@@ -221,9 +245,20 @@ bool make_map(CUtensorMap* m, const void* base, moe_dtype dt, long rows, long co
   cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType t =
       dt == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  return fn(m, t, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, t, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : fail_cuda(kEncodeErrorBase + static_cast<int>(r));
+}
+
+// Output extents of a GEMM launch for the debug build's checks: rows of out,
+// entries of the tile table, entries of an out_rows map.
+GemmBounds out_bounds(long out_rows, int max_tiles = 0, long out_map = 0) {
+  GemmBounds b;
+  b.out_rows = out_rows;
+  b.max_tiles = max_tiles;
+  b.out_map = out_map;
+  return b;
 }
 
 // One grouped GEMM launch. A = weights [slabs*rows_per_slab, Kdim]; B = token
@@ -234,12 +269,12 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
              long split_stride = 0, int dense_T = 0, bool pair = false,
              float* part = nullptr, const int32_t* out_rows = nullptr,
-             const float* out_scale = nullptr, int b_cap = 0) {
+             const float* out_scale = nullptr, int b_cap = 0, GemmBounds bnd = {}) {
   CUtensorMap ma, mb;
   // CTA pairs in SiLU mode stage 64 gate and 64 up rows per CTA: 64-row boxes
   const int a_box = (pair && mode == kGemmSiluUp) ? 64 : 128;
-  if (!make_map(&ma, A, dt, a_rows, Kdim, a_box)) return MOE_ERR_CUDA;
-  if (!make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax)) return MOE_ERR_CUDA;
+  MOE_TRY(make_map(&ma, A, dt, a_rows, Kdim, a_box));
+  MOE_TRY(make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax));
   GemmArgs g;
   g.mapA = &ma;
   g.mapB = &mb;
@@ -262,11 +297,13 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.b_cap = b_cap;
   g.m_valid = m_valid;
   g.status = status;
+  bnd.a_rows = a_rows;
+  bnd.b_rows = b_rows;
+  g.bnd = bnd;
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
-  if (pair) return launch_gemm_pair(mode, nmax, g, sms, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  return launch_gemm(mode, dt == MOE_F32, nmax, g, sms, st) == cudaSuccess ? MOE_OK
-                                                                           : MOE_ERR_CUDA;
+  if (pair) return cuda_ok(launch_gemm_pair(mode, nmax, g, sms, st));
+  return cuda_ok(launch_gemm(mode, dt == MOE_F32, nmax, g, sms, st));
 }
 
 // -------------------------------------------------------------- layouts
@@ -412,26 +449,20 @@ P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
 }
 
-int cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Record a caller's timing event on `st`. Under stream capture the event
 // becomes an event-record node, so a replayed graph still timestamps stages.
 int record_event(void* ev, cudaStream_t st) {
   if (!ev) return MOE_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY(cuda_ok(cudaStreamIsCapturing(st, &cs)));
   const cudaError_t e =
       cs == cudaStreamCaptureStatusActive
           ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st, cudaEventRecordExternal)
           : cudaEventRecord(static_cast<cudaEvent_t>(ev), st);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return cuda_ok(e);
 }
 
-#define MOE_TRY(x)              \
-  do {                          \
-    const int _rc = (x);        \
-    if (_rc != MOE_OK) return _rc; \
-  } while (0)
 
 // ------------------------------------------------------------- stage bodies
 int do_route(const moe_config* c, int T, const void* x, const void* router_w,
@@ -444,7 +475,8 @@ int do_route(const moe_config* c, int T, const void* x, const void* router_w,
     n_part = router_ksplit(c, T);
     MOE_TRY(run_gemm(kGemmLogits, MOE_BF16, nm, router_w, E, x, T, H, nullptr, nullptr, 1,
                      (E + 127) / 128, 0, 0, 0, logits, E, E, status, st, n_part,
-                     static_cast<long>(T) * E, T, false, logits));
+                     static_cast<long>(T) * E, T, false, logits, nullptr, nullptr, 0,
+                     out_bounds(T)));
   } else {
     n_part = router_ksplit(c, T);
     MOE_TRY(cuda_ok(launch_router_logits(c->act_dtype == MOE_BF16, c->router_dtype == MOE_BF16,
@@ -479,11 +511,10 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   if (fused) {
     const int ks = gemm1_ksplit(c, T);
     CUtensorMap m13, m2, mh, mx;
-    if (!make_map(&m13, w13, c->act_dtype, static_cast<long>(El) * 2 * I, H, 128) ||
-        !make_map(&m2, w2, c->act_dtype, static_cast<long>(El) * H, I, 128) ||
-        !make_map(&mh, h_perm, c->act_dtype, cap, I, 32) ||
-        !make_map(&mx, x_perm, c->act_dtype, cap, H, 32))
-      return MOE_ERR_CUDA;
+    MOE_TRY(make_map(&m13, w13, c->act_dtype, static_cast<long>(El) * 2 * I, H, 128));
+    MOE_TRY(make_map(&m2, w2, c->act_dtype, static_cast<long>(El) * H, I, 128));
+    MOE_TRY(make_map(&mh, h_perm, c->act_dtype, cap, I, 32));
+    MOE_TRY(make_map(&mx, x_perm, c->act_dtype, cap, H, 32));
     MlpFusedArgs a;
     a.mapW13 = &m13;
     a.mapW2 = &m2;
@@ -502,25 +533,36 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     a.h = h_perm;
     a.y = y_perm;
     a.status = status;
+    a.bnd = out_bounds(cap, max_tiles);
+    a.bnd.a_rows = static_cast<long>(El) * 2 * I;
+    a.bnd.b_rows = cap;
     const int sms = sm_count();
     if (sms <= 0) return MOE_ERR_CUDA;
-    MOE_TRY(cuda_ok(launch_mlp_fused(a, sms, st)));
-    if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
-    return MOE_OK;
+    const cudaError_t e = launch_mlp_fused(a, sms, st);
+    if (e != cudaErrorCooperativeLaunchTooLarge) {
+      MOE_TRY(cuda_ok(e));
+      if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
+      return MOE_OK;
+    }
+    // not every CTA can be resident on the SMs this context may use: clear
+    // the launch error and run the two GEMM kernels on the same tile table
+    (void)cudaGetLastError();
   }
   const int ks1 = pairs ? 1 : gemm1_ksplit(c, T);  // pairs: long segments, never split
   if (ks1 > 1) {
     // split over K: raw gate/up partials, then the SiLU*up epilogue
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, 2 * I, I, status,
-                     st, ks1, static_cast<long>(cap) * 2 * I, 0, false, part1));
+                     st, ks1, static_cast<long>(cap) * 2 * I, 0, false, part1, nullptr, nullptr,
+                     0, out_bounds(cap, max_tiles)));
     MOE_TRY(cuda_ok(launch_silu_finalize(c->act_dtype == MOE_BF16, part1, ks1,
                                          static_cast<long>(cap) * 2 * I, offsets + El, cap, I,
                                          h_perm, st)));
   } else {
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st,
-                     1, 0, 0, pairs, nullptr, nullptr, nullptr, pairs ? cap : 0));
+                     1, 0, 0, pairs, nullptr, nullptr, nullptr, pairs ? cap : 0,
+                     out_bounds(cap, max_tiles)));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
   // with y_rows (CTA pairs only) GEMM2 writes segment position p to row
@@ -528,7 +570,9 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   MOE_TRY(run_gemm(kGemmPlain, c->act_dtype, nmax, w2, static_cast<long>(El) * H, h_perm, cap, I,
                    tiles, groups, El, H / (pairs ? 256 : 128), H, 0, 0, y_perm, H, H, status, st,
                    1, 0, 0, pairs, nullptr, pairs ? y_rows : nullptr,
-                   pairs && y_rows ? w_perm : nullptr, pairs ? cap : 0));
+                   pairs && y_rows ? w_perm : nullptr, pairs ? cap : 0,
+                   pairs && y_rows ? out_bounds(n_items, max_tiles, cap)
+                                   : out_bounds(cap, max_tiles)));
   return MOE_OK;
 }
 
@@ -922,10 +966,12 @@ static int forward_impl(const moe_config* cfg, int T, const void* x, const void*
     void* y_sh = at<void>(ws, L.y_sh);
     MOE_TRY(run_gemm(kGemmSiluUp, cfg->act_dtype, nm, shared_w13, static_cast<long>(S) * 2 * Is,
                      x, T, H, nullptr, nullptr, S, Is / 128, 2 * Is, Is, 0, h_sh, Is, Is, status,
-                     st, 1, 0, T, sp));
+                     st, 1, 0, T, sp, nullptr, nullptr, nullptr, 0,
+                     out_bounds(static_cast<long>(S) * T)));
     MOE_TRY(run_gemm(kGemmPlain, cfg->act_dtype, nm, shared_w2, static_cast<long>(S) * H, h_sh,
                      static_cast<long>(S) * T, Is, nullptr, nullptr, S, H / (sp ? 256 : 128), H,
-                     0, 1, y_sh, H, H, status, st, 1, 0, T, sp));
+                     0, 1, y_sh, H, H, status, st, 1, 0, T, sp, nullptr, nullptr, nullptr, 0,
+                     out_bounds(static_cast<long>(S) * T)));
     shared_y = y_sh;
   }
   MOE_TRY(mark(6));
@@ -962,22 +1008,70 @@ int moe_set_wait_limit_ns(uint64_t ns) {
       set_wait_limit_gemm, set_wait_limit_gemm_pair, set_wait_limit_mlp_fused,
       set_wait_limit_route};
   for (auto set : setters)
-    if (set(v) != cudaSuccess) return MOE_ERR_CUDA;
+    MOE_TRY(cuda_ok(set(v)));
   return MOE_OK;
 }
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 int moe_get_status(const void* ws, void* stream, uint32_t* flags) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
-  if (cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY(cuda_ok(cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st)));
+  MOE_TRY(cuda_ok(cudaStreamSynchronize(st)));
   if (flags) *flags = v;
   if (v == 0) return MOE_OK;
   return (v & MOE_DEV_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_STATUS;
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Debug build (MOE_DEBUG): the bounds-check records of every translation unit.
+namespace moe {
+namespace {
+
+// One failed check and no memory access, so that a test can see the record
+// path of the debug build work.
+__global__ void dbg_selftest_kernel(int i, int n) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) (void)MOE_DCHECK(i, n);
+}
+
+}  // namespace
+
+MOE_DEBUG_TAKER(take_dbg_api)
+
+}  // namespace moe
+
+extern "C" int moe_debug_build(void) { return MOE_DEBUG_BUILD; }
+
+extern "C" int moe_debug_take(moe_debug_record* rec) {
+  if (!rec) return MOE_ERR_INVALID_ARG;
+  std::memset(rec, 0, sizeof(*rec));
+  if (!MOE_DEBUG_BUILD) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(cuda_ok(cudaDeviceSynchronize()));
+  cudaError_t (*const takers[])(DbgRecord*) = {take_dbg_api,       take_dbg_gemm,
+                                               take_dbg_gemm_pair, take_dbg_mlp_fused,
+                                               take_dbg_route,     take_dbg_align};
+  for (auto take : takers) {
+    DbgRecord r = {};
+    MOE_TRY(cuda_ok(take(&r)));
+    if (r.count && !rec->count) {
+      rec->site = r.site;
+      rec->index = r.index;
+      rec->bound = r.bound;
+    }
+    rec->count += r.count;
+  }
+  return MOE_OK;
+}
+
+extern "C" int moe_debug_selftest(void* stream) {
+  if (!MOE_DEBUG_BUILD) return MOE_ERR_UNSUPPORTED;
+  dbg_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(5, 4);
+  return cuda_ok(cudaGetLastError());
+}
 
 // ---------------------------------------------------------------------------
 // moe_align_permute_noalloc: the align/permute launch with its scratch in a
@@ -996,8 +1090,8 @@ namespace {
 // that first call belongs before any stream capture.
 int noalloc_scratch(void** out) {
   void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, moe_align_noalloc_scratch) != cudaSuccess || !p)
-    return MOE_ERR_CUDA;
+  MOE_TRY(cuda_ok(cudaGetSymbolAddress(&p, moe_align_noalloc_scratch)));
+  if (!p) return fail_cuda(static_cast<int>(cudaErrorInvalidSymbol));
   *out = p;
   return MOE_OK;
 }

@@ -20,6 +20,8 @@
 
 #include <cstdint>
 
+#include "dbg.cuh"  // the including unit declares moe::kDbgFileCode first
+
 namespace moe {
 
 // flags of the routing kernels
@@ -160,6 +162,7 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
     }
   }
   if (lane < K) {
+    (void)MOE_DCHECK(my_id, E);
     ids_row[lane] = my_id;
     w_row[lane] = renorm ? my_w / wsum : my_w;
   }

@@ -58,6 +58,15 @@
 extern "C" {
 #endif
 
+/* The entry points below are the library's only exported symbols; it is
+ * compiled with hidden visibility, so that two builds loaded in one process
+ * (libmoe.so and libmoe_debug.so) share no internal state. */
+#if defined(__GNUC__) || defined(__clang__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* bad config, size, pointer or alignment     */
@@ -144,7 +153,7 @@ typedef struct {
 #define MOE_BIAS_SELECT 1
 
 /* Human-readable name of a moe_status. Never NULL. */
-const char* moe_strerror(int status);
+MOE_API const char* moe_strerror(int status);
 
 /* Host-only validation of a config (no CUDA call). Returns MOE_OK,
  * MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED. Checks: E % ep_size == 0 and
@@ -154,11 +163,11 @@ const char* moe_strerror(int status);
  * H and I multiples of 128, S >= 0 with I_s a multiple of 128 when S > 0.
  * Kernel limits (MOE_ERR_UNSUPPORTED): E <= 512, K <= 32, n_group <= 32,
  * E_local <= 1024, S <= 1024, and act_dtype F32 needs router_dtype F32. */
-int moe_validate_config(const moe_config* cfg);
+MOE_API int moe_validate_config(const moe_config* cfg);
 
 /* Rows of the padded permutation buffers for T tokens and segment padding
  * block_m: T*K + E_local*(block_m-1). Returns 0 on an invalid config. */
-size_t moe_align_cap(const moe_config* cfg, int T, int block_m);
+MOE_API size_t moe_align_cap(const moe_config* cfg, int T, int block_m);
 
 /* ------------------------------------------------------------------------ */
 /* moe_route: router logits, fp32 softmax over E, top-k, renormalise.
@@ -175,10 +184,10 @@ size_t moe_align_cap(const moe_config* cfg, int T, int block_m);
  *                       (renormalised to sum 1 when cfg->renormalize).
  *                       routed_scaling_factor is NOT applied here.
  * ws: moe_route_workspace_size(cfg, T) bytes (status word + fp32 logits). */
-size_t moe_route_workspace_size(const moe_config* cfg, int T);
-int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
-              const float* router_bias, int32_t* topk_ids, float* topk_w,
-              void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_route_workspace_size(const moe_config* cfg, int T);
+MOE_API int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
+                      const float* router_bias, int32_t* topk_ids, float* topk_w,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_align_permute: keep local experts, sort work items by local expert.
@@ -202,11 +211,11 @@ int moe_route(const moe_config* cfg, int T, const void* x, const void* router_w,
  *   cap         rows of sorted_ids. Must be >= moe_align_cap(cfg,T,block_m),
  *               else MOE_ERR_WORKSPACE.
  * ws: moe_align_workspace_size(cfg, T) bytes. */
-size_t moe_align_workspace_size(const moe_config* cfg, int T);
-int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
-                      const int32_t* expert_map, int block_m, int32_t* counts,
-                      int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
-                      int cap, void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_align_workspace_size(const moe_config* cfg, int T);
+MOE_API int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
+                              const int32_t* expert_map, int block_m, int32_t* counts,
+                              int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
+                              int cap, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_align_permute_noalloc: moe_align_permute for callers that cannot
  * allocate device memory. The source pages have no counterpart to this entry
@@ -239,10 +248,10 @@ int moe_align_permute(const moe_config* cfg, int T, const int32_t* topk_ids,
  *     Out-of-range expert ids are still dropped, exactly as moe_align_permute
  *     drops them. */
 #define MOE_ALIGN_NOALLOC_SCRATCH_BYTES (1u << 20)
-int moe_align_permute_noalloc(const moe_config* cfg, int T, const int32_t* topk_ids,
-                              const int32_t* expert_map, int block_m, int32_t* counts,
-                              int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
-                              int cap, void* stream);
+MOE_API int moe_align_permute_noalloc(const moe_config* cfg, int T, const int32_t* topk_ids,
+                                      const int32_t* expert_map, int block_m, int32_t* counts,
+                                      int32_t* offsets, int32_t* sorted_ids, int32_t* inv_pos,
+                                      int cap, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_grouped_mlp: the local experts' SiLU-gated MLPs on permuted rows.
@@ -261,12 +270,12 @@ int moe_align_permute_noalloc(const moe_config* cfg, int T, const int32_t* topk_
  * kind::tf32), with fp32 accumulation. The SiLU*up product is rounded to
  * act_dtype between them.
  * ws: moe_grouped_mlp_workspace_size(cfg, T, cap) bytes. */
-size_t moe_grouped_mlp_workspace_size(const moe_config* cfg, int T, int cap);
-int moe_grouped_mlp(const moe_config* cfg, int T, const void* x,
-                    const int32_t* sorted_ids, const int32_t* counts,
-                    const int32_t* offsets, int cap, const void* w13,
-                    const void* w2, void* y_perm, void* ws, size_t ws_bytes,
-                    void* stream);
+MOE_API size_t moe_grouped_mlp_workspace_size(const moe_config* cfg, int T, int cap);
+MOE_API int moe_grouped_mlp(const moe_config* cfg, int T, const void* x,
+                            const int32_t* sorted_ids, const int32_t* counts,
+                            const int32_t* offsets, int cap, const void* w13,
+                            const void* w2, void* y_perm, void* ws, size_t ws_bytes,
+                            void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_combine: weighted gather back to token order.
@@ -282,10 +291,10 @@ int moe_grouped_mlp(const moe_config* cfg, int T, const void* x,
  *   shared_out [T, H] act_dtype, nullable
  *   out        [T, H] act_dtype out
  * ws: NULL, or >= 4 bytes for the status word. */
-int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap,
-                const int32_t* inv_pos, const float* topk_w,
-                const void* shared_out, void* out, void* ws, size_t ws_bytes,
-                void* stream);
+MOE_API int moe_combine(const moe_config* cfg, int T, const void* y_perm, int cap,
+                        const int32_t* inv_pos, const float* topk_w,
+                        const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_forward: the whole layer (route -> align/permute -> grouped MLP of the
@@ -310,13 +319,13 @@ typedef struct {
   int block_m;    /* segment padding used by moe_forward */
 } moe_workspace_offsets;
 
-size_t moe_workspace_size(const moe_config* cfg, int T);
-int moe_workspace_layout(const moe_config* cfg, int T, moe_workspace_offsets* out);
-int moe_forward(const moe_config* cfg, int T, const void* x,
-                const void* router_w, const float* router_bias,
-                const void* w13, const void* w2, const void* shared_w13,
-                const void* shared_w2, const int32_t* expert_map, void* out,
-                void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_workspace_size(const moe_config* cfg, int T);
+MOE_API int moe_workspace_layout(const moe_config* cfg, int T, moe_workspace_offsets* out);
+MOE_API int moe_forward(const moe_config* cfg, int T, const void* x,
+                        const void* router_w, const float* router_bias,
+                        const void* w13, const void* w2, const void* shared_w13,
+                        const void* shared_w2, const int32_t* expert_map, void* out,
+                        void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward plus instrumentation. No page counterpart: this entry point is
  * there so that each kernel's duration can be measured live on the stream that
@@ -329,12 +338,12 @@ int moe_forward(const moe_config* cfg, int T, const void* x,
  * results are identical to moe_forward. When `stream` is being captured into a
  * CUDA graph, the events are recorded as external event nodes
  * (cudaEventRecordExternal), so every replay timestamps the stages. */
-int moe_forward_timed(const moe_config* cfg, int T, const void* x,
-                      const void* router_w, const float* router_bias,
-                      const void* w13, const void* w2, const void* shared_w13,
-                      const void* shared_w2, const int32_t* expert_map, void* out,
-                      void* ws, size_t ws_bytes, void* stream,
-                      void* const* events, int* kernels_launched);
+MOE_API int moe_forward_timed(const moe_config* cfg, int T, const void* x,
+                              const void* router_w, const float* router_bias,
+                              const void* w13, const void* w2, const void* shared_w13,
+                              const void* shared_w2, const int32_t* expert_map, void* out,
+                              void* ws, size_t ws_bytes, void* stream,
+                              void* const* events, int* kernels_launched);
 
 /* ------------------------------------------------------------------------ */
 /* Expert-parallel dispatch and combine: the rank-local halves of
@@ -372,11 +381,11 @@ int moe_forward_timed(const moe_config* cfg, int T, const void* x,
  *            [T*K] int32 out (token index); rows past send_offsets[ep_size]
  *            are left untouched.
  * ws: moe_ep_dispatch_workspace_size(cfg, T) bytes. */
-size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T);
-int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
-                    const float* topk_w, const int32_t* phys_map, int32_t* send_counts,
-                    int32_t* send_offsets, int32_t* send_pos, void* send_x, int32_t* send_ids,
-                    float* send_w, int32_t* send_tok, void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_ep_dispatch_workspace_size(const moe_config* cfg, int T);
+MOE_API int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* topk_ids,
+                            const float* topk_w, const int32_t* phys_map, int32_t* send_counts,
+                            int32_t* send_offsets, int32_t* send_pos, void* send_x, int32_t* send_ids,
+                            float* send_w, int32_t* send_tok, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_ep_expert_compute (step 3): the R items this rank received, each run
  * through its expert with top_k = 1 and weighted, as the page's call to
@@ -390,10 +399,10 @@ int moe_ep_dispatch(const moe_config* cfg, int T, const void* x, const int32_t* 
  *   y      [R, H] act_dtype out
  * cfg's top_k, shared experts, routed_scaling_factor and routing fields are
  * not used. ws: moe_ep_expert_compute_workspace_size(cfg, R) bytes. */
-size_t moe_ep_expert_compute_workspace_size(const moe_config* cfg, int R);
-int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
-                          const int32_t* recv_ids, const float* recv_w, const void* w13,
-                          const void* w2, void* y, void* ws, size_t ws_bytes, void* stream);
+MOE_API size_t moe_ep_expert_compute_workspace_size(const moe_config* cfg, int R);
+MOE_API int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
+                                  const int32_t* recv_ids, const float* recv_w, const void* w13,
+                                  const void* w2, void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_ep_combine (step 4): the rows returned to this rank (in its send
  * order) are added back by token, unweighted (the expert-holding rank applied
@@ -403,9 +412,9 @@ int moe_ep_expert_compute(const moe_config* cfg, int R, const void* recv_x,
  *   ret [T*K, H] act_dtype, send_pos [T*K] int32 (from moe_ep_dispatch),
  *   shared_out [T, H] nullable, out [T, H] act_dtype out.
  * ws: NULL, or >= 4 bytes for the status word. */
-int moe_ep_combine(const moe_config* cfg, int T, const void* ret, const int32_t* send_pos,
-                   const void* shared_out, void* out, void* ws, size_t ws_bytes,
-                   void* stream);
+MOE_API int moe_ep_combine(const moe_config* cfg, int T, const void* ret, const int32_t* send_pos,
+                           const void* shared_out, void* out, void* ws, size_t ws_bytes,
+                           void* stream);
 
 /* The kernel plan moe_forward follows for (cfg, T): which variant runs each
  * stage. No page counterpart; it describes this library's own kernels, for
@@ -422,10 +431,12 @@ typedef struct {
   int gemm1_k_split;       /* 1, or K ranges of GEMM1 whose fp32 partials are
                               summed by a finalize kernel or, fused, in-kernel */
   int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */
-  int fused_mlp;           /* 1: token gather, GEMM1 and GEMM2 in one
-                              persistent kernel                               */
+  int fused_mlp;           /* 1: GEMM1 and GEMM2 in one persistent kernel,
+                              launched cooperatively (every CTA resident at
+                              once); where the context's SMs cannot hold its
+                              grid, the call runs the two GEMM kernels       */
 } moe_plan;
-int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
+MOE_API int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 
 /* Sets the time limit of the library's pipeline waits on the current device,
  * in ns of the GPU's global timer; 0 restores the default of 1 s. No page
@@ -438,14 +449,58 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
  * returns (it synchronises with the device) until it is set again; a process
  * with several host threads must not change it while others launch. Returns
  * MOE_ERR_CUDA if a copy to the device fails. */
-int moe_set_wait_limit_ns(uint64_t ns);
+MOE_API int moe_set_wait_limit_ns(uint64_t ns);
+
+/* The failure behind the calling host thread's latest MOE_ERR_CUDA: the
+ * cudaError_t of the CUDA call that failed, or 10000 + the CUresult of a TMA
+ * tensor-map encoding that failed; 0 if no call of this thread has failed.
+ * Not cleared by later successful calls. No CUDA call. */
+MOE_API int moe_last_cuda_error(void);
 
 /* ------------------------------------------------------------------------ */
 /* Synchronises `stream` and reads the device status word at the start of
  * `ws`. Writes the raw MOE_DEV_* bits to *flags (nullable). Returns MOE_OK if
  * no flag is set, MOE_ERR_TIMEOUT if MOE_DEV_TIMEOUT is set, else
  * MOE_ERR_DEVICE_STATUS. MOE_ERR_CUDA if the synchronisation fails. */
-int moe_get_status(const void* ws, void* stream, uint32_t* flags);
+MOE_API int moe_get_status(const void* ws, void* stream, uint32_t* flags);
+
+/* ------------------------------------------------------------------------ */
+/* Debug build. No page counterpart: it stands in for a memory checker.
+ * libmoe_debug.so is this library compiled with MOE_DEBUG. Its kernels also
+ * check the indices they derive themselves and trust in libmoe.so: tile-table
+ * entries (index, expert, first row, row count) against the tile table and
+ * the permuted buffers, output rows and columns against the output, weight
+ * rows against the weight tensor, the sorted positions read by the gather
+ * and the combine, and the top-k ids against E. A failed check skips the
+ * access or clamps the value into range (the outputs are then unusable) and
+ * is counted in a device record, which also keeps the site, index and bound
+ * of the first failure. Same entry points and results otherwise; slower. */
+typedef struct {
+  uint32_t count; /* failed check evaluations since the last take (one bad
+                     value may be checked, and counted, several times)      */
+  uint32_t site;  /* first failure: file code * 65536 + source line; file
+                     codes 1 moe_api.cu, 2 kernels_gemm.cu,
+                     3 kernels_gemm_pair.cu, 4 kernels_mlp_fused.cu,
+                     5 kernels_route.cu (and topk_warp.cuh there),
+                     6 kernels_align.cu                                     */
+  int64_t index;  /* first failure: the index checked                       */
+  int64_t bound;  /* first failure: the bound; 0 <= index < bound failed    */
+} moe_debug_record;
+
+/* 1 in libmoe_debug.so, 0 in libmoe.so. No CUDA call. */
+MOE_API int moe_debug_build(void);
+
+/* Synchronises the current device, then reads and clears the records of
+ * the device code's translation units: *rec gets the sum of their counts
+ * and the first failure of the first unit with one, in file-code order.
+ * MOE_ERR_UNSUPPORTED (and *rec zeroed, no CUDA call) in libmoe.so;
+ * MOE_ERR_INVALID_ARG if rec is NULL; MOE_ERR_CUDA if a copy fails. */
+MOE_API int moe_debug_take(moe_debug_record* rec);
+
+/* libmoe_debug.so: enqueues one kernel on `stream` that fails one check
+ * (index 5 against bound 4) and touches no memory, so that a test can see a
+ * record arrive. MOE_ERR_UNSUPPORTED in libmoe.so. */
+MOE_API int moe_debug_selftest(void* stream);
 
 #ifdef __cplusplus
 }

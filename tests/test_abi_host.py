@@ -18,6 +18,53 @@ def test_library_exports_every_header_function():
     assert set(names) == set(B._SIGS)
 
 
+def test_debug_library_exports_every_header_function():
+    L = B.lib(debug=True)
+    for n in B.header_functions():
+        assert hasattr(L, n), f"{n} declared in include/moe.h but not in libmoe_debug.so"
+    # the build flag is a plain host function in both libraries
+    assert L.moe_debug_build() == 1
+    assert B.lib(debug=False).moe_debug_build() == 0
+
+
+@pytest.mark.parametrize("debug", [False, True])
+def test_only_the_header_functions_are_exported(debug):
+    """Hidden visibility: two builds in one process (libmoe.so and
+    libmoe_debug.so) must share no internal symbol. Template statics with
+    default visibility become process-wide unique symbols, and one library's
+    per-kernel set-up flags then skip the other's set-up."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    B.lib(debug=debug)
+    from expert_moe_layer_gb300 import _build
+    out = subprocess.run([nm, "-D", "--defined-only", _build.lib_path(debug)],
+                         capture_output=True, text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if len(line.split()) >= 3}
+    assert syms and syms <= set(B.header_functions()), sorted(syms - set(B.header_functions()))
+
+
+def test_debug_entry_points_in_the_release_library_make_no_cuda_call():
+    L = B.lib()
+    rec = B.DebugRecord(count=7, site=9, index=3, bound=2)
+    assert L.moe_debug_take(ctypes.byref(rec)) == 2  # MOE_ERR_UNSUPPORTED
+    assert (rec.count, rec.site, rec.index, rec.bound) == (0, 0, 0, 0)
+    assert L.moe_debug_take(None) == 1
+    assert L.moe_debug_selftest(None) == 2
+    assert ctypes.sizeof(B.DebugRecord) == 24
+    assert isinstance(L.moe_last_cuda_error(), int)
+
+
+def test_debug_library_switch_is_scoped():
+    assert not B.debug_build()
+    with B.debug_library():
+        assert B.debug_build()
+    assert not B.debug_build()
+    assert B.debug_site((3 << 16) | 321) == "kernels_gemm_pair.cu:321"
+
+
 def test_strerror_covers_all_codes():
     for code in range(7):
         assert B.strerror(code) and B.strerror(code) != "unknown status"
