@@ -193,6 +193,9 @@ struct MlpFusedArgs {
 };
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st);
 size_t mlp_fused_smem_bytes();
+// One CTA of the fused kernel fits on an SM of the current device (checked
+// once per device).
+bool mlp_fused_fits();
 
 // Expert-parallel dispatch: the physical id of each item (the global id, or
 // with a global replica map [E, R] replica (i / K) mod n of the id's row,

@@ -27,11 +27,14 @@
 // 8 blocks x I/128, then loads the h rows. All GEMM1 units precede all GEMM2
 // units in every CTA's sequence, so GEMM1 work never waits and no wait can
 // deadlock once every CTA is resident (one CTA per SM; a wait that runs out
-// sets MOE_DEV_TIMEOUT). The launch is cooperative, so the runtime starts the
-// grid only when all its CTAs can be resident together (after kernels of
-// other streams free their SMs) and refuses a grid that never can be (fewer
-// SMs for this context, as under an MPS limit); the caller then runs the two
-// GEMM kernels instead. The counters are zeroed before the kernel.
+// sets MOE_DEV_TIMEOUT). The grid is one CTA per SM that the current context
+// may use, and the caller takes this kernel only where one CTA fits on an SM
+// (mlp_fused_fits); otherwise it runs the two GEMM kernels. Kernels of other
+// streams that hold SMs only delay some CTAs: they finish without waiting on
+// this one. A cooperative launch would also guarantee residency, but measured
+// 1.8 us slower per decode step (T = 1 and 8) with the same kernel time, so
+// the launch stays a plain dependent launch. The counters are zeroed before
+// the kernel.
 //
 // Stage layout (40 KB): two 128-row weight boxes and two token-row boxes of
 // 32 rows, each box 128 bytes of K with the 128-byte swizzle.
@@ -486,25 +489,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+std::atomic<unsigned long long> g_smem_set{0};  // devices with the shared memory opt-in
+
 }  // namespace
 
 size_t mlp_fused_smem_bytes() { return kSmemBytes; }
 
+bool mlp_fused_fits() {
+  static std::atomic<unsigned long long> checked{0}, fits{0};  // devices, one bit each
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (checked.load(std::memory_order_acquire) & bit))
+    return (fits.load(std::memory_order_acquire) & bit) != 0;
+  int n = 0;
+  const bool ok =
+      opt_in_smem(reinterpret_cast<const void*>(moe_mlp_fused), kSmemBytes, g_smem_set) ==
+          cudaSuccess &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, moe_mlp_fused, kThreads, kSmemBytes) ==
+          cudaSuccess &&
+      n >= 1;
+  if (bit) {
+    if (ok) fits.fetch_or(bit, std::memory_order_acq_rel);
+    checked.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return ok;
+}
+
 cudaError_t launch_mlp_fused(const MlpFusedArgs& a, int num_sms, cudaStream_t st) {
-  static std::atomic<unsigned long long> smem_set{0};  // devices, one bit each
   const cudaError_t e =
-      opt_in_smem(reinterpret_cast<const void*>(moe_mlp_fused), kSmemBytes, smem_set);
+      opt_in_smem(reinterpret_cast<const void*>(moe_mlp_fused), kSmemBytes, g_smem_set);
   if (e != cudaSuccess) return e;
   if (a.H % 128 != 0 || a.I % 128 != 0 || a.n_groups > kMaxGroups || a.ks1 < 1 ||
       a.ks1 > kMaxSplit || (a.ks1 > 1 && (!a.part || !a.split_cnt)))
     return cudaErrorInvalidValue;
   if (MOE_DEBUG_BUILD && (a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 || a.bnd.max_tiles <= 0))
     return cudaErrorInvalidValue;
-  return launch_pdl_ex(true, moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st,
-                       *a.mapW13, *a.mapW2, *a.mapH, *a.mapX, a.tiles, a.group_start,
-                       a.n_groups, a.H, a.I, a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
-                       static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y),
-                       a.status, a.bnd);
+  return launch_pdl(moe_mlp_fused, dim3(num_sms), dim3(kThreads), kSmemBytes, st, *a.mapW13,
+                    *a.mapW2, *a.mapH, *a.mapX, a.tiles, a.group_start, a.n_groups, a.H, a.I,
+                    a.ks1, a.part, a.part_stride, a.split_cnt, a.ready,
+                    static_cast<__nv_bfloat16*>(a.h), static_cast<__nv_bfloat16*>(a.y), a.status,
+                    a.bnd);
 }
 
 MOE_WAIT_LIMIT_SETTER(set_wait_limit_mlp_fused)

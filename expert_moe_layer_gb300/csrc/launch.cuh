@@ -72,32 +72,20 @@ inline cudaError_t opt_in_smem(const void* kern, int bytes,
   return e;
 }
 
-// With co_resident, the launch is also cooperative: the runtime starts the
-// grid only with every CTA resident at once, and refuses one that cannot be
-// (cudaErrorCooperativeLaunchTooLarge), for a kernel whose CTAs wait on one
-// another.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_ex(bool co_resident, void (*kern)(KArgs...), dim3 grid, dim3 block,
-                          size_t smem, cudaStream_t st, Args&&... args) {
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = co_resident ? 2 : 1;
+  cfg.numAttrs = 1;
   return counted(cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...));
-}
-
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t st, Args&&... args) {
-  return launch_pdl_ex(false, kern, grid, block, smem, st, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

@@ -203,18 +203,45 @@ bool shared_on_pairs(const moe_config* c, int T) {
   return c->act_dtype == MOE_BF16 && T >= 512 && c->hidden_size % 256 == 0;
 }
 
+// SMs of the current context's SM resource (a green context holds part of
+// the device), or 0 where the driver reports none.
+int context_sms() {
+  static PFN_cuCtxGetCurrent_v4000 get_ctx = nullptr;
+  static PFN_cuCtxGetDevResource_v12040 get_res = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetDevResource", &p, 12040, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_res = reinterpret_cast<PFN_cuCtxGetDevResource_v12040>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_ctx || !get_res || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  CUdevResource r;
+  std::memset(&r, 0, sizeof(r));
+  if (get_res(ctx, &r, CU_DEV_RESOURCE_TYPE_SM) != CUDA_SUCCESS) return 0;
+  return static_cast<int>(r.sm.smCount);
+}
+
+// SMs the persistent grids run on: those of the current context where it
+// has fewer than the device (the fused decode kernel's CTAs wait on one
+// another, so its grid must fit), else the device's. Not cached: one device
+// may run under several contexts.
 int sm_count() {
-  static int cache[64] = {0};
   int dev = 0;
   if (cuda_ok(cudaGetDevice(&dev)) != MOE_OK) return 0;
-  if (dev < 0 || dev >= 64) return fail_cuda(static_cast<int>(cudaErrorInvalidDevice)), 0;
-  if (!cache[dev]) {
-    int n = 0;
-    if (cuda_ok(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != MOE_OK)
-      return 0;
-    cache[dev] = n;
-  }
-  return cache[dev];
+  int n = 0;
+  if (cuda_ok(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != MOE_OK)
+    return 0;
+  const int c = context_sms();
+  return (c > 0 && c < n) ? c : n;
 }
 
 // -------------------------------------------------------------- tensor maps
@@ -499,7 +526,9 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   const int nmax = routed_nmax(c, T);
   const long n_items = static_cast<long>(T) * K;
   const bool pairs = gemms_on_pairs(c, T);
-  const bool fused = mlp_fused(c, T);
+  // the fused kernel needs one CTA resident on every SM of its grid; where
+  // one does not fit, the two GEMM kernels run on the same tile table
+  const bool fused = mlp_fused(c, T) && mlp_fused_fits();
   const int max_tiles = static_cast<int>(max_routed_tiles(c, T));
   if (!tiles_ready)
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
@@ -538,15 +567,9 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     a.bnd.b_rows = cap;
     const int sms = sm_count();
     if (sms <= 0) return MOE_ERR_CUDA;
-    const cudaError_t e = launch_mlp_fused(a, sms, st);
-    if (e != cudaErrorCooperativeLaunchTooLarge) {
-      MOE_TRY(cuda_ok(e));
-      if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
-      return MOE_OK;
-    }
-    // not every CTA can be resident on the SMs this context may use: clear
-    // the launch error and run the two GEMM kernels on the same tile table
-    (void)cudaGetLastError();
+    MOE_TRY(cuda_ok(launch_mlp_fused(a, sms, st)));
+    if (ev) MOE_TRY(record_event(ev[1], st));  // GEMM1 and GEMM2 share one kernel
+    return MOE_OK;
   }
   const int ks1 = pairs ? 1 : gemm1_ksplit(c, T);  // pairs: long segments, never split
   if (ks1 > 1) {

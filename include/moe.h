@@ -432,9 +432,9 @@ typedef struct {
                               summed by a finalize kernel or, fused, in-kernel */
   int cta_pairs;           /* 1: routed GEMMs on CTA pairs (cta_group::2)     */
   int fused_mlp;           /* 1: GEMM1 and GEMM2 in one persistent kernel,
-                              launched cooperatively (every CTA resident at
-                              once); where the context's SMs cannot hold its
-                              grid, the call runs the two GEMM kernels       */
+                              one CTA per SM of the current context; where
+                              one CTA does not fit on an SM, the call runs
+                              the two GEMM kernels instead                   */
 } moe_plan;
 MOE_API int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 
