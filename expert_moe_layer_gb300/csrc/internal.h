@@ -55,9 +55,23 @@ struct GemmArgs {
   int m_valid;                 // weight rows with an output (router: E)
   unsigned* status;
   GemmBounds bnd;
+  // grouped GEMM (single CTAs) only, routed tiles and one K range:
+  int* publish = nullptr;      // GEMM1: per-tile counters; each epilogue warp adds 1 per
+                               //   unit once its rows are stored
+  const int* ready = nullptr;  // GEMM2: those counters; it then starts before GEMM1 ends
+                               //   and loads a tile's rows once its count is ready_target
+  int ready_target = 0;
+  int* sched = nullptr;        // grid-wide unit counter (zeroed); nullptr: each CTA takes
+                               //   units blockIdx.x, + gridDim.x, ...
+  int* published = nullptr;    // with publish / ready: the adds over all tiles (zeroed);
+                               //   GEMM2 stops checking tiles once it is complete
 };
 
 enum GemmMode { kGemmSiluUp = 0, kGemmPlain = 1, kGemmLogits = 2 };
+
+// Epilogue warps of the grouped GEMM: with `publish`, each adds 1 to its
+// unit's tile counter, so a tile of GEMM1 is complete at m_tiles * this.
+constexpr int kGemmEpiWarps = 8;
 
 // tcgen05 grouped GEMM, D[w_row, token] = sum_k W[w_row, k] * B[token, k].
 //   kGemmSiluUp: W = w13 rows, out = silu(gate) * up (act dtype)

@@ -17,7 +17,7 @@
 #include "launch.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgAlign;
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgAlign;
 namespace {
 
 constexpr int kItemsPerWarp = 256;

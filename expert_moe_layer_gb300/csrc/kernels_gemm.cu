@@ -21,6 +21,19 @@
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
 // overlaps the main loop of the next.
 //
+// The producer takes the CTA's units in turn (blockIdx.x, + gridDim.x, ... or,
+// with a grid-wide counter, whichever unit is next) and passes each to the
+// MMA issuer and the epilogue through a ring of unit slots in shared memory.
+//
+// A GEMM1 with `publish` adds 1 per epilogue warp and unit to its tile's
+// counter once the warp's h rows are stored. A GEMM2 given those counters
+// (`ready`) starts before GEMM1 has finished: it skips the launch dependency
+// wait, takes its units from the grid-wide counter (CTAs that start on SMs
+// GEMM1 has left take more of them), and loads a tile's h rows only once the
+// tile's count is complete. GEMM1's CTAs are all resident before GEMM2 can
+// launch and never wait on it, so every count completes. GEMM2 waits for
+// GEMM1's completion at its end, before it lets the next kernel launch.
+//
 // Work units are ordered group by group (a group = one expert's tiles, or one
 // shared-expert slab), then by weight tile m, then by token tile. CTAs running
 // at the same time therefore work on one expert. The 128-row weight tiles of
@@ -35,11 +48,12 @@
 #include "ptx.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgGemm;
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgGemm;
 namespace {
 
 constexpr int kThreads = 320;       // 10 warps
 constexpr int kEpiThreads = 256;    // warps 2..9
+static_assert(kEpiThreads / 32 == kGemmEpiWarps, "tile counts assume one add per epilogue warp");
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
 
 // A pipeline stage holds KPS consecutive K blocks (128 bytes of K each), each
@@ -68,8 +82,11 @@ struct GemmShape {
                                    : kTmemNeed <= 256 ? 256
                                                       : 512;
   static constexpr int kMaxGroups = 1024;
-  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4;  // + ofull[2 halves][2 bufs]
-  static constexpr int kBarBytes = 8 * kNBars + 16 + 4 * (kMaxGroups + 1);
+  static constexpr int kUnitRing = 8;  // unit slots from the producer to the other roles
+  // full/empty per stage, tfull/tempty per accumulator, drain, ofull[2 halves][2 bufs],
+  // ufull/uempty per unit slot
+  static constexpr int kNBars = 2 * kStages + 2 * kNAcc + 1 + 4 + 2 * kUnitRing;
+  static constexpr int kBarBytes = 8 * kNBars + 16 + 4 * kUnitRing + 4 * (kMaxGroups + 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOutBytes + kBarBytes;
   static_assert(kTmemNeed <= 512, "TMEM overflow");
   static_assert(kStages >= 2, "need at least two stages");
@@ -111,8 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int k_blocks, int k_split, int a_rows_per_expert, int a_up_offset,
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
                 float* __restrict__ part, int m_valid, unsigned* status,
-                const GemmBounds bnd) {
+                const GemmBounds bnd, int* __restrict__ sched, const int* __restrict__ ready,
+                int ready_target, int* __restrict__ publish, int* __restrict__ published) {
   constexpr bool kStaged = sizeof(TOut) == 2;
+  const bool early = ready != nullptr;  // GEMM2 overlapping the GEMM1 before it
   using S = GemmShape<MODE, NMAX, kStaged, KPS>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
@@ -139,9 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tempty0 = tfull0 + 8 * S::kNAcc;
   const uint32_t drain = tempty0 + 8 * S::kNAcc;
   const uint32_t ofull0 = drain + 8;  // [half][buffer]: a chunk's outputs are staged
+  const uint32_t ufull0 = ofull0 + 32;  // [slot]: the unit in the slot is posted
+  const uint32_t uempty0 = ufull0 + 8 * S::kUnitRing;  // [slot]: every role has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + S::kNBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* gstart = reinterpret_cast<int*>(tmem_slot + 4);
+  volatile int* uslot = reinterpret_cast<volatile int*>(tmem_slot + 4);
+  int* gstart = reinterpret_cast<int*>(tmem_slot + 4 + S::kUnitRing);
   for (int i = threadIdx.x; i <= n_groups; i += kThreads)
     gstart[i] = tiles ? group_start[i] : i * dense_per;
   // The debug build checks every entry and clamps a bad one into range, so
@@ -178,6 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(drain, 1);
     for (int x = 0; x < 4; ++x) ptx::mbar_init(ofull0 + 8 * x, 4);  // the half's 4 warps
+    for (int x = 0; x < S::kUnitRing; ++x) {
+      ptx::mbar_init(ufull0 + 8 * x, 1);
+      ptx::mbar_init(uempty0 + 8 * x, 1 + kEpiThreads / 32);  // MMA thread + epilogue warps
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async();
@@ -196,10 +222,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      int taken = 0, posted = 0;
+      // With the grid-wide counter, the next unit's ticket is drawn one unit
+      // ahead, so the atomic's round trip overlaps the current unit's loads.
+      int ticket = sched ? atomicAdd(sched, 1) : 0;
+      // the CTA's next unit, or total when none is left
+      auto take_unit = [&]() -> int {
+        int u;
+        if (sched) {
+          u = ticket;
+          if (u < total) ticket = atomicAdd(sched, 1);
+        } else {
+          u = static_cast<int>(blockIdx.x) + taken * static_cast<int>(gridDim.x);
+        }
+        ++taken;
+        return u < total ? u : total;
+      };
+      // unit u into the next slot of the ring, for the MMA issuer and the epilogue
+      auto post_unit = [&](int u) -> bool {
+        const int slot = posted % S::kUnitRing;
+        if (posted >= S::kUnitRing &&
+            !ptx::mbar_wait(uempty0 + 8 * slot, ((posted / S::kUnitRing) & 1) ^ 1, abort_flag,
+                            status))
+          return false;
+        uslot[slot] = u;
+        ptx::mbar_arrive(ufull0 + 8 * slot);
+        ++posted;
+        return true;
+      };
       // Operand A (weights) of the first kStages stages before the
-      // dependency wait; operand B (token rows) only after it.
-      int pre = 0;
-      for (int u = blockIdx.x; u < total && pre < S::kStages; u += gridDim.x) {
+      // dependency wait; operand B (token rows) only after it. These units
+      // (at most kStages, so the ring does not fill) stay in their slots.
+      int pre = 0, n_pre = 0;
+      while (pre < S::kStages) {
+        const int u = take_unit();
+        post_unit(u);
+        ++n_pre;
+        if (u >= total) break;
         int ti, m;
         const int ks = u % k_split;
         decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
@@ -218,10 +277,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      pdl_enter();
+      if (!early) pdl_enter();
       int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      // every tile published (GEMM1 has stored all its rows): from then on no
+      // unit needs its own acquire and proxy fence
+      bool all_ready = false;
+      const int all_target = (tiles ? gstart[n_groups] : 0) * ready_target;
+      for (int j = 0;; ++j) {
+        // after a failure only the stages whose weights went out before the
+        // wait still get their token rows, so that their copies complete
+        if (!ok && it >= pre) break;
+        int u;
+        if (j < n_pre) {
+          u = uslot[j % S::kUnitRing];
+        } else {
+          if (!ok) break;
+          u = take_unit();
+          if (!post_unit(u)) {
+            ok = false;
+            break;
+          }
+        }
+        if (u >= total) break;
         int ti, m;
         const int ks = u % k_split;
         decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
@@ -231,11 +309,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)MOE_DCHECK(tl.x * static_cast<long>(a_rows_per_expert) + m * 128 +
                              (MODE == kGemmSiluUp ? a_up_offset : 0),
                          bnd.a_rows);
+        if (ok && early && !all_ready) {
+          // the tile's h rows: every GEMM1 epilogue warp of every weight tile
+          if (ptx::ld_acquire(published) >= all_target) {
+            all_ready = true;
+            ptx::fence_proxy_async_global();
+          } else if (ptx::wait_count(ready + ti, ready_target, abort_flag, status)) {
+            ptx::fence_proxy_async_global();
+          } else {
+            ok = false;
+          }
+        }
         for (int kb = ks * kb_per; kb < kb1; kb += KPS, ++it) {
           const int s = it % S::kStages;
           const uint32_t ph = (it / S::kStages) & 1;
           const uint32_t st0 = sbase + s * S::kStageBytes;
           if (it >= pre) {  // stages of the early loads are fresh: no empty wait
+            if (!ok) break;
             if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
               ok = false;
               break;
@@ -258,24 +348,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
-        // unwinding: let every load this thread issued land before exit
-        // (a failed empty wait implies it >= pre: every early stage got its B)
+        // unwinding: let every load this thread issued land before exit (every
+        // stage below `it` has both operands; none at or above it was issued)
         const int n = it < S::kStages ? it : S::kStages;
         for (int i = 0; i < n; ++i) {
-          const int j = it - 1 - i;
-          ptx::mbar_wait_drain(full0 + 8 * (j % S::kStages), (j / S::kStages) & 1);
+          const int jj = it - 1 - i;
+          ptx::mbar_wait_drain(full0 + 8 * (jj % S::kStages), (jj / S::kStages) & 1);
         }
       }
-    } else {
+    } else if (!early) {
       pdl_enter();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    pdl_enter();
+    if (!early) pdl_enter();
     if (lane == 0) {
-      int it = 0, ai = 0;
+      int it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x, ++ai) {
+      for (int ai = 0; ok; ++ai) {
+        const int slot = ai % S::kUnitRing;
+        if (!ptx::mbar_wait(ufull0 + 8 * slot, (ai / S::kUnitRing) & 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const int u = uslot[slot];
+        ptx::mbar_arrive(uempty0 + 8 * slot);
+        if (u >= total) break;
         int ti, m;
         const int ks = u % k_split;
         decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
@@ -327,11 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_enter();
+    if (!early) pdl_enter();
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // two warps per quarter split the columns
-    int ai = 0, cc = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++ai) {
+    int cc = 0;
+    for (int ai = 0;; ++ai) {
+      const int slot = ai % S::kUnitRing;
+      if (!ptx::mbar_wait(ufull0 + 8 * slot, (ai / S::kUnitRing) & 1, abort_flag, status)) break;
+      const int u = uslot[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(uempty0 + 8 * slot);
+      if (u >= total) break;
       int ti, m;
       const int ks = u % k_split;
       decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
@@ -413,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ptx::tc_fence_before();
         ptx::mbar_arrive(tempty0 + 8 * b);
+        if (publish) ptx::publish_rows(publish + ti, published, lane);
         continue;
       }
       TOut* orow = out + static_cast<long>(tl.z) * out_ld + row;
@@ -435,6 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty0 + 8 * b);
+      if (publish) ptx::publish_rows(publish + ti, published, lane);
     }
   }
 
@@ -444,6 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, S::kTmemCols);
   }
+  // overlapping GEMM2: the GEMM1 before it has completed before the next
+  // kernel may launch
+  if (early) pdl_enter();
 }
 
 template <int MODE, bool TF32, typename TOut, int NMAX, int KPS = 1>
@@ -456,7 +565,8 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
   return launch_pdl(kern, dim3(num_sms), dim3(kThreads), S::kSmemBytes, st, *a.mapA, *a.mapB,
                     a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
                     a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),
-                    a.out_ld, a.split_stride, a.part, a.m_valid, a.status, a.bnd);
+                    a.out_ld, a.split_stride, a.part, a.m_valid, a.status, a.bnd, a.sched,
+                    a.ready, a.ready_target, a.publish, a.published);
 }
 
 }  // namespace
@@ -464,6 +574,11 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
 cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, int num_sms,
                         cudaStream_t st) {
   if (a.k_split < 1 || (a.k_split > 1 && a.part == nullptr)) return cudaErrorInvalidValue;
+  // the overlap needs the tile table (and one K range: the tile's count is
+  // of whole units)
+  if ((a.ready || a.publish) && (!a.tiles || a.k_split != 1)) return cudaErrorInvalidValue;
+  if ((a.ready || a.publish) && !a.published) return cudaErrorInvalidValue;
+  if (a.ready && (!a.sched || a.ready_target <= 0)) return cudaErrorInvalidValue;
   if (MOE_DEBUG_BUILD && (a.bnd.a_rows <= 0 || a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 ||
                           (a.tiles && a.bnd.max_tiles <= 0)))
     return cudaErrorInvalidValue;

@@ -37,7 +37,7 @@
 #include "ptx.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgGemmPair;
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgGemmPair;
 namespace {
 
 constexpr int kThreads = 320;

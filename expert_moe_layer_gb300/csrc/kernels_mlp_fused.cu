@@ -51,7 +51,7 @@
 #include "ptx.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgMlpFused;
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgMlpFused;
 namespace {
 
 constexpr int kThreads = 320;
@@ -112,53 +112,6 @@ __device__ __forceinline__ UnitInfo unit_info(int u, int U1, const int* gstart, 
     r.n_st = (kb2 + 1) >> 1;
   }
   return r;
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int add_acq_rel(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Wait until *p >= target, bounded like the mbarrier waits.
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort,
-                                           unsigned* status) {
-  if (ld_acquire(p) >= target) return true;
-  const uint64_t t0 = ptx::globaltimer();
-  const uint64_t limit = ptx::g_wait_limit_ns;
-  for (uint32_t n = 1;; ++n) {
-    if (ld_acquire(p) >= target) return true;
-    if ((n & 15u) == 0) {
-      if (*abort) return false;
-      if (ptx::globaltimer() - t0 > limit) {
-        *abort = 1;
-        if (status) atomicOr(status, MOE_DEV_TIMEOUT);
-        return false;
-      }
-    }
-    __nanosleep(64);
-  }
-}
-
-// Publish a warp's block of h (generic stores) to the GEMM2 producers, which
-// read it through the async proxy.
-__device__ __forceinline__ void publish_h(int* ready, int lane) {
-  fence_proxy_async_global();
-  __syncwarp();
-  if (lane == 0) add_acq_rel(ready, 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -312,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (two) ptx::tma_load_2d(st + kABytes, &mapW2, fb, (2 * j + 1) * 64, arow);
           }
           // on failure the issued weight boxes still land; their stages never fill
-          if (ok && !wait_count(ready + ui.ti, ready_target, abort_flag, status)) ok = false;
-          if (ok) fence_proxy_async_global();
+          if (ok && !ptx::wait_count(ready + ui.ti, ready_target, abort_flag, status)) ok = false;
+          if (ok) ptx::fence_proxy_async_global();
           for (j = 0; j < ui.n_st && ok; ++j) {
             const int i2 = it + j;
             const int s = i2 % kStages;
@@ -438,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j)
           if (c0 + j < tl.w) hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu(v[j]) * w[j]);
-        publish_h(ready + ui.ti, lane);
+        ptx::publish_rows(ready + ui.ti, nullptr, lane);
         continue;
       }
       // K split: raw partials of this slab ([row][gate I | up I] fp32), then
@@ -453,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       int old = 0;
-      if (lane == 0) old = add_acq_rel(split_cnt + (ui.ti * m1 + ui.m) * kEpiWarps + blk, 1);
+      if (lane == 0) old = ptx::add_acq_rel(split_cnt + (ui.ti * m1 + ui.m) * kEpiWarps + blk, 1);
       old = __shfl_sync(0xffffffffu, old, 0);
       if (old != ks1 - 1) continue;
       // every slab's value is loaded before the sum, which runs in slab order;
@@ -477,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         hrow[static_cast<long>(c0 + j) * I] = __float2bfloat16_rn(silu(g) * up);
       }
-      publish_h(ready + ui.ti, lane);
+      ptx::publish_rows(ready + ui.ti, nullptr, lane);
     }
   }
 

@@ -9,7 +9,7 @@
 #include "ptx.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgRoute;  // before topk_warp.cuh, which checks ids
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgRoute;  // before topk_warp.cuh, which checks ids
 }  // namespace moe
 
 #include "topk_warp.cuh"

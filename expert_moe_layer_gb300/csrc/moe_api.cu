@@ -13,7 +13,7 @@
 #include "launch.cuh"
 
 namespace moe {
-constexpr DbgFile kDbgFileCode = kDbgApi;  // before topk_warp.cuh
+[[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgApi;  // before topk_warp.cuh
 }  // namespace moe
 
 #include "topk_warp.cuh"
@@ -168,21 +168,29 @@ bool mlp_fused(const moe_config* c, int T) {
   return c->act_dtype == MOE_BF16 && routed_nmax(c, T) == 32 && n_local(c) <= 1024;
 }
 
+bool gemm2_early(const moe_config* c, int T);
+
 // Zeroed at the start of every call (one memset): the status word, the
 // small-batch route tickets and, on the fused MLP path, its per-tile ready
-// counters and per-block split counters. Offsets from the start of ws.
+// counters and per-block split counters; where GEMM2 overlaps GEMM1, GEMM2's
+// unit counter, the count of tile publishes and the per-tile ready counters.
+// Offsets from the start of ws.
 struct SyncRegion {
-  size_t bytes, ready, split;
+  size_t bytes, ready, split, sched;
 };
 SyncRegion sync_region(const moe_config* c, int T) {
   SyncRegion r;
   size_t off = 4 + 4 * static_cast<size_t>(kRouteTickets);
-  r.ready = r.split = off;
+  r.ready = r.split = r.sched = off;
+  const size_t tiles = static_cast<size_t>(max_routed_tiles(c, T));
   if (mlp_fused(c, T)) {
-    const size_t tiles = static_cast<size_t>(max_routed_tiles(c, T));
     off += 4 * tiles;
     r.split = off;
     if (gemm1_ksplit(c, T) > 1) off += 4 * tiles * (c->intermediate_size / 128) * 8;
+  } else if (gemm2_early(c, T)) {
+    off += 16;
+    r.ready = off;
+    off += 4 * tiles;
   }
   r.bytes = off;
   return r;
@@ -195,6 +203,15 @@ SyncRegion sync_region(const moe_config* c, int T) {
 // output rows on the pair.
 bool gemms_on_pairs(const moe_config* c, int T) {
   return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
+}
+
+// GEMM2 starts while GEMM1's last units run, on the SMs GEMM1 has left, when
+// both run on single CTAs with one K range: GEMM1 publishes each tile's h rows
+// and GEMM2 takes its units from a counter, loading a tile's rows once they
+// are all published. The fused decode kernel and the CTA-pair GEMMs keep
+// their own schedules.
+bool gemm2_early(const moe_config* c, int T) {
+  return !mlp_fused(c, T) && !gemms_on_pairs(c, T) && gemm1_ksplit(c, T) == 1;
 }
 
 // Shared experts over at least two 256-token tiles per slab run on CTA pairs
@@ -296,7 +313,9 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              int m_valid, unsigned* status, cudaStream_t st, int k_split = 1,
              long split_stride = 0, int dense_T = 0, bool pair = false,
              float* part = nullptr, const int32_t* out_rows = nullptr,
-             const float* out_scale = nullptr, int b_cap = 0, GemmBounds bnd = {}) {
+             const float* out_scale = nullptr, int b_cap = 0, GemmBounds bnd = {},
+             int* publish = nullptr, const int* ready = nullptr, int ready_target = 0,
+             int* sched = nullptr, int* published = nullptr) {
   CUtensorMap ma, mb;
   // CTA pairs in SiLU mode stage 64 gate and 64 up rows per CTA: 64-row boxes
   const int a_box = (pair && mode == kGemmSiluUp) ? 64 : 128;
@@ -327,6 +346,11 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   bnd.a_rows = a_rows;
   bnd.b_rows = b_rows;
   g.bnd = bnd;
+  g.publish = publish;
+  g.ready = ready;
+  g.ready_target = ready_target;
+  g.sched = sched;
+  g.published = published;
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   if (pair) return cuda_ok(launch_gemm_pair(mode, nmax, g, sms, st));
@@ -572,6 +596,10 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     return MOE_OK;
   }
   const int ks1 = pairs ? 1 : gemm1_ksplit(c, T);  // pairs: long segments, never split
+  // GEMM2 overlapping GEMM1's last units (counters zeroed with the status word)
+  const bool early = ks1 == 1 && gemm2_early(c, T);
+  int* ready = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + sync.ready);
+  int* sched = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + sync.sched);
   if (ks1 > 1) {
     // split over K: raw gate/up partials, then the SiLU*up epilogue
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
@@ -585,7 +613,8 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st,
                      1, 0, 0, pairs, nullptr, nullptr, nullptr, pairs ? cap : 0,
-                     out_bounds(cap, max_tiles)));
+                     out_bounds(cap, max_tiles), early ? ready : nullptr, nullptr, 0, nullptr,
+                     early ? sched + 1 : nullptr));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
   // with y_rows (CTA pairs only) GEMM2 writes segment position p to row
@@ -595,7 +624,9 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
                    1, 0, 0, pairs, nullptr, pairs ? y_rows : nullptr,
                    pairs && y_rows ? w_perm : nullptr, pairs ? cap : 0,
                    pairs && y_rows ? out_bounds(n_items, max_tiles, cap)
-                                   : out_bounds(cap, max_tiles)));
+                                   : out_bounds(cap, max_tiles),
+                   nullptr, early ? ready : nullptr, (I / 128) * kGemmEpiWarps,
+                   early ? sched : nullptr, early ? sched + 1 : nullptr));
   return MOE_OK;
 }
 
@@ -879,6 +910,7 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   p.fused_mlp = mlp_fused(cfg, T) ? 1 : 0;
   p.gemm1_k_split = gemm1_ksplit(cfg, T);
   p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
+  p.gemm2_overlap = gemm2_early(cfg, T) ? 1 : 0;
   p.kernels = 0;
   if (T > 0) {
     // logits + top-k and align (or the fused route kernel), the routed MLP

@@ -105,6 +105,63 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// ------------------------------------------------- cross-CTA counters
+// Counters in global memory through which one CTA hands finished output rows
+// to another (possibly of the next grid): the writer stores the rows with
+// generic stores, fences them for the async proxy and adds to the counter
+// with release semantics; the reader waits (bounded) for the count with
+// acquire loads, fences, and only then reads the rows with TMA.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *p >= target, bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort,
+                                           unsigned* status) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  const uint64_t limit = g_wait_limit_ns;
+  for (uint32_t n = 1;; ++n) {
+    if (ld_acquire(p) >= target) return true;
+    if ((n & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > limit) {
+        *abort = 1;
+        if (status) atomicOr(status, MOE_DEV_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
+// Publish a warp's stored rows to readers that load them through the async
+// proxy: fence, then one release add per warp (also to `total`, a count over
+// all tiles, when given).
+__device__ __forceinline__ void publish_rows(int* counter, int* total, int lane) {
+  fence_proxy_async_global();
+  __syncwarp();
+  if (lane == 0) {
+    add_acq_rel(counter, 1);
+    if (total) add_acq_rel(total, 1);
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 // Untiled bulk copy global -> shared: 16-byte aligned addresses, size a
 // multiple of 16. Completes `bytes` transactions on the mbarrier.

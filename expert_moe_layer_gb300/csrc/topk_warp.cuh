@@ -96,15 +96,21 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
 #pragma unroll
   for (int j = 0; j < VPL; ++j) ck[j] = fkey(lane + 32 * j < E ? p[j] + sb[j] : -CUDART_INF_F);
   if (n_group > 0) {
+    // each slot's group, from one integer quotient per slot (not one per
+    // slot and group)
     const int gs = E / n_group;
+    int gj[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      gj[j] = e < E ? e / gs : -1;
+    }
     uint32_t my_score = 0;  // lane g holds the key of group g's score
     for (int g = 0; g < n_group; ++g) {
       uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && e / gs == g) m = max(m, ck[j]);
-      }
+      for (int j = 0; j < VPL; ++j)
+        if (gj[j] == g) m = max(m, ck[j]);
       m = __reduce_max_sync(0xffffffffu, m);
       if (lane == g) my_score = m;
     }
@@ -118,10 +124,8 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
     const unsigned keep = __ballot_sync(0xffffffffu, taken);
     const uint32_t ninf = fkey(-CUDART_INF_F);
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E && !((keep >> (e / gs)) & 1u)) ck[j] = ninf;
-    }
+    for (int j = 0; j < VPL; ++j)
+      if (gj[j] >= 0 && !((keep >> gj[j]) & 1u)) ck[j] = ninf;
   }
 
   float my_w = 0.f;

@@ -435,6 +435,9 @@ typedef struct {
                               one CTA per SM of the current context; where
                               one CTA does not fit on an SM, the call runs
                               the two GEMM kernels instead                   */
+  int gemm2_overlap;       /* 1: GEMM2 starts on the SMs GEMM1 has left and
+                              takes each token tile once GEMM1 has published
+                              its rows (single-CTA GEMMs, one K range)       */
 } moe_plan;
 MOE_API int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 

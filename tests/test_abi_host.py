@@ -168,6 +168,7 @@ def test_forward_plan_per_workload():
     # fp32 router on CUDA cores split into 256-column slices of H
     p = _plan(synth.MIXTRAL)
     assert (p.tile_rows, p.cta_pairs, p.fused_mlp, p.gemm1_k_split) == (256, 1, 0, 1)
+    assert p.gemm2_overlap == 0  # CTA pairs keep their own schedule
     assert (p.router_tensor_cores, p.router_partials) == (0, 4096 // 256)
     # route 2, align 1, gather + GEMM1 + GEMM2, combine
     assert p.kernels == 2 + 1 + 3 + 1
@@ -178,6 +179,7 @@ def test_forward_plan_per_workload():
     for T in (8, 64):
         p = _plan(synth.QWEN_DECODE, T)
         assert (p.tile_rows, p.fused_mlp, p.gemm1_k_split, p.cta_pairs) == (32, 1, 1, 0)
+        assert p.gemm2_overlap == 0
         assert (p.fused_route, p.align_kernels, p.router_partials) == (1, 0, 1)
         assert p.kernels == 1 + 2 + 1  # route+align, gather + fused MLP, combine
     p = _plan(synth.QWEN_DECODE, 1)
@@ -190,6 +192,11 @@ def test_forward_plan_per_workload():
     p = _plan(synth.DEEPSEEK)
     assert p.align_kernels == 3 and p.fused_mlp == 0 and p.fused_route == 0
     assert p.kernels == 2 + 3 + 3 + 2 + 1
+    # single-CTA routed GEMMs over 128-token tiles, one K range: GEMM2
+    # overlaps GEMM1 (here and on the EP shard)
+    assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (128, 0, 1, 1)
+    p = _plan(synth.EP_SHARD)
+    assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (128, 0, 1, 1)
     # fp32 layers never take the bf16-only fused or pair kernels
     p = _plan(synth.TINY)
     assert (p.fused_mlp, p.cta_pairs, p.router_tensor_cores) == (0, 0, 0)

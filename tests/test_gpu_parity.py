@@ -84,7 +84,13 @@ SMALL = {
                            router="f32", x_std=0.3),
     "f32_router_wide": W("f32_router_wide", T=300, H=256, I=128, E=64, K=6, router="f32",
                          router_bias=True),
+    # 128-token tiles with at least 152 GEMM1 units: GEMM2 overlaps GEMM1 and
+    # takes each tile once GEMM1 has published it (one tile per expert, then
+    # ragged segments of one or two tiles)
+    "overlap_prefill": W("overlap_prefill", T=2048, H=256, I=384, E=64, K=2),
+    "overlap_ragged": W("overlap_ragged", T=1500, H=384, I=512, E=40, K=3, router_bias=True),
 }
+OVERLAP = ("overlap_prefill", "overlap_ragged")
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
@@ -383,7 +389,8 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
     assert B.moe_get_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED])
+@pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED,
+                                  *OVERLAP])
 def test_plan_matches_the_kernels_launched(name):
     """moe_forward_plan (host only) names the path; moe_forward_timed counts
     the kernels that path launched. The fused cases must take the fused
@@ -397,6 +404,7 @@ def test_plan_matches_the_kernels_launched(name):
         assert plan.fused_route == 1
     if name in ("pair_prefill", "ragged_prefill"):
         assert plan.fused_route == 0 and plan.align_kernels == 1
+    assert plan.gemm2_overlap == (1 if name in OVERLAP else 0)
     ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
     out = torch.empty(wl.T, wl.H, dtype=d["x"].dtype, device="cuda")
     n = B.moe_forward_timed(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"],
