@@ -196,6 +196,117 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
   }
 }
 
+// Passes 2 and 3 in one kernel, where the per-warp counts are few (at most
+// kFoldHist entries) and E_l <= 256: every CTA sums the column of each expert
+// itself (all warps for the count, the warps before its own for its base),
+// so no single-CTA scan runs between two grid-wide passes. CTA 0 writes
+// counts, offsets and the tile table. The order of the items is that of the
+// three passes.
+constexpr long kFoldHist = 32768;
+
+__global__ void __launch_bounds__(256) align_scan_scatter_kernel(
+    const int32_t* __restrict__ ids, long n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, const int* __restrict__ hist, int n_warps, int block_m,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap, unsigned* status,
+    Tile* __restrict__ tiles, int* __restrict__ group_start, int nmax, int max_tiles) {
+  pdl_enter();
+  ids = fresh(ids);
+  hist = fresh(hist);
+  extern __shared__ int run[];  // [kWarpsPerBlock][E_l]
+  __shared__ int warp_sums[32];
+  __shared__ int part_c[256], part_b[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = threadIdx.x;
+  const int w0 = blockIdx.x * kWarpsPerBlock;  // this CTA's first warp
+  // G = 256 / E_l threads share each expert's column: thread (g, e') sums
+  // the rows w = g, g + G, ... (all of them for the count, those before w0
+  // for this CTA's base); the G partial sums are then added in order
+  {
+    const int G = 256 / E_l;
+    const int ge = threadIdx.x % E_l, g = threadIdx.x / E_l;
+    int pc = 0, pb = 0;
+    if (g < G) {
+#pragma unroll 16
+      for (int w = g; w < n_warps; w += G) {
+        const int h = hist[static_cast<long>(w) * E_l + ge];
+        if (w < w0) pb += h;
+        pc += h;
+      }
+    }
+    part_c[threadIdx.x] = pc;
+    part_b[threadIdx.x] = pb;
+  }
+  __syncthreads();
+  int c = 0, before = 0;
+  if (e < E_l) {
+    for (int g = 0; g < 256 / E_l; ++g) {
+      c += part_c[g * E_l + e];
+      before += part_b[g * E_l + e];
+    }
+  }
+  const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
+  int total = 0;
+  const int start = block_exclusive_scan(padded, warp_sums, total);
+  if (blockIdx.x == 0) {
+    if (e < E_l) {
+      counts[e] = c;
+      offsets[e] = start;
+    }
+    if (threadIdx.x == 0) {
+      offsets[E_l] = total;
+      if (total > cap && status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+    }
+    if (tiles)
+      write_tile_table(e, E_l, e < E_l ? c : 0, start, nmax, tiles, group_start, max_tiles,
+                       warp_sums, status);
+  }
+  if (e < E_l) {
+    int r = start + before;
+    for (int wi = 0; wi < kWarpsPerBlock; ++wi) {
+      run[wi * E_l + e] = r;
+      if (w0 + wi < n_warps) r += hist[static_cast<long>(w0 + wi) * E_l + e];
+    }
+  }
+  __syncthreads();
+  const int gw = w0 + warp;
+  if (gw >= n_warps) return;
+  int* my = run + warp * E_l;
+  const long base = static_cast<long>(gw) * kItemsPerWarp;
+  int idv[kItemsPerWarp / 32];  // all of this lane's ids in flight at once
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    idv[i] = item < n_items ? ids[item] : 0;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    int le = -1;
+    // status already recorded by pass 1 for bad ids
+    if (item < n_items)
+      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (item < n_items) {
+      int pos = -1;
+      if (le >= 0) {
+        pos = my[le] + __popc(peers & lt);
+        if (pos < cap) {
+          sorted_ids[pos] = static_cast<int32_t>(item);
+        } else {
+          if (status) atomicOr(status, MOE_DEV_CAP_OVERFLOW);
+          pos = -1;
+        }
+      }
+      inv_pos[item] = pos;
+    }
+    __syncwarp();
+    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 // Small inputs (n_items <= kSmallItems, E_l <= kSmallExperts): the three
 // passes above in one CTA of 32 warps (align_small_block).
 __global__ void __launch_bounds__(1024) align_small_kernel(
@@ -597,7 +708,8 @@ int grid_for(long work, int per_block, int cap_blocks) {
 }  // namespace
 
 int align_kernel_count(long n_items, int E_l) {
-  return (n_items <= kSmallItems && E_l <= kSmallExperts) ? 1 : 3;
+  if (n_items <= kSmallItems && E_l <= kSmallExperts) return 1;
+  return (E_l <= 256 && static_cast<long>(align_warps(n_items)) * E_l <= kFoldHist) ? 2 : 3;
 }
 
 int align_warps(long n_items) {
@@ -623,6 +735,11 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                              K, emap, R, E, E_l, ep_start, hist, n_warps, sorted_ids, cap,
                              status);
   if (e != cudaSuccess) return e;
+  if (E_l <= 256 && static_cast<long>(n_warps) * E_l <= kFoldHist)
+    return launch_pdl(align_scan_scatter_kernel, dim3(blocks), dim3(256), smem, st, ids,
+                      n_items, K, emap, R, E, E_l, ep_start, static_cast<const int*>(hist),
+                      n_warps, block_m, counts, offsets, sorted_ids, inv_pos, cap, status, tiles,
+                      group_start, nmax, max_tiles);
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, st, hist, n_warps, E_l, block_m,
                  counts, offsets, cap, status, tiles, group_start, nmax, max_tiles);
   if (e != cudaSuccess) return e;

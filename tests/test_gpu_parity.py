@@ -89,6 +89,10 @@ SMALL = {
     # ragged segments of one or two tiles)
     "overlap_prefill": W("overlap_prefill", T=2048, H=256, I=384, E=64, K=2),
     "overlap_ragged": W("overlap_ragged", T=1500, H=384, I=512, E=40, K=3, router_bias=True),
+    # more items than the single-CTA align takes: per-warp counts, then scan
+    # and scatter in one pass (64 local experts), or the three passes (300)
+    "align_fold": W("align_fold", T=1200, H=128, I=128, E=64, K=8),
+    "align_three_pass": W("align_three_pass", T=640, H=128, I=128, E=300, K=16),
 }
 OVERLAP = ("overlap_prefill", "overlap_ragged")
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
@@ -185,12 +189,14 @@ def _align(c, ids_np, block, emap=None, cap=None):
 
 @pytest.mark.parametrize("block", [1, 7, 16, 64, 128])
 @pytest.mark.parametrize("name", ["ragged_prefill", "ep_rank1", "single_token", "ep_tiny",
-                                  "wide_router"])
+                                  "wide_router", "align_fold", "align_three_pass"])
 def test_align_entry_point(name, block):
-    """Per-warp counting sort (ragged_prefill, ep_rank1) and the small-batch
-    path of up to 64 items (single_token: 4 items; ep_tiny: 24 items over 64
-    local experts; wide_router: 48 items of an EP shard with 160 local
-    experts)."""
+    """The single-CTA per-warp counting sort (ragged_prefill, ep_rank1), the
+    small-batch path of up to 64 items (single_token: 4 items; ep_tiny: 24
+    items over 64 local experts; wide_router: 48 items of an EP shard with 160
+    local experts), and the multi-CTA passes: count, then scan and scatter in
+    one kernel (align_fold: 9600 items, 64 experts) or in two (align_three_pass:
+    10240 items, 300 experts)."""
     c = case(name)
     counts, offsets, sorted_ids, inv_pos, st, cap = _align(c, c.ids, block)
     assert st == (0, 0)
@@ -201,11 +207,11 @@ def test_align_entry_point(name, block):
     np.testing.assert_array_equal(inv_pos, ri)
 
 
-@pytest.mark.parametrize("name", ["ep_rank1", "ep_tiny"])
+@pytest.mark.parametrize("name", ["ep_rank1", "ep_tiny", "align_fold", "align_three_pass"])
 def test_align_general_expert_map_and_bad_ids(name):
     """A permuted partial expert map, then flagged bad ids and map values, on
-    the three-pass align (ep_rank1: 4000 items) and the small-batch one
-    (ep_tiny: 24 items)."""
+    the single-CTA align (ep_rank1: 4000 items), the small-batch one (ep_tiny:
+    24 items) and the multi-CTA passes (align_fold, align_three_pass)."""
     c = case(name)
     wl = c.wl
     rng = np.random.default_rng(7)
