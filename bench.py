@@ -203,10 +203,13 @@ def aggregate_over_ranks(local_ms, tokens_per_rank, steps, world, device=None):
 
 
 # --------------------------------------------------------------------------- our arm
-def dominant_kernel_roofline(wl, plan, A, touched, k_ms, peaks):
+def dominant_kernel_roofline(wl, plan, A, touched, rows, k_ms, peaks):
     """Roofline of the layer's dominant kernel: GEMM1 (gate/up with the SiLU
     epilogue), or for decode-sized batches the fused kernel that runs GEMM1
-    and GEMM2 together. Algorithmic FLOPs and bytes per launch over its
+    and GEMM2 together. GEMM1 on CTA pairs reads the A permuted token rows;
+    on single CTAs it gathers them from x itself, where the algorithmic
+    bytes count each of the `rows` distinct token rows once (the repeats of
+    a row hit L2). Algorithmic FLOPs and bytes per launch over its
     measured duration, against the measured peak: the bf16 burst peak for a
     tensor-bound kernel (the timed regions here last milliseconds, not the
     seconds of the sustained figure, which is reported beside it), the HBM
@@ -224,7 +227,8 @@ def dominant_kernel_roofline(wl, plan, A, touched, k_ms, peaks):
                        if plan.cta_pairs else
                        ("moe_gemm_tc<SiLU> (GEMM1)", "kernels_gemm.cu"))
         k_flops = 4 * A * wl.H * wl.I
-        k_bytes = w13_bytes + A * wl.H * eb + A * wl.I * eb
+        x_rows = A if plan.cta_pairs else rows
+        k_bytes = w13_bytes + x_rows * wl.H * eb + A * wl.I * eb
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if k_flops / max(k_bytes, 1) >= ridge:
         ach = k_flops / (k_ms / 1e3) / 1e12
@@ -304,6 +308,9 @@ def time_layer(args, wl, d, device, world, headline):
     counts = ws[lay.counts:lay.counts + 4 * El].view(torch.int32).cpu().numpy()
     A = int(counts.sum())
     touched = int((counts > 0).sum())
+    # distinct token rows with at least one local assignment
+    tk = ws[lay.topk_ids:lay.topk_ids + 4 * T * wl.K].view(torch.int32).view(T, wl.K)
+    rows = int(((tk // El) == wl.ep_rank).any(dim=1).sum().item())
 
     def new_events(n):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(n)]
@@ -393,7 +400,7 @@ def time_layer(args, wl, d, device, world, headline):
     ms_per_step = total_ms / args.steps
     flops, alg_bytes = layer_work(wl, A, touched)
     plan = B.forward_plan(cfg, T)
-    roof = dominant_kernel_roofline(wl, plan, A, touched, stages["gemm1_silu"], peaks)
+    roof = dominant_kernel_roofline(wl, plan, A, touched, rows, stages["gemm1_silu"], peaks)
     path = {f: getattr(plan, f) for f, _ in B.Plan._fields_}
     e2e = run_e2e(args, wl, cfg, d, ws, out, flush, stream, device, world, alg_bytes)
     res = {

@@ -27,6 +27,7 @@ struct GemmBounds {
   long out_map = 0;   // CTA-pair plain mode with out_rows: entries of out_rows /
                       //   out_scale (0 without them)
   int max_tiles = 0;  // entries of the tile table (0 for dense problems)
+  long x_rows = 0;    // gathered token rows: rows of x
 };
 
 struct GemmArgs {
@@ -65,6 +66,16 @@ struct GemmArgs {
                                //   units blockIdx.x, + gridDim.x, ...
   int* published = nullptr;    // with publish / ready: the adds over all tiles (zeroed);
                                //   GEMM2 stops checking tiles once it is complete
+  // Token rows gathered by the kernel itself (routed tiles): B row r of a
+  // tile is row gather_ids[tile.y + r] / gather_div of gather_x (row stride
+  // gather_ld elements), fetched with per-lane copies instead of mapB (which
+  // must still be a valid map). The tile table may then come from the kernel
+  // just before.
+  const void* gather_x = nullptr;
+  const int32_t* gather_ids = nullptr;
+  int gather_div = 1;
+  long gather_ld = 0;
+  long gather_items = 0;       // ids outside [0, gather_items) read row 0 of gather_x
 };
 
 enum GemmMode { kGemmSiluUp = 0, kGemmPlain = 1, kGemmLogits = 2 };

@@ -7,9 +7,10 @@
 // and decode (a few rows per expert, nmax = 32). Only the N of the
 // instruction changes.
 //
-// Per CTA (persistent, one per SM, 320 threads):
+// Per CTA (persistent, one per SM, 448 threads):
 //   warp 0      TMA producer: weights (A) and token rows (B) into a ring of
-//               shared-memory stages with the 128-byte swizzle
+//               shared-memory stages with the 128-byte swizzle (when the
+//               kernel gathers its token rows itself, A only)
 //   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of
 //               K = 128 bytes per stage; in SiLU mode a second accumulator for
 //               the "up" rows shares the same B stage
@@ -18,6 +19,9 @@
 //               plain, store to global. bf16 outputs go through a staging
 //               buffer in shared memory per 16-column chunk, so the stores
 //               are 16-byte vectors along output rows.
+//   warps 10-13 with gathered token rows: copy each stage's rows of x by the
+//               permutation (per-lane cp.async into the swizzled layout);
+//               otherwise idle
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
 // overlaps the main loop of the next.
 //
@@ -33,6 +37,14 @@
 // tile's count is complete. GEMM1's CTAs are all resident before GEMM2 can
 // launch and never wait on it, so every count completes. GEMM2 waits for
 // GEMM1's completion at its end, before it lets the next kernel launch.
+//
+// A GEMM1 given x and the sorted item ids gathers its token rows itself: the
+// row warps copy row sorted_ids[p] / K of x for segment position p straight
+// into the stage, so no permuted copy of x is written and read back. It waits
+// for the kernel before it (which wrote the tile table and the ids) at its
+// start and reads what that kernel wrote through L2: a CTA launched early by
+// the dependent launch may otherwise read stale lines through the read-only
+// path even after the wait.
 //
 // Work units are ordered group by group (a group = one expert's tiles, or one
 // shared-expert slab), then by weight tile m, then by token tile. CTAs running
@@ -51,7 +63,8 @@ namespace moe {
 [[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgGemm;
 namespace {
 
-constexpr int kThreads = 320;       // 10 warps
+constexpr int kRowWarps = 4;        // warps 10..13: gathered token rows
+constexpr int kThreads = 320 + 32 * kRowWarps;
 constexpr int kEpiThreads = 256;    // warps 2..9
 static_assert(kEpiThreads / 32 == kGemmEpiWarps, "tile counts assume one add per epilogue warp");
 constexpr int kABytes = 128 * 128;  // one 128-row x 128-byte weight box
@@ -129,9 +142,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int b_from_out, TOut* __restrict__ out, long out_ld, long split_stride,
                 float* __restrict__ part, int m_valid, unsigned* status,
                 const GemmBounds bnd, int* __restrict__ sched, const int* __restrict__ ready,
-                int ready_target, int* __restrict__ publish, int* __restrict__ published) {
+                int ready_target, int* __restrict__ publish, int* __restrict__ published,
+                const void* __restrict__ gx, const int32_t* __restrict__ gids, int gdiv,
+                long gld, long gitems) {
   constexpr bool kStaged = sizeof(TOut) == 2;
   const bool early = ready != nullptr;  // GEMM2 overlapping the GEMM1 before it
+  const bool gather = gx != nullptr;    // token rows fetched by this kernel from x
+  // the tile table of a gathering GEMM1 (and the ids it gathers by) come from
+  // the kernel just before: wait first, and read them through laundered
+  // pointers so that no load moves above the wait
+  if (gather) {
+    pdl_enter();
+    tiles = fresh(tiles);
+    group_start = fresh(group_start);
+    gids = fresh(gids);
+  }
   using S = GemmShape<MODE, NMAX, kStaged, KPS>;
   constexpr uint32_t kAB = TF32 ? 2u : 1u;   // operand type code
   constexpr int kKe = TF32 ? 32 : 64;         // K elements per 128-byte row
@@ -143,7 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Dense problems (router, shared experts: every token of T for each of
   // n_groups weight slabs) pass no tile table; their tiles are implicit.
   const int dense_per = (dense_T + NMAX - 1) / NMAX;
-  const int total = (tiles ? group_start[n_groups] : n_groups * dense_per) * m_tiles * k_split;
+  // A gathering GEMM1 may have started before the kernel that wrote its tile
+  // table and ids finished; it reads them from L2 (not through the read-only
+  // path), after its dependency wait.
+  auto ld_group = [&](int i) -> int { return gather ? __ldcg(group_start + i) : group_start[i]; };
+  const int total = (tiles ? ld_group(n_groups) : n_groups * dense_per) * m_tiles * k_split;
   const int kb_per = (k_blocks + k_split - 1) / k_split;
   if (static_cast<int>(blockIdx.x) >= total) return;  // uniform across the CTA
 
@@ -165,13 +194,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* uslot = reinterpret_cast<volatile int*>(tmem_slot + 4);
   int* gstart = reinterpret_cast<int*>(tmem_slot + 4 + S::kUnitRing);
   for (int i = threadIdx.x; i <= n_groups; i += kThreads)
-    gstart[i] = tiles ? group_start[i] : i * dense_per;
+    gstart[i] = tiles ? ld_group(i) : i * dense_per;
   // The debug build checks every entry and clamps a bad one into range, so
   // that all roles still walk the same pipeline.
   auto tile_at = [&](int ti) -> Tile {
     Tile tl;
     if (tiles) {
-      tl = tiles[MOE_DCHECK(ti, bnd.max_tiles) ? ti : 0];
+      const int tj = MOE_DCHECK(ti, bnd.max_tiles) ? ti : 0;
+      tl = gather ? __ldcg(tiles + tj) : tiles[tj];
     } else {
       const int s = ti / dense_per, t0 = (ti - s * dense_per) * NMAX;
       tl = make_int4(s, t0, s * dense_T + t0, min(NMAX, dense_T - t0));
@@ -191,7 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
-      ptx::mbar_init(full0 + 8 * s, 1);
+      // gathering: the weights' bytes, and one arrival per producer lane
+      // once its copies of the token rows have landed
+      ptx::mbar_init(full0 + 8 * s, gather ? 1 + 32 * kRowWarps : 1);
       ptx::mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < S::kNAcc; ++b) {
@@ -202,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 4; ++x) ptx::mbar_init(ofull0 + 8 * x, 4);  // the half's 4 warps
     for (int x = 0; x < S::kUnitRing; ++x) {
       ptx::mbar_init(ufull0 + 8 * x, 1);
-      ptx::mbar_init(uempty0 + 8 * x, 1 + kEpiThreads / 32);  // MMA thread + epilogue warps
+      // read by the MMA thread, the epilogue warps and, gathering, the row warps
+      ptx::mbar_init(uempty0 + 8 * x, 1 + kEpiThreads / 32 + (gather ? kRowWarps : 0));
     }
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -219,7 +252,62 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == 0 && gather) {
+    // ---------------------------------------- weight producer (gathering)
+    // Lane 0 takes the units, passes them on and issues each stage's weight
+    // boxes with TMA; the row warps fill the stage's token rows.
+    if (lane == 0) {
+      int it = 0, posted = 0;
+      bool ok = true;
+      for (int j = 0;; ++j) {
+        int u = static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x);
+        u = u < total ? u : total;
+        const int slot = posted % S::kUnitRing;
+        if (posted >= S::kUnitRing &&
+            !ptx::mbar_wait(uempty0 + 8 * slot, ((posted / S::kUnitRing) & 1) ^ 1, abort_flag,
+                            status)) {
+          ok = false;
+          break;
+        }
+        uslot[slot] = u;
+        ptx::mbar_arrive(ufull0 + 8 * slot);
+        ++posted;
+        if (u >= total) break;
+        int ti, m;
+        const int ks = u % k_split;
+        decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+        const Tile tl = tile_at(ti);
+        const int a_row = tl.x * a_rows_per_expert + m * 128;
+        const int kb1 = min(k_blocks, (ks + 1) * kb_per);
+        for (int kb = ks * kb_per; kb < kb1; kb += KPS, ++it) {
+          const int s = it % S::kStages;
+          const uint32_t ph = (it / S::kStages) & 1;
+          if (!ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full0 + 8 * s, KPS * S::kNA * kABytes);
+#pragma unroll
+          for (int p = 0; p < KPS; ++p) {
+            const uint32_t st = sbase + s * S::kStageBytes + p * S::kSubBytes;
+            ptx::tma_load_2d(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row);
+            if (MODE == kGemmSiluUp)
+              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
+                               a_row + a_up_offset);
+          }
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        // unwinding: let the weight boxes issued land before exit
+        const int n = it < S::kStages ? it : S::kStages;
+        for (int i = 0; i < n; ++i) {
+          const int jj = it - 1 - i;
+          ptx::mbar_wait_drain(full0 + 8 * (jj % S::kStages), (jj / S::kStages) & 1);
+        }
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int taken = 0, posted = 0;
@@ -397,6 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
+          // gathered token rows were written through the generic proxy
+          if (gather) ptx::fence_proxy_async();
 #pragma unroll
           for (int p = 0; p < KPS; ++p) {
             const uint32_t st = sbase + s * S::kStageBytes + p * S::kSubBytes;
@@ -423,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait_drain(drain, 0);
       }
     }
-  } else {
+  } else if (warp <= 9) {
     // ------------------------------------------------------------ epilogue
     if (!early) pdl_enter();
     const int q = warp & 3;              // TMEM lane quarter this warp may access
@@ -542,6 +632,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(tempty0 + 8 * b);
       if (publish) ptx::publish_rows(publish + ti, published, lane);
     }
+  } else if (gather) {
+    // ----------------------------------------------------------- row warps
+    // Copy each stage's token rows from x, 16 bytes per lane and copy,
+    // straight into the 128-byte-swizzled layout the MMA reads (chunk c of
+    // row r at r * 128 + ((c ^ (r & 7)) * 16)). Row warp w takes the groups
+    // of four rows g = w, w + kRowWarps, ...; in a group, lanes 8i..8i+7 take
+    // row 4g + i, one chunk each, so each warp-wide copy fills four whole
+    // rows. Each lane's copies of a stage arrive on the stage's barrier once
+    // they have landed (it expects the weights' bytes and every row-warp
+    // lane); the MMA thread then fences the rows for the async proxy.
+    constexpr int kBOff = S::kNA * kABytes;
+    constexpr int kPer = NMAX / (4 * kRowWarps);  // row groups per warp
+    static_assert(kPer >= 1 && kPer * 4 * kRowWarps == NMAX, "row groups per warp");
+    const int rw = warp - 10;
+    const int rsub = lane >> 3, chunk = lane & 7;
+    const char* xb = static_cast<const char*>(gx);
+    const long row_bytes = gld * (TF32 ? 4 : 2);
+    int it = 0;
+    for (int ai = 0;; ++ai) {
+      const int slot = ai % S::kUnitRing;
+      if (!ptx::mbar_wait(ufull0 + 8 * slot, (ai / S::kUnitRing) & 1, abort_flag, status)) break;
+      const int u = uslot[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(uempty0 + 8 * slot);
+      if (u >= total) break;
+      int ti, m;
+      const int ks = u % k_split;
+      decode_unit(u / k_split, gstart, n_groups, m_tiles, ti, m);
+      const Tile tl = tile_at(ti);
+      const int kb1 = min(k_blocks, (ks + 1) * kb_per);
+      // this lane's rows and their tokens; rows past the segment repeat its
+      // first row (their columns of the accumulator are never stored). An
+      // item id outside [0, gitems), possible only in caller-made segments,
+      // reads row 0: its output row is garbage, as from an unwritten x_perm.
+      long src[kPer];
+      int dst[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int r = 4 * (i * kRowWarps + rw) + rsub;
+        const int id = __ldcg(gids + tl.y + (r < tl.w ? r : 0));
+        int tok = (id >= 0 && id < gitems) ? id / gdiv : 0;
+        if (!MOE_DCHECK(tok, bnd.x_rows)) tok = 0;
+        src[i] = static_cast<long>(tok) * row_bytes + chunk * 16;
+        dst[i] = r * 128 + ((chunk ^ (r & 7)) << 4);
+      }
+      bool ok = true;
+      for (int kb = ks * kb_per; kb < kb1; kb += KPS, ++it) {
+        const int s = it % S::kStages;
+        const uint32_t ph = (it / S::kStages) & 1;
+        int w_ok = 1;
+        if (lane == 0) w_ok = ptx::mbar_wait(empty0 + 8 * s, ph ^ 1, abort_flag, status) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        const uint32_t st0 = sbase + s * S::kStageBytes;
+#pragma unroll
+        for (int p = 0; p < KPS; ++p) {
+          const uint32_t bdst = st0 + p * S::kSubBytes + kBOff;
+          const long kbyte = static_cast<long>(kb + p) * 128;
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) ptx::cp_async16(bdst + dst[i], xb + src[i] + kbyte);
+        }
+        ptx::cp_async_arrive_noinc(full0 + 8 * s);
+      }
+      if (!ok) break;
+    }
+    ptx::cp_async_wait<0>();  // nothing of this warp is in flight when the CTA exits
+  } else if (!early) {
+    pdl_enter();  // the row warps idle when the token rows come through mapB
   }
 
   ptx::tc_fence_before();
@@ -566,7 +727,8 @@ cudaError_t launch_variant(const GemmArgs& a, int num_sms, cudaStream_t st) {
                     a.tiles, a.group_start, a.n_groups, a.dense_T, a.m_tiles, a.k_blocks, a.k_split,
                     a.a_rows_per_expert, a.a_up_offset, a.b_from_out, static_cast<TOut*>(a.out),
                     a.out_ld, a.split_stride, a.part, a.m_valid, a.status, a.bnd, a.sched,
-                    a.ready, a.ready_target, a.publish, a.published);
+                    a.ready, a.ready_target, a.publish, a.published, a.gather_x,
+                    a.gather_ids, a.gather_div, a.gather_ld, a.gather_items);
 }
 
 }  // namespace
@@ -578,6 +740,10 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
   // of whole units)
   if ((a.ready || a.publish) && (!a.tiles || a.k_split != 1)) return cudaErrorInvalidValue;
   if ((a.ready || a.publish) && !a.published) return cudaErrorInvalidValue;
+  // gathering needs the tile table, whole token tiles and one K range per unit
+  if (a.gather_x && (!a.tiles || !a.gather_ids || a.gather_div < 1 || a.gather_ld <= 0 ||
+                     a.gather_items <= 0 || a.ready))
+    return cudaErrorInvalidValue;
   if (a.ready && (!a.sched || a.ready_target <= 0)) return cudaErrorInvalidValue;
   if (MOE_DEBUG_BUILD && (a.bnd.a_rows <= 0 || a.bnd.b_rows <= 0 || a.bnd.out_rows <= 0 ||
                           (a.tiles && a.bnd.max_tiles <= 0)))

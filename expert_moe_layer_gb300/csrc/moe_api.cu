@@ -315,12 +315,16 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
              float* part = nullptr, const int32_t* out_rows = nullptr,
              const float* out_scale = nullptr, int b_cap = 0, GemmBounds bnd = {},
              int* publish = nullptr, const int* ready = nullptr, int ready_target = 0,
-             int* sched = nullptr, int* published = nullptr) {
+             int* sched = nullptr, int* published = nullptr, const void* gather_x = nullptr,
+             const int32_t* gather_ids = nullptr, int gather_div = 1, long gather_rows = 0) {
   CUtensorMap ma, mb;
   // CTA pairs in SiLU mode stage 64 gate and 64 up rows per CTA: 64-row boxes
   const int a_box = (pair && mode == kGemmSiluUp) ? 64 : 128;
   MOE_TRY(make_map(&ma, A, dt, a_rows, Kdim, a_box));
-  MOE_TRY(make_map(&mb, B, dt, b_rows, Kdim, pair ? nmax / 2 : nmax));
+  // a kernel that gathers its token rows reads no B map; it gets a valid one
+  // over x
+  MOE_TRY(make_map(&mb, gather_x ? gather_x : B, dt, gather_x ? gather_rows : b_rows, Kdim,
+                   pair ? nmax / 2 : nmax));
   GemmArgs g;
   g.mapA = &ma;
   g.mapB = &mb;
@@ -351,6 +355,14 @@ int run_gemm(GemmMode mode, moe_dtype dt, int nmax, const void* A, long a_rows, 
   g.ready_target = ready_target;
   g.sched = sched;
   g.published = published;
+  if (gather_x) {
+    g.gather_x = gather_x;
+    g.gather_ids = gather_ids;
+    g.gather_div = gather_div;
+    g.gather_ld = Kdim;
+    g.gather_items = gather_rows * gather_div;
+    g.bnd.x_rows = gather_rows;
+  }
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   if (pair) return cuda_ok(launch_gemm_pair(mode, nmax, g, sms, st));
@@ -557,9 +569,13 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
   if (!tiles_ready)
     MOE_TRY(cuda_ok(launch_build_tiles(counts, offsets, El, nmax, tiles, groups, max_tiles,
                                        cap, status, st)));
-  MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
-                                n_items, K, H, x_perm, st, y_rows ? w_items : nullptr,
-                                y_rows ? w_perm : nullptr)));
+  // GEMM1 on single CTAs fetches its token rows from x itself; the CTA-pair
+  // and fused kernels read them from x_perm
+  const bool self_gather = !pairs && !fused;
+  if (!self_gather)
+    MOE_TRY(cuda_ok(launch_gather(c->act_dtype == MOE_BF16, x, sorted_ids, offsets + El, cap,
+                                  n_items, K, H, x_perm, st, y_rows ? w_items : nullptr,
+                                  y_rows ? w_perm : nullptr)));
   if (ev) MOE_TRY(record_event(ev[0], st));
   if (fused) {
     const int ks = gemm1_ksplit(c, T);
@@ -605,7 +621,8 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
     MOE_TRY(run_gemm(kGemmSiluUp, c->act_dtype, nmax, w13, static_cast<long>(El) * 2 * I, x_perm,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, 2 * I, I, status,
                      st, ks1, static_cast<long>(cap) * 2 * I, 0, false, part1, nullptr, nullptr,
-                     0, out_bounds(cap, max_tiles)));
+                     0, out_bounds(cap, max_tiles), nullptr, nullptr, 0, nullptr, nullptr,
+                     self_gather ? x : nullptr, sorted_ids, K, T));
     MOE_TRY(cuda_ok(launch_silu_finalize(c->act_dtype == MOE_BF16, part1, ks1,
                                          static_cast<long>(cap) * 2 * I, offsets + El, cap, I,
                                          h_perm, st)));
@@ -614,7 +631,7 @@ int do_mlp(const moe_config* c, int T, const void* x, const int32_t* sorted_ids,
                      cap, H, tiles, groups, El, I / 128, 2 * I, I, 0, h_perm, I, I, status, st,
                      1, 0, 0, pairs, nullptr, nullptr, nullptr, pairs ? cap : 0,
                      out_bounds(cap, max_tiles), early ? ready : nullptr, nullptr, 0, nullptr,
-                     early ? sched + 1 : nullptr));
+                     early ? sched + 1 : nullptr, self_gather ? x : nullptr, sorted_ids, K, T));
   }
   if (ev) MOE_TRY(record_event(ev[1], st));
   // with y_rows (CTA pairs only) GEMM2 writes segment position p to row
@@ -914,9 +931,11 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   p.kernels = 0;
   if (T > 0) {
     // logits + top-k and align (or the fused route kernel), the routed MLP
-    // (fused kernel, or gather + GEMMs), shared GEMMs, combine
+    // (gather + fused kernel; gather + GEMMs on CTA pairs; GEMMs on single
+    // CTAs, which gather their token rows themselves, with a finalize kernel
+    // when GEMM1 is split over K), shared GEMMs, combine
     p.kernels = (p.fused_route ? 1 : 2 + p.align_kernels) +
-                (p.fused_mlp ? 2 : p.gemm1_k_split > 1 ? 4 : 3) +
+                (p.fused_mlp ? 2 : p.cta_pairs ? 3 : p.gemm1_k_split > 1 ? 3 : 2) +
                 (cfg->num_shared_experts > 0 ? 2 : 0) + 1;
   }
   *out = p;

@@ -162,6 +162,29 @@ __device__ __forceinline__ void publish_rows(int* counter, int* total, int lane)
   }
 }
 
+// ------------------------------------------------ per-thread async copies
+// 16 bytes global -> shared (cached in L2 only), tracked per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// One arrival on mbarrier `bar` once every cp.async this thread issued so far
+// has landed. The arrival is not counted in advance: the barrier's expected
+// count must include it.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// This thread's copies so far form one group; wait until at most N of its
+// groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 // Untiled bulk copy global -> shared: 16-byte aligned addresses, size a
 // multiple of 16. Completes `bytes` transactions on the mbarrier.

@@ -4,7 +4,8 @@
  * One layer forward is:
  *   route         router GEMM, fp32 softmax, (grouped) top-k, renormalise
  *   align/permute expert_map mask, per-local-expert padded segments
- *   grouped MLP   gather rows, GEMM1 with the SiLU(gate)*up epilogue, GEMM2
+ *   grouped MLP   GEMM1 with the SiLU(gate)*up epilogue on the token rows
+ *                 gathered by expert, GEMM2
  *   combine       weighted gather back to token order, routed_scaling_factor,
  *                 plus the shared-expert output
  * Each stage is a hand-written CUDA kernel. moe_forward runs all of them.
@@ -332,7 +333,9 @@ MOE_API int moe_forward(const moe_config* cfg, int T, const void* x,
  * runs it. events: 8 caller-created cudaEvent_t (as void*; any may be NULL),
  * recorded on `stream` at the stage boundaries:
  *   [0] start  [1] after routing  [2] after align/permute
- *   [3] after the tile table and row gather  [4] after GEMM1 (SiLU*up)
+ *   [3] after the tile table (and the row gather kernel on the CTA-pair and
+ *       fused paths; on single CTAs GEMM1 gathers its rows itself)
+ *   [4] after GEMM1 (SiLU*up)
  *   [5] after GEMM2  [6] after the shared experts  [7] after combine.
  * kernels_launched (nullable): number of kernels this call launched. The
  * results are identical to moe_forward. When `stream` is being captured into a

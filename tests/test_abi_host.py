@@ -189,10 +189,11 @@ def test_forward_plan_per_workload():
     assert _plan(synth.QWEN_DECODE, 128).fused_route == 1
     assert _plan(synth.QWEN_DECODE, 129).fused_route == 0
     # DeepSeek-V2 shape: count, then scan and scatter in one pass (few
-    # per-warp counts); shared experts add two GEMMs
+    # per-warp counts); GEMM1 on single CTAs gathers its own token rows (no
+    # gather kernel); shared experts add two GEMMs
     p = _plan(synth.DEEPSEEK)
     assert p.align_kernels == 2 and p.fused_mlp == 0 and p.fused_route == 0
-    assert p.kernels == 2 + 2 + 3 + 2 + 1
+    assert p.kernels == 2 + 2 + 2 + 2 + 1
     # single-CTA routed GEMMs over 128-token tiles, one K range: GEMM2
     # overlaps GEMM1 (here and on the EP shard)
     assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (128, 0, 1, 1)

@@ -67,7 +67,8 @@ def test_tensor_bound_roofline_takes_the_burst_peak():
     """The dominant kernel runs inside a timed region of milliseconds, so a
     tensor-bound fraction is taken against the burst bf16 peak; the sustained
     fraction is a secondary key. An HBM-bound kernel is taken against the copy
-    peak."""
+    peak. GEMM1 on CTA pairs reads the permuted rows (one per assignment); on
+    single CTAs it gathers from x, each distinct token row counted once."""
     import synth
 
     class Plan:
@@ -79,7 +80,7 @@ def test_tensor_bound_roofline_takes_the_burst_peak():
     A, touched = 8192, 8
     flops = 4 * A * wl.H * wl.I
     k_ms = flops / 1.5e15 * 1e3          # 1500 TFLOP/s
-    r = bench.dominant_kernel_roofline(wl, Plan, A, touched, k_ms, peaks)
+    r = bench.dominant_kernel_roofline(wl, Plan, A, touched, 4096, k_ms, peaks)
     assert r["bound"] == "tensor" and r["peak"] == 2000.0
     assert abs(r["frac"] - 0.75) < 1e-3 and abs(r["frac_of_sustained"] - 0.9375) < 1e-3
 
@@ -88,10 +89,21 @@ def test_tensor_bound_roofline_takes_the_burst_peak():
 
     wl = synth.QWEN_DECODE.with_(T=8)
     A, touched = 64, 36
-    r = bench.dominant_kernel_roofline(wl, Fused, A, touched, 0.05, peaks)
+    r = bench.dominant_kernel_roofline(wl, Fused, A, touched, 8, 0.05, peaks)
     assert r["bound"] == "hbm" and r["peak"] == 6000.0
     want = (touched * 3 * wl.H * wl.I * 2 + (2 * A * wl.H + 2 * A * wl.I) * 2) / 0.05e-3 / 1e9
     assert abs(r["achieved"] - want) < 0.1
+
+    class Single:
+        fused_mlp, cta_pairs = 0, 0
+
+    wl = synth.EP_SHARD
+    A, touched, rows = 16384, 64, 7400
+    r = bench.dominant_kernel_roofline(wl, Single, A, touched, rows, 0.1, peaks)
+    assert r["bound"] == "hbm"
+    assert r["algorithmic_bytes"] == (touched * 2 * wl.I * wl.H + rows * wl.H + A * wl.I) * 2
+    r = bench.dominant_kernel_roofline(wl, Plan, A, touched, rows, 0.1, peaks)
+    assert r["algorithmic_bytes"] == (touched * 2 * wl.I * wl.H + A * wl.H + A * wl.I) * 2
 
 
 def test_layer_roofline_and_extra_workload_list():

@@ -329,6 +329,27 @@ def test_no_local_items_gives_shared_only():
     assert (out.float() == 0).all()
 
 
+@pytest.mark.parametrize("fill", [0xFF, 0x7F])
+@pytest.mark.parametrize("name", ["sigmoid_f32", "f32_ragged", "ragged_prefill", "overlap_prefill",
+                                  "overlap_ragged", "align_fold", "fused_decode", "pair_prefill",
+                                  "ep_rank1", "grouped_shared"])
+def test_forward_ignores_stale_workspace(name, fill):
+    """moe_forward must not depend on what the workspace held before the call:
+    every region it reads is written (or zeroed) by the call first. The
+    workspace is filled with NaN bytes or huge finite values; the layer must
+    still match the oracle on every path (fp32 with K split, 128-token tiles
+    with GEMM2 overlapping GEMM1, the fused decode kernel, CTA pairs, an EP
+    shard, shared experts)."""
+    c = case(name)
+    wl, d = c.wl, c.d
+    ws = torch.full((B.workspace_size(c.cfg, wl.T),), fill, dtype=torch.uint8, device="cuda")
+    out = torch.full((wl.T, wl.H), float("nan"), dtype=d["x"].dtype, device="cuda")
+    B.moe_forward(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"], d["w2"],
+                  d["shared_w13"], d["shared_w2"], None, out, ws)
+    assert B.moe_get_status(ws) == (0, 0)
+    assert_close(out.float().cpu().numpy(), c.oracle_out(), f"{name} out, workspace {fill:#x}")
+
+
 def test_zero_tokens_is_noop_and_repeat_calls_agree():
     c = case("ragged_decode")
     wl = c.wl
