@@ -63,6 +63,7 @@ namespace moe {
 [[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgGemm;
 namespace {
 
+constexpr bool kWeightEvictFirst = true;  // L2 policy of grouped weight boxes
 constexpr int kRowWarps = 4;        // warps 10..13: gathered token rows
 constexpr int kThreads = 320 + 32 * kRowWarps;
 constexpr int kEpiThreads = 256;    // warps 2..9
@@ -251,6 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A grouped GEMM reads each weight box once, or again only for the other
+  // token tiles of the same expert, which run at the same time: its weights
+  // go into L2 first in line for eviction, so that they do not push out the
+  // activations the next kernels read back. The router and shared-expert
+  // weights (used by every token tile) keep the default priority.
+  const uint64_t wpol =
+      (kWeightEvictFirst && tiles) ? ptx::policy_evict_first() : ptx::policy_evict_normal();
 
   if (warp == 0 && gather) {
     // ---------------------------------------- weight producer (gathering)
@@ -290,10 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int p = 0; p < KPS; ++p) {
             const uint32_t st = sbase + s * S::kStageBytes + p * S::kSubBytes;
-            ptx::tma_load_2d(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row);
+            ptx::tma_load_2d_hint(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row, wpol);
             if (MODE == kGemmSiluUp)
-              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
-                               a_row + a_up_offset);
+              ptx::tma_load_2d_hint(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
+                                    a_row + a_up_offset, wpol);
           }
         }
         if (!ok) break;
@@ -358,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int p = 0; p < KPS; ++p) {
             const uint32_t st = sbase + pre * S::kStageBytes + p * S::kSubBytes;
-            ptx::tma_load_2d(st, &mapA, full0 + 8 * pre, (kb + p) * kKe, a_row);
+            ptx::tma_load_2d_hint(st, &mapA, full0 + 8 * pre, (kb + p) * kKe, a_row, wpol);
             if (MODE == kGemmSiluUp)
-              ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * pre, (kb + p) * kKe,
-                               a_row + a_up_offset);
+              ptx::tma_load_2d_hint(st + kABytes, &mapA, full0 + 8 * pre, (kb + p) * kKe,
+                                    a_row + a_up_offset, wpol);
           }
         }
       }
@@ -423,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int p = 0; p < KPS; ++p) {
               const uint32_t st = st0 + p * S::kSubBytes;
-              ptx::tma_load_2d(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row);
+              ptx::tma_load_2d_hint(st, &mapA, full0 + 8 * s, (kb + p) * kKe, a_row, wpol);
               if (MODE == kGemmSiluUp)
-                ptx::tma_load_2d(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
-                                 a_row + a_up_offset);
+                ptx::tma_load_2d_hint(st + kABytes, &mapA, full0 + 8 * s, (kb + p) * kKe,
+                                      a_row + a_up_offset, wpol);
             }
           }
 #pragma unroll
