@@ -791,11 +791,17 @@ cudaError_t launch_gemm(GemmMode mode, bool tf32, int nmax, const GemmArgs& a, i
                    : launch_variant<kGemmPlain, false, __nv_bfloat16, 32, 2>(a, num_sms, st);
       return big ? launch_variant<kGemmPlain, false, __nv_bfloat16, 128>(a, num_sms, st)
                  : launch_variant<kGemmPlain, false, __nv_bfloat16, 32>(a, num_sms, st);
-    case kGemmLogits:
+    case kGemmLogits: {
       if (tf32) return cudaErrorInvalidValue;
-      if (two && big) return launch_variant<kGemmPlain, false, float, 128, 2>(a, num_sms, st);
+      // router logits split over K: two K blocks per stage where every K
+      // range holds an even number of blocks
+      const int kb_per = (a.k_blocks + a.k_split - 1) / a.k_split;
+      const bool two_split = a.k_blocks % 2 == 0 && kb_per % 2 == 0;
+      if ((two || two_split) && big)
+        return launch_variant<kGemmPlain, false, float, 128, 2>(a, num_sms, st);
       return big ? launch_variant<kGemmPlain, false, float, 128>(a, num_sms, st)
                  : launch_variant<kGemmPlain, false, float, 32>(a, num_sms, st);
+    }
   }
   return cudaErrorInvalidValue;
 }

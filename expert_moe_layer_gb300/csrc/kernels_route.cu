@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(256, 2) router_logits_split_kernel(const TX* _
 
 // --------------------------------------------------------------- top-k
 // One warp per token (large batches): logits = sum of n_part partial slabs.
-template <int VPL>
+template <int VPL, bool PART>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
                                                    int n_part, long partial_stride,
                                                    const float* __restrict__ bias, int T,
@@ -256,17 +256,40 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 #pragma unroll
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
-    p[j] = -CUDART_INF_F;
+    p[j] = e < E ? row[e] : 0.f;
+  }
+  // The partial slabs of a router split over K (PART: n_part > 1) are added
+  // in slab order, four slabs at a time: their loads are all issued before
+  // the first add, so a token waits for one L2 round trip per four slabs, not
+  // one per slab. Without slabs the variant keeps the registers of one row.
+  if constexpr (PART) {
+    for (int s0 = 1; s0 < n_part; s0 += 4) {
+      float v[4][VPL];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+          const int e = lane + 32 * j;
+          v[q][j] = (s0 + q < n_part && e < E) ? row[(s0 + q) * partial_stride + e] : 0.f;
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j)
+          if (s0 + q < n_part) p[j] += v[q][j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane + 32 * j;
+    float l = e < E ? p[j] : -CUDART_INF_F;
     sb[j] = 0.f;
     if (e < E) {
-      float l = row[e];
-#pragma unroll 8
-      for (int s = 1; s < n_part; ++s) l += row[s * partial_stride + e];
       const float b = bias ? bias[e] : 0.f;
       if (flags & kRouteBiasSelect) sb[j] = b;
       else l += b;
-      p[j] = l;
     }
+    p[j] = l;
   }
   topk_warp<VPL>(p, sb, lane, E, K, renorm, flags, n_group, topk_group,
                  ids + static_cast<long>(t) * K, wout + static_cast<long>(t) * K);
@@ -573,7 +596,11 @@ cudaError_t topk_launch(const float* logits, int n_part, long partial_stride, co
     return launch_pdl(topk_cta_kernel<V>, dim3(T), dim3(256), 0, st, logits, n_part,
                       partial_stride, bias, T, E, K, renorm, flags, n_group, topk_group, ids,
                       w);
-  return launch_pdl(topk_kernel<V>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
+  if (n_part > 1)
+    return launch_pdl(topk_kernel<V, true>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
+                      partial_stride, bias, T, E, K, renorm, flags, n_group, topk_group, ids,
+                      w);
+  return launch_pdl(topk_kernel<V, false>, dim3((T + 7) / 8), dim3(256), 0, st, logits, n_part,
                     partial_stride, bias, T, E, K, renorm, flags, n_group, topk_group, ids, w);
 }
 
