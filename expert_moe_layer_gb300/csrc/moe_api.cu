@@ -131,7 +131,9 @@ int router_ksplit(const moe_config* c, int T) {
   const long base = static_cast<long>((c->num_experts + 127) / 128) *
                     dense_tile_count(T, 1, router_nmax(T));
   if (2 * base >= 152) return 1;  // fills half the SMs: fp32 partials would cost more
-  long ks = (304 + base - 1) / base;
+  // one wave of units on the 152 SMs: each unit pays a pipeline fill and an
+  // epilogue, so fewer, longer units beat two waves of short ones
+  long ks = 152 / base;
   if (ks > 16) ks = 16;
   if (ks > k_blocks) ks = k_blocks;
   if (ks < 1) ks = 1;
