@@ -15,6 +15,7 @@
 #include "act.cuh"
 #include "internal.h"
 #include "launch.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 [[maybe_unused]] constexpr DbgFile kDbgFileCode = kDbgAlign;
@@ -698,6 +699,184 @@ __global__ void __launch_bounds__(256) ep_pack_kernel(
   }
 }
 
+// ------------------------------------------------------------ ring combine
+// The same combine for prefill-sized batches, with the rows streamed through
+// shared memory. Each CTA (one per SM) takes a contiguous range of tokens.
+// Warp 0 stages the slot positions and weights of up to kRingMetaTok tokens at
+// a time, then for each token copies its local rows of y_perm and its shared
+// expert rows with bulk copies (one row per lane) into a ring of row slots,
+// kRingEntries tokens ahead of the reducers. Warps 1..8 wait for a token's
+// rows, sum them across the columns (8 per thread and pass) in the same order
+// and with the same roundings as combine_kernel, store the output row and
+// release the token's slots. Up to kRingBytes of rows per SM are in flight,
+// against a few KB per warp for register loads.
+constexpr int kRingThreads = 288;           // warp 0 copies, warps 1..8 sum
+constexpr int kRingEntries = 32;            // tokens in the ring at most
+constexpr int kRingMetaTok = 64;            // tokens whose slots are staged at once
+constexpr int kRingBytes = 192 * 1024;      // row slots
+constexpr int kRingMinTokens = 1024;        // fewer tokens: combine_kernel
+// Bulk copies complete at about two per microsecond per SM whatever their
+// size, so the ring pays only where a token brings many bytes (its expected
+// local rows and the shared rows): DeepSeek-V2's eight 10 KB rows, not an EP
+// shard's two 4 KB rows.
+constexpr long kRingMinTokenBytes = 48 * 1024;
+constexpr int kRingCtas = 152;              // one per SM
+struct RingEntry {
+  int n;          // local rows (weighted), then the shared rows
+  int slot0;      // first row slot (the token's rows wrap around the ring)
+  int tok;
+  int pad;
+  float w[32];    // weights of the local rows, in slot order
+};
+constexpr int kRingSmem = kRingBytes + kRingMetaTok * 32 * 8 + kRingEntries * sizeof(RingEntry) +
+                          2 * kRingEntries * 8 + 16 + 128;
+
+template <typename TE>
+__global__ void __launch_bounds__(kRingThreads, 1) combine_ring_kernel(
+    const TE* __restrict__ y_perm, int cap, const int32_t* __restrict__ inv_pos,
+    const float* __restrict__ topk_w, int K, const TE* __restrict__ shared, int n_shared,
+    long shared_stride, float rsf, TE* __restrict__ out, int T, int H, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* rows = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+  int* meta_p = reinterpret_cast<int*>(rows + kRingBytes);      // [kRingMetaTok][K]
+  float* meta_w = reinterpret_cast<float*>(meta_p + kRingMetaTok * 32);
+  RingEntry* ent = reinterpret_cast<RingEntry*>(meta_w + kRingMetaTok * 32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ent + kRingEntries);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kRingEntries);
+  const uint32_t full0 = ptx::smem_u32(bars);           // [entry]: the token's rows landed
+  const uint32_t empty0 = full0 + 8 * kRingEntries;     // [entry]: the reducers are done
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = static_cast<uint32_t>(H) * sizeof(TE);
+  const int n_slots = kRingBytes / static_cast<int>(row_bytes);  // >= K + n_shared (host)
+  if (threadIdx.x == 0) {
+    for (int e = 0; e < kRingEntries; ++e) {
+      ptx::mbar_init(full0 + 8 * e, 1);
+      ptx::mbar_init(empty0 + 8 * e, kRingThreads / 32 - 1);
+    }
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_enter();
+  inv_pos = fresh(inv_pos);
+  topk_w = fresh(topk_w);
+  y_perm = fresh(y_perm);
+  shared = fresh(shared);
+  const int per = (T + gridDim.x - 1) / gridDim.x;
+  const int t_begin = static_cast<int>(blockIdx.x) * per;
+  const int n_tok = max(0, min(T, t_begin + per) - t_begin);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ copier
+    int head = 0, freed = 0, rel = 0, issued = 0;
+    bool ok = true;
+    for (int i = 0; i < n_tok && ok; ++i) {
+      const int mi = i % kRingMetaTok;
+      if (mi == 0) {  // stage the next batch's slots (all loads in flight together)
+        const int nb = min(kRingMetaTok, n_tok - i);
+        const long base = static_cast<long>(t_begin + i) * K;
+        for (int x = lane; x < nb * K; x += 32) {
+          meta_p[x] = inv_pos[base + x];
+          meta_w[x] = topk_w ? topk_w[base + x] : 1.f;
+        }
+        __syncwarp();
+      }
+      const int t = t_begin + i;
+      const int e = i % kRingEntries;
+      int p = -1;
+      float w = 0.f;
+      if (lane < K) {
+        p = meta_p[mi * K + lane];
+        w = meta_w[mi * K + lane];
+        if (p >= cap) {
+          if (status) atomicOr(status, MOE_DEV_BAD_SEGMENT);
+          p = -1;
+        }
+      }
+      const unsigned local = __ballot_sync(0xffffffffu, p >= 0);
+      const int n = __popc(local);
+      const int rows_t = n + n_shared;
+      // the entry's previous token, and older ones while the ring lacks room
+      while (rel <= i - kRingEntries || head + rows_t - freed > n_slots) {
+        const int er = rel % kRingEntries;
+        int w_ok = 1;
+        if (lane == 0)
+          w_ok = ptx::mbar_wait(empty0 + 8 * er, (rel / kRingEntries) & 1, abort_flag, status);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        freed += ent[er].n;
+        ++rel;
+      }
+      if (!ok) break;
+      const int j = __popc(local & ((1u << lane) - 1u));
+      if (p >= 0) ent[e].w[j] = w;
+      if (lane == 0) {
+        ent[e].n = rows_t;
+        ent[e].slot0 = head % n_slots;
+        ent[e].tok = t;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * e, rows_t * row_bytes);
+      __syncwarp();
+      if (p >= 0) {  // 0 <= p < cap, checked above
+        const int slot = (head + j) % n_slots;
+        ptx::bulk_load(ptx::smem_u32(rows + static_cast<long>(slot) * row_bytes),
+                       y_perm + static_cast<long>(p) * H, row_bytes, full0 + 8 * e);
+      }
+      if (lane < n_shared) {
+        const int slot = (head + n + lane) % n_slots;
+        ptx::bulk_load(ptx::smem_u32(rows + static_cast<long>(slot) * row_bytes),
+                       shared + lane * shared_stride + static_cast<long>(t) * H, row_bytes,
+                       full0 + 8 * e);
+      }
+      head += rows_t;
+      issued = i + 1;
+    }
+    if (!ok && lane == 0) {
+      // unwinding: let the copies already issued land before the CTA exits
+      for (int k = rel; k < issued; ++k)
+        ptx::mbar_wait_drain(full0 + 8 * (k % kRingEntries), (k / kRingEntries) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ reducers
+    const int ct = threadIdx.x - 32;
+    for (int i = 0; i < n_tok; ++i) {
+      const int e = i % kRingEntries;
+      if (!ptx::mbar_wait(full0 + 8 * e, (i / kRingEntries) & 1, abort_flag, status)) break;
+      const int rows_t = ent[e].n, slot0 = ent[e].slot0;
+      const int n = rows_t - n_shared;
+      const long t = ent[e].tok;
+      for (int c = ct * 8; c < H; c += (kRingThreads - 32) * 8) {
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+        int slot = slot0;
+        for (int r = 0; r < rows_t; ++r) {
+          if (r == n) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] *= rsf;
+          }
+          Raw8<TE> y;
+          y.load(reinterpret_cast<const TE*>(rows + static_cast<long>(slot) * row_bytes) + c);
+          y.add_to(acc, r < n ? ent[e].w[r] : 1.f);
+          slot = slot + 1 == n_slots ? 0 : slot + 1;
+        }
+        if (n == rows_t) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] *= rsf;
+        }
+        st8(out + t * H + c, acc);
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(empty0 + 8 * e);
+    }
+  }
+}
+
 int grid_for(long work, int per_block, int cap_blocks) {
   long g = (work + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -813,6 +992,29 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
                            const float* topk_w, int K, int k_local, const void* shared,
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st, bool slots_early) {
+  // Prefill-sized batches whose rows per token fit the ring: the ring combine,
+  // one CTA per SM.
+  const int ns = shared ? n_shared : 0;
+  const long row_bytes = static_cast<long>(H) * (bf16 ? 2 : 4);
+  const int kl_ring = k_local < 1 ? 1 : k_local > K ? K : k_local;
+  if (T >= kRingMinTokens && K <= 32 && (K + ns) * row_bytes <= kRingBytes &&
+      (kl_ring + ns) * row_bytes >= kRingMinTokenBytes) {
+    const int grid = T < kRingCtas ? T : kRingCtas;
+#define MOE_RING(TE)                                                                         \
+  do {                                                                                       \
+    static std::atomic<unsigned long long> smem_set{0};                                      \
+    const cudaError_t e = opt_in_smem(reinterpret_cast<const void*>(combine_ring_kernel<TE>), \
+                                      kRingSmem, smem_set);                                  \
+    if (e != cudaSuccess) return e;                                                          \
+    return launch_pdl(combine_ring_kernel<TE>, dim3(grid), dim3(kRingThreads), kRingSmem, st, \
+                      static_cast<const TE*>(y_perm), cap, inv_pos, topk_w, K,               \
+                      static_cast<const TE*>(shared), ns, shared_stride, rsf,                \
+                      static_cast<TE*>(out), T, H, status);                                  \
+  } while (0)
+    if (bf16) MOE_RING(__nv_bfloat16);
+    MOE_RING(float);
+#undef MOE_RING
+  }
   // Rows loaded together (KB) follow the expected number of local rows per
   // token, not K: on an EP shard most slots are elsewhere, and a narrower
   // batch over more column chunks keeps more bytes in flight per warp. A

@@ -93,6 +93,14 @@ SMALL = {
     # and scatter in one pass (64 local experts), or the three passes (300)
     "align_fold": W("align_fold", T=1200, H=128, I=128, E=64, K=8),
     "align_three_pass": W("align_three_pass", T=640, H=128, I=128, E=300, K=16),
+    # from 1024 tokens whose rows bring at least 48 KB each, the combine
+    # streams them through a shared-memory ring: 8 KB rows, four routed and two
+    # shared per token with rsf; an fp32 layer of six routed rows whose last
+    # CTA takes fewer tokens
+    "ring_shared": W("ring_shared", T=1024, H=4096, I=128, E=8, K=4, n_shared=2,
+                     I_shared=128, rsf=2.5),
+    "ring_f32": W("ring_f32", T=1030, H=2048, I=128, E=8, K=6, act="f32", router="f32",
+                  x_std=0.3),
 }
 OVERLAP = ("overlap_prefill", "overlap_ragged")
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
