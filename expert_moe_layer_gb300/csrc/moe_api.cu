@@ -23,6 +23,9 @@ namespace moe {
 namespace {
 
 constexpr int kMaxT = 1 << 18;
+// 256-token tiles from this many GEMM1 units (single CTAs below 512, CTA
+// pairs from 512)
+constexpr long kTile256MinUnits = 256;
 constexpr int kForwardBlock = 1;    // moe_forward leaves segments unpadded (the GEMMs
                                     // read past a segment's end but never store there)
 constexpr size_t kAlignBytes = 256;
@@ -102,11 +105,14 @@ int local_rows(const moe_config* c) { return (c->top_k + c->ep_size - 1) / c->ep
 // 256 (bf16) from 192 rows when that still leaves >= 512 GEMM1 work units
 // (several per SM), 128 from 48 rows, else 32. A larger N means more FLOPs
 // per byte staged into shared memory; more units mean better balance.
+// GEMM1 units on 256-token tiles (weight tiles x full token tiles)
+long units256(const moe_config* c, int T) {
+  const long local_items = static_cast<long>(T) * c->top_k / c->ep_size;
+  return (local_items / 256) * (c->intermediate_size / 128);
+}
 int routed_nmax(const moe_config* c, int T) {
   const long avg = static_cast<long>(T) * c->top_k / c->num_experts;
-  const long local_items = static_cast<long>(T) * c->top_k / c->ep_size;
-  const long units256 = (local_items / 256) * (c->intermediate_size / 128);
-  if (avg >= 192 && c->act_dtype == MOE_BF16 && units256 >= 512) return 256;
+  if (avg >= 192 && c->act_dtype == MOE_BF16 && units256(c, T) >= kTile256MinUnits) return 256;
   return avg >= 48 ? 128 : 32;
 }
 int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
@@ -204,7 +210,7 @@ SyncRegion sync_region(const moe_config* c, int T) {
 // accumulators of the double buffer fit in TMEM); GEMM2 puts 256 consecutive
 // output rows on the pair.
 bool gemms_on_pairs(const moe_config* c, int T) {
-  return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0;
+  return routed_nmax(c, T) == 256 && c->hidden_size % 256 == 0 && units256(c, T) >= 512;
 }
 
 // GEMM2 starts while GEMM1's last units run, on the SMs GEMM1 has left, when

@@ -195,10 +195,15 @@ def test_forward_plan_per_workload():
     assert p.align_kernels == 2 and p.fused_mlp == 0 and p.fused_route == 0
     assert p.kernels == 2 + 2 + 2 + 2 + 1
     # single-CTA routed GEMMs over 128-token tiles, one K range: GEMM2
-    # overlaps GEMM1 (here and on the EP shard)
+    # overlaps GEMM1
     assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (128, 0, 1, 1)
+    # EP shard: 256 rows per expert and 256 GEMM1 units on 256-token tiles,
+    # under the 512 that CTA pairs take: 256-token tiles on single CTAs, GEMM2
+    # overlapping GEMM1
     p = _plan(synth.EP_SHARD)
-    assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (128, 0, 1, 1)
+    assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (256, 0, 1, 1)
+    # 255 units on 256-token tiles: 128-token tiles
+    assert _plan(synth.EP_SHARD.with_(T=8160)).tile_rows == 128
     # fp32 layers never take the bf16-only fused or pair kernels
     p = _plan(synth.TINY)
     assert (p.fused_mlp, p.cta_pairs, p.router_tensor_cores) == (0, 0, 0)

@@ -36,6 +36,9 @@ SMALL = {
     "wide_prefill": W("wide_prefill", T=1100, H=256, I=384, E=5, K=1),
     # long segments with enough work units: 256-token tiles on CTA pairs
     "pair_prefill": W("pair_prefill", T=4096, H=256, I=2048, E=8, K=2),
+    # long segments with 256 to 511 units: 256-token tiles on single CTAs,
+    # token rows gathered by GEMM1, GEMM2 overlapping it
+    "single256": W("single256", T=2048, H=256, I=2048, E=8, K=2),
     # decode-sized segments with >= 152 GEMM1 units: both GEMMs in the fused
     # kernel (one tile per expert; then up to two ragged tiles per expert)
     "fused_decode": W("fused_decode", T=64, H=256, I=512, E=64, K=8, router_bias=True),
