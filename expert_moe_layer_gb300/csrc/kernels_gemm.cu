@@ -7,7 +7,7 @@
 // and decode (a few rows per expert, nmax = 32). Only the N of the
 // instruction changes.
 //
-// Per CTA (persistent, one per SM, 448 threads):
+// Per CTA (persistent, one per SM, 576 threads):
 //   warp 0      TMA producer: weights (A) and token rows (B) into a ring of
 //               shared-memory stages with the 128-byte swizzle (when the
 //               kernel gathers its token rows itself, A only)
@@ -19,7 +19,7 @@
 //               plain, store to global. bf16 outputs go through a staging
 //               buffer in shared memory per 16-column chunk, so the stores
 //               are 16-byte vectors along output rows.
-//   warps 10-13 with gathered token rows: copy each stage's rows of x by the
+//   warps 10-17 with gathered token rows: copy each stage's rows of x by the
 //               permutation (per-lane cp.async into the swizzled layout);
 //               otherwise idle
 // Accumulators are double-buffered in TMEM, so the epilogue of one work unit
@@ -64,7 +64,7 @@ namespace moe {
 namespace {
 
 constexpr bool kWeightEvictFirst = true;  // L2 policy of grouped weight boxes
-constexpr int kRowWarps = 4;        // warps 10..13: gathered token rows
+constexpr int kRowWarps = 8;        // warps 10..17: gathered token rows
 constexpr int kThreads = 320 + 32 * kRowWarps;
 constexpr int kEpiThreads = 256;    // warps 2..9
 static_assert(kEpiThreads / 32 == kGemmEpiWarps, "tile counts assume one add per epilogue warp");
