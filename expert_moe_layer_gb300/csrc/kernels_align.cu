@@ -197,48 +197,110 @@ __global__ void __launch_bounds__(256) align_scatter_kernel(
   }
 }
 
-// Passes 2 and 3 in one kernel, where the per-warp counts are few (at most
-// kFoldHist entries) and E_l <= 256: every CTA sums the column of each expert
-// itself (all warps for the count, the warps before its own for its base),
-// so no single-CTA scan runs between two grid-wide passes. CTA 0 writes
-// counts, offsets and the tile table. The order of the items is that of the
-// three passes.
+// Two passes, where E_l <= 256 and the per-CTA counts are few (at most
+// kFoldHist entries): CTAs of kFoldWarps warps x kFoldItemsPerWarp items.
+// The count pass writes one row of expert counts per CTA. In the second pass
+// every CTA sums each expert's column itself (all rows for the count, the
+// rows before its own for its base), so no single-CTA scan runs between two
+// grid-wide passes; it counts its own warps' items again in shared memory for
+// their bases and places them. CTA 0 writes counts, offsets and the tile
+// table. The order of the items is that of the three passes.
 constexpr long kFoldHist = 32768;
+constexpr int kFoldItemsPerWarp = 64;
+constexpr int kFoldWarps = 8;
+constexpr int kFoldItems = kFoldItemsPerWarp * kFoldWarps;  // per CTA
 
-__global__ void __launch_bounds__(256) align_scan_scatter_kernel(
+__global__ void __launch_bounds__(256) align_fold_count_kernel(
     const int32_t* __restrict__ ids, long n_items, int K, const int32_t* __restrict__ emap, int R,
-    int E, int E_l, int ep_start, const int* __restrict__ hist, int n_warps, int block_m,
+    int E, int E_l, int ep_start, int* __restrict__ bhist, int32_t* __restrict__ sorted_ids,
+    int cap, unsigned* status) {
+  pdl_enter();
+  ids = fresh(ids);
+  __shared__ int cnt[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long r = blockIdx.x * 256L + threadIdx.x; r < cap; r += 256L * gridDim.x)
+    sorted_ids[r] = static_cast<int32_t>(n_items);
+  if (threadIdx.x < E_l) cnt[threadIdx.x] = 0;
+  __syncthreads();
+  const long base = static_cast<long>(blockIdx.x) * kFoldItems + warp * kFoldItemsPerWarp;
+  int idv[kFoldItemsPerWarp / 32];
+#pragma unroll
+  for (int i = 0; i < kFoldItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    idv[i] = item < n_items ? ids[item] : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < kFoldItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    int le = -1;
+    if (item < n_items)
+      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, status);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    if (le >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[le], __popc(peers));
+  }
+  __syncthreads();
+  if (threadIdx.x < E_l)
+    bhist[static_cast<long>(blockIdx.x) * E_l + threadIdx.x] = cnt[threadIdx.x];
+}
+
+__global__ void __launch_bounds__(256) align_fold_scatter_kernel(
+    const int32_t* __restrict__ ids, long n_items, int K, const int32_t* __restrict__ emap, int R,
+    int E, int E_l, int ep_start, const int* __restrict__ bhist, int n_blocks, int block_m,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ sorted_ids, int32_t* __restrict__ inv_pos, int cap, unsigned* status,
     Tile* __restrict__ tiles, int* __restrict__ group_start, int nmax, int max_tiles) {
   pdl_enter();
   ids = fresh(ids);
-  hist = fresh(hist);
-  extern __shared__ int run[];  // [kWarpsPerBlock][E_l]
+  bhist = fresh(bhist);
+  __shared__ int run[kFoldWarps][256];  // per-warp counts, then the warps' next rows
   __shared__ int warp_sums[32];
   __shared__ int part_c[256], part_b[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = threadIdx.x;
-  const int w0 = blockIdx.x * kWarpsPerBlock;  // this CTA's first warp
-  // G = 256 / E_l threads share each expert's column: thread (g, e') sums
-  // the rows w = g, g + G, ... (all of them for the count, those before w0
-  // for this CTA's base); the G partial sums are then added in order
+  for (int i = threadIdx.x; i < kFoldWarps * 256; i += 256) (&run[0][0])[i] = 0;
+  const long base = static_cast<long>(blockIdx.x) * kFoldItems + warp * kFoldItemsPerWarp;
+  int idv[kFoldItemsPerWarp / 32];  // this lane's ids, loaded before the column sums
+#pragma unroll
+  for (int i = 0; i < kFoldItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    idv[i] = item < n_items ? ids[item] : 0;
+  }
+  // G = 256 / E_l threads share each expert's column of the per-CTA counts:
+  // thread (g, e') sums the rows b = g, g + G, ... (all of them for the
+  // count, those before this CTA for its base); the G partial sums are then
+  // added in order
   {
     const int G = 256 / E_l;
     const int ge = threadIdx.x % E_l, g = threadIdx.x / E_l;
     int pc = 0, pb = 0;
     if (g < G) {
 #pragma unroll 16
-      for (int w = g; w < n_warps; w += G) {
-        const int h = hist[static_cast<long>(w) * E_l + ge];
-        if (w < w0) pb += h;
+      for (int b = g; b < n_blocks; b += G) {
+        const int h = bhist[static_cast<long>(b) * E_l + ge];
+        if (b < static_cast<int>(blockIdx.x)) pb += h;
         pc += h;
       }
     }
     part_c[threadIdx.x] = pc;
     part_b[threadIdx.x] = pb;
   }
-  __syncthreads();
+  __syncthreads();  // run zeroed, partial sums in
+  // this CTA's items: their local experts, and each warp's count per expert
+  int lev[kFoldItemsPerWarp / 32];
+  unsigned pev[kFoldItemsPerWarp / 32];
+#pragma unroll
+  for (int i = 0; i < kFoldItemsPerWarp / 32; ++i) {
+    const long item = base + 32 * i + lane;
+    int le = -1;
+    // status already recorded by the count pass for bad ids
+    if (item < n_items)
+      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, nullptr);
+    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    lev[i] = le;
+    pev[i] = peers;
+    if (le >= 0 && lane == __ffs(peers) - 1) run[warp][le] += __popc(peers);
+    __syncwarp();
+  }
   int c = 0, before = 0;
   if (e < E_l) {
     for (int g = 0; g < 256 / E_l; ++g) {
@@ -248,6 +310,7 @@ __global__ void __launch_bounds__(256) align_scan_scatter_kernel(
   }
   const int padded = e < E_l ? ((c + block_m - 1) / block_m) * block_m : 0;
   int total = 0;
+  // (the scan's barriers also make every warp's counts visible below)
   const int start = block_exclusive_scan(padded, warp_sums, total);
   if (blockIdx.x == 0) {
     if (e < E_l) {
@@ -264,35 +327,23 @@ __global__ void __launch_bounds__(256) align_scan_scatter_kernel(
   }
   if (e < E_l) {
     int r = start + before;
-    for (int wi = 0; wi < kWarpsPerBlock; ++wi) {
-      run[wi * E_l + e] = r;
-      if (w0 + wi < n_warps) r += hist[static_cast<long>(w0 + wi) * E_l + e];
+    for (int wi = 0; wi < kFoldWarps; ++wi) {
+      const int n = run[wi][e];
+      run[wi][e] = r;
+      r += n;
     }
   }
   __syncthreads();
-  const int gw = w0 + warp;
-  if (gw >= n_warps) return;
-  int* my = run + warp * E_l;
-  const long base = static_cast<long>(gw) * kItemsPerWarp;
-  int idv[kItemsPerWarp / 32];  // all of this lane's ids in flight at once
-#pragma unroll
-  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
-    const long item = base + 32 * i + lane;
-    idv[i] = item < n_items ? ids[item] : 0;
-  }
   const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-  for (int i = 0; i < kItemsPerWarp / 32; ++i) {
+  for (int i = 0; i < kFoldItemsPerWarp / 32; ++i) {
     const long item = base + 32 * i + lane;
-    int le = -1;
-    // status already recorded by pass 1 for bad ids
-    if (item < n_items)
-      le = local_expert(idv[i], static_cast<int>(item / K), emap, R, E, E_l, ep_start, nullptr);
-    const unsigned peers = __match_any_sync(0xffffffffu, le);
+    const int le = lev[i];
+    const unsigned peers = pev[i];
     if (item < n_items) {
       int pos = -1;
       if (le >= 0) {
-        pos = my[le] + __popc(peers & lt);
+        pos = run[warp][le] + __popc(peers & lt);
         if (pos < cap) {
           sorted_ids[pos] = static_cast<int32_t>(item);
         } else {
@@ -303,7 +354,7 @@ __global__ void __launch_bounds__(256) align_scan_scatter_kernel(
       inv_pos[item] = pos;
     }
     __syncwarp();
-    if (le >= 0 && lane == __ffs(peers) - 1) my[le] += __popc(peers);
+    if (le >= 0 && lane == __ffs(peers) - 1) run[warp][le] += __popc(peers);
     __syncwarp();
   }
 }
@@ -886,9 +937,16 @@ int grid_for(long work, int per_block, int cap_blocks) {
 
 }  // namespace
 
+namespace {
+bool align_fold(long n_items, int E_l) {
+  return E_l <= 256 && ((n_items + kFoldItems - 1) / kFoldItems) * E_l <= kFoldHist;
+}
+
+}  // namespace
+
 int align_kernel_count(long n_items, int E_l) {
   if (n_items <= kSmallItems && E_l <= kSmallExperts) return 1;
-  return (E_l <= 256 && static_cast<long>(align_warps(n_items)) * E_l <= kFoldHist) ? 2 : 3;
+  return align_fold(n_items, E_l) ? 2 : 3;
 }
 
 int align_warps(long n_items) {
@@ -907,6 +965,18 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                       offsets, sorted_ids, inv_pos, cap, status, tiles, group_start, nmax,
                       max_tiles);
   }
+  if (align_fold(n_items, E_l)) {
+    // per-CTA counts: (n_items / kFoldItems) x E_l ints, within hist's
+    // align_warps(n_items) x E_l
+    const int fb = static_cast<int>((n_items + kFoldItems - 1) / kFoldItems);
+    cudaError_t e = launch_pdl(align_fold_count_kernel, dim3(fb), dim3(256), 0, st, ids, n_items,
+                               K, emap, R, E, E_l, ep_start, hist, sorted_ids, cap, status);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(align_fold_scatter_kernel, dim3(fb), dim3(256), 0, st, ids, n_items, K,
+                      emap, R, E, E_l, ep_start, static_cast<const int*>(hist), fb, block_m,
+                      counts, offsets, sorted_ids, inv_pos, cap, status, tiles, group_start,
+                      nmax, max_tiles);
+  }
   const int n_warps = align_warps(n_items);
   const int blocks = (n_warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const size_t smem = sizeof(int) * kWarpsPerBlock * E_l;
@@ -914,11 +984,6 @@ cudaError_t launch_align(const int32_t* ids, long n_items, const int32_t* emap, 
                              K, emap, R, E, E_l, ep_start, hist, n_warps, sorted_ids, cap,
                              status);
   if (e != cudaSuccess) return e;
-  if (E_l <= 256 && static_cast<long>(n_warps) * E_l <= kFoldHist)
-    return launch_pdl(align_scan_scatter_kernel, dim3(blocks), dim3(256), smem, st, ids,
-                      n_items, K, emap, R, E, E_l, ep_start, static_cast<const int*>(hist),
-                      n_warps, block_m, counts, offsets, sorted_ids, inv_pos, cap, status, tiles,
-                      group_start, nmax, max_tiles);
   e = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, st, hist, n_warps, E_l, block_m,
                  counts, offsets, cap, status, tiles, group_start, nmax, max_tiles);
   if (e != cudaSuccess) return e;

@@ -189,7 +189,7 @@ def test_forward_plan_per_workload():
     assert _plan(synth.QWEN_DECODE, 128).fused_route == 1
     assert _plan(synth.QWEN_DECODE, 129).fused_route == 0
     # DeepSeek-V2 shape: count, then scan and scatter in one pass (few
-    # per-warp counts); GEMM1 on single CTAs gathers its own token rows (no
+    # per-CTA counts); GEMM1 on single CTAs gathers its own token rows (no
     # gather kernel); shared experts add two GEMMs
     p = _plan(synth.DEEPSEEK)
     assert p.align_kernels == 2 and p.fused_mlp == 0 and p.fused_route == 0

@@ -205,7 +205,7 @@ def test_align_entry_point(name, block):
     """The single-CTA per-warp counting sort (ragged_prefill, ep_rank1), the
     small-batch path of up to 64 items (single_token: 4 items; ep_tiny: 24
     items over 64 local experts; wide_router: 48 items of an EP shard with 160
-    local experts), and the multi-CTA passes: count, then scan and scatter in
+    local experts), and the multi-CTA passes: per-CTA counts, then scan and scatter in
     one kernel (align_fold: 9600 items, 64 experts) or in two (align_three_pass:
     10240 items, 300 experts)."""
     c = case(name)
