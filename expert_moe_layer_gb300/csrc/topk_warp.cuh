@@ -7,12 +7,13 @@
 // Order: larger selection score first, equal scores -> lower expert id.
 // Every argmax is two single-instruction warp reductions (redux.sync) on an
 // order-preserving 32-bit key of the float: the largest key, then the lowest
-// expert id among the lanes that hold it. A lane's candidates stay in expert
-// order (expert lane + 32*j in slot j); each round the lane offers its best
-// remaining one (ties to the lower slot, which is the lower id) and the
-// owner of the winner marks that slot taken. Nothing per lane is sorted, so
-// no id array is kept: the routing kernel runs this in CTAs of 1024 threads,
-// whose 64-register budget would otherwise push an array into local memory.
+// expert id among the lanes that hold it. Each lane first sorts its VPL
+// candidates (expert lane + 32*j in slot j) with a bitonic network on 64-bit
+// values key << 32 | (16 - j), so that equal keys keep the lower slot (the
+// lower id) first and an emptied entry (0) sorts below every real one. A
+// round then offers each lane's first entry, and the owner of the winner
+// drops it (a shift of its list), instead of every lane scanning its
+// remaining slots every round.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -128,23 +129,40 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
       if (gj[j] >= 0 && !((keep >> gj[j]) & 1u)) ck[j] = ninf;
   }
 
+  static_assert(VPL >= 1 && VPL <= 16 && (VPL & (VPL - 1)) == 0, "VPL: a power of two <= 16");
+  // this lane's candidates, sorted: larger key first, then lower slot (slots
+  // beyond E hold -inf keys with ids >= E: they never win while a real expert
+  // remains; a NaN score has key 0)
+  uint64_t v[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j)
+    v[j] = (static_cast<uint64_t>(ck[j]) << 32) | static_cast<uint32_t>(16 - j);
+#pragma unroll
+  for (int kk = 2; kk <= VPL; kk <<= 1) {
+#pragma unroll
+    for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int l = i ^ jj;
+        if (l > i) {
+          const bool desc = (i & kk) == 0;
+          const uint64_t a = v[i], b = v[l];
+          const bool sw = desc ? (a < b) : (a > b);
+          v[i] = sw ? b : a;
+          v[l] = sw ? a : b;
+        }
+      }
+    }
+  }
+
   float my_w = 0.f;
   int my_id = 0;
   float wsum = 0.f;
-  uint32_t taken = 0u;  // bit j: slot j already chosen
   for (int k = 0; k < K; ++k) {
     // this lane's best remaining candidate, or id 0x7fffffff when none is left
-    // (slots beyond E hold -inf keys with ids >= E; they never win while a
-    // real expert remains; a NaN score has key 0 and is offered last)
-    uint32_t key = 0u;
-    int id = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      if (!((taken >> j) & 1u) && (id == 0x7fffffff || ck[j] > key)) {
-        key = ck[j];
-        id = lane + 32 * j;
-      }
-    }
+    const uint32_t low = static_cast<uint32_t>(v[0]) & 31u;
+    uint32_t key = low ? static_cast<uint32_t>(v[0] >> 32) : 0u;
+    int id = low ? lane + 32 * (16 - static_cast<int>(low)) : 0x7fffffff;
     warp_argmax_key(key, id);
     // the winner's score: the key itself, or with a selection correction the
     // uncorrected score from the lane that holds it (picked by a bit mask,
@@ -158,7 +176,11 @@ __device__ __forceinline__ void topk_warp(float (&p)[VPL], const float (&sb)[VPL
       for (int j = 0; j < VPL; ++j) mine |= __float_as_uint(p[j]) & (0u - (ws == j));
       pw = __shfl_sync(0xffffffffu, __uint_as_float(mine), id & 31);
     }
-    if (lane == (id & 31) && ws < VPL) taken |= 1u << ws;  // the owner retires the slot
+    if (id != 0x7fffffff && lane == (id & 31)) {  // the owner drops its first entry
+#pragma unroll
+      for (int j = 0; j + 1 < VPL; ++j) v[j] = v[j + 1];
+      v[VPL - 1] = 0;
+    }
     wsum += pw;
     if (lane == k) {
       my_w = pw;
