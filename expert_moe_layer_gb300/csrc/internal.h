@@ -256,6 +256,7 @@ cudaError_t set_wait_limit_gemm(unsigned long long ns);
 cudaError_t set_wait_limit_gemm_pair(unsigned long long ns);
 cudaError_t set_wait_limit_mlp_fused(unsigned long long ns);
 cudaError_t set_wait_limit_route(unsigned long long ns);
+cudaError_t set_wait_limit_align(unsigned long long ns);
 
 // Debug build: each translation unit's record of failed bounds checks, read
 // and cleared (all zero in the release build).

@@ -1114,5 +1114,6 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
 }
 
 MOE_DEBUG_TAKER(take_dbg_align)
+MOE_WAIT_LIMIT_SETTER(set_wait_limit_align)
 
 }  // namespace moe

@@ -1088,7 +1088,7 @@ int moe_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns ? ns : 1000000000ull;  // 0: the default, 1 s
   cudaError_t (*const setters[])(unsigned long long) = {
       set_wait_limit_gemm, set_wait_limit_gemm_pair, set_wait_limit_mlp_fused,
-      set_wait_limit_route};
+      set_wait_limit_route, set_wait_limit_align};
   for (auto set : setters)
     MOE_TRY(cuda_ok(set(v)));
   return MOE_OK;
