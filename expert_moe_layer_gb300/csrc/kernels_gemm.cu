@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
-    ptx::cp_async_wait<0>();  // nothing of this warp is in flight when the CTA exits
+    ptx::cp_async_wait_all();  // nothing of this warp is in flight when the CTA exits
   } else if (!early) {
     pdl_enter();  // the row warps idle when the token rows come through mapB
   }
