@@ -72,7 +72,7 @@ class Plan(ctypes.Structure):
                 ("router_partials", ctypes.c_int), ("align_kernels", ctypes.c_int),
                 ("tile_rows", ctypes.c_int), ("gemm1_k_split", ctypes.c_int),
                 ("cta_pairs", ctypes.c_int), ("fused_mlp", ctypes.c_int),
-                ("gemm2_overlap", ctypes.c_int)]
+                ("gemm2_overlap", ctypes.c_int), ("combine_ring", ctypes.c_int)]
 
 
 def make_config(num_experts, top_k, hidden_size, intermediate_size, renormalize=True,

@@ -245,6 +245,9 @@ cudaError_t launch_ep_pack(bool bf16, const void* x, const int32_t* ids, const f
 // variant. slots_early: inv_pos and topk_w were written by a kernel at least
 // two launches back on this stream (true only inside moe_forward), so the
 // kernel may read them before its dependency wait.
+// Whether launch_combine streams the rows through the shared-memory ring
+// (n_shared: the shared-expert outputs it adds, 0 without them).
+bool combine_uses_ring(bool bf16, int T, int K, int k_local, int n_shared, int H);
 cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t* inv_pos,
                            const float* topk_w, int K, int k_local, const void* shared,
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,

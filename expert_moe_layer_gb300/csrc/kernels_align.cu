@@ -944,6 +944,13 @@ bool align_fold(long n_items, int E_l) {
 
 }  // namespace
 
+bool combine_uses_ring(bool bf16, int T, int K, int k_local, int n_shared, int H) {
+  const long row_bytes = static_cast<long>(H) * (bf16 ? 2 : 4);
+  const int kl = k_local < 1 ? 1 : k_local > K ? K : k_local;
+  return T >= kRingMinTokens && K <= 32 && (K + n_shared) * row_bytes <= kRingBytes &&
+         (kl + n_shared) * row_bytes >= kRingMinTokenBytes;
+}
+
 int align_kernel_count(long n_items, int E_l) {
   if (n_items <= kSmallItems && E_l <= kSmallExperts) return 1;
   return align_fold(n_items, E_l) ? 2 : 3;
@@ -1057,13 +1064,10 @@ cudaError_t launch_combine(bool bf16, const void* y_perm, int cap, const int32_t
                            const float* topk_w, int K, int k_local, const void* shared,
                            int n_shared, long shared_stride, float rsf, void* out, int T, int H,
                            unsigned* status, cudaStream_t st, bool slots_early) {
-  // Prefill-sized batches whose rows per token fit the ring: the ring combine,
-  // one CTA per SM.
+  // Prefill-sized batches whose rows per token fit the ring and bring enough
+  // bytes: the ring combine, one CTA per SM.
   const int ns = shared ? n_shared : 0;
-  const long row_bytes = static_cast<long>(H) * (bf16 ? 2 : 4);
-  const int kl_ring = k_local < 1 ? 1 : k_local > K ? K : k_local;
-  if (T >= kRingMinTokens && K <= 32 && (K + ns) * row_bytes <= kRingBytes &&
-      (kl_ring + ns) * row_bytes >= kRingMinTokenBytes) {
+  if (combine_uses_ring(bf16, T, K, k_local, ns, H)) {
     const int grid = T < kRingCtas ? T : kRingCtas;
 #define MOE_RING(TE)                                                                         \
   do {                                                                                       \

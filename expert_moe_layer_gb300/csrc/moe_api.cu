@@ -102,8 +102,8 @@ int n_local(const moe_config* c) {
 int local_rows(const moe_config* c) { return (c->top_k + c->ep_size - 1) / c->ep_size; }
 
 // Token tile (MMA N) of the routed GEMMs, from the average segment length:
-// 256 (bf16) from 192 rows when that still leaves >= 512 GEMM1 work units
-// (several per SM), 128 from 48 rows, else 32. A larger N means more FLOPs
+// 256 (bf16) from 192 rows when that still leaves >= 256 GEMM1 work units
+// (CTA pairs from 512, single CTAs below), 128 from 48 rows, else 32. A larger N means more FLOPs
 // per byte staged into shared memory; more units mean better balance.
 // GEMM1 units on 256-token tiles (weight tiles x full token tiles)
 long units256(const moe_config* c, int T) {
@@ -936,6 +936,11 @@ int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out) {
   p.gemm1_k_split = gemm1_ksplit(cfg, T);
   p.cta_pairs = gemms_on_pairs(cfg, T) ? 1 : 0;
   p.gemm2_overlap = gemm2_early(cfg, T) ? 1 : 0;
+  p.combine_ring = T > 0 && combine_uses_ring(cfg->act_dtype == MOE_BF16, T, cfg->top_k,
+                                              local_rows(cfg), cfg->num_shared_experts,
+                                              cfg->hidden_size)
+                       ? 1
+                       : 0;
   p.kernels = 0;
   if (T > 0) {
     // logits + top-k and align (or the fused route kernel), the routed MLP

@@ -429,7 +429,8 @@ typedef struct {
   int fused_route;         /* 1: logits, top-k and align in one kernel        */
   int router_tensor_cores; /* 1: router GEMM on tcgen05, 0: CUDA cores        */
   int router_partials;     /* partial logit slabs the top-k kernel sums       */
-  int align_kernels;       /* 0 (fused route), 1 (one CTA) or 3 (3 passes)    */
+  int align_kernels;       /* 0 (fused route), 1 (one CTA), 2 (per-CTA counts,
+                              then scan and scatter) or 3 (three passes)     */
   int tile_rows;           /* token rows per routed GEMM tile: 32, 128 or 256 */
   int gemm1_k_split;       /* 1, or K ranges of GEMM1 whose fp32 partials are
                               summed by a finalize kernel or, fused, in-kernel */
@@ -441,6 +442,9 @@ typedef struct {
   int gemm2_overlap;       /* 1: GEMM2 starts on the SMs GEMM1 has left and
                               takes each token tile once GEMM1 has published
                               its rows (single-CTA GEMMs, one K range)       */
+  int combine_ring;        /* 1: the combine streams each token's rows through
+                              a shared-memory ring (from 1024 tokens whose
+                              expected routed and shared rows bring >= 48 KB) */
 } moe_plan;
 MOE_API int moe_forward_plan(const moe_config* cfg, int T, moe_plan* out);
 

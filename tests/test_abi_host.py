@@ -200,8 +200,14 @@ def test_forward_plan_per_workload():
     # EP shard: 256 rows per expert and 256 GEMM1 units on 256-token tiles,
     # under the 512 that CTA pairs take: 256-token tiles on single CTAs, GEMM2
     # overlapping GEMM1
+    # six routed and two shared rows of 10 KB per token: the ring combine
+    assert p.combine_ring == 1
     p = _plan(synth.EP_SHARD)
     assert (p.tile_rows, p.cta_pairs, p.gemm1_k_split, p.gemm2_overlap) == (256, 0, 1, 1)
+    # two expected local rows of 4 KB per token: the register combine
+    assert p.combine_ring == 0
+    assert _plan(synth.MIXTRAL).combine_ring == 0
+    assert _plan(synth.DEEPSEEK.with_(T=1023)).combine_ring == 0
     # 255 units on 256-token tiles: 128-token tiles
     assert _plan(synth.EP_SHARD.with_(T=8160)).tile_rows == 128
     # fp32 layers never take the bf16-only fused or pair kernels

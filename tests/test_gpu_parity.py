@@ -106,6 +106,8 @@ SMALL = {
                   x_std=0.3),
 }
 OVERLAP = ("overlap_prefill", "overlap_ragged")
+# the combine streams their rows through the shared-memory ring
+RING = ("ring_shared", "ring_f32")
 SCORING = ("sigmoid_select", "sigmoid_select_mid", "sigmoid_select_wide", "sigmoid_f32")
 FUSED = ("fused_decode", "fused_two_tiles", "grouped_shared")
 ROUTE_FUSED = ("tiny_f32", "ragged_decode", "single_token", "f32_router_decode",
@@ -428,7 +430,7 @@ def test_forward_captured_in_cuda_graph_matches_eager(name):
 
 
 @pytest.mark.parametrize("name", ["pair_prefill", "ragged_prefill", *FUSED, *ROUTE_FUSED,
-                                  *OVERLAP])
+                                  *OVERLAP, *RING])
 def test_plan_matches_the_kernels_launched(name):
     """moe_forward_plan (host only) names the path; moe_forward_timed counts
     the kernels that path launched. The fused cases must take the fused
@@ -443,6 +445,7 @@ def test_plan_matches_the_kernels_launched(name):
     if name in ("pair_prefill", "ragged_prefill"):
         assert plan.fused_route == 0 and plan.align_kernels == 1
     assert plan.gemm2_overlap == (1 if name in OVERLAP else 0)
+    assert plan.combine_ring == (1 if name in RING else 0)
     ws = torch.empty(B.workspace_size(c.cfg, wl.T), dtype=torch.uint8, device="cuda")
     out = torch.empty(wl.T, wl.H, dtype=d["x"].dtype, device="cuda")
     n = B.moe_forward_timed(c.cfg, wl.T, d["x"], d["router_w"], d["router_b"], d["w13"],
