@@ -120,8 +120,9 @@ int dense_nmax(int T) { return T >= 64 ? 128 : 32; }
 // The router runs as a tcgen05 GEMM whenever x and the router weights are
 // bf16 (fp32 routers run on CUDA cores, split over H into 256-column slices
 // when E <= 32). Tensor-core routers whose units (expert tiles x token tiles)
-// fill less than half the SMs split K = H so that ~2 units per SM exist; the
-// top-k kernel sums the fp32 partials in a fixed order.
+// fill less than half the SMs split K = H into ranges, as many as still fit
+// the units into one wave; the top-k kernel sums the fp32 partials in slab
+// order.
 int route_flags(const moe_config* c) {
   return (c->scoring_func == MOE_SCORE_SIGMOID ? kRouteSigmoid : 0) |
          (c->bias_mode == MOE_BIAS_SELECT ? kRouteBiasSelect : 0);
