@@ -481,7 +481,8 @@ MOE_API int moe_get_status(const void* ws, void* stream, uint32_t* flags);
  * entries (index, expert, first row, row count) against the tile table and
  * the permuted buffers, output rows and columns against the output, weight
  * rows against the weight tensor, the sorted positions read by the gather
- * and the combine, and the top-k ids against E. A failed check skips the
+ * and the combine, the token rows GEMM1's row warps copy from x, and the
+ * top-k ids against E. A failed check skips the
  * access or clamps the value into range (the outputs are then unusable) and
  * is counted in a device record, which also keeps the site, index and bound
  * of the first failure. Same entry points and results otherwise; slower. */
