@@ -345,14 +345,14 @@ def test_no_local_items_gives_shared_only():
 @pytest.mark.parametrize("fill", [0xFF, 0x7F])
 @pytest.mark.parametrize("name", ["sigmoid_f32", "f32_ragged", "ragged_prefill", "overlap_prefill",
                                   "overlap_ragged", "align_fold", "fused_decode", "pair_prefill",
-                                  "ep_rank1", "grouped_shared"])
+                                  "ep_rank1", "grouped_shared", "single256", "ring_shared"])
 def test_forward_ignores_stale_workspace(name, fill):
     """moe_forward must not depend on what the workspace held before the call:
     every region it reads is written (or zeroed) by the call first. The
     workspace is filled with NaN bytes or huge finite values; the layer must
     still match the oracle on every path (fp32 with K split, 128-token tiles
     with GEMM2 overlapping GEMM1, the fused decode kernel, CTA pairs, an EP
-    shard, shared experts)."""
+    shard, shared experts, 256-token tiles on single CTAs, the ring combine)."""
     c = case(name)
     wl, d = c.wl, c.d
     ws = torch.full((B.workspace_size(c.cfg, wl.T),), fill, dtype=torch.uint8, device="cuda")
