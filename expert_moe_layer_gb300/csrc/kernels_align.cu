@@ -938,8 +938,13 @@ int grid_for(long work, int per_block, int cap_blocks) {
 }  // namespace
 
 namespace {
+// Every scatter CTA of the fold sums the count rows of all CTAs, so its work
+// grows with the square of the CTA count: past kFoldWork row entries in all
+// (about 64 MB of L2 reads) the three passes cost less.
+constexpr long kFoldWork = 1L << 24;
 bool align_fold(long n_items, int E_l) {
-  return E_l <= 256 && ((n_items + kFoldItems - 1) / kFoldItems) * E_l <= kFoldHist;
+  const long fb = (n_items + kFoldItems - 1) / kFoldItems;
+  return E_l <= 256 && fb * E_l <= kFoldHist && fb * fb * E_l <= kFoldWork;
 }
 
 }  // namespace

@@ -188,6 +188,11 @@ def test_forward_plan_per_workload():
     # the fused route kernel stops at 128 tokens
     assert _plan(synth.QWEN_DECODE, 128).fused_route == 1
     assert _plan(synth.QWEN_DECODE, 129).fused_route == 0
+    # the one-pass scan and scatter stops where its per-CTA sums would read
+    # more than 2^24 count entries: 2^19 items over 32 local experts take
+    # three passes
+    assert _plan(synth.Workload("fold_edge", T=1 << 18, H=128, I=128, E=32, K=2)).align_kernels == 3
+    assert _plan(synth.Workload("fold_ok", T=1 << 15, H=128, I=128, E=32, K=2)).align_kernels == 2
     # DeepSeek-V2 shape: count, then scan and scatter in one pass (few
     # per-CTA counts); GEMM1 on single CTAs gathers its own token rows (no
     # gather kernel); shared experts add two GEMMs
